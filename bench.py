@@ -1,0 +1,525 @@
+#!/usr/bin/env python3
+"""Decode-attention benchmark over a quantized paged KV cache.
+
+Metric: decode-attention microseconds per step and effective cache GB/s (as a
+fraction of the GB300's measured HBM bandwidth) against context length.  One
+step = kvq_append of the step's new token(s) + kvq_decode + kvq_combine, all
+inputs resident in HBM.  Default workload: GQA 6:1, int8 per-row absmax,
+B=1, Hq=24, Hkv=4, D=256, block 256, context 262,144 (the kv-quant-attn
+page's geometry); the context sweep 1K..262,144 is reported beside it.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line (rank 0).  Under torchrun every rank runs an independent
+replica (the path does not shard); the time is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode-attention µs/step and cache GB/s (% of GB300 HBM peak) vs context length"
+SWEEP = [1024, 4096, 16384, 65536, 262144]
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=30)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", default="gqa", choices=["tiny", "gqa", "paged", "spec", "mixed"])
+    p.add_argument("--ctx", type=int, default=None, help="context length (gqa: 262144, spec: 32768, tiny: 256)")
+    p.add_argument("--no-sweep", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args()
+
+
+# --------------------------------------------------------------------------- helpers
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+class Clocks:
+    """nvidia-smi sampling of SM clocks and throttle reasons during a region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.out, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.out.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
+                except ValueError:
+                    continue
+        os.unlink(self.path)
+        if not rows:
+            return None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for _, _, r in rows for n, v in zip(names, r) if v.lower().startswith("active")})
+        busy = [s for s, _, _ in rows]
+        return {"sm_mhz": statistics.median(busy), "sm_max_mhz": max(m for _, m, _ in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+def dist_setup():
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def describe(w, window=0):
+    names = {1: "int8", 2: "fp8-e4m3", 3: "int4"}
+    modes = {1: "per-row", 2: "per-tensor", 3: "per-channel"}
+    L = w.seq_lens
+    ctx = f"ctx={int(L[0])}" if (L == L[0]).all() else f"ctx=ragged[{int(L.min())}..{int(L.max())}] sum={int(L.sum())}"
+    s = (f"{w.name}: {names[w.dtype]} K {modes[w.k_mode]} / V {modes[w.v_mode]}, B={w.batch} Hq={w.num_q_heads} "
+         f"Hkv={w.num_kv_heads} D={w.head_dim} T={w.q_tokens} block={w.block_size} {ctx}")
+    if w.softcap:
+        s += f" softcap={w.softcap:g}"
+    if w.use_sink:
+        s += " head_sink"
+    if window:
+        s += f" window={window}"
+    return s
+
+
+def make_workload(args):
+    from decode_attention_quantized_gb300 import synth
+    ctx = args.ctx
+    if ctx is None and args.workload == "gqa":
+        ctx = 262144
+    if args.workload in ("tiny", "gqa", "spec"):
+        return synth.make(args.workload, ctx=ctx)
+    return synth.make(args.workload, max_ctx=ctx)
+
+
+# --------------------------------------------------------------------------- GPU arm
+
+def measure(w, steps, warmup, *, windows=(0,), e2e=False):
+    """Time `steps` decode steps of workload w on the current GPU.  Caches are
+    replicated so that consecutive steps read different memory and the
+    replicas together exceed 4x the L2 size (inputs larger than L2)."""
+    import numpy as np
+    import torch
+    from decode_attention_quantized_gb300 import kvq, synth
+    from decode_attention_quantized_gb300.workload import GpuWorkload
+
+    dev = torch.cuda.current_device()
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    kv_bytes = synth.step_bytes(w)["kv"]
+    reps = max(2, math.ceil(4 * l2 / max(kv_bytes, 1)))
+    reps = min(reps, 512)
+    gws = [GpuWorkload(w, device=f"cuda:{dev}", gen_device="cuda")]
+    gws[0].fill_history()
+    for _ in range(reps - 1):
+        g = GpuWorkload.__new__(GpuWorkload)
+        g.__dict__.update(gws[0].__dict__)
+        src = gws[0].cache
+        c = kvq.QuantizedPagedCache.__new__(kvq.QuantizedPagedCache)
+        c.__dict__.update(src.__dict__)
+        c.k_codes, c.v_codes = src.k_codes.clone(), src.v_codes.clone()
+        c.k_scale, c.v_scale = src.k_scale.clone(), src.v_scale.clone()
+        g.cache = c
+        gws.append(g)
+    k_new, v_new, slots = gws[0].new_tokens()
+    nq = 8
+    qs = [w.q("cuda", i).to(f"cuda:{dev}") for i in range(nq)]
+    plist = [gws[0].params(window=wd) for wd in windows]
+    bufs = [gws[0].buffers(p) for p in plist]
+    stream = torch.cuda.current_stream()
+
+    def one(i, ev=None):
+        g = gws[i % reps]
+        j = i % len(windows)
+        p, b = plist[j], bufs[j]
+        if ev is not None:
+            ev[0].record(stream)
+        kvq.kvq_append(g.cache, k_new, v_new, slots, stream)
+        if ev is not None:
+            ev[1].record(stream)
+        kvq.kvq_decode(g.cache, p, qs[i % nq], g.block_table, g.seq_lens, b.workspace, stream)
+        if ev is not None:
+            ev[2].record(stream)
+        kvq.kvq_combine(g.cache, p, b.workspace, g.head_sink, b.out, b.lse, stream)
+        if ev is not None:
+            ev[3].record(stream)
+
+    for i in range(warmup):
+        one(i)
+    torch.cuda.synchronize()
+    assert kvq.kvq_get_device_error() == 0, "device error flags set during warm-up"
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    t0.record(stream)
+    for i in range(steps):
+        one(warmup + i, evs[i])
+    t1.record(stream)
+    torch.cuda.synchronize()
+    total_ms = t0.elapsed_time(t1)
+    dec = [e[1].elapsed_time(e[2]) for e in evs]
+    app = [e[0].elapsed_time(e[1]) for e in evs]
+    comb = [e[2].elapsed_time(e[3]) for e in evs]
+    step = [e[0].elapsed_time(e[3]) for e in evs]
+    res = dict(total_ms=total_ms, steps=steps, decode_ms=dec, append_ms=app, combine_ms=comb, step_ms=step,
+               launches=3 * steps, reps=reps, l2=l2)
+    sb = [synth.step_bytes(w, wd) for wd in windows]
+    res["step_bytes"] = sum(sum(sb[i % len(windows)].values()) for i in range(warmup, warmup + steps))
+    res["decode_bytes"] = [synth.decode_bytes(w, windows[i % len(windows)]) for i in range(warmup, warmup + steps)]
+
+    if e2e:
+        res["e2e"] = measure_e2e(w, gws, plist, windows, steps, warmup, k_new, v_new, slots, qs)
+    return res
+
+
+def measure_e2e(w, gws, plist, windows, steps, warmup, k_new, v_new, slots, qs):
+    """Same steps through the public API with host buffers: every step copies
+    its inputs (q, new K/V rows, slot_mapping, seq_lens) from pinned host memory,
+    runs append + decode + combine, and reads the output (and LSE) back."""
+    import torch
+    from decode_attention_quantized_gb300 import kvq
+
+    dev = torch.cuda.current_device()
+    stream = torch.cuda.current_stream()
+    h_q = [q.cpu().pin_memory() for q in qs]
+    h_k, h_v, h_s = k_new.cpu().pin_memory(), v_new.cpu().pin_memory(), slots.cpu().pin_memory()
+    h_l = gws[0].seq_lens.cpu().pin_memory()
+    d_q = torch.empty_like(qs[0])
+    d_k, d_v, d_s = torch.empty_like(k_new), torch.empty_like(v_new), torch.empty_like(slots)
+    d_l = torch.empty_like(gws[0].seq_lens)
+    bufs = [gws[0].buffers(p) for p in plist]
+    h_out = torch.empty(bufs[0].out.shape, dtype=bufs[0].out.dtype).pin_memory()
+    h_lse = torch.empty(bufs[0].lse.shape, dtype=torch.float32).pin_memory()
+    reps = len(gws)
+
+    def one(i):
+        g = gws[i % reps]
+        j = i % len(windows)
+        d_q.copy_(h_q[i % len(h_q)], non_blocking=True)
+        d_k.copy_(h_k, non_blocking=True)
+        d_v.copy_(h_v, non_blocking=True)
+        d_s.copy_(h_s, non_blocking=True)
+        d_l.copy_(h_l, non_blocking=True)
+        kvq.kvq_append(g.cache, d_k, d_v, d_s, stream)
+        kvq.kvq_decode(g.cache, plist[j], d_q, g.block_table, d_l, bufs[j].workspace, stream)
+        kvq.kvq_combine(g.cache, plist[j], bufs[j].workspace, g.head_sink, bufs[j].out, bufs[j].lse, stream)
+        h_out.copy_(bufs[j].out, non_blocking=True)
+        h_lse.copy_(bufs[j].lse, non_blocking=True)
+        stream.synchronize()
+
+    for i in range(warmup):
+        one(i)
+    torch.cuda.synchronize()
+    t = time.perf_counter()
+    for i in range(steps):
+        one(warmup + i)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t
+    h2d = (qs[0].numel() * 2 + k_new.numel() * 2 + v_new.numel() * 2 + slots.numel() * 8 + h_l.numel() * 4)
+    d2h = h_out.numel() * 2 + h_lse.numel() * 4
+    return dict(wall_s=wall, h2d=h2d, d2h=d2h)
+
+
+def traffic_from_profiles(kernel_tag: str):
+    """DRAM bytes per launch of the decode kernel from the committed ncu
+    summary, if it was taken on the current kernel source."""
+    from decode_attention_quantized_gb300 import build as b
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        ent = d.get(kernel_tag)
+        if ent and ent.get("source_stamp") == b._stamp():
+            return ent["dram_bytes_per_launch"]
+    except Exception:
+        pass
+    return None
+
+
+def run_ours(args):
+    import torch
+    from decode_attention_quantized_gb300 import build as cuda_build
+    from decode_attention_quantized_gb300 import kvq, synth
+
+    world, rank, local = dist_setup()
+    cuda_build.build()
+    kvq.load()
+    peak, peak_kind = load_peaks()
+    w = make_workload(args)
+    windows = (w.window_for_call(0), w.window_for_call(1)) if w.window else (0,)
+
+    clocks = Clocks(local)
+    barrier(world)
+    torch.cuda.synchronize()
+    clocks.start()
+    res = measure(w, args.steps, args.warmup, windows=windows, e2e=not args.no_e2e)
+    clk = clocks.stop()
+    barrier(world)
+    total_ms = max_over_ranks(res["total_ms"], world)
+
+    sweep = []
+    if not args.no_sweep and args.workload == "gqa" and world == 1:
+        for ctx in SWEEP:
+            if ctx == w.seq_lens[0]:
+                r = res
+                wc = w
+            else:
+                wc = synth.make("gqa", ctx=ctx)
+                r = measure(wc, max(10, args.steps), max(3, args.warmup))
+            dec_ms = statistics.median(r["decode_ms"])
+            kvb = synth.decode_bytes(wc)
+            sweep.append({"ctx": ctx, "us_per_step": round(1e3 * r["total_ms"] / r["steps"], 2),
+                          "decode_us_median": round(1e3 * dec_ms, 2),
+                          "decode_gbs": round(kvb / (dec_ms * 1e-3) / 1e9, 1),
+                          "frac_of_hbm": round(kvb / (dec_ms * 1e-3) / 1e9 / peak, 3),
+                          "cache_mb": round(synth.step_bytes(wc)["kv"] / 1e6, 2),
+                          "replicas": r["reps"]})
+            del r
+            torch.cuda.empty_cache()
+
+    K = args.steps
+    step_bytes = res["step_bytes"] * world
+    value = step_bytes / (total_ms * 1e-3) / 1e9
+    dec_mean_ms = statistics.mean(res["decode_ms"])
+    dec_bytes = statistics.mean(res["decode_bytes"])
+    achieved = dec_bytes / (dec_mean_ms * 1e-3) / 1e9
+    tag = f"{args.workload}-{int(w.seq_lens.max())}"
+    line = {
+        "metric": METRIC,
+        "value": round(value, 1),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": round(total_ms / K, 4),
+        "us_per_step": round(1e3 * total_ms / K, 2),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f16",
+        "data": "synthetic (seeded torch generators; no dataset)",
+        "config": {
+            "workload": describe(w),
+            "cache_dtype": {1: "int8", 2: "fp8-e4m3", 3: "int4"}[w.dtype],
+            "compute": "f16 x f16 -> f32 tensor-core mma, fp32 softmax",
+            "step": "kvq_append (new tokens) + kvq_decode + kvq_combine",
+            "windows_per_call": list(windows),
+            "l2": f"inputs larger than L2: {res['reps']} cache replicas rotated per step, "
+                  f"{res['reps'] * synth.step_bytes(w)['kv'] / 1e6:.0f} MB total vs L2 {res['l2'] / 1e6:.0f} MB",
+            "parallelism": "replicas" if world > 1 else "single-gpu",
+        },
+        "step_breakdown_us_median": {
+            "append": round(1e3 * statistics.median(res["append_ms"]), 2),
+            "decode": round(1e3 * statistics.median(res["decode_ms"]), 2),
+            "combine": round(1e3 * statistics.median(res["combine_ms"]), 2),
+        },
+        "roofline": {
+            "kernel": "decode_kernel",
+            "bound": "hbm",
+            "achieved": round(achieved, 1),
+            "peak": peak,
+            "peak_kind": f"of {peak_kind}",
+            "unit": "GB/s",
+            "frac": round(achieved / peak, 4),
+            "traffic": traffic_from_profiles(tag),
+            "algorithmic_bytes_per_launch": int(dec_bytes),
+        },
+        "gpu_launches": res["launches"],
+        "clocks": clk,
+    }
+    if sweep:
+        line["sweep"] = sweep
+    if "e2e" in res:
+        e = res["e2e"]
+        e2e_wall = max_over_ranks(e["wall_s"], world)
+        line["e2e"] = {"value": round(step_bytes / e2e_wall / 1e9, 1), "unit": "GB/s",
+                       "us_per_step": round(1e6 * e2e_wall / K, 2),
+                       "h2d_bytes_per_step": e["h2d"], "d2h_bytes_per_step": e["d2h"]}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, windows[0], budget_s=12.0)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+# --------------------------------------------------------------------------- oracle (CPU) arm
+
+def oracle_sample(w, window, kv_heads):
+    """Oracle cache of sequence 0 restricted to the given kv heads' query rows;
+    returns a callable that runs one timed sample and its algorithmic bytes."""
+    import numpy as np
+    import torch
+    from decode_attention_quantized_gb300 import synth
+    from oracle import oracle
+
+    def bits(t):
+        return t.cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+    gen = "cuda" if torch.cuda.is_available() else "cpu"
+    b = int(np.argmax(w.seq_lens))
+    L = int(w.seq_lens[b])
+    bs = w.block_size
+    nbk = max(1, math.ceil(L / bs))
+    ks = synth.calibrate_static(w, gen, "k")
+    vs = synth.calibrate_static(w, gen, "v")
+    oc = oracle.OracleCache(w.dtype, w.k_mode, w.v_mode, nbk, bs, w.num_kv_heads, w.head_dim,
+                            None if ks is None else ks.cpu().numpy(), None if vs is None else vs.cpu().numpy())
+    k, v = w.seq_kv(b, gen)
+    table = np.arange(nbk, dtype=np.int32)[None, :]
+    oc.append(bits(k), bits(v), np.arange(L, dtype=np.int64))
+    q = bits(w.q(gen))[b:b + 1]
+    sink = w.head_sink(gen)
+    sink = None if sink is None else sink.cpu().numpy()
+    G, T = w.group, w.q_tokens
+    rows = np.array([(0, t, h * G + g) for h in kv_heads for t in range(T) for g in range(G)], np.int32)
+    lens = np.array([L], np.int32)
+    cores = os.cpu_count() or 1
+    per_key = 2 * w.row_bytes() + (4 if w.k_mode == 1 else 0) + (4 if w.v_mode == 1 else 0)
+    lo = max(0, L - T + 1 - window) if window else 0
+    nbytes = (L - lo) * per_key * len(kv_heads) + len(rows) * w.head_dim * 2 * 2
+
+    def run():
+        t = time.perf_counter()
+        oc.attend(q, table, lens, q_tokens=T, softcap=w.softcap, window=window, head_sink=sink, rows=rows,
+                  nthreads=cores)
+        return time.perf_counter() - t
+
+    desc = (f"sequence {b} (L={L}), {len(rows)} query rows of kv head(s) {list(kv_heads)} "
+            f"of {w.batch * T * w.num_q_heads} in the step; oracle dequantizes each row's keys in fp64")
+    return run, nbytes, cores, desc
+
+
+def cpu_baseline(w, window, budget_s=12.0):
+    run, nbytes, cores, desc = oracle_sample(w, window, kv_heads=list(range(w.num_kv_heads)))
+    t = run()
+    reps = 1
+    while t * (reps + 1) / reps < budget_s and reps < 3:
+        t += run()
+        reps += 1
+    return {"value": round(nbytes * reps / t / 1e9, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": desc + f"; {reps} run(s), {t:.1f} s"}
+
+
+def run_reference(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    from decode_attention_quantized_gb300 import synth
+    from oracle import oracle
+    oracle.build()
+    w = make_workload(args)
+    run, nbytes, cores, desc = oracle_sample(w, w.window_for_call(0), kv_heads=[0])
+    for _ in range(args.warmup):
+        run()
+    times = [run() for _ in range(args.steps)]
+    total = sum(times)
+    value = nbytes * args.steps / total / 1e9
+    line = {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": round(value, 4),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(1e3 * total / args.steps, 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic (seeded torch generators; no dataset)",
+        "config": {"workload": describe(w), "note": "the CPU fp64 oracle, one bounded sample per step"},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    a = parse()
+    if a.impl == "reference":
+        run_reference(a)
+    else:
+        run_ours(a)

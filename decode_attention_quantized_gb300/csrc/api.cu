@@ -1,0 +1,363 @@
+// api.cu -- the C ABI of include/kvq.h: host-side validation, split planning,
+// TMA descriptor encoding and kernel launches.  No allocation, no host sync
+// (except kvq_get_device_error, which says so), no device data read back.
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "kvq_internal.h"
+
+namespace kvq {
+
+// Per-device flag word for data violations (KVQ_DEVERR_*).
+__device__ unsigned int g_error_word;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+  bool init = false;
+  int sms = 0;
+  unsigned int* err = nullptr;
+};
+
+std::mutex g_mu;
+DeviceInfo g_dev[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+kvq_status current_device(DeviceInfo** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return KVQ_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceInfo& d = g_dev[dev];
+  if (!d.init) {
+    if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return KVQ_ERR_CUDA;
+    if (cudaGetSymbolAddress(reinterpret_cast<void**>(&d.err), g_error_word) != cudaSuccess) return KVQ_ERR_CUDA;
+    d.init = true;
+  }
+  *out = &d;
+  return KVQ_OK;
+}
+
+kvq_status encoder(PFN_cuTensorMapEncodeTiled_v12000* out) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_encode) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !fn)
+      return KVQ_ERR_CUDA;
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  *out = g_encode;
+  return KVQ_OK;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+bool pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
+int ilog2(int x) {
+  int l = 0;
+  while ((1 << l) < x) ++l;
+  return l;
+}
+int row_bytes(const kvq_cache* c) { return c->dtype == KVQ_INT4 ? c->head_dim / 2 : c->head_dim; }
+
+kvq_status check_cache(const kvq_cache* c) {
+  if (!c) return KVQ_ERR_INVALID_ARG;
+  if (c->dtype < KVQ_INT8 || c->dtype > KVQ_INT4) return KVQ_ERR_INVALID_ARG;
+  for (int m : {c->k_mode, c->v_mode})
+    if (m < KVQ_SCALE_PER_ROW || m > KVQ_SCALE_PER_CHANNEL) return KVQ_ERR_INVALID_ARG;
+  if (c->num_blocks <= 0 || c->num_kv_heads <= 0 || c->head_dim <= 0) return KVQ_ERR_INVALID_ARG;
+  if (!pow2(c->block_size) || c->block_size < 16 || c->block_size > (1 << 20)) return KVQ_ERR_INVALID_ARG;
+  if ((long long)c->num_blocks * c->block_size > (1LL << 31) - 1) return KVQ_ERR_INVALID_ARG;
+  if (c->head_dim != 64 && c->head_dim != 128 && c->head_dim != 256) return KVQ_ERR_UNSUPPORTED;
+  if (!c->k_codes || !c->v_codes || !c->k_scale || !c->v_scale) return KVQ_ERR_INVALID_ARG;
+  if (!aligned(c->k_codes, 16) || !aligned(c->v_codes, 16)) return KVQ_ERR_INVALID_ARG;
+  if (!aligned(c->k_scale, c->k_mode == KVQ_SCALE_PER_ROW ? 16 : 4)) return KVQ_ERR_INVALID_ARG;
+  if (!aligned(c->v_scale, c->v_mode == KVQ_SCALE_PER_ROW ? 16 : 4)) return KVQ_ERR_INVALID_ARG;
+  return KVQ_OK;
+}
+
+kvq_status check_params(const kvq_cache* c, const kvq_decode_params* p) {
+  if (!p) return KVQ_ERR_INVALID_ARG;
+  if (p->batch < 0 || p->num_q_heads <= 0 || p->q_tokens <= 0 || p->max_blocks_per_seq <= 0 ||
+      p->max_seq_len < 0 || p->window < 0)
+    return KVQ_ERR_INVALID_ARG;
+  if (p->num_q_heads % c->num_kv_heads != 0) return KVQ_ERR_INVALID_ARG;
+  if (!std::isfinite(p->sm_scale) || !std::isfinite(p->softcap) || p->softcap < 0.0f) return KVQ_ERR_INVALID_ARG;
+  if ((long long)p->max_blocks_per_seq * c->block_size > (1LL << 30)) return KVQ_ERR_INVALID_ARG;
+  if (p->num_q_heads / c->num_kv_heads > 8 || p->q_tokens > 8 || p->batch > kMaxBatch) return KVQ_ERR_UNSUPPORTED;
+  return KVQ_OK;
+}
+
+// Launch shape of the decode kernel and the workspace it implies.
+struct Plan {
+  int rows, row_groups, key_warps, threads, stages, grid, units_max;
+  size_t smem, ws_plan, ws_lse, ws_o, ws_total;
+};
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+size_t stage_stride(const kvq_cache* c) {
+  const size_t code = (size_t)kTile * row_bytes(c);
+  return (2 * code + 2 * kTile * 4 + 1023) / 1024 * 1024;
+}
+
+size_t fixed_smem(const kvq_cache* c, int n_cw, int batch, int stages) {
+  size_t s = 1024;                                  // alignment slack of the ring
+  s += (size_t)n_cw * 8 * c->head_dim * 4;          // merge scratch (accumulators)
+  s += (size_t)n_cw * 16 * 4;                       // merge scratch (m, l)
+  s += ((size_t)batch * 3 + 5 + ((batch * 3 + 5) & 1)) * 4;  // split plan
+  s += (size_t)stages * 2 * 8;                      // mbarriers
+  return s;
+}
+
+cudaError_t occupancy(const kvq_cache* c, int threads, size_t smem, int* n) {
+  switch (c->dtype) {
+    case KVQ_INT8: return occupancy_decode_int8(c->head_dim, threads, smem, n);
+    case KVQ_FP8_E4M3: return occupancy_decode_fp8(c->head_dim, threads, smem, n);
+    default: return occupancy_decode_int4(c->head_dim, threads, smem, n);
+  }
+}
+
+kvq_status make_plan(const kvq_cache* c, const kvq_decode_params* p, const DeviceInfo& dev, Plan* out) {
+  Plan P{};
+  const int G = p->num_q_heads / c->num_kv_heads;
+  P.rows = G * p->q_tokens;
+  P.row_groups = (P.rows + 7) / 8;
+  P.key_warps = P.row_groups <= 2 ? 4 : (P.row_groups <= 4 ? 2 : 1);
+  const int n_cw = P.row_groups * P.key_warps;
+  P.threads = 32 * (n_cw + 1);
+  const int B = p->batch > 0 ? p->batch : 1;
+  const size_t stride = stage_stride(c);
+  int occ = 0;
+  for (int target : {2, 1}) {
+    const size_t budget = target == 2 ? (size_t)113 * 1024 : (size_t)227 * 1024;
+    const size_t fixed = fixed_smem(c, n_cw, B, 0);
+    if (fixed + 2 * (stride + 16) > budget) continue;
+    int stages = (int)((budget - fixed) / (stride + 16));
+    stages = stages > kMaxStages ? kMaxStages : stages;
+    if (target == 2 && stages < 3) continue;
+    const size_t smem = fixed_smem(c, n_cw, B, stages) + (size_t)stages * stride;
+    int n = 0;
+    if (occupancy(c, P.threads, smem, &n) != cudaSuccess) return KVQ_ERR_CUDA;
+    if (n >= target || (target == 1 && n >= 1)) {
+      occ = target;
+      P.stages = stages;
+      P.smem = smem;
+      break;
+    }
+  }
+  if (occ == 0) return KVQ_ERR_UNSUPPORTED;
+  const long long cap = (long long)p->max_blocks_per_seq * c->block_size;
+  const long long maxlen = (p->max_seq_len > 0 && p->max_seq_len < cap) ? p->max_seq_len : cap;
+  long long grid = (long long)dev.sms * occ;
+  const long long useful = (long long)B * c->num_kv_heads * ((maxlen + kTile - 1) / kTile + 1);
+  if (grid > useful) grid = useful;
+  P.grid = (int)(grid < 1 ? 1 : grid);
+  P.units_max = P.grid * kWaves + B * c->num_kv_heads;
+  P.ws_plan = align256((size_t)(4 + B + 1) * 4);
+  P.ws_lse = align256((size_t)P.units_max * P.rows * 4);
+  P.ws_o = (size_t)P.units_max * P.rows * c->head_dim * 4;
+  P.ws_total = P.ws_plan + P.ws_lse + P.ws_o;
+  *out = P;
+  return KVQ_OK;
+}
+
+kvq_status encode_codes_map(const kvq_cache* c, void* base, CUtensorMap* tm) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc;
+  if (kvq_status s = encoder(&enc)) return s;
+  const int dp = row_bytes(c);
+  const int span = dp >= 128 ? 128 : dp;
+  const cuuint64_t dims[4] = {(cuuint64_t)dp, (cuuint64_t)c->block_size, (cuuint64_t)c->num_kv_heads,
+                              (cuuint64_t)c->num_blocks};
+  const cuuint64_t strides[3] = {(cuuint64_t)dp, (cuuint64_t)dp * c->block_size,
+                                 (cuuint64_t)dp * c->block_size * c->num_kv_heads};
+  const cuuint32_t box[4] = {(cuuint32_t)span, (cuuint32_t)(c->block_size < kTile ? c->block_size : kTile), 1, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  const CUtensorMapSwizzle sw = span == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                                : span == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                             : CU_TENSOR_MAP_SWIZZLE_32B;
+  const CUresult r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, base, dims, strides, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? KVQ_OK : KVQ_ERR_CUDA;
+}
+
+kvq_status from_cuda(cudaError_t e) { return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA; }
+
+}  // namespace
+}  // namespace kvq
+
+using namespace kvq;
+
+extern "C" {
+
+KVQ_API const char* kvq_status_string(kvq_status s) {
+  switch (s) {
+    case KVQ_OK: return "ok";
+    case KVQ_ERR_INVALID_ARG: return "invalid argument";
+    case KVQ_ERR_UNSUPPORTED: return "unsupported shape or type";
+    case KVQ_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case KVQ_ERR_CUDA: return "CUDA error";
+    case KVQ_ERR_DEVICE_TIMEOUT: return "device wait timed out";
+  }
+  return "unknown status";
+}
+
+KVQ_API kvq_status kvq_append(const kvq_cache* cache, const void* k_new, const void* v_new,
+                              const int64_t* slot_mapping, int32_t n_tokens, kvq_stream_t stream) {
+  if (kvq_status s = check_cache(cache)) return s;
+  if (n_tokens < 0) return KVQ_ERR_INVALID_ARG;
+  if (n_tokens == 0) return KVQ_OK;
+  if (!k_new || !v_new || !slot_mapping) return KVQ_ERR_INVALID_ARG;
+  if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(slot_mapping, 8)) return KVQ_ERR_INVALID_ARG;
+  if ((long long)n_tokens * cache->num_kv_heads * 2 > (1LL << 31) - 1) return KVQ_ERR_INVALID_ARG;
+  DeviceInfo* dev;
+  if (kvq_status s = current_device(&dev)) return s;
+  AppendArgs a{};
+  a.k_new = static_cast<const uint16_t*>(k_new);
+  a.v_new = static_cast<const uint16_t*>(v_new);
+  a.slots = slot_mapping;
+  a.k_codes = static_cast<uint8_t*>(cache->k_codes);
+  a.v_codes = static_cast<uint8_t*>(cache->v_codes);
+  a.k_scale = cache->k_scale;
+  a.v_scale = cache->v_scale;
+  a.capacity = (long long)cache->num_blocks * cache->block_size;
+  a.n_tokens = n_tokens;
+  a.num_kv_heads = cache->num_kv_heads;
+  a.head_dim = cache->head_dim;
+  a.block_size = cache->block_size;
+  a.log2_bs = ilog2(cache->block_size);
+  a.dtype = cache->dtype;
+  a.k_mode = cache->k_mode;
+  a.v_mode = cache->v_mode;
+  a.err = dev->err;
+  return from_cuda(launch_append(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+KVQ_API kvq_status kvq_decode_workspace_size(const kvq_cache* cache, const kvq_decode_params* params,
+                                             size_t* workspace_bytes) {
+  if (kvq_status s = check_cache(cache)) return s;
+  if (kvq_status s = check_params(cache, params)) return s;
+  if (!workspace_bytes) return KVQ_ERR_INVALID_ARG;
+  DeviceInfo* dev;
+  if (kvq_status s = current_device(&dev)) return s;
+  Plan P;
+  if (kvq_status s = make_plan(cache, params, *dev, &P)) return s;
+  *workspace_bytes = P.ws_total;
+  return KVQ_OK;
+}
+
+KVQ_API kvq_status kvq_decode(const kvq_cache* cache, const kvq_decode_params* params, const void* q,
+                              const int32_t* block_table, const int32_t* seq_lens, void* workspace,
+                              size_t workspace_bytes, kvq_stream_t stream) {
+  if (kvq_status s = check_cache(cache)) return s;
+  if (kvq_status s = check_params(cache, params)) return s;
+  if (params->batch == 0) return KVQ_OK;
+  if (!q || !block_table || !seq_lens || !workspace) return KVQ_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(block_table, 4) || !aligned(seq_lens, 4) || !aligned(workspace, 256))
+    return KVQ_ERR_INVALID_ARG;
+  DeviceInfo* dev;
+  if (kvq_status s = current_device(&dev)) return s;
+  Plan P;
+  if (kvq_status s = make_plan(cache, params, *dev, &P)) return s;
+  if (workspace_bytes < P.ws_total) return KVQ_ERR_WORKSPACE_TOO_SMALL;
+
+  alignas(64) CUtensorMap tk, tv;
+  if (kvq_status s = encode_codes_map(cache, cache->k_codes, &tk)) return s;
+  if (kvq_status s = encode_codes_map(cache, cache->v_codes, &tv)) return s;
+
+  DecodeArgs a{};
+  a.q = static_cast<const uint16_t*>(q);
+  a.block_table = block_table;
+  a.seq_lens = seq_lens;
+  a.k_scale = cache->k_scale;
+  a.v_scale = cache->v_scale;
+  a.k_mode = cache->k_mode;
+  a.v_mode = cache->v_mode;
+  a.num_blocks = cache->num_blocks;
+  a.block_size = cache->block_size;
+  a.log2_bs = ilog2(cache->block_size);
+  a.num_kv_heads = cache->num_kv_heads;
+  a.batch = params->batch;
+  a.num_q_heads = params->num_q_heads;
+  a.q_tokens = params->q_tokens;
+  a.group = params->num_q_heads / cache->num_kv_heads;
+  a.rows = P.rows;
+  a.max_blocks_per_seq = params->max_blocks_per_seq;
+  a.max_seq_len = params->max_seq_len;
+  a.sm_scale = params->sm_scale > 0.0f ? params->sm_scale : 1.0f / std::sqrt((float)cache->head_dim);
+  a.softcap = params->softcap;
+  a.window = params->window;
+  a.row_groups = P.row_groups;
+  a.key_warps = P.key_warps;
+  a.stages = P.stages;
+  a.units_max = P.units_max;
+  char* ws = static_cast<char*>(workspace);
+  a.plan = reinterpret_cast<int*>(ws);
+  a.part_lse = reinterpret_cast<float*>(ws + P.ws_plan);
+  a.part_o = reinterpret_cast<float*>(ws + P.ws_plan + P.ws_lse);
+  a.err = dev->err;
+
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  switch (cache->dtype) {
+    case KVQ_INT8: e = launch_decode_int8(cache->head_dim, tk, tv, a, P.grid, P.threads, P.smem, st); break;
+    case KVQ_FP8_E4M3: e = launch_decode_fp8(cache->head_dim, tk, tv, a, P.grid, P.threads, P.smem, st); break;
+    default: e = launch_decode_int4(cache->head_dim, tk, tv, a, P.grid, P.threads, P.smem, st); break;
+  }
+  return from_cuda(e);
+}
+
+KVQ_API kvq_status kvq_combine(const kvq_cache* cache, const kvq_decode_params* params, const void* workspace,
+                               size_t workspace_bytes, const float* head_sink, void* out, float* lse_out,
+                               kvq_stream_t stream) {
+  if (kvq_status s = check_cache(cache)) return s;
+  if (kvq_status s = check_params(cache, params)) return s;
+  if (params->batch == 0) return KVQ_OK;
+  if (!workspace || !out) return KVQ_ERR_INVALID_ARG;
+  if (!aligned(workspace, 256) || !aligned(out, 16) || (lse_out && !aligned(lse_out, 4)) ||
+      (head_sink && !aligned(head_sink, 4)))
+    return KVQ_ERR_INVALID_ARG;
+  DeviceInfo* dev;
+  if (kvq_status s = current_device(&dev)) return s;
+  Plan P;
+  if (kvq_status s = make_plan(cache, params, *dev, &P)) return s;
+  if (workspace_bytes < P.ws_total) return KVQ_ERR_WORKSPACE_TOO_SMALL;
+  const char* ws = static_cast<const char*>(workspace);
+  CombineArgs a{};
+  a.plan = reinterpret_cast<const int*>(ws);
+  a.part_lse = reinterpret_cast<const float*>(ws + P.ws_plan);
+  a.part_o = reinterpret_cast<const float*>(ws + P.ws_plan + P.ws_lse);
+  a.head_sink = head_sink;
+  a.v_mode = cache->v_mode;
+  a.v_scale = cache->v_mode == KVQ_SCALE_PER_ROW ? nullptr : cache->v_scale;
+  a.out = static_cast<uint16_t*>(out);
+  a.lse_out = lse_out;
+  a.batch = params->batch;
+  a.q_tokens = params->q_tokens;
+  a.num_q_heads = params->num_q_heads;
+  a.num_kv_heads = cache->num_kv_heads;
+  a.group = params->num_q_heads / cache->num_kv_heads;
+  a.rows = P.rows;
+  a.head_dim = cache->head_dim;
+  return from_cuda(launch_combine(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+KVQ_API kvq_status kvq_get_device_error(uint32_t* flags, int32_t clear, kvq_stream_t stream) {
+  if (!flags) return KVQ_ERR_INVALID_ARG;
+  DeviceInfo* dev;
+  if (kvq_status s = current_device(&dev)) return s;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(st) != cudaSuccess) return KVQ_ERR_CUDA;
+  uint32_t v = 0;
+  if (cudaMemcpy(&v, dev->err, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess) return KVQ_ERR_CUDA;
+  if (clear && cudaMemset(dev->err, 0, sizeof v) != cudaSuccess) return KVQ_ERR_CUDA;
+  *flags = v;
+  return (v & KVQ_DEVERR_TIMEOUT) ? KVQ_ERR_DEVICE_TIMEOUT : KVQ_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,147 @@
+// append.cu -- quantize-on-write of new K/V rows into their paged-cache slots
+// (ReshapeAndCache in onnxruntime PR #29912; per-row absmax scales as in the
+// kv-quant-attn page, section "Method"; int4 two-per-byte packing as in
+// onnxruntime PR #32515).
+//
+// One warp per (token, kv head, side): each lane holds D/32 consecutive
+// channels, the row's absmax is a warp max-reduction (exact, order free), the
+// scale and every code use IEEE fp32 division (never a reciprocal multiply,
+// which overflows for subnormal scales), codes round half to even.
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+
+#include "kvq_internal.h"
+
+namespace kvq {
+namespace {
+
+template <int E>
+__device__ __forceinline__ void load_bf16(const uint16_t* p, float (&x)[E]) {
+  if constexpr (E == 8) {
+    uint4 v = *reinterpret_cast<const uint4*>(p);
+    uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      x[2 * i] = __uint_as_float(w[i] << 16);
+      x[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+  } else if constexpr (E == 4) {
+    uint2 v = *reinterpret_cast<const uint2*>(p);
+    x[0] = __uint_as_float(v.x << 16);
+    x[1] = __uint_as_float(v.x & 0xFFFF0000u);
+    x[2] = __uint_as_float(v.y << 16);
+    x[3] = __uint_as_float(v.y & 0xFFFF0000u);
+  } else {
+    uint32_t v = *reinterpret_cast<const uint32_t*>(p);
+    x[0] = __uint_as_float(v << 16);
+    x[1] = __uint_as_float(v & 0xFFFF0000u);
+  }
+}
+
+template <int NB>
+__device__ __forceinline__ void store_bytes(uint8_t* dst, const uint8_t (&b)[NB]) {
+  if constexpr (NB == 8) {
+    uint2 v;
+    v.x = b[0] | (b[1] << 8) | (b[2] << 16) | ((uint32_t)b[3] << 24);
+    v.y = b[4] | (b[5] << 8) | (b[6] << 16) | ((uint32_t)b[7] << 24);
+    *reinterpret_cast<uint2*>(dst) = v;
+  } else if constexpr (NB == 4) {
+    *reinterpret_cast<uint32_t*>(dst) = b[0] | (b[1] << 8) | (b[2] << 16) | ((uint32_t)b[3] << 24);
+  } else if constexpr (NB == 2) {
+    *reinterpret_cast<uint16_t*>(dst) = (uint16_t)(b[0] | (b[1] << 8));
+  } else {
+    dst[0] = b[0];
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(256) append_kernel(const AppendArgs a) {
+  constexpr int E = D / 32;  // channels per lane
+  const int wg = (int)((blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5);
+  const int lane = threadIdx.x & 31;
+  if (wg >= a.n_tokens * a.num_kv_heads * 2) return;
+  const int side = wg & 1;  // 0: K, 1: V
+  const int n = (wg >> 1) / a.num_kv_heads;
+  const int h = (wg >> 1) % a.num_kv_heads;
+  const long long slot = a.slots[n];
+  if (slot < 0) return;  // padding token
+  if (slot >= a.capacity) {
+    if (lane == 0) atomicOr(a.err, KVQ_DEVERR_SLOT);
+    return;
+  }
+  const long long blk = slot >> a.log2_bs;
+  const int row = (int)(slot & (a.block_size - 1));
+  const size_t ridx = ((size_t)blk * a.num_kv_heads + h) * a.block_size + row;
+
+  float x[E];
+  load_bf16<E>((side ? a.v_new : a.k_new) + ((size_t)n * a.num_kv_heads + h) * D + lane * E, x);
+
+  const int mode = side ? a.v_mode : a.k_mode;
+  float* sc = side ? a.v_scale : a.k_scale;
+  const float qmax = a.dtype == KVQ_INT8 ? 127.0f : (a.dtype == KVQ_INT4 ? 7.0f : 448.0f);
+  float s[E];
+  if (mode == KVQ_SCALE_PER_ROW) {
+    float amax = 0.0f;
+#pragma unroll
+    for (int e = 0; e < E; ++e) amax = fmaxf(amax, fabsf(x[e]));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    const float rs = __fdiv_rn(amax, qmax);
+#pragma unroll
+    for (int e = 0; e < E; ++e) s[e] = rs;
+    if (lane == 0) sc[ridx] = rs;
+  } else if (mode == KVQ_SCALE_PER_TENSOR) {
+    const float t = sc[0];
+#pragma unroll
+    for (int e = 0; e < E; ++e) s[e] = t;
+  } else {
+#pragma unroll
+    for (int e = 0; e < E; ++e) s[e] = sc[(size_t)h * D + lane * E + e];
+  }
+
+  uint8_t* codes = side ? a.v_codes : a.k_codes;
+  if (a.dtype == KVQ_INT4) {
+    uint8_t b[E / 2];
+#pragma unroll
+    for (int j = 0; j < E / 2; ++j) {
+      int c[2];
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int e = 2 * j + u;
+        c[u] = 0;
+        if (s[e] != 0.0f) c[u] = min(7, max(-7, __float2int_rn(__fdiv_rn(x[e], s[e]))));
+      }
+      b[j] = (uint8_t)((c[0] & 0xF) | ((c[1] & 0xF) << 4));
+    }
+    store_bytes<E / 2>(codes + ridx * (D / 2) + lane * (E / 2), b);
+  } else {
+    uint8_t b[E];
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      if (s[e] == 0.0f) {
+        b[e] = 0;
+      } else if (a.dtype == KVQ_INT8) {
+        b[e] = (uint8_t)(int8_t)min(127, max(-127, __float2int_rn(__fdiv_rn(x[e], s[e]))));
+      } else {
+        b[e] = (uint8_t)__nv_cvt_float_to_fp8(__fdiv_rn(x[e], s[e]), __NV_SATFINITE, __NV_E4M3);
+      }
+    }
+    store_bytes<E>(codes + ridx * D + lane * E, b);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_append(const AppendArgs& a, cudaStream_t stream) {
+  const long long warps = (long long)a.n_tokens * a.num_kv_heads * 2;
+  const unsigned blocks = (unsigned)((warps + 7) / 8);
+  switch (a.head_dim) {
+    case 64: append_kernel<64><<<blocks, 256, 0, stream>>>(a); break;
+    case 128: append_kernel<128><<<blocks, 256, 0, stream>>>(a); break;
+    case 256: append_kernel<256><<<blocks, 256, 0, stream>>>(a); break;
+    default: return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace kvq

@@ -1,0 +1,666 @@
+// decode.cuh -- split-KV flash-decoding over a quantized paged KV cache.
+//
+// What it computes (one query row = (b, draft t, query head i), kv head
+// h = i / G): logits s_j = sm_scale * <q, dequant(k_j)> for the keys the row
+// sees, optional softcap, softmax, o = sum_j p_j dequant(v_j) / sum_j p_j.
+// Sources: PagedAttention paged decode (onnxruntime PR #29912, Summary of
+// Changes: split-KV, block-table aware, softcap, sliding window, on-the-fly
+// dequantization); kv-quant-attn page, section "Method" (one block owns a
+// (batch, kv head) pair and resolves every query head of the GQA group from
+// one read; warps keep private (max, sumexp, accumulator) state with no
+// barrier or atomic in the loop; partials merged in a fixed order); per-channel
+// K scale folded into Q with a power-of-two normaliser (onnxruntime PR #32515,
+// Description: the fold is exact, the normaliser keeps |q*s| <= |q|).
+//
+// Structure (one persistent CTA per SM slot):
+//  * every CTA builds the same split plan from seq_lens in shared memory:
+//    each sequence's key range is cut into chunks of `chunk` keys (a multiple
+//    of the 64-key tile) so that about gridDim.x * kWaves work units exist; a
+//    unit is (sequence, chunk, kv head) and CTA x takes units x, x+grid, ...
+//  * one producer warp streams each unit's pages through a ring of shared
+//    memory stages: TMA tensor copies (cp.async.bulk.tensor, 128/64/32-byte
+//    swizzle) of the K and V code rows, the block id taken from the block
+//    table as the copy's outer coordinate, plus 1-D bulk copies of per-row
+//    scales; completion is counted on an mbarrier per stage;
+//  * consumer warps (key warps x row groups of 8 query rows) take 16-key
+//    sub-tiles: QK^T on tensor cores with keys as MMA-M and query rows as
+//    MMA-N (ldmatrix of the codes, exact in-register code->f16 conversion),
+//    online softmax in fp32, P moved into the PV operand layout with
+//    movmatrix, PV with channels as MMA-M (ldmatrix.trans of the V codes);
+//  * at the end of a unit the key warps of a row group merge their states
+//    in fixed warp order through shared memory and write the unit's partial
+//    (base-2 log-sum-exp, normalized output) to the workspace.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "kvq_internal.h"
+#include "ptx.cuh"
+
+namespace kvq {
+
+constexpr int round_up_c(int x, int m) { return (x + m - 1) / m * m; }
+
+template <int DT, int D>
+struct Geo {
+  static constexpr int DP = DT == KVQ_INT4 ? D / 2 : D;  // bytes per cached row
+  static constexpr int SPAN = DP >= 128 ? 128 : DP;      // TMA box inner bytes = swizzle span
+  static constexpr int SLABS = DP / SPAN;                // column slabs per row
+  static constexpr int NCH = DP / 16;                    // 16-byte chunks per row
+  static constexpr int NMT = D / 16;                     // 16-channel MMA tiles
+  static constexpr int CODE_BYTES = kTile * DP;          // one side of one stage
+  static constexpr int STAGE_STRIDE = round_up_c(2 * CODE_BYTES + 2 * kTile * 4, 1024);
+};
+
+namespace dev {
+
+// byte offset o inside a slab of SPAN-byte rows -> swizzled offset written by
+// the TMA unit (16-byte granule index XOR row-group bits 7.., period 8 rows).
+template <int SPAN>
+__device__ __forceinline__ uint32_t swz(uint32_t o) {
+  return o ^ (((o >> 7) & (SPAN / 16 - 1)) << 4);
+}
+
+// Smallest e with 2^e >= x for finite x > 0 (read off the IEEE fields).
+__device__ __forceinline__ int ceil_log2(float x) {
+  const uint32_t u = __float_as_uint(x);
+  int e = (int)((u >> 23) & 0xFFu) - 127;
+  if (u & 0x7FFFFFu) e += 1;
+  return e;
+}
+
+// 2^e for e in [-126, 127], exact.
+__device__ __forceinline__ float pow2i(int e) { return __uint_as_float((uint32_t)(e + 127) << 23); }
+
+__device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
+  const __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// Exact code -> f16 conversions producing MMA operand pairs (low half first).
+// int8: bytes i, j of x = w ^ 0x80808080 placed under exponent byte 0x64
+// (1024 + code + 128), minus 1152.
+__device__ __forceinline__ uint32_t i8pair(uint32_t x, uint32_t sel) {
+  return ptx::hsub2_u32(ptx::prmt(x, 0x64646464u, sel), 0x64806480u);
+}
+// int4: nibbles n, n+4 of x = w ^ 0x88888888 (shift = 4n) as 1024 + code + 8,
+// minus 1032.
+__device__ __forceinline__ uint32_t i4pair(uint32_t x, int shift) {
+  return ptx::hsub2_u32(((x >> shift) & 0x000F000Fu) | 0x64006400u, 0x64086408u);
+}
+// e4m3: byte b = s.eeee.mmm moved to bits 15..8 of a half, then sign kept
+// and eeee.mmm shifted right by one: exactly the f16 value b * 2^-8
+// (subnormals included; the 2^8 is applied to the logit / output scale).
+__device__ __forceinline__ uint32_t f8pair(uint32_t w, uint32_t sel) {
+  const uint32_t y = ptx::prmt(w, 0u, sel);
+  return (y & 0x80008000u) | ((y >> 1) & 0x3F803F80u);
+}
+
+// Output channel held by accumulator element e of channel tile mt in lane
+// group g (the PV operand permutation chosen for the ldmatrix.trans layout).
+template <int DT>
+__device__ __forceinline__ int out_channel(int mt, int e, int g) {
+  if constexpr (DT == KVQ_INT4)
+    return 32 * (mt >> 1) + 4 * g + 2 * (mt & 1) + (e >> 1);
+  else
+    return 16 * mt + 2 * g + (e >> 1);
+}
+
+}  // namespace dev
+
+template <int DT, int D, int MINB>
+__global__ void __launch_bounds__(288, MINB)
+    decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
+                  const DecodeArgs a) {
+  using Gm = Geo<DT, D>;
+  constexpr float kLog2e = 1.4426950408889634f;
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  const uint32_t pad = (1024u - (ptx::smem_u32(smem_raw) & 1023u)) & 1023u;
+  uint8_t* ring = smem_raw + pad;
+
+  const int n_cw = a.row_groups * a.key_warps;
+  float* scr_acc = reinterpret_cast<float*>(ring + (size_t)a.stages * Gm::STAGE_STRIDE);
+  float* scr_ml = scr_acc + (size_t)n_cw * 8 * D;
+  int* pl_lo = reinterpret_cast<int*>(scr_ml + n_cw * 16);
+  int* pl_hi = pl_lo + a.batch;
+  int* pl_pre = pl_hi + a.batch;      // [B + 1]
+  int* pl_misc = pl_pre + a.batch + 1;  // [4]
+  uint64_t* bar_full = reinterpret_cast<uint64_t*>(pl_misc + 4 + ((a.batch * 3 + 5) & 1));
+  uint64_t* bar_empty = bar_full + a.stages;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int B = a.batch, T = a.q_tokens, Hkv = a.num_kv_heads;
+
+  if (tid == 0) {
+    for (int s = 0; s < a.stages; ++s) {
+      ptx::mbar_init(&bar_full[s], 1);
+      ptx::mbar_init(&bar_empty[s], (uint32_t)n_cw);
+    }
+    ptx::fence_mbar_init();
+  }
+
+  // ---------------------------------------------------------------- plan
+  {
+    const int cap = a.max_blocks_per_seq * a.block_size;
+    const int lim = (a.max_seq_len > 0 && a.max_seq_len < cap) ? a.max_seq_len : cap;
+    for (int b = tid; b < B; b += blockDim.x) {
+      int L = a.seq_lens[b];
+      if (L < 0 || L > lim) {
+        if (blockIdx.x == 0) atomicOr(a.err, KVQ_DEVERR_SEQ_LEN);
+        L = L < 0 ? 0 : lim;
+      }
+      int lo = 0;
+      if (a.window > 0) lo = max(0, L - T - a.window + 1);
+      lo &= ~(kTile - 1);
+      pl_lo[b] = lo;
+      pl_hi[b] = L;
+      pl_pre[b] = max(0, L - lo);  // length for now
+    }
+  }
+  __syncthreads();
+  if (warp == 0) {
+    const int seg = (B + 31) / 32;
+    const int s0 = min(B, lane * seg), s1 = min(B, s0 + seg);
+    long long tot = 0;
+    for (int b = s0; b < s1; ++b) tot += pl_pre[b];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
+    const long long target = (long long)gridDim.x * kWaves;
+    long long ch = (tot * Hkv + target - 1) / target;
+    ch = (ch + kTile - 1) / kTile * kTile;
+    const int chunk = (int)max((long long)kTile, min(ch, (long long)(1 << 30)));
+    int cnt = 0;
+    for (int b = s0; b < s1; ++b) cnt += (pl_pre[b] + chunk - 1) / chunk;
+    int incl = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    int run = incl - cnt;
+    for (int b = s0; b < s1; ++b) {
+      const int len = pl_pre[b];
+      pl_pre[b] = run;
+      run += (len + chunk - 1) / chunk;
+    }
+    if (lane == 31) {
+      int items = incl;
+      if ((long long)items * Hkv > a.units_max) {  // unreachable by construction of `chunk`
+        atomicOr(a.err, KVQ_DEVERR_PLAN);
+        items = a.units_max / Hkv;
+      }
+      pl_pre[B] = incl;
+      pl_misc[0] = chunk;
+      pl_misc[1] = items;
+    }
+  }
+  __syncthreads();
+  const int chunk = pl_misc[0];
+  const int total_units = pl_misc[1] * Hkv;
+  if (blockIdx.x == 0) {
+    for (int i = tid; i <= B; i += blockDim.x) a.plan[4 + i] = min(pl_pre[i], pl_misc[1]);
+    if (tid == 0) {
+      a.plan[0] = chunk;
+      a.plan[1] = pl_misc[1];
+      a.plan[2] = B;
+      a.plan[3] = a.units_max;
+    }
+  }
+
+  // unit -> (b, h, key range)
+  auto unit_info = [&](int u, int& b, int& h, int& k0, int& k1, int& L) {
+    const int item = u / Hkv;
+    h = u - item * Hkv;
+    int lo = 0, hi = B - 1;  // last b with pre[b] <= item
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (pl_pre[mid] <= item) lo = mid; else hi = mid - 1;
+    }
+    b = lo;
+    L = pl_hi[b];
+    k0 = pl_lo[b] + (item - pl_pre[b]) * chunk;
+    k1 = min(k0 + chunk, L);
+  };
+
+  const bool k_row = a.k_mode == KVQ_SCALE_PER_ROW, v_row = a.v_mode == KVQ_SCALE_PER_ROW;
+
+  // =============================================================== producer
+  if (warp == n_cw) {
+    if (lane != 0) return;
+    const int seg_rows = min(a.block_size, kTile);
+    const int n_seg = kTile / seg_rows;
+    uint32_t it = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < total_units; u += gridDim.x) {
+      int b, h, k0, k1, L;
+      unit_info(u, b, h, k0, k1, L);
+      const int32_t* bt = a.block_table + (size_t)b * a.max_blocks_per_seq;
+      for (int key0 = k0; key0 < k1; key0 += kTile, ++it) {
+        const int stage = (int)(it % (uint32_t)a.stages);
+        if (it >= (uint32_t)a.stages && ok) {
+          ok = ptx::mbar_wait_bounded(&bar_empty[stage], ((it / a.stages) - 1) & 1);
+          if (!ok) atomicOr(a.err, KVQ_DEVERR_TIMEOUT);
+        }
+        if (!ok) {
+          ptx::mbar_arrive(&bar_full[stage]);
+          continue;
+        }
+        int blk[kTile / 16];
+        uint32_t bytes = 0;
+        for (int s = 0; s < n_seg; ++s) {
+          blk[s] = -1;
+          const int skey = key0 + s * seg_rows;
+          if (skey >= k1) continue;
+          const int id = bt[skey >> a.log2_bs];
+          if (id < 0 || id >= a.num_blocks) {
+            atomicOr(a.err, KVQ_DEVERR_BLOCK_ID);
+            continue;
+          }
+          blk[s] = id;
+          bytes += (uint32_t)seg_rows * (2 * Gm::DP + (k_row ? 4 : 0) + (v_row ? 4 : 0));
+        }
+        uint8_t* st = ring + (size_t)stage * Gm::STAGE_STRIDE;
+        ptx::mbar_arrive_expect_tx(&bar_full[stage], bytes);
+        for (int s = 0; s < n_seg; ++s) {
+          if (blk[s] < 0) continue;
+          const int row0 = (key0 + s * seg_rows) & (a.block_size - 1);
+#pragma unroll
+          for (int sl = 0; sl < Gm::SLABS; ++sl) {
+            uint8_t* dk = st + sl * (kTile * Gm::SPAN) + s * seg_rows * Gm::SPAN;
+            ptx::tma_load_4d(dk, &tmk, sl * Gm::SPAN, row0, h, blk[s], &bar_full[stage]);
+            ptx::tma_load_4d(dk + Gm::CODE_BYTES, &tmv, sl * Gm::SPAN, row0, h, blk[s], &bar_full[stage]);
+          }
+          const size_t srow = ((size_t)blk[s] * Hkv + h) * a.block_size + row0;
+          if (k_row)
+            ptx::bulk_load(st + 2 * Gm::CODE_BYTES + s * seg_rows * 4, a.k_scale + srow, seg_rows * 4,
+                           &bar_full[stage]);
+          if (v_row)
+            ptx::bulk_load(st + 2 * Gm::CODE_BYTES + kTile * 4 + s * seg_rows * 4, a.v_scale + srow,
+                           seg_rows * 4, &bar_full[stage]);
+        }
+      }
+    }
+    // let every copy this thread issued land before the CTA can exit
+    const uint32_t S = (uint32_t)a.stages;
+    for (uint32_t s = 0; s < S && s < it; ++s) {
+      const uint32_t last = it - 1 - ((it - 1 - s) % S);
+      if (!ptx::mbar_wait_bounded(&bar_full[s], (last / S) & 1)) atomicOr(a.err, KVQ_DEVERR_TIMEOUT);
+    }
+    return;
+  }
+
+  // =============================================================== consumers
+  const int cw = warp;
+  const int rg = cw % a.row_groups, kw = cw / a.row_groups;
+  const int g = lane >> 2, c = lane & 3;
+  const int G = a.group, Hq = a.num_q_heads;
+  const float softcap = a.softcap;
+  const float inv_cap = softcap > 0.0f ? 1.0f / softcap : 0.0f;
+  // ldmatrix row address of this lane: matrix (lane >> 3) covers keys
+  // 0-7 / 8-15 of the sub-tile and the even / odd 16-byte chunk of a pair
+  const int ld_key = ((lane >> 3) & 1) * 8 + (lane & 7);
+  const int ld_chunk = lane >> 4;
+  uint32_t it = 0;
+  bool ok = true;
+
+  for (int u = blockIdx.x; u < total_units; u += gridDim.x) {
+    int b, h, k0, k1, L;
+    unit_info(u, b, h, k0, k1, L);
+
+    // ---- Q prologue: this lane's channels of query row g of the row group
+    constexpr int CPL = (DT == KVQ_INT4) ? 8 : 4;  // channels per 16-byte code chunk per lane
+    constexpr int NQC = D / (4 * CPL);             // code chunks per row
+    uint32_t qf[Gm::NMT][2];
+    float alpha_g;
+    {
+      const int rq = rg * 8 + g;
+      const bool qvalid = rq < a.rows;
+      const int tq = qvalid ? rq / G : 0, gq = qvalid ? rq % G : 0;
+      const uint16_t* qp = a.q + (((size_t)b * T + tq) * Hq + (size_t)h * G + gq) * D;
+      float qv[NQC][CPL];
+#pragma unroll
+      for (int j = 0; j < NQC; ++j) {
+        const int ch0 = j * 4 * CPL + c * CPL;
+        if constexpr (CPL == 8) {
+          const uint4 w = qvalid ? *reinterpret_cast<const uint4*>(qp + ch0) : make_uint4(0, 0, 0, 0);
+          const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            qv[j][2 * i] = __uint_as_float(ww[i] << 16);
+            qv[j][2 * i + 1] = __uint_as_float(ww[i] & 0xFFFF0000u);
+          }
+        } else {
+          const uint2 w = qvalid ? *reinterpret_cast<const uint2*>(qp + ch0) : make_uint2(0, 0);
+          qv[j][0] = __uint_as_float(w.x << 16);
+          qv[j][1] = __uint_as_float(w.x & 0xFFFF0000u);
+          qv[j][2] = __uint_as_float(w.y << 16);
+          qv[j][3] = __uint_as_float(w.y & 0xFFFF0000u);
+        }
+      }
+      int e_tot = 0;
+      if (a.k_mode == KVQ_SCALE_PER_CHANNEL) {
+        // fold the K channel scale into q, normalised by the power of two
+        // just above max|k_scale| so the product cannot overflow
+        const float* ks = a.k_scale + (size_t)h * D;
+        float km = 0.0f;
+#pragma unroll
+        for (int j = 0; j < NQC; ++j)
+#pragma unroll
+          for (int i = 0; i < CPL; ++i) km = fmaxf(km, fabsf(ks[j * 4 * CPL + c * CPL + i]));
+        km = fmaxf(km, __shfl_xor_sync(0xffffffffu, km, 1));
+        km = fmaxf(km, __shfl_xor_sync(0xffffffffu, km, 2));
+        const int ek = km > 0.0f ? min(126, max(-126, dev::ceil_log2(km))) : 0;
+        const float sk = dev::pow2i(-ek);
+#pragma unroll
+        for (int j = 0; j < NQC; ++j)
+#pragma unroll
+          for (int i = 0; i < CPL; ++i) qv[j][i] *= ks[j * 4 * CPL + c * CPL + i] * sk;
+        e_tot += ek;
+      }
+      float qm = 0.0f;
+#pragma unroll
+      for (int j = 0; j < NQC; ++j)
+#pragma unroll
+        for (int i = 0; i < CPL; ++i) qm = fmaxf(qm, fabsf(qv[j][i]));
+      qm = fmaxf(qm, __shfl_xor_sync(0xffffffffu, qm, 1));
+      qm = fmaxf(qm, __shfl_xor_sync(0xffffffffu, qm, 2));
+      const int eq = qm > 0.0f ? min(126, max(-126, dev::ceil_log2(qm))) : 0;
+      const float sq = dev::pow2i(-eq);
+      e_tot += eq;
+#pragma unroll
+      for (int j = 0; j < NQC; ++j) {
+        if constexpr (DT == KVQ_INT4) {
+#pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            qf[2 * j + t][0] = dev::pack_h2(qv[j][2 * t] * sq, qv[j][2 * t + 4] * sq);
+            qf[2 * j + t][1] = dev::pack_h2(qv[j][2 * t + 1] * sq, qv[j][2 * t + 5] * sq);
+          }
+        } else {
+          qf[j][0] = dev::pack_h2(qv[j][0] * sq, qv[j][1] * sq);
+          qf[j][1] = dev::pack_h2(qv[j][2] * sq, qv[j][3] * sq);
+        }
+      }
+      float base = a.sm_scale;
+      if (a.k_mode == KVQ_SCALE_PER_TENSOR) base *= a.k_scale[0];
+      if constexpr (DT == KVQ_FP8_E4M3) base *= 256.0f;
+      alpha_g = ldexpf(base, e_tot);
+      if (softcap <= 0.0f) alpha_g *= kLog2e;
+      // a scale beyond fp32 (e.g. a channel scale near FLT_MAX) stays finite,
+      // so an all-zero code row still gives a zero logit instead of inf * 0
+      alpha_g = fminf(alpha_g, 3.4028234e38f);
+    }
+    const int r0 = rg * 8 + 2 * c, r1 = r0 + 1;
+    const float al0 = __shfl_sync(0xffffffffu, alpha_g, (2 * c) * 4);
+    const float al1 = __shfl_sync(0xffffffffu, alpha_g, (2 * c + 1) * 4);
+    const int pos0 = r0 < a.rows ? L - T + r0 / G : -1;
+    const int pos1 = r1 < a.rows ? L - T + r1 / G : -1;
+    const int W = a.window;
+
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.0f, l1 = 0.0f;
+    int F = v_row ? -126 : 0;  // V-scale normaliser exponent (warp uniform)
+    float acc[Gm::NMT][4];
+#pragma unroll
+    for (int mt = 0; mt < Gm::NMT; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.0f;
+
+    for (int key0 = k0; key0 < k1; key0 += kTile, ++it) {
+      const int stage = (int)(it % (uint32_t)a.stages);
+      if (ok) {
+        ok = ptx::mbar_wait_bounded(&bar_full[stage], (it / a.stages) & 1);
+        if (!ok) atomicOr(a.err, KVQ_DEVERR_TIMEOUT);
+      }
+      const uint8_t* st = ring + (size_t)stage * Gm::STAGE_STRIDE;
+      const uint32_t sk_base = ptx::smem_u32(st);
+      const uint32_t sv_base = sk_base + Gm::CODE_BYTES;
+      const float* ks_row = reinterpret_cast<const float*>(st + 2 * Gm::CODE_BYTES);
+      const float* vs_row = ks_row + kTile;
+      for (int sub = kw; ok && sub < kTile / kSub; sub += a.key_warps) {
+        const int kb = key0 + sub * kSub;
+        if (kb >= k1) break;
+        const uint32_t row_off = (uint32_t)(sub * kSub + ld_key) * Gm::SPAN;
+
+        // ---- S = K Q^T for 16 keys x 8 rows (keys are MMA-M)
+        float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int kk = 0; kk < Gm::NCH / 2; ++kk) {
+          const uint32_t byte = (uint32_t)(2 * kk + ld_chunk) * 16;
+          const uint32_t addr =
+              sk_base + (byte / Gm::SPAN) * (kTile * Gm::SPAN) + dev::swz<Gm::SPAN>(row_off + byte % Gm::SPAN);
+          uint32_t R[4];
+          ptx::ldmatrix_x4(R, addr);
+#pragma unroll
+          for (int h2 = 0; h2 < 2; ++h2) {
+            const int j = 2 * kk + h2;
+            const uint32_t wl = R[2 * h2], wh = R[2 * h2 + 1];
+            if constexpr (DT == KVQ_INT4) {
+              const uint32_t xl = wl ^ 0x88888888u, xh = wh ^ 0x88888888u;
+#pragma unroll
+              for (int t = 0; t < 2; ++t) {
+                const uint32_t A[4] = {dev::i4pair(xl, 8 * t), dev::i4pair(xh, 8 * t), dev::i4pair(xl, 8 * t + 4),
+                                       dev::i4pair(xh, 8 * t + 4)};
+                if (t == 0)
+                  ptx::mma_16816(sa, A, qf[2 * j + t][0], qf[2 * j + t][1]);
+                else
+                  ptx::mma_16816(sb, A, qf[2 * j + t][0], qf[2 * j + t][1]);
+              }
+            } else {
+              uint32_t A[4];
+              if constexpr (DT == KVQ_INT8) {
+                const uint32_t xl = wl ^ 0x80808080u, xh = wh ^ 0x80808080u;
+                A[0] = dev::i8pair(xl, 0x4140u);
+                A[1] = dev::i8pair(xh, 0x4140u);
+                A[2] = dev::i8pair(xl, 0x4342u);
+                A[3] = dev::i8pair(xh, 0x4342u);
+              } else {
+                A[0] = dev::f8pair(wl, 0x1404u);
+                A[1] = dev::f8pair(wh, 0x1404u);
+                A[2] = dev::f8pair(wl, 0x3424u);
+                A[3] = dev::f8pair(wh, 0x3424u);
+              }
+              if (h2 == 0)
+                ptx::mma_16816(sa, A, qf[j][0], qf[j][1]);
+              else
+                ptx::mma_16816(sb, A, qf[j][0], qf[j][1]);
+            }
+          }
+        }
+
+        // ---- logits: element e -> key kb + g (+8 for e >= 2), row 2c (+1 for odd e)
+        const int key_a = kb + g, key_b = key_a + 8;
+        float ksa = 1.0f, ksb = 1.0f;
+        if (k_row) {
+          ksa = ks_row[sub * kSub + g];
+          ksb = ks_row[sub * kSub + g + 8];
+        }
+        float x[4] = {(sa[0] + sb[0]) * al0 * ksa, (sa[1] + sb[1]) * al1 * ksa, (sa[2] + sb[2]) * al0 * ksb,
+                      (sa[3] + sb[3]) * al1 * ksb};
+        if (softcap > 0.0f) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) x[e] = softcap * tanhf(x[e] * inv_cap) * kLog2e;
+        }
+        const bool va0 = key_a <= pos0 && (W == 0 || key_a > pos0 - W);
+        const bool va1 = key_a <= pos1 && (W == 0 || key_a > pos1 - W);
+        const bool vb0 = key_b <= pos0 && (W == 0 || key_b > pos0 - W);
+        const bool vb1 = key_b <= pos1 && (W == 0 || key_b > pos1 - W);
+        x[0] = va0 ? x[0] : -INFINITY;
+        x[1] = va1 ? x[1] : -INFINITY;
+        x[2] = vb0 ? x[2] : -INFINITY;
+        x[3] = vb1 ? x[3] : -INFINITY;
+
+        // ---- online softmax (rows 2c, 2c+1; reduce over the 8 key lanes)
+        float t0 = fmaxf(x[0], x[2]), t1 = fmaxf(x[1], x[3]);
+#pragma unroll
+        for (int o = 4; o < 32; o <<= 1) {
+          t0 = fmaxf(t0, __shfl_xor_sync(0xffffffffu, t0, o));
+          t1 = fmaxf(t1, __shfl_xor_sync(0xffffffffu, t1, o));
+        }
+        const float mn0 = fmaxf(m0, t0), mn1 = fmaxf(m1, t1);
+        const float mu0 = mn0 == -INFINITY ? 0.0f : mn0;
+        const float mu1 = mn1 == -INFINITY ? 0.0f : mn1;
+        const float c0 = ptx::fast_exp2(m0 - mu0), c1 = ptx::fast_exp2(m1 - mu1);
+        m0 = mn0;
+        m1 = mn1;
+        const float p0 = ptx::fast_exp2(x[0] - mu0), p1 = ptx::fast_exp2(x[1] - mu1);
+        const float p2 = ptx::fast_exp2(x[2] - mu0), p3 = ptx::fast_exp2(x[3] - mu1);
+        l0 = l0 * c0 + p0 + p2;
+        l1 = l1 * c1 + p1 + p3;
+
+        // ---- per-row V scales enter P, normalised by 2^F >= their maximum
+        float vsa = 1.0f, vsb = 1.0f, fs = 1.0f;
+        if (v_row) {
+          const float ua = key_a < L ? vs_row[sub * kSub + g] : 0.0f;
+          const float ub = key_b < L ? vs_row[sub * kSub + g + 8] : 0.0f;
+          float vm = fmaxf(ua, ub);
+#pragma unroll
+          for (int o = 4; o < 32; o <<= 1) vm = fmaxf(vm, __shfl_xor_sync(0xffffffffu, vm, o));
+          if (vm > 0.0f) {
+            const int fn = min(126, max(-126, dev::ceil_log2(vm)));
+            if (fn > F) {
+              fs = (F - fn < -126) ? 0.0f : dev::pow2i(F - fn);
+              F = fn;
+            }
+          }
+          const float inv = dev::pow2i(-F);
+          vsa = ua * inv;
+          vsb = ub * inv;
+        }
+        const float rs0 = c0 * fs, rs1 = c1 * fs;
+        if (!__all_sync(0xffffffffu, rs0 == 1.0f && rs1 == 1.0f)) {
+#pragma unroll
+          for (int mt = 0; mt < Gm::NMT; ++mt) {
+            acc[mt][0] *= rs0;
+            acc[mt][1] *= rs1;
+            acc[mt][2] *= rs0;
+            acc[mt][3] *= rs1;
+          }
+        }
+        // P (keys x rows) -> PV operand (rows x keys) by an 8x8 transpose
+        const uint32_t pb0 = ptx::movmatrix_trans(dev::pack_h2(p0 * vsa, p1 * vsa));
+        const uint32_t pb1 = ptx::movmatrix_trans(dev::pack_h2(p2 * vsb, p3 * vsb));
+
+        // ---- O += V^T P^T for all channels (channels are MMA-M)
+#pragma unroll
+        for (int jj = 0; jj < Gm::NCH / 2; ++jj) {
+          const uint32_t byte = (uint32_t)(2 * jj + ld_chunk) * 16;
+          const uint32_t addr =
+              sv_base + (byte / Gm::SPAN) * (kTile * Gm::SPAN) + dev::swz<Gm::SPAN>(row_off + byte % Gm::SPAN);
+          uint32_t R[4];
+          ptx::ldmatrix_x4_trans(R, addr);
+#pragma unroll
+          for (int h2 = 0; h2 < 2; ++h2) {
+            const int j = 2 * jj + h2;
+            const uint32_t wl = R[2 * h2], wh = R[2 * h2 + 1];
+            if constexpr (DT == KVQ_INT4) {
+              const uint32_t xl = wl ^ 0x88888888u, xh = wh ^ 0x88888888u;
+#pragma unroll
+              for (int t = 0; t < 2; ++t) {
+                const uint32_t A[4] = {dev::i4pair(xl, 8 * t), dev::i4pair(xl, 8 * t + 4), dev::i4pair(xh, 8 * t),
+                                       dev::i4pair(xh, 8 * t + 4)};
+                ptx::mma_16816(acc[2 * j + t], A, pb0, pb1);
+              }
+            } else {
+              uint32_t A[4];
+              if constexpr (DT == KVQ_INT8) {
+                const uint32_t xl = wl ^ 0x80808080u, xh = wh ^ 0x80808080u;
+                A[0] = dev::i8pair(xl, 0x4240u);
+                A[1] = dev::i8pair(xl, 0x4341u);
+                A[2] = dev::i8pair(xh, 0x4240u);
+                A[3] = dev::i8pair(xh, 0x4341u);
+              } else {
+                A[0] = dev::f8pair(wl, 0x2404u);
+                A[1] = dev::f8pair(wl, 0x3414u);
+                A[2] = dev::f8pair(wh, 0x2404u);
+                A[3] = dev::f8pair(wh, 0x3414u);
+              }
+              ptx::mma_16816(acc[j], A, pb0, pb1);
+            }
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&bar_empty[stage]);
+    }
+
+    // ---- unit end: warp state -> shared scratch -> fixed-order merge
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) {
+      l0 += __shfl_xor_sync(0xffffffffu, l0, o);
+      l1 += __shfl_xor_sync(0xffffffffu, l1, o);
+    }
+    {
+      float fac = v_row ? dev::pow2i(F) : 1.0f;
+      if constexpr (DT == KVQ_FP8_E4M3) fac *= 256.0f;
+      float* sa_w = scr_acc + (size_t)cw * 8 * D;
+#pragma unroll
+      for (int mt = 0; mt < Gm::NMT; ++mt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          sa_w[(2 * c + (e & 1)) * D + dev::out_channel<DT>(mt, e, g)] = acc[mt][e] * fac;
+      if (g == 0) {
+        scr_ml[cw * 16 + (2 * c) * 2] = m0;
+        scr_ml[cw * 16 + (2 * c) * 2 + 1] = l0;
+        scr_ml[cw * 16 + (2 * c + 1) * 2] = m1;
+        scr_ml[cw * 16 + (2 * c + 1) * 2 + 1] = l1;
+      }
+    }
+    ptx::named_bar_sync(1, (uint32_t)n_cw * 32);
+    {
+      const int RG = a.row_groups, KW = a.key_warps;
+      const int nthr = n_cw * 32;
+      for (int e = cw * 32 + lane; e < RG * 8 * D; e += nthr) {
+        const int rgi = e / (8 * D), row = (e / D) & 7, ch = e % D;
+        const int rr = rgi * 8 + row;
+        if (rr >= a.rows) continue;
+        float M = -INFINITY;
+        for (int k = 0; k < KW; ++k) M = fmaxf(M, scr_ml[(k * RG + rgi) * 16 + row * 2]);
+        float lt = 0.0f, o = 0.0f;
+        if (M != -INFINITY) {
+          for (int k = 0; k < KW; ++k) {
+            const int w = k * RG + rgi;
+            const float f = ptx::fast_exp2(scr_ml[w * 16 + row * 2] - M);
+            lt += scr_ml[w * 16 + row * 2 + 1] * f;
+            o += scr_acc[((size_t)w * 8 + row) * D + ch] * f;
+          }
+        }
+        const size_t pu = (size_t)u * a.rows + rr;
+        a.part_o[pu * D + ch] = lt > 0.0f ? o / lt : 0.0f;
+        if (ch == 0) a.part_lse[pu] = lt > 0.0f ? M + ptx::fast_log2(lt) : -INFINITY;
+      }
+    }
+    ptx::named_bar_sync(1, (uint32_t)n_cw * 32);
+  }
+}
+
+template <int DT>
+cudaError_t launch_decode_t(int head_dim, const CUtensorMap& tk, const CUtensorMap& tv, const DecodeArgs& a,
+                            int grid, int threads, size_t smem, cudaStream_t stream) {
+  auto go = [&](auto kernel) -> cudaError_t {
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    kernel<<<grid, threads, smem, stream>>>(tk, tv, a);
+    return cudaGetLastError();
+  };
+  switch (head_dim) {
+    case 64: return go(decode_kernel<DT, 64, 2>);
+    case 128: return go(decode_kernel<DT, 128, 2>);
+    case 256: return go(decode_kernel<DT, 256, 1>);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+template <int DT>
+cudaError_t occupancy_decode_t(int head_dim, int threads, size_t smem, int* blocks_per_sm) {
+  auto q = [&](auto kernel) -> cudaError_t {
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, kernel, threads, smem);
+  };
+  switch (head_dim) {
+    case 64: return q(decode_kernel<DT, 64, 2>);
+    case 128: return q(decode_kernel<DT, 128, 2>);
+    case 256: return q(decode_kernel<DT, 256, 1>);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace kvq

@@ -1,0 +1,80 @@
+// kvq_internal.h -- launch arguments and launchers shared between the host
+// shim (api.cu) and the kernel translation units.  Not part of the C ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+#include "kvq.h"
+
+namespace kvq {
+
+constexpr int kTile = 64;       // keys per pipeline stage (4 sub-tiles of 16)
+constexpr int kSub = 16;        // keys per MMA sub-tile
+constexpr int kWaves = 2;       // target work units per persistent CTA
+constexpr int kMaxBatch = 1024; // sequences whose split plan fits in shared memory
+constexpr int kMaxStages = 8;
+
+struct AppendArgs {
+  const uint16_t* k_new;  // bf16 bits [N, Hkv, D]
+  const uint16_t* v_new;
+  const int64_t* slots;   // [N]
+  uint8_t* k_codes;
+  uint8_t* v_codes;
+  float* k_scale;
+  float* v_scale;
+  long long capacity;     // num_blocks * block_size
+  int n_tokens, num_kv_heads, head_dim, block_size, log2_bs;
+  int dtype, k_mode, v_mode;
+  unsigned int* err;
+};
+
+struct DecodeArgs {
+  const uint16_t* q;            // bf16 bits [B, T, Hq, D]
+  const int32_t* block_table;   // [B, max_blocks_per_seq]
+  const int32_t* seq_lens;      // [B]
+  const float* k_scale;         // PER_ROW array or static scales
+  const float* v_scale;
+  int k_mode, v_mode;
+  int num_blocks, block_size, log2_bs, num_kv_heads;
+  int batch, num_q_heads, q_tokens, group, rows, max_blocks_per_seq, max_seq_len;
+  float sm_scale, softcap;
+  int window;
+  int row_groups, key_warps, stages;
+  int units_max;
+  int* plan;        // workspace: [0] chunk, [1] items, [2] batch, [3] units_max, then prefix[B+1]
+  float* part_lse;  // [units_max, rows]   base-2 log-sum-exp of each split
+  float* part_o;    // [units_max, rows, D] normalized split output
+  unsigned int* err;
+};
+
+struct CombineArgs {
+  const int* plan;
+  const float* part_lse;
+  const float* part_o;
+  const float* head_sink;  // [Hq] or null
+  const float* v_scale;    // static V scale (PER_TENSOR [1] / PER_CHANNEL [Hkv, D]) or null
+  int v_mode;
+  uint16_t* out;           // bf16 bits [B, T, Hq, D]
+  float* lse_out;          // [B, T, Hq] or null
+  int batch, q_tokens, num_q_heads, num_kv_heads, group, rows, head_dim;
+};
+
+cudaError_t launch_append(const AppendArgs& a, cudaStream_t stream);
+cudaError_t launch_combine(const CombineArgs& a, cudaStream_t stream);
+cudaError_t launch_decode_int8(int head_dim, const CUtensorMap& tk, const CUtensorMap& tv, const DecodeArgs& a,
+                               int grid, int threads, size_t smem, cudaStream_t stream);
+cudaError_t launch_decode_fp8(int head_dim, const CUtensorMap& tk, const CUtensorMap& tv, const DecodeArgs& a,
+                              int grid, int threads, size_t smem, cudaStream_t stream);
+cudaError_t launch_decode_int4(int head_dim, const CUtensorMap& tk, const CUtensorMap& tv, const DecodeArgs& a,
+                               int grid, int threads, size_t smem, cudaStream_t stream);
+
+cudaError_t occupancy_decode_int8(int head_dim, int threads, size_t smem, int* blocks_per_sm);
+cudaError_t occupancy_decode_fp8(int head_dim, int threads, size_t smem, int* blocks_per_sm);
+cudaError_t occupancy_decode_int4(int head_dim, int threads, size_t smem, int* blocks_per_sm);
+
+}  // namespace kvq

@@ -214,18 +214,37 @@ def make(name: str, *, ctx: Optional[int] = None, seed: int = 0, batch: Optional
     raise KeyError(name)
 
 
-def cache_bytes_read(w: Workload, window: int = 0) -> int:
-    """Algorithmic bytes of one decode step: the K and V codes (+ per-row
-    scales) of every key some query row sees, plus q, out, the block-table
-    entries used and seq_lens."""
-    total_keys = 0
+def step_bytes(w: Workload, window: int = 0) -> dict:
+    """Algorithmic bytes of one decode step, by component:
+      kv     K and V codes (+ per-row scales) of every key some query row sees
+      q      the queries, read once
+      table  block-table entries of the pages those keys sit in, and seq_lens
+      out    the bf16 output, written once
+      append the T new rows per sequence: bf16 K/V read, codes (+ scales) and
+             slot_mapping written/read
+    Split partials in the workspace are implementation overhead, not counted."""
+    keys = 0
     pages = 0
     for b in range(w.batch):
         L = int(w.seq_lens[b])
         lo = max(0, L - w.q_tokens + 1 - window) if window > 0 else 0
-        total_keys += max(0, L - lo)
+        keys += max(0, L - lo)
         if L > lo:
             pages += (L - 1) // w.block_size - lo // w.block_size + 1
-    per_key = 2 * w.row_bytes() + (4 if w.k_mode == PER_ROW else 0) + (4 if w.v_mode == PER_ROW else 0)
-    qo = 2 * w.batch * w.q_tokens * w.num_q_heads * w.head_dim * 2
-    return total_keys * w.num_kv_heads * per_key + qo + 4 * pages + 4 * w.batch
+    scales = (4 if w.k_mode == PER_ROW else 0) + (4 if w.v_mode == PER_ROW else 0)
+    per_key = 2 * w.row_bytes() + scales
+    qo = w.batch * w.q_tokens * w.num_q_heads * w.head_dim * 2
+    new = w.batch * w.q_tokens
+    return dict(kv=keys * w.num_kv_heads * per_key, q=qo, table=4 * pages + 4 * w.batch, out=qo,
+                append=new * w.num_kv_heads * (2 * w.head_dim * 2 + per_key) + 8 * new)
+
+
+def decode_bytes(w: Workload, window: int = 0) -> int:
+    """Algorithmic bytes the decode kernel itself moves (kv + q + table)."""
+    s = step_bytes(w, window)
+    return s["kv"] + s["q"] + s["table"]
+
+
+def cache_bytes_read(w: Workload, window: int = 0) -> int:
+    """All algorithmic bytes of one step (decode, combine output, append)."""
+    return sum(step_bytes(w, window).values())

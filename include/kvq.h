@@ -1,0 +1,191 @@
+/*
+ * kvq.h -- decode attention over a quantized, paged KV cache (GB300, sm_103a).
+ *
+ * A C ABI: plain structs, pointers and sizes.  Every device pointer is caller
+ * owned; the library never allocates, frees, or synchronizes the stream it is
+ * given (kvq_get_device_error is the one call that waits, and says so).  All
+ * compute calls are asynchronous on `stream` and take their grid and workspace
+ * extents from host-side shapes only, so a sequence of calls can be captured
+ * in a CUDA graph.
+ *
+ * The operations follow these pages:
+ *  - onnxruntime issue #29783 (quantized KV cache in GroupQueryAttention):
+ *    per-token scales, quantize the appended token on write, dequantize on
+ *    read, no fp16 copy of the past.
+ *  - onnxruntime PR #29912 "[CUDA] PagedAttention: quantized KV cache, XQA
+ *    decode, MLA, QK-Norm and head sink", Summary of Changes: slot_mapping,
+ *    head_sink, k_scale / v_scale with PER_TENSOR / PER_CHANNEL granularity,
+ *    int8 / float8e4m3fn cache types, ReshapeAndCache (quantize on write),
+ *    split-KV paged decode with softcap and sliding window, ApplyHeadSink, and
+ *    the attention_metadata upper bound that keeps a step capturable.
+ *  - onnxruntime PR #32515 "[CUDA] Add INT4 paged KV cache with per-channel
+ *    scales", Description: int4 packed two per byte, cache head dimension
+ *    (head_size+1)/2, per-channel scale folded into Q and re-applied to the
+ *    output, speculative decode with several query tokens.
+ *  - "kv-quant-attn" page, sections "Method" and "Correctness": per-row absmax
+ *    scales, one block per (batch, kv head) resolving the whole GQA group from
+ *    one read, warp-private softmax state, fixed-order merge (bitwise
+ *    reproducible), GQA ratio at most 8, head dimension at most 256.
+ *
+ * Data layout (all tensors dense, row-major, innermost last):
+ *   codes       uint8  [num_blocks, num_kv_heads, block_size, Dp]
+ *               Dp = head_dim (int8, e4m3) or head_dim/2 (int4: channel 2j in
+ *               the low nibble of byte j, channel 2j+1 in the high nibble,
+ *               two's-complement nibbles)
+ *   PER_ROW     scales fp32 [num_blocks, num_kv_heads, block_size]
+ *   PER_TENSOR  scale  fp32 [1]
+ *   PER_CHANNEL scales fp32 [num_kv_heads, head_dim]
+ *   cache slot  s = block * block_size + row
+ *   q, out      bf16   [batch, q_tokens, num_q_heads, head_dim]
+ *   k_new/v_new bf16   [n_tokens, num_kv_heads, head_dim]
+ *   block_table int32  [batch, max_blocks_per_seq]
+ *   seq_lens    int32  [batch]   (each includes the q_tokens new tokens)
+ *   lse_out     fp32   [batch, q_tokens, num_q_heads] (natural log)
+ *
+ * Supported on the GPU path: head_dim in {64, 128, 256}; num_q_heads a
+ * multiple of num_kv_heads with a ratio of at most 8; q_tokens in [1, 8];
+ * block_size a power of two >= 16; batch <= 1024.  Pointers 16-byte aligned.
+ */
+#ifndef KVQ_H
+#define KVQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define KVQ_API __attribute__((visibility("default")))
+
+/* A cudaStream_t (the same type: a pointer to the runtime's stream object);
+ * NULL is the legacy default stream. */
+typedef struct CUstream_st* kvq_stream_t;
+
+typedef enum {
+  KVQ_OK = 0,
+  KVQ_ERR_INVALID_ARG = 1,         /* bad enum, shape, null or misaligned pointer */
+  KVQ_ERR_UNSUPPORTED = 2,         /* valid, but outside what the GPU path covers */
+  KVQ_ERR_WORKSPACE_TOO_SMALL = 3, /* workspace_bytes < kvq_decode_workspace_size */
+  KVQ_ERR_CUDA = 4,                /* a CUDA runtime call or a launch failed */
+  KVQ_ERR_DEVICE_TIMEOUT = 5       /* a bounded device-side wait gave up */
+} kvq_status;
+
+/* Cache element types (PR #29912: int8, float8e4m3fn; PR #32515: packed int4). */
+typedef enum { KVQ_INT8 = 1, KVQ_FP8_E4M3 = 2, KVQ_INT4 = 3 } kvq_dtype;
+
+/* Scale granularity: PER_ROW is one absmax scale per (token, kv head) row,
+ * computed on append (kv-quant-attn "Method"; issue #29783 per-token);
+ * PER_TENSOR and PER_CHANNEL are static caller-given scales (PR #29912). */
+typedef enum {
+  KVQ_SCALE_PER_ROW = 1,
+  KVQ_SCALE_PER_TENSOR = 2,
+  KVQ_SCALE_PER_CHANNEL = 3
+} kvq_scale_mode;
+
+/* Device-side data violations, OR-ed into a per-device flag word.  The
+ * offending access is skipped (never trapped); outputs that depend on it are
+ * unspecified.  Read with kvq_get_device_error. */
+#define KVQ_DEVERR_SLOT 0x1u      /* append: slot_mapping[n] >= num_blocks * block_size */
+#define KVQ_DEVERR_BLOCK_ID 0x2u  /* decode: block_table entry outside [0, num_blocks) */
+#define KVQ_DEVERR_SEQ_LEN 0x4u   /* decode: seq_len < 0, > capacity, or > max_seq_len */
+#define KVQ_DEVERR_TIMEOUT 0x8u   /* a bounded pipeline wait gave up */
+#define KVQ_DEVERR_PLAN 0x10u     /* decode: split plan exceeded the workspace bound (not expected) */
+
+/* The paged cache: one descriptor per layer (kv-quant-attn "Usage": one cache
+ * object per layer).  All pointers are device memory owned by the caller.
+ * k_scale / v_scale: PER_ROW arrays written by kvq_append, or the static
+ * scales (finite and > 0: the precondition the PR #447 scale loader checks). */
+typedef struct {
+  int32_t dtype;        /* kvq_dtype */
+  int32_t k_mode;       /* kvq_scale_mode of K */
+  int32_t v_mode;       /* kvq_scale_mode of V */
+  int32_t num_blocks;   /* pool size in blocks */
+  int32_t block_size;   /* tokens per block (power of two >= 16) */
+  int32_t num_kv_heads; /* Hkv */
+  int32_t head_dim;     /* D */
+  void* k_codes;        /* uint8 [num_blocks, Hkv, block_size, Dp] */
+  void* v_codes;
+  float* k_scale;
+  float* v_scale;
+} kvq_cache;
+
+/* One decode call (PagedAttention's inputs, PR #29912 Summary of Changes). */
+typedef struct {
+  int32_t batch;              /* B (<= 1024) */
+  int32_t num_q_heads;        /* Hq; Hq / Hkv <= 8; query head i reads kv head i / (Hq/Hkv) */
+  int32_t q_tokens;           /* T in [1, 8]: 1, or 1 + drafts (PR #32515, speculative
+                                 decode); draft t sits at position seq_len - T + t and
+                                 sees keys 0..that position (causal among drafts) */
+  int32_t max_blocks_per_seq; /* block_table row length; capacity = it * block_size */
+  int32_t max_seq_len;        /* host upper bound on seq_lens, like attention_metadata
+                                 [max_kv_len] (PR #29912); 0 = capacity.  Sizes the grid,
+                                 never read back from the device. */
+  float sm_scale;             /* logit scale; <= 0 selects 1/sqrt(head_dim) */
+  float softcap;              /* > 0: logit s -> softcap * tanh(s / softcap); 0 = off */
+  int32_t window;             /* > 0: keep the `window` most recent keys up to and
+                                 including the query position; 0 = off */
+} kvq_decode_params;
+
+/* Human-readable name of a status code (static storage). */
+KVQ_API const char* kvq_status_string(kvq_status status);
+
+/* kvq_append -- quantize-on-write of new K/V rows into their cache slots
+ * (ReshapeAndCache, PR #29912; per-row absmax, kv-quant-attn "Method";
+ * int4 nibble packing, PR #32515).
+ * For each token n and kv head h, the D bf16 values of k_new[n, h, :] (and of
+ * v_new) are quantized: PER_ROW scale = absmax / qmax (IEEE fp32 division,
+ * qmax 127 / 7 / 448, an all-zero row stores scale 0 and zero codes), then
+ * code = clamp(round_half_even(x / scale), -qmax, qmax) for int8 / int4, or
+ * the nearest e4m3 value (ties to even, finite overflow saturated to 448).
+ * slot_mapping int64 [n_tokens] (device): slot < 0 skips the token (padding);
+ * slot >= num_blocks * block_size sets KVQ_DEVERR_SLOT and skips it.
+ * Rows already in the cache are never touched.  n_tokens == 0 is a no-op. */
+KVQ_API kvq_status kvq_append(const kvq_cache* cache, const void* k_new, const void* v_new,
+                              const int64_t* slot_mapping, int32_t n_tokens,
+                              kvq_stream_t stream);
+
+/* Bytes of workspace kvq_decode needs for these shapes on the current device
+ * (split partials and the device-side split plan).  Host-only arithmetic plus
+ * one cached device-attribute query. */
+KVQ_API kvq_status kvq_decode_workspace_size(const kvq_cache* cache,
+                                             const kvq_decode_params* params,
+                                             size_t* workspace_bytes);
+
+/* kvq_decode -- split-KV flash-decoding over the quantized pages
+ * (PagedAttention paged decode, PR #29912; kv-quant-attn "Method").
+ * Reads q, block_table, seq_lens and the cache on the device, dequantizes on
+ * the fly, and writes per-split partials (log-sum-exp and normalized output)
+ * plus the split plan into `workspace` (device, caller owned, at least
+ * kvq_decode_workspace_size bytes, 256-byte aligned).  The result is
+ * completed by kvq_combine with the same cache, params and workspace on the
+ * same stream.  Per query row, logits are sm_scale * <q, k_j>, capped by
+ * softcap, masked to keys j <= pos (and j > pos - window when set). */
+KVQ_API kvq_status kvq_decode(const kvq_cache* cache, const kvq_decode_params* params,
+                              const void* q, const int32_t* block_table,
+                              const int32_t* seq_lens, void* workspace,
+                              size_t workspace_bytes, kvq_stream_t stream);
+
+/* kvq_combine -- fixed-order log-sum-exp merge of the split partials
+ * (kv-quant-attn "Method": partials merged in a fixed order, bitwise
+ * reproducible), then the exact head-sink rescale o *= 1/(1+exp(s_h - lse))
+ * (ApplyHeadSink, PR #29912), the static V scale (PER_TENSOR, or PER_CHANNEL
+ * per output channel: the fold of PR #32515), and a round-to-nearest-even
+ * bf16 store to out [B, T, Hq, D].
+ * head_sink fp32 [Hq] or NULL; lse_out fp32 [B, T, Hq] or NULL (natural-log
+ * LSE of the logits, before the sink; -inf for an empty key set, whose output
+ * row is zero). */
+KVQ_API kvq_status kvq_combine(const kvq_cache* cache, const kvq_decode_params* params,
+                               const void* workspace, size_t workspace_bytes,
+                               const float* head_sink, void* out, float* lse_out,
+                               kvq_stream_t stream);
+
+/* Reads the current device's KVQ_DEVERR_* flag word into *flags (host).  This
+ * call synchronizes `stream` before reading.  clear != 0 resets the word. */
+KVQ_API kvq_status kvq_get_device_error(uint32_t* flags, int32_t clear, kvq_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVQ_H */

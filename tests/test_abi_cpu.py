@@ -1,0 +1,131 @@
+"""The C-ABI library on the host: it builds, loads, exports every symbol
+include/kvq.h declares, and rejects invalid arguments before any CUDA call.
+No compute call runs here (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def kvq():
+    from decode_attention_quantized_gb300 import build, kvq
+    build.build()
+    kvq.load()
+    return kvq
+
+
+def declared_symbols():
+    text = open(os.path.join(ROOT, "include", "kvq.h")).read()
+    return sorted(set(re.findall(r"KVQ_API\s+[\w\s\*]*?\b(kvq_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_entry_points():
+    syms = declared_symbols()
+    for name in ("kvq_append", "kvq_decode", "kvq_combine", "kvq_decode_workspace_size",
+                 "kvq_get_device_error", "kvq_status_string"):
+        assert name in syms
+
+
+def test_library_exports_every_declared_symbol(kvq):
+    lib = kvq.load()
+    for name in declared_symbols():
+        assert hasattr(lib, name), name
+        assert name in kvq.SIGNATURES, f"binding lacks {name}"
+    # and nothing beyond the ABI is exported as a kvq_ symbol
+    out = os.popen(f"nm -D --defined-only {kvq.LIB_PATH}").read()
+    exported = set(re.findall(r"\b(kvq_\w+)\b", out))
+    assert exported == set(declared_symbols())
+
+
+def test_status_strings(kvq):
+    lib = kvq.load()
+    assert lib.kvq_status_string(0) == b"ok"
+    assert lib.kvq_status_string(3) == b"workspace too small"
+    assert lib.kvq_status_string(99) == b"unknown status"
+
+
+FAKE = 0x7F0000000000  # an aligned address that is never dereferenced on the host
+
+
+def good_cache(kvq, **kw):
+    d = dict(dtype=1, k_mode=1, v_mode=1, num_blocks=8, block_size=16, num_kv_heads=2, head_dim=128,
+             k_codes=FAKE, v_codes=FAKE + 4096, k_scale=FAKE + 8192, v_scale=FAKE + 16384)
+    d.update(kw)
+    return kvq.CacheDesc(**d)
+
+
+def good_params(kvq, **kw):
+    d = dict(batch=2, num_q_heads=8, q_tokens=1, max_blocks_per_seq=4, max_seq_len=0, sm_scale=0.0,
+             softcap=0.0, window=0)
+    d.update(kw)
+    return kvq.DecodeParams(**d)
+
+
+@pytest.mark.parametrize("bad,status", [
+    (dict(dtype=0), 1), (dict(dtype=4), 1), (dict(k_mode=0), 1), (dict(v_mode=7), 1),
+    (dict(num_blocks=0), 1), (dict(block_size=24), 1), (dict(block_size=8), 1), (dict(num_kv_heads=0), 1),
+    (dict(head_dim=96), 2), (dict(head_dim=32), 2), (dict(head_dim=-64), 1),
+    (dict(k_codes=None), 1), (dict(v_scale=None), 1), (dict(k_codes=FAKE + 8), 1),
+    (dict(k_scale=FAKE + 4), 1),
+])
+def test_append_rejects_bad_cache(kvq, bad, status):
+    lib = kvq.load()
+    c = good_cache(kvq, **bad)
+    st = lib.kvq_append(ctypes.byref(c), FAKE, FAKE, FAKE, 4, None)
+    assert st == status
+
+
+def test_append_rejects_bad_tokens(kvq):
+    lib = kvq.load()
+    c = good_cache(kvq)
+    assert lib.kvq_append(ctypes.byref(c), FAKE, FAKE, FAKE, -1, None) == 1
+    assert lib.kvq_append(ctypes.byref(c), FAKE, FAKE, FAKE, 0, None) == 0       # no-op, no launch
+    assert lib.kvq_append(ctypes.byref(c), None, FAKE, FAKE, 3, None) == 1
+    assert lib.kvq_append(ctypes.byref(c), FAKE + 2, FAKE, FAKE, 3, None) == 1   # misaligned bf16 rows
+    assert lib.kvq_append(None, FAKE, FAKE, FAKE, 3, None) == 1
+
+
+@pytest.mark.parametrize("bad,status", [
+    (dict(batch=-1), 1), (dict(num_q_heads=7), 1), (dict(num_q_heads=18), 2), (dict(q_tokens=0), 1),
+    (dict(q_tokens=9), 2), (dict(max_blocks_per_seq=0), 1), (dict(max_seq_len=-5), 1), (dict(window=-1), 1),
+    (dict(softcap=-1.0), 1), (dict(softcap=float("inf")), 1), (dict(sm_scale=float("nan")), 1),
+    (dict(batch=1025), 2),
+])
+def test_decode_rejects_bad_params(kvq, bad, status):
+    lib = kvq.load()
+    c = good_cache(kvq)
+    p = good_params(kvq, **bad)
+    n = ctypes.c_size_t(0)
+    assert lib.kvq_decode_workspace_size(ctypes.byref(c), ctypes.byref(p), ctypes.byref(n)) == status
+    assert lib.kvq_decode(ctypes.byref(c), ctypes.byref(p), FAKE, FAKE, FAKE, FAKE, 1 << 30, None) == status
+    assert lib.kvq_combine(ctypes.byref(c), ctypes.byref(p), FAKE, 1 << 30, None, FAKE, None, None) == status
+
+
+def test_decode_rejects_null_and_misaligned(kvq):
+    lib = kvq.load()
+    c = good_cache(kvq)
+    p = good_params(kvq)
+    assert lib.kvq_decode(ctypes.byref(c), ctypes.byref(p), None, FAKE, FAKE, FAKE, 1 << 30, None) == 1
+    assert lib.kvq_decode(ctypes.byref(c), ctypes.byref(p), FAKE, FAKE, FAKE, FAKE + 16, 1 << 30, None) == 1
+    assert lib.kvq_combine(ctypes.byref(c), ctypes.byref(p), FAKE, 1 << 30, None, None, None, None) == 1
+    assert lib.kvq_combine(ctypes.byref(c), ctypes.byref(p), FAKE, 1 << 30, FAKE + 2, FAKE, None, None) == 1
+    # an empty batch is a valid no-op
+    p0 = good_params(kvq, batch=0)
+    assert lib.kvq_decode(ctypes.byref(c), ctypes.byref(p0), None, None, None, None, 0, None) == 0
+    assert lib.kvq_combine(ctypes.byref(c), ctypes.byref(p0), None, 0, None, None, None, None) == 0
+    assert lib.kvq_get_device_error(None, 0, None) == 1
+
+
+def test_binding_refuses_to_run_without_the_library(tmp_path):
+    from decode_attention_quantized_gb300 import kvq
+    saved = kvq._lib
+    kvq._lib = None
+    try:
+        with pytest.raises(RuntimeError, match="build the CUDA library"):
+            kvq.load(str(tmp_path / "missing.so"))
+    finally:
+        kvq._lib = saved

@@ -1,0 +1,172 @@
+"""kvq_decode + kvq_combine on the GPU against the fp64 oracle, at sizes the
+oracle finishes in seconds that still span several 64-key tiles, several
+splits and a ragged tail; plus determinism, edge cases and device-side data
+checks."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from decode_attention_quantized_gb300 import kvq, synth
+from decode_attention_quantized_gb300.workload import GpuWorkload
+
+from parity import OracleSide, bits, check_lse, check_rows
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from decode_attention_quantized_gb300 import build
+    build.build()
+    return kvq.load()
+
+
+def run_case(orc, w, *, window=0, gen="cpu", step=0, check_cache=True, max_seq_len=None):
+    gw = GpuWorkload(w, gen_device=gen)
+    gw.fill_history()
+    k_new, v_new, slots = gw.new_tokens()
+    params = gw.params(window=window, max_seq_len=max_seq_len)
+    bufs = gw.buffers(params)
+    q = w.q(gen, step).to("cuda")
+    out, lse = gw.step(q, k_new, v_new, slots, params, bufs)
+    torch.cuda.synchronize()
+    assert kvq.kvq_get_device_error(clear=True) == 0
+    side = OracleSide(orc, w, range(w.batch), gen, gw.k_static, gw.v_static)
+    if check_cache:
+        side.compare_cache(gw)
+    ref, ref_lse = side.attend(q, window=window, sink=gw.head_sink)
+    got = out.float().cpu().numpy().astype(np.float64)
+    err = check_rows(got, ref)
+    check_lse(lse.cpu().numpy().astype(np.float64), ref_lse)
+    return gw, params, bufs, q, err
+
+
+SMALL = [
+    ("tiny", dict()),
+    ("gqa", dict(ctx=3000)),
+    ("gqa", dict(ctx=1, batch=2)),
+    ("paged", dict(batch=5, max_ctx=700)),
+    ("spec", dict(ctx=301, batch=2)),
+    ("mixed", dict(batch=6, max_ctx=5000)),
+]
+
+
+@pytest.mark.parametrize("name,kw", SMALL, ids=[f"{n}-{i}" for i, (n, _) in enumerate(SMALL)])
+def test_workloads_small(lib, orc, name, kw):
+    w = synth.make(name, **kw)
+    run_case(orc, w)
+    if w.window:
+        run_case(orc, w, window=w.window, check_cache=False)
+
+
+@pytest.mark.parametrize("dt", [kvq.INT8, kvq.FP8_E4M3, kvq.INT4])
+@pytest.mark.parametrize("km,vm", [(1, 1), (2, 2), (3, 3), (1, 3), (3, 1), (2, 1)])
+@pytest.mark.parametrize("D", [64, 128, 256])
+def test_type_and_scale_grid(lib, orc, dt, km, vm, D):
+    L = [150, 77, 1]
+    w = synth.Workload("grid", dt, km, vm, 3, 8, 2, D, 2, 32, np.array(L, np.int32),
+                       np.arange(3 * 5, dtype=np.int32).reshape(3, 5)[:, ::-1].copy(), 15,
+                       k_channel_lognormal=0.5, seed=dt * 100 + km * 10 + vm)
+    run_case(orc, w)
+
+
+@pytest.mark.parametrize("G,T", [(1, 1), (2, 3), (5, 1), (8, 1), (6, 8), (8, 8), (3, 5)])
+def test_group_and_draft_shapes(lib, orc, G, T):
+    Hkv = 2
+    L = np.array([200, T, 66], np.int32)
+    bs = 16
+    mb = 14
+    w = synth.Workload("shapes", kvq.INT8, kvq.PER_ROW, kvq.PER_ROW, 3, G * Hkv, Hkv, 128, T, bs, L,
+                       np.random.default_rng(G * 10 + T).permutation(3 * mb).astype(np.int32).reshape(3, mb),
+                       3 * mb, seed=G * 10 + T)
+    run_case(orc, w)
+
+
+def test_edges_empty_short_and_windows(lib, orc):
+    """seq_len 0 (empty: zero rows, lse -inf), seq_len < T (early drafts see
+    nothing), a window smaller than a tile and one larger than the sequence,
+    block sizes below and above the 64-key tile."""
+    for bs, W in ((16, 5), (512, 3000), (64, 64), (256, 1)):
+        L = np.array([0, 2, 1, 700, 129], np.int32)
+        mb = max(1, math.ceil(700 / bs))
+        w = synth.Workload("edges", kvq.INT8, kvq.PER_ROW, kvq.PER_ROW, 5, 12, 3, 64, 4, bs, L,
+                           np.arange(5 * mb, dtype=np.int32).reshape(5, mb), 5 * mb, use_sink=True, seed=bs)
+        run_case(orc, w)
+        run_case(orc, w, window=W, check_cache=False)
+
+
+def test_softcap_and_sink_together(lib, orc):
+    w = synth.make("paged", batch=3, max_ctx=500)
+    w.use_sink = True
+    w.softcap = 3.0      # tight enough that the cap changes the result
+    run_case(orc, w)
+
+
+def test_determinism_and_fresh_workspace(lib, orc):
+    """kv-quant-attn "Correctness": repeated decodes are bitwise identical
+    (fixed merge order, no atomics), also with a re-created workspace."""
+    w = synth.make("mixed", batch=5, max_ctx=6000)
+    gw, params, bufs, q, _ = run_case(orc, w)
+    ref = bufs.out.clone()
+    ref_lse = bufs.lse.clone()
+    for i in range(10):
+        kvq.decode_step(gw.cache, params, q, gw.block_table, gw.seq_lens, bufs, gw.head_sink)
+        assert torch.equal(bufs.out, ref) and torch.equal(bufs.lse, ref_lse)
+    fresh = gw.buffers(params)
+    fresh.workspace.fill_(0x7F7F7F7F)
+    kvq.decode_step(gw.cache, params, q, gw.block_table, gw.seq_lens, fresh, gw.head_sink)
+    assert torch.equal(fresh.out, ref)
+
+
+def test_large_per_channel_k_scale_with_zero_codes_is_finite(lib, orc):
+    """INT4 PR #32515: q * k_scale far beyond fp16 range with every K code
+    zero must not become inf * 0 = NaN; the output is the mean of V."""
+    D, L = 256, 100
+    w = synth.Workload("huge", kvq.INT4, kvq.PER_CHANNEL, kvq.PER_CHANNEL, 1, 6, 1, D, 1, 32,
+                       np.array([L], np.int32), np.arange(4, dtype=np.int32).reshape(1, 4), 4, seed=5)
+    ks = torch.full((1, D), 3.0e38)
+    gw = GpuWorkload(w, gen_device="cpu", k_static=ks, v_static=None)
+    gw.fill_history()
+    k_new, v_new, slots = gw.new_tokens()
+    kvq.kvq_append(gw.cache, torch.zeros_like(k_new), v_new, slots)
+    gw.cache.k_codes.zero_()
+    params = gw.params()
+    bufs = gw.buffers(params)
+    q = (w.q("cpu") * 100).to("cuda")
+    out, lse = kvq.decode_step(gw.cache, params, q, gw.block_table, gw.seq_lens, bufs)
+    torch.cuda.synchronize()
+    o = out.float().cpu().numpy()
+    assert np.isfinite(o).all()
+    vs = gw.v_static.cpu().numpy()[0]
+    vc = gw.cache.v_codes.cpu().numpy()[:, 0].reshape(-1, D // 2)[:L]
+    lo = (vc & 15).astype(np.int16)
+    hi = (vc >> 4).astype(np.int16)
+    codes = np.stack([np.where(lo > 7, lo - 16, lo), np.where(hi > 7, hi - 16, hi)], -1).reshape(L, D)
+    mean = codes.mean(0) * vs
+    assert np.allclose(o[0, 0, 0], mean, rtol=1e-2, atol=2e-2 * np.abs(mean).max())
+    assert np.allclose(lse.cpu().numpy(), math.log(L), atol=1e-4)
+
+
+def test_bad_block_id_and_seq_len_are_flagged_not_faulted(lib):
+    w = synth.make("paged", batch=3, max_ctx=300)
+    gw = GpuWorkload(w, gen_device="cpu")
+    gw.fill_history()
+    params = gw.params()
+    bufs = gw.buffers(params)
+    q = w.q("cpu").to("cuda")
+    kvq.kvq_get_device_error(clear=True)
+    bt = gw.block_table.clone()
+    bt[1, 0] = w.num_blocks + 5
+    bt[2, 0] = -3
+    kvq.decode_step(gw.cache, params, q, bt, gw.seq_lens, bufs)
+    assert kvq.kvq_get_device_error(clear=True) & kvq.DEVERR_BLOCK_ID
+    sl = gw.seq_lens.clone()
+    sl[0] = w.max_blocks * w.block_size + 1
+    kvq.decode_step(gw.cache, params, q, gw.block_table, sl, bufs)
+    assert kvq.kvq_get_device_error(clear=True) & kvq.DEVERR_SEQ_LEN
+    # the context still works afterwards
+    out, _ = kvq.decode_step(gw.cache, params, q, gw.block_table, gw.seq_lens, bufs)
+    torch.cuda.synchronize()
+    assert torch.isfinite(out.float()).all()
