@@ -55,6 +55,8 @@ SIGNATURES = {
     "kvq_combine": (_I32, [ctypes.POINTER(CacheDesc), ctypes.POINTER(DecodeParams), _VP, _SZ, _VP, _VP, _VP,
                            _VP]),
     "kvq_get_device_error": (_I32, [ctypes.POINTER(ctypes.c_uint32), _I32, _VP]),
+    "kvq_attend_noalloc": (_I32, [ctypes.POINTER(CacheDesc), ctypes.POINTER(DecodeParams), _VP, _VP, _VP, _VP, _VP,
+                                  _VP, _VP]),
 }
 
 _lib = None
@@ -178,6 +180,17 @@ def kvq_get_device_error(clear: bool = True, stream=None) -> int:
     if st not in (0, 5):
         raise KvqError("kvq_get_device_error", st)
     return v.value
+
+
+def kvq_attend_noalloc(cache: QuantizedPagedCache, params: DecodeParams, q: torch.Tensor, block_table: torch.Tensor,
+                       seq_lens: torch.Tensor, head_sink: Optional[torch.Tensor], out: torch.Tensor,
+                       lse_out: Optional[torch.Tensor] = None, stream=None):
+    """Decode + combine with the library's fixed device scratch (no workspace
+    argument, nothing allocated by the library)."""
+    d = cache.desc()
+    _check("kvq_attend_noalloc", load().kvq_attend_noalloc(ctypes.byref(d), ctypes.byref(params), _ptr(q),
+                                                           _ptr(block_table), _ptr(seq_lens), _ptr(head_sink),
+                                                           _ptr(out), _ptr(lse_out), _stream(stream)))
 
 
 @dataclass

@@ -180,6 +180,24 @@ KVQ_API kvq_status kvq_combine(const kvq_cache* cache, const kvq_decode_params* 
                                const float* head_sink, void* out, float* lse_out,
                                kvq_stream_t stream);
 
+/* kvq_attend_noalloc -- kvq_decode then kvq_combine, with the split-partial
+ * scratch in a library-owned 16 MiB device array instead of a caller
+ * workspace.  The pages have no counterpart: this exists for callers that
+ * cannot allocate device memory where they run attention (a plugin inside a
+ * runtime that owns all device memory and offers no scratch allocator, or a
+ * loop that must not pay cudaMalloc's implicit synchronization).  It allocates
+ * and frees nothing.  Arguments and results are those of kvq_decode and
+ * kvq_combine; KVQ_ERR_WORKSPACE_TOO_SMALL when the shapes need more than
+ * 16 MiB of scratch (kvq_decode_workspace_size tells).  The first call on a
+ * device looks up the array's device address (cudaGetSymbolAddress); make
+ * that first call before any stream capture.  The array holds the previous
+ * call's contents and is shared by all calls on the device: calls that
+ * overlap on the GPU (different streams without ordering) race. */
+KVQ_API kvq_status kvq_attend_noalloc(const kvq_cache* cache, const kvq_decode_params* params,
+                                      const void* q, const int32_t* block_table,
+                                      const int32_t* seq_lens, const float* head_sink, void* out,
+                                      float* lse_out, kvq_stream_t stream);
+
 /* Reads the current device's KVQ_DEVERR_* flag word into *flags (host).  This
  * call synchronizes `stream` before reading.  clear != 0 resets the word. */
 KVQ_API kvq_status kvq_get_device_error(uint32_t* flags, int32_t clear, kvq_stream_t stream);
