@@ -41,6 +41,7 @@ def parse():
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default="gqa", choices=["tiny", "gqa", "paged", "spec", "mixed"])
     p.add_argument("--ctx", type=int, default=None, help="context length (gqa: 262144, spec: 32768, tiny: 256)")
+    p.add_argument("--reps", type=int, default=0, help="cache replicas rotated per step (0: enough for 4x L2)")
     p.add_argument("--no-sweep", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -172,7 +173,7 @@ def make_workload(args):
 
 # --------------------------------------------------------------------------- GPU arm
 
-def measure(w, steps, warmup, *, windows=(0,), e2e=False):
+def measure(w, steps, warmup, *, windows=(0,), e2e=False, reps=0):
     """Time `steps` decode steps of workload w on the current GPU.  Caches are
     replicated so that consecutive steps read different memory and the
     replicas together exceed 4x the L2 size (inputs larger than L2)."""
@@ -184,8 +185,8 @@ def measure(w, steps, warmup, *, windows=(0,), e2e=False):
     dev = torch.cuda.current_device()
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     kv_bytes = synth.step_bytes(w)["kv"]
-    reps = max(2, math.ceil(4 * l2 / max(kv_bytes, 1)))
-    reps = min(reps, 512)
+    if reps <= 0:
+        reps = min(512, max(2, math.ceil(4 * l2 / max(kv_bytes, 1))))
     gws = [GpuWorkload(w, device=f"cuda:{dev}", gen_device="cuda")]
     gws[0].fill_history()
     for _ in range(reps - 1):
@@ -205,41 +206,60 @@ def measure(w, steps, warmup, *, windows=(0,), e2e=False):
     bufs = [gws[0].buffers(p) for p in plist]
     stream = torch.cuda.current_stream()
 
-    def one(i, ev=None):
+    def step_args(i):
         g = gws[i % reps]
         j = i % len(windows)
-        p, b = plist[j], bufs[j]
-        if ev is not None:
-            ev[0].record(stream)
-        kvq.kvq_append(g.cache, k_new, v_new, slots, stream)
-        if ev is not None:
-            ev[1].record(stream)
-        kvq.kvq_decode(g.cache, p, qs[i % nq], g.block_table, g.seq_lens, b.workspace, stream)
-        if ev is not None:
-            ev[2].record(stream)
-        kvq.kvq_combine(g.cache, p, b.workspace, g.head_sink, b.out, b.lse, stream)
-        if ev is not None:
-            ev[3].record(stream)
+        return g, plist[j], bufs[j], qs[i % nq]
 
-    for i in range(warmup):
+    def k_append(i):
+        g, p, b, q = step_args(i)
+        kvq.kvq_append(g.cache, k_new, v_new, slots)
+
+    def k_decode(i):
+        g, p, b, q = step_args(i)
+        kvq.kvq_decode(g.cache, p, q, g.block_table, g.seq_lens, b.workspace)
+
+    def k_combine(i):
+        g, p, b, q = step_args(i)
+        kvq.kvq_combine(g.cache, p, b.workspace, g.head_sink, b.out, b.lse)
+
+    def one(i):
+        k_append(i)
+        k_decode(i)
+        k_combine(i)
+
+    for i in range(warmup):  # eager warm-up: per-device set-up, plan cache, smem limits
         one(i)
     torch.cuda.synchronize()
     assert kvq.kvq_get_device_error() == 0, "device error flags set during warm-up"
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
-    t0 = torch.cuda.Event(enable_timing=True)
-    t1 = torch.cuda.Event(enable_timing=True)
-    torch.cuda.synchronize()
-    t0.record(stream)
-    for i in range(steps):
-        one(warmup + i, evs[i])
-    t1.record(stream)
-    torch.cuda.synchronize()
-    total_ms = t0.elapsed_time(t1)
-    dec = [e[1].elapsed_time(e[2]) for e in evs]
-    app = [e[0].elapsed_time(e[1]) for e in evs]
-    comb = [e[2].elapsed_time(e[3]) for e in evs]
-    step = [e[0].elapsed_time(e[3]) for e in evs]
-    res = dict(total_ms=total_ms, steps=steps, decode_ms=dec, append_ms=app, combine_ms=comb, step_ms=step,
+
+    def graph_of(fn):
+        """K launches of fn captured once (the ABI is capture-safe)."""
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr):
+            for i in range(steps):
+                fn(warmup + i)
+        gr.replay()  # warm replay
+        torch.cuda.synchronize()
+        return gr
+
+    def timed(gr):
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        t0.record(stream)
+        gr.replay()
+        t1.record(stream)
+        torch.cuda.synchronize()
+        return t0.elapsed_time(t1)
+
+    g_step = graph_of(one)
+    total_ms = timed(g_step)
+    dec_ms = timed(graph_of(k_decode)) / steps
+    app_ms = timed(graph_of(k_append)) / steps
+    comb_ms = timed(graph_of(k_combine)) / steps
+    assert kvq.kvq_get_device_error() == 0, "device error flags set during the timed steps"
+    res = dict(total_ms=total_ms, steps=steps, decode_ms=[dec_ms], append_ms=[app_ms], combine_ms=[comb_ms],
                launches=3 * steps, reps=reps, l2=l2)
     sb = [synth.step_bytes(w, wd) for wd in windows]
     res["step_bytes"] = sum(sum(sb[i % len(windows)].values()) for i in range(warmup, warmup + steps))
@@ -330,7 +350,7 @@ def run_ours(args):
     barrier(world)
     torch.cuda.synchronize()
     clocks.start()
-    res = measure(w, args.steps, args.warmup, windows=windows, e2e=not args.no_e2e)
+    res = measure(w, args.steps, args.warmup, windows=windows, e2e=not args.no_e2e, reps=args.reps)
     clk = clocks.stop()
     barrier(world)
     total_ms = max_over_ranks(res["total_ms"], world)
@@ -344,10 +364,10 @@ def run_ours(args):
             else:
                 wc = synth.make("gqa", ctx=ctx)
                 r = measure(wc, max(10, args.steps), max(3, args.warmup))
-            dec_ms = statistics.median(r["decode_ms"])
+            dec_ms = statistics.mean(r["decode_ms"])
             kvb = synth.decode_bytes(wc)
             sweep.append({"ctx": ctx, "us_per_step": round(1e3 * r["total_ms"] / r["steps"], 2),
-                          "decode_us_median": round(1e3 * dec_ms, 2),
+                          "decode_us": round(1e3 * dec_ms, 2),
                           "decode_gbs": round(kvb / (dec_ms * 1e-3) / 1e9, 1),
                           "frac_of_hbm": round(kvb / (dec_ms * 1e-3) / 1e9 / peak, 3),
                           "cache_mb": round(synth.step_bytes(wc)["kv"] / 1e6, 2),
@@ -381,15 +401,17 @@ def run_ours(args):
             "cache_dtype": {1: "int8", 2: "fp8-e4m3", 3: "int4"}[w.dtype],
             "compute": "f16 x f16 -> f32 tensor-core mma, fp32 softmax",
             "step": "kvq_append (new tokens) + kvq_decode + kvq_combine",
+            "timing": "K steps captured once in a CUDA graph and replayed between CUDA events; per-kernel "
+                      "times from graphs of K launches of that kernel alone",
             "windows_per_call": list(windows),
             "l2": f"inputs larger than L2: {res['reps']} cache replicas rotated per step, "
                   f"{res['reps'] * synth.step_bytes(w)['kv'] / 1e6:.0f} MB total vs L2 {res['l2'] / 1e6:.0f} MB",
             "parallelism": "replicas" if world > 1 else "single-gpu",
         },
-        "step_breakdown_us_median": {
-            "append": round(1e3 * statistics.median(res["append_ms"]), 2),
-            "decode": round(1e3 * statistics.median(res["decode_ms"]), 2),
-            "combine": round(1e3 * statistics.median(res["combine_ms"]), 2),
+        "step_breakdown_us_mean": {
+            "append": round(1e3 * statistics.mean(res["append_ms"]), 2),
+            "decode": round(1e3 * statistics.mean(res["decode_ms"]), 2),
+            "combine": round(1e3 * statistics.mean(res["combine_ms"]), 2),
         },
         "roofline": {
             "kernel": "decode_kernel",

@@ -105,12 +105,11 @@ size_t stage_stride(const kvq_cache* c) {
   return (2 * code + 2 * kTile * 4 + 1023) / 1024 * 1024;
 }
 
-size_t fixed_smem(const kvq_cache* c, int n_cw, int batch, int stages) {
-  size_t s = 1024;                                  // alignment slack of the ring
-  s += (size_t)n_cw * 8 * c->head_dim * 4;          // merge scratch (accumulators)
-  s += (size_t)n_cw * 16 * 4;                       // merge scratch (m, l)
-  s += ((size_t)batch * 3 + 5 + ((batch * 3 + 5) & 1)) * 4;  // split plan
-  s += (size_t)stages * 2 * 8;                      // mbarriers
+size_t fixed_smem(const kvq_cache* c, int row_groups, int key_warps, int batch, int stages) {
+  size_t s = 1024;  // alignment slack of the ring
+  if (key_warps > 1) s += (size_t)row_groups * (c->head_dim / 16 * 4 + 4) * 32 * 4;  // merge slot per row group
+  s += ((size_t)batch + 5 + ((batch + 5) & 1)) * 4;                                  // split plan
+  s += (size_t)stages * 2 * 8;                                                       // mbarriers
   return s;
 }
 
@@ -122,7 +121,7 @@ cudaError_t occupancy(const kvq_cache* c, int threads, size_t smem, int* n) {
   }
 }
 
-kvq_status make_plan(const kvq_cache* c, const kvq_decode_params* p, const DeviceInfo& dev, Plan* out) {
+kvq_status make_plan_uncached(const kvq_cache* c, const kvq_decode_params* p, const DeviceInfo& dev, Plan* out) {
   Plan P{};
   const int G = p->num_q_heads / c->num_kv_heads;
   P.rows = G * p->q_tokens;
@@ -134,13 +133,13 @@ kvq_status make_plan(const kvq_cache* c, const kvq_decode_params* p, const Devic
   const size_t stride = stage_stride(c);
   int occ = 0;
   for (int target : {2, 1}) {
+    // per-SM shared memory is 228 KiB with 1 KiB reserved per resident CTA
     const size_t budget = target == 2 ? (size_t)113 * 1024 : (size_t)227 * 1024;
-    const size_t fixed = fixed_smem(c, n_cw, B, 0);
+    const size_t fixed = fixed_smem(c, P.row_groups, P.key_warps, B, 0);
     if (fixed + 2 * (stride + 16) > budget) continue;
     int stages = (int)((budget - fixed) / (stride + 16));
     stages = stages > kMaxStages ? kMaxStages : stages;
-    if (target == 2 && stages < 3) continue;
-    const size_t smem = fixed_smem(c, n_cw, B, stages) + (size_t)stages * stride;
+    const size_t smem = fixed_smem(c, P.row_groups, P.key_warps, B, stages) + (size_t)stages * stride;
     int n = 0;
     if (occupancy(c, P.threads, smem, &n) != cudaSuccess) return KVQ_ERR_CUDA;
     if (n >= target || (target == 1 && n >= 1)) {
@@ -162,6 +161,51 @@ kvq_status make_plan(const kvq_cache* c, const kvq_decode_params* p, const Devic
   P.ws_lse = align256((size_t)P.units_max * P.rows * 4);
   P.ws_o = (size_t)P.units_max * P.rows * c->head_dim * 4;
   P.ws_total = P.ws_plan + P.ws_lse + P.ws_o;
+  *out = P;
+  return KVQ_OK;
+}
+
+// The launch plan depends only on shapes and the device; calls with the same
+// shapes reuse it (no occupancy query on the hot path).
+struct PlanKey {
+  int dev, dtype, k_mode, v_mode, head_dim, num_kv_heads, block_size, batch, num_q_heads, q_tokens,
+      max_blocks_per_seq, max_seq_len;
+  bool operator==(const PlanKey& o) const { return std::memcmp(this, &o, sizeof(PlanKey)) == 0; }
+};
+constexpr int kPlanCache = 64;
+PlanKey g_plan_keys[kPlanCache];
+Plan g_plans[kPlanCache];
+int g_plan_count = 0, g_plan_next = 0;
+
+kvq_status make_plan(const kvq_cache* c, const kvq_decode_params* p, const DeviceInfo& dev, Plan* out) {
+  PlanKey k;
+  std::memset(&k, 0, sizeof k);
+  if (cudaGetDevice(&k.dev) != cudaSuccess) return KVQ_ERR_CUDA;
+  k.dtype = c->dtype;
+  k.k_mode = c->k_mode;
+  k.v_mode = c->v_mode;
+  k.head_dim = c->head_dim;
+  k.num_kv_heads = c->num_kv_heads;
+  k.block_size = c->block_size;
+  k.batch = p->batch;
+  k.num_q_heads = p->num_q_heads;
+  k.q_tokens = p->q_tokens;
+  k.max_blocks_per_seq = p->max_blocks_per_seq;
+  k.max_seq_len = p->max_seq_len;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    for (int i = 0; i < g_plan_count; ++i)
+      if (g_plan_keys[i] == k) {
+        *out = g_plans[i];
+        return KVQ_OK;
+      }
+  }
+  Plan P;
+  if (kvq_status s = make_plan_uncached(c, p, dev, &P)) return s;
+  std::lock_guard<std::mutex> lk(g_mu);
+  const int slot = g_plan_count < kPlanCache ? g_plan_count++ : (g_plan_next++ % kPlanCache);
+  g_plan_keys[slot] = k;
+  g_plans[slot] = P;
   *out = P;
   return KVQ_OK;
 }

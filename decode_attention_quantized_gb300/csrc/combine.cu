@@ -7,8 +7,8 @@
 // per-channel V scale applied to the output (the V half of the per-channel
 // fold): onnxruntime PR #32515, Description.
 //
-// One warp per output row (b, t, query head); each lane owns D/32 consecutive
-// channels.  Splits are visited in ascending key order by every lane.
+// One CTA per output row (b, t, query head); each lane owns D/32 consecutive
+// channels.
 #include <cuda_bf16.h>
 
 #include "kvq_internal.h"
@@ -17,13 +17,20 @@
 namespace kvq {
 namespace {
 
+constexpr int kCombineWarps = 8;
+
+// One CTA per output row; warp w folds splits w, w + 8, ... (ascending), then
+// warp 0 adds the eight warp sums in warp order.  Every split's weight is
+// taken against the row's maximum log-sum-exp, so the result does not depend
+// on how splits are spread over warps beyond that fixed order.
 template <int D>
-__global__ void __launch_bounds__(256) combine_kernel(const CombineArgs a) {
+__global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const CombineArgs a) {
   constexpr int E = D / 32;
-  const int lane = threadIdx.x & 31;
-  const int row_id = (int)((blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5);
-  const int n_rows = a.batch * a.q_tokens * a.num_q_heads;
-  if (row_id >= n_rows) return;
+  __shared__ float s_acc[kCombineWarps][D];
+  __shared__ float s_w[kCombineWarps];
+  __shared__ float s_m[kCombineWarps];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int row_id = blockIdx.x;
   const int hq = row_id % a.num_q_heads;
   const int t = (row_id / a.num_q_heads) % a.q_tokens;
   const int b = row_id / (a.num_q_heads * a.q_tokens);
@@ -32,22 +39,27 @@ __global__ void __launch_bounds__(256) combine_kernel(const CombineArgs a) {
 
   const int* prefix = a.plan + 4;
   const int i0 = prefix[b], i1 = prefix[b + 1];
+  auto lse_of = [&](int it) { return a.part_lse[((size_t)it * a.num_kv_heads + h) * a.rows + r]; };
 
   float m = -INFINITY;
-  for (int it = i0 + lane; it < i1; it += 32) m = fmaxf(m, a.part_lse[((size_t)it * a.num_kv_heads + h) * a.rows + r]);
+  for (int it = i0 + threadIdx.x; it < i1; it += blockDim.x) m = fmaxf(m, lse_of(it));
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  if (lane == 0) s_m[warp] = m;
+  __syncthreads();
+  m = s_m[0];
+#pragma unroll
+  for (int w = 1; w < kCombineWarps; ++w) m = fmaxf(m, s_m[w]);
 
   float acc[E];
 #pragma unroll
   for (int e = 0; e < E; ++e) acc[e] = 0.0f;
   float wsum = 0.0f;
   if (m != -INFINITY) {
-    for (int it = i0; it < i1; ++it) {
+    for (int it = i0 + warp; it < i1; it += kCombineWarps) {
       const size_t u = ((size_t)it * a.num_kv_heads + h) * a.rows + r;
       const float l2 = a.part_lse[u];
-      if (l2 == -INFINITY) continue;
-      const float w = ptx::fast_exp2(l2 - m);
+      const float w = l2 == -INFINITY ? 0.0f : ptx::fast_exp2(l2 - m);
       wsum += w;
       const float* po = a.part_o + u * D + lane * E;
       if constexpr (E % 4 == 0) {
@@ -68,6 +80,21 @@ __global__ void __launch_bounds__(256) combine_kernel(const CombineArgs a) {
         }
       }
     }
+  }
+#pragma unroll
+  for (int e = 0; e < E; ++e) s_acc[warp][lane * E + e] = acc[e];
+  if (lane == 0) s_w[warp] = wsum;
+  __syncthreads();
+  if (warp != 0) return;
+
+  wsum = s_w[0];
+#pragma unroll
+  for (int e = 0; e < E; ++e) acc[e] = s_acc[0][lane * E + e];
+#pragma unroll
+  for (int w = 1; w < kCombineWarps; ++w) {
+    wsum += s_w[w];
+#pragma unroll
+    for (int e = 0; e < E; ++e) acc[e] += s_acc[w][lane * E + e];
   }
 
   float lse_nat = -INFINITY;
@@ -110,12 +137,12 @@ __global__ void __launch_bounds__(256) combine_kernel(const CombineArgs a) {
 }  // namespace
 
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t stream) {
-  const long long rows = (long long)a.batch * a.q_tokens * a.num_q_heads;
-  const unsigned blocks = (unsigned)((rows + 7) / 8);
+  const unsigned blocks = (unsigned)((long long)a.batch * a.q_tokens * a.num_q_heads);
+  constexpr int threads = kCombineWarps * 32;
   switch (a.head_dim) {
-    case 64: combine_kernel<64><<<blocks, 256, 0, stream>>>(a); break;
-    case 128: combine_kernel<128><<<blocks, 256, 0, stream>>>(a); break;
-    case 256: combine_kernel<256><<<blocks, 256, 0, stream>>>(a); break;
+    case 64: combine_kernel<64><<<blocks, threads, 0, stream>>>(a); break;
+    case 128: combine_kernel<128><<<blocks, threads, 0, stream>>>(a); break;
+    case 256: combine_kernel<256><<<blocks, threads, 0, stream>>>(a); break;
     default: return cudaErrorInvalidValue;
   }
   return cudaGetLastError();

@@ -28,8 +28,8 @@
 //    online softmax in fp32, P moved into the PV operand layout with
 //    movmatrix, PV with channels as MMA-M (ldmatrix.trans of the V codes);
 //  * at the end of a unit the key warps of a row group merge their states
-//    in fixed warp order through shared memory and write the unit's partial
-//    (base-2 log-sum-exp, normalized output) to the workspace.
+//    in a fixed chain through one shared slot and the last one writes the
+//    unit's partial (base-2 log-sum-exp, normalized output) to the workspace.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -120,17 +120,28 @@ __global__ void __launch_bounds__(288, MINB)
   uint8_t* ring = smem_raw + pad;
 
   const int n_cw = a.row_groups * a.key_warps;
-  float* scr_acc = reinterpret_cast<float*>(ring + (size_t)a.stages * Gm::STAGE_STRIDE);
-  float* scr_ml = scr_acc + (size_t)n_cw * 8 * D;
-  int* pl_lo = reinterpret_cast<int*>(scr_ml + n_cw * 16);
-  int* pl_hi = pl_lo + a.batch;
-  int* pl_pre = pl_hi + a.batch;      // [B + 1]
-  int* pl_misc = pl_pre + a.batch + 1;  // [4]
-  uint64_t* bar_full = reinterpret_cast<uint64_t*>(pl_misc + 4 + ((a.batch * 3 + 5) & 1));
+  constexpr int kScrPerRg = (Gm::NMT * 4 + 4) * 32;  // floats: accumulators + (m, l) of one warp, [elem][lane]
+  float* scr = reinterpret_cast<float*>(ring + (size_t)a.stages * Gm::STAGE_STRIDE);
+  const int scr_floats = a.key_warps > 1 ? a.row_groups * kScrPerRg : 0;
+  int* pl_pre = reinterpret_cast<int*>(scr + scr_floats);  // [B + 1]
+  int* pl_misc = pl_pre + a.batch + 1;                     // [4]
+  uint64_t* bar_full = reinterpret_cast<uint64_t*>(pl_misc + 4 + ((a.batch + 5) & 1));
   uint64_t* bar_empty = bar_full + a.stages;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int B = a.batch, T = a.q_tokens, Hkv = a.num_kv_heads;
+  const int cap = a.max_blocks_per_seq * a.block_size;
+  const int lim = (a.max_seq_len > 0 && a.max_seq_len < cap) ? a.max_seq_len : cap;
+
+  // key range [lo, L) of sequence b: L clamped to the capacity bound, lo the
+  // first key any query row sees (window) rounded down to the tile
+  auto seq_range = [&](int b, int& L, int& lo) {
+    L = a.seq_lens[b];
+    L = L < 0 ? 0 : (L > lim ? lim : L);
+    lo = 0;
+    if (a.window > 0) lo = max(0, L - T - a.window + 1);
+    lo &= ~(kTile - 1);
+  };
 
   if (tid == 0) {
     for (int s = 0; s < a.stages; ++s) {
@@ -141,32 +152,33 @@ __global__ void __launch_bounds__(288, MINB)
   }
 
   // ---------------------------------------------------------------- plan
-  {
-    const int cap = a.max_blocks_per_seq * a.block_size;
-    const int lim = (a.max_seq_len > 0 && a.max_seq_len < cap) ? a.max_seq_len : cap;
-    for (int b = tid; b < B; b += blockDim.x) {
-      int L = a.seq_lens[b];
-      if (L < 0 || L > lim) {
-        if (blockIdx.x == 0) atomicOr(a.err, KVQ_DEVERR_SEQ_LEN);
-        L = L < 0 ? 0 : lim;
-      }
-      int lo = 0;
-      if (a.window > 0) lo = max(0, L - T - a.window + 1);
-      lo &= ~(kTile - 1);
-      pl_lo[b] = lo;
-      pl_hi[b] = L;
-      pl_pre[b] = max(0, L - lo);  // length for now
-    }
+  for (int b = tid; b < B; b += blockDim.x) {
+    const int raw = a.seq_lens[b];
+    if ((raw < 0 || raw > lim) && blockIdx.x == 0) atomicOr(a.err, KVQ_DEVERR_SEQ_LEN);
+    int L, lo;
+    seq_range(b, L, lo);
+    pl_pre[b] = max(0, L - lo);  // length for now
   }
   __syncthreads();
   if (warp == 0) {
     const int seg = (B + 31) / 32;
     const int s0 = min(B, lane * seg), s1 = min(B, s0 + seg);
     long long tot = 0;
-    for (int b = s0; b < s1; ++b) tot += pl_pre[b];
+    int mn = 0x7FFFFFFF, mx = 0;
+    for (int b = s0; b < s1; ++b) {
+      tot += pl_pre[b];
+      mn = min(mn, pl_pre[b]);
+      mx = max(mx, pl_pre[b]);
+    }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
-    const long long target = (long long)gridDim.x * kWaves;
+    for (int o = 16; o > 0; o >>= 1) {
+      tot += __shfl_xor_sync(0xffffffffu, tot, o);
+      mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+      mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    }
+    // equal lengths split evenly with one unit per CTA; ragged lengths get
+    // kWaves units per CTA so that the shorter ones can balance the longer
+    const long long target = (long long)gridDim.x * (mn == mx ? 1 : kWaves);
     long long ch = (tot * Hkv + target - 1) / target;
     ch = (ch + kTile - 1) / kTile * kTile;
     const int chunk = (int)max((long long)kTile, min(ch, (long long)(1 << 30)));
@@ -218,8 +230,9 @@ __global__ void __launch_bounds__(288, MINB)
       if (pl_pre[mid] <= item) lo = mid; else hi = mid - 1;
     }
     b = lo;
-    L = pl_hi[b];
-    k0 = pl_lo[b] + (item - pl_pre[b]) * chunk;
+    int klo;
+    seq_range(b, L, klo);
+    k0 = klo + (item - pl_pre[b]) * chunk;
     k1 = min(k0 + chunk, L);
   };
 
@@ -581,84 +594,122 @@ __global__ void __launch_bounds__(288, MINB)
       if (lane == 0) ptx::mbar_arrive(&bar_empty[stage]);
     }
 
-    // ---- unit end: warp state -> shared scratch -> fixed-order merge
+    // ---- unit end: the key warps of a row group merge their states in a
+    // fixed chain (warp 0 into 1, the result into 2, ...) through one shared
+    // slot per row group; the last warp of the chain writes the partial
 #pragma unroll
     for (int o = 4; o < 32; o <<= 1) {
       l0 += __shfl_xor_sync(0xffffffffu, l0, o);
       l1 += __shfl_xor_sync(0xffffffffu, l1, o);
     }
-    {
-      float fac = v_row ? dev::pow2i(F) : 1.0f;
-      if constexpr (DT == KVQ_FP8_E4M3) fac *= 256.0f;
-      float* sa_w = scr_acc + (size_t)cw * 8 * D;
+    float to_true = v_row ? dev::pow2i(F) : 1.0f;  // acc * to_true = sum_j p_j dequant(v_j)
+    if constexpr (DT == KVQ_FP8_E4M3) to_true *= 256.0f;
+    float* slot = scr + rg * kScrPerRg;
+    for (int k = 1; k < a.key_warps; ++k) {
+      if (kw == k - 1) {
 #pragma unroll
-      for (int mt = 0; mt < Gm::NMT; ++mt)
+        for (int mt = 0; mt < Gm::NMT; ++mt)
 #pragma unroll
-        for (int e = 0; e < 4; ++e)
-          sa_w[(2 * c + (e & 1)) * D + dev::out_channel<DT>(mt, e, g)] = acc[mt][e] * fac;
-      if (g == 0) {
-        scr_ml[cw * 16 + (2 * c) * 2] = m0;
-        scr_ml[cw * 16 + (2 * c) * 2 + 1] = l0;
-        scr_ml[cw * 16 + (2 * c + 1) * 2] = m1;
-        scr_ml[cw * 16 + (2 * c + 1) * 2 + 1] = l1;
+          for (int e = 0; e < 4; ++e) slot[(mt * 4 + e) * 32 + lane] = acc[mt][e] * to_true;
+        slot[(Gm::NMT * 4 + 0) * 32 + lane] = m0;
+        slot[(Gm::NMT * 4 + 1) * 32 + lane] = m1;
+        slot[(Gm::NMT * 4 + 2) * 32 + lane] = l0;
+        slot[(Gm::NMT * 4 + 3) * 32 + lane] = l1;
       }
-    }
-    ptx::named_bar_sync(1, (uint32_t)n_cw * 32);
-    {
-      const int RG = a.row_groups, KW = a.key_warps;
-      const int nthr = n_cw * 32;
-      for (int e = cw * 32 + lane; e < RG * 8 * D; e += nthr) {
-        const int rgi = e / (8 * D), row = (e / D) & 7, ch = e % D;
-        const int rr = rgi * 8 + row;
-        if (rr >= a.rows) continue;
-        float M = -INFINITY;
-        for (int k = 0; k < KW; ++k) M = fmaxf(M, scr_ml[(k * RG + rgi) * 16 + row * 2]);
-        float lt = 0.0f, o = 0.0f;
-        if (M != -INFINITY) {
-          for (int k = 0; k < KW; ++k) {
-            const int w = k * RG + rgi;
-            const float f = ptx::fast_exp2(scr_ml[w * 16 + row * 2] - M);
-            lt += scr_ml[w * 16 + row * 2 + 1] * f;
-            o += scr_acc[((size_t)w * 8 + row) * D + ch] * f;
-          }
+      ptx::named_bar_sync(1, (uint32_t)n_cw * 32);
+      if (kw == k) {
+        const float pm0 = slot[(Gm::NMT * 4 + 0) * 32 + lane], pm1 = slot[(Gm::NMT * 4 + 1) * 32 + lane];
+        const float pl0 = slot[(Gm::NMT * 4 + 2) * 32 + lane], pl1 = slot[(Gm::NMT * 4 + 3) * 32 + lane];
+        const float M0 = fmaxf(m0, pm0), M1 = fmaxf(m1, pm1);
+        const float a0 = M0 == -INFINITY ? 0.0f : ptx::fast_exp2(m0 - M0);
+        const float b0 = M0 == -INFINITY ? 0.0f : ptx::fast_exp2(pm0 - M0);
+        const float a1 = M1 == -INFINITY ? 0.0f : ptx::fast_exp2(m1 - M1);
+        const float b1 = M1 == -INFINITY ? 0.0f : ptx::fast_exp2(pm1 - M1);
+#pragma unroll
+        for (int mt = 0; mt < Gm::NMT; ++mt) {
+          acc[mt][0] = acc[mt][0] * to_true * a0 + slot[(mt * 4 + 0) * 32 + lane] * b0;
+          acc[mt][1] = acc[mt][1] * to_true * a1 + slot[(mt * 4 + 1) * 32 + lane] * b1;
+          acc[mt][2] = acc[mt][2] * to_true * a0 + slot[(mt * 4 + 2) * 32 + lane] * b0;
+          acc[mt][3] = acc[mt][3] * to_true * a1 + slot[(mt * 4 + 3) * 32 + lane] * b1;
         }
-        const size_t pu = (size_t)u * a.rows + rr;
-        a.part_o[pu * D + ch] = lt > 0.0f ? o / lt : 0.0f;
-        if (ch == 0) a.part_lse[pu] = lt > 0.0f ? M + ptx::fast_log2(lt) : -INFINITY;
+        l0 = l0 * a0 + pl0 * b0;
+        l1 = l1 * a1 + pl1 * b1;
+        m0 = M0;
+        m1 = M1;
+        to_true = 1.0f;
+      }
+      ptx::named_bar_sync(1, (uint32_t)n_cw * 32);
+    }
+    if (kw == a.key_warps - 1) {
+      const float f0 = l0 > 0.0f ? to_true / l0 : 0.0f, f1 = l1 > 0.0f ? to_true / l1 : 0.0f;
+      const int rr0 = rg * 8 + 2 * c, rr1 = rr0 + 1;
+      float* o0 = a.part_o + ((size_t)u * a.rows + rr0) * D;
+      float* o1 = o0 + D;
+#pragma unroll
+      for (int mt = 0; mt < Gm::NMT; ++mt) {
+        const int ch = dev::out_channel<DT>(mt, 0, g);
+        if (rr0 < a.rows) *reinterpret_cast<float2*>(o0 + ch) = make_float2(acc[mt][0] * f0, acc[mt][2] * f0);
+        if (rr1 < a.rows) *reinterpret_cast<float2*>(o1 + ch) = make_float2(acc[mt][1] * f1, acc[mt][3] * f1);
+      }
+      if (g == 0) {
+        if (rr0 < a.rows) a.part_lse[(size_t)u * a.rows + rr0] = l0 > 0.0f ? m0 + ptx::fast_log2(l0) : -INFINITY;
+        if (rr1 < a.rows) a.part_lse[(size_t)u * a.rows + rr1] = l1 > 0.0f ? m1 + ptx::fast_log2(l1) : -INFINITY;
       }
     }
-    ptx::named_bar_sync(1, (uint32_t)n_cw * 32);
   }
+}
+
+// Raises (never lowers) the kernel's dynamic shared-memory limit on the
+// current device; shared by the occupancy query and the launch so that a
+// query for a small plan cannot undercut a larger plan launched later.
+template <int DT, int D, int MINB>
+cudaError_t ensure_smem(size_t smem) {
+  static int smem_set[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (smem_set[dev] < (int)smem) {
+    e = cudaFuncSetAttribute(decode_kernel<DT, D, MINB>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    smem_set[dev] = (int)smem;
+  }
+  return cudaSuccess;
+}
+
+template <int DT, int D, int MINB>
+cudaError_t launch_decode_d(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeArgs& a, int grid,
+                            int threads, size_t smem, cudaStream_t stream) {
+  cudaError_t e = ensure_smem<DT, D, MINB>(smem);
+  if (e != cudaSuccess) return e;
+  decode_kernel<DT, D, MINB><<<grid, threads, smem, stream>>>(tk, tv, a);
+  return cudaGetLastError();
+}
+
+template <int DT, int D, int MINB>
+cudaError_t occupancy_decode_d(int threads, size_t smem, int* blocks_per_sm) {
+  cudaError_t e = ensure_smem<DT, D, MINB>(smem);
+  if (e != cudaSuccess) return e;
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, decode_kernel<DT, D, MINB>, threads, smem);
 }
 
 template <int DT>
 cudaError_t launch_decode_t(int head_dim, const CUtensorMap& tk, const CUtensorMap& tv, const DecodeArgs& a,
                             int grid, int threads, size_t smem, cudaStream_t stream) {
-  auto go = [&](auto kernel) -> cudaError_t {
-    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    kernel<<<grid, threads, smem, stream>>>(tk, tv, a);
-    return cudaGetLastError();
-  };
   switch (head_dim) {
-    case 64: return go(decode_kernel<DT, 64, 2>);
-    case 128: return go(decode_kernel<DT, 128, 2>);
-    case 256: return go(decode_kernel<DT, 256, 1>);
+    case 64: return launch_decode_d<DT, 64, 2>(tk, tv, a, grid, threads, smem, stream);
+    case 128: return launch_decode_d<DT, 128, 2>(tk, tv, a, grid, threads, smem, stream);
+    case 256: return launch_decode_d<DT, 256, 1>(tk, tv, a, grid, threads, smem, stream);
     default: return cudaErrorInvalidValue;
   }
 }
 
 template <int DT>
 cudaError_t occupancy_decode_t(int head_dim, int threads, size_t smem, int* blocks_per_sm) {
-  auto q = [&](auto kernel) -> cudaError_t {
-    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, kernel, threads, smem);
-  };
   switch (head_dim) {
-    case 64: return q(decode_kernel<DT, 64, 2>);
-    case 128: return q(decode_kernel<DT, 128, 2>);
-    case 256: return q(decode_kernel<DT, 256, 1>);
+    case 64: return occupancy_decode_d<DT, 64, 2>(threads, smem, blocks_per_sm);
+    case 128: return occupancy_decode_d<DT, 128, 2>(threads, smem, blocks_per_sm);
+    case 256: return occupancy_decode_d<DT, 256, 1>(threads, smem, blocks_per_sm);
     default: return cudaErrorInvalidValue;
   }
 }
