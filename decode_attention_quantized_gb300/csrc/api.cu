@@ -89,6 +89,9 @@ kvq_status check_params(const kvq_cache* c, const kvq_decode_params* p) {
   if (!std::isfinite(p->sm_scale) || !std::isfinite(p->softcap) || p->softcap < 0.0f) return KVQ_ERR_INVALID_ARG;
   if ((long long)p->max_blocks_per_seq * c->block_size > (1LL << 30)) return KVQ_ERR_INVALID_ARG;
   if (p->num_q_heads / c->num_kv_heads > 8 || p->q_tokens > 8 || p->batch > kMaxBatch) return KVQ_ERR_UNSUPPORTED;
+  // the tile space of all (sequence, kv head) ranges must index with int
+  const long long tiles = (long long)p->max_blocks_per_seq * c->block_size / kTile + 1;
+  if ((long long)p->batch * c->num_kv_heads * tiles >= (1LL << 31)) return KVQ_ERR_UNSUPPORTED;
   return KVQ_OK;
 }
 
@@ -131,18 +134,21 @@ kvq_status make_plan_uncached(const kvq_cache* c, const kvq_decode_params* p, co
   P.threads = 32 * (n_cw + 1);
   const int B = p->batch > 0 ? p->batch : 1;
   const size_t stride = stage_stride(c);
+  // the most CTAs per SM whose ring still holds >= 3 stages (more warps per
+  // SM hide more latency); one CTA with >= 2 stages as the last resort
   int occ = 0;
-  for (int target : {2, 1}) {
+  for (int target : {4, 3, 2, 1}) {
     // per-SM shared memory is 228 KiB with 1 KiB reserved per resident CTA
-    const size_t budget = target == 2 ? (size_t)113 * 1024 : (size_t)227 * 1024;
+    const size_t budget = (size_t)228 * 1024 / target - 1024;
     const size_t fixed = fixed_smem(c, P.row_groups, P.key_warps, B, 0);
-    if (fixed + 2 * (stride + 16) > budget) continue;
+    const int min_stages = target > 1 ? 3 : 2;
+    if (fixed + (size_t)min_stages * (stride + 16) > budget) continue;
     int stages = (int)((budget - fixed) / (stride + 16));
     stages = stages > kMaxStages ? kMaxStages : stages;
     const size_t smem = fixed_smem(c, P.row_groups, P.key_warps, B, stages) + (size_t)stages * stride;
     int n = 0;
     if (occupancy(c, P.threads, smem, &n) != cudaSuccess) return KVQ_ERR_CUDA;
-    if (n >= target || (target == 1 && n >= 1)) {
+    if (n >= target) {
       occ = target;
       P.stages = stages;
       P.smem = smem;
@@ -156,7 +162,7 @@ kvq_status make_plan_uncached(const kvq_cache* c, const kvq_decode_params* p, co
   const long long useful = (long long)B * c->num_kv_heads * ((maxlen + kTile - 1) / kTile + 1);
   if (grid > useful) grid = useful;
   P.grid = (int)(grid < 1 ? 1 : grid);
-  P.units_max = P.grid * kWaves + B * c->num_kv_heads;
+  P.units_max = P.grid + B * c->num_kv_heads;  // partial slots: segment + CTA index
   P.ws_plan = align256((size_t)(4 + B + 1) * 4);
   P.ws_lse = align256((size_t)P.units_max * P.rows * 4);
   P.ws_o = (size_t)P.units_max * P.rows * c->head_dim * 4;

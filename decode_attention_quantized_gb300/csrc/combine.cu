@@ -19,7 +19,7 @@ namespace {
 
 constexpr int kCombineWarps = 8;
 
-// One CTA per output row; warp w folds splits w, w + 8, ... (ascending), then
+// One CTA per output row; warp w folds pieces w, w + 8, ... (ascending), then
 // warp 0 adds the eight warp sums in warp order.  Every split's weight is
 // taken against the row's maximum log-sum-exp, so the result does not depend
 // on how splits are spread over warps beyond that fixed order.
@@ -37,9 +37,16 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const Combi
   const int h = hq / a.group;
   const int r = t * a.group + (hq % a.group);  // row inside a work unit
 
-  const int* prefix = a.plan + 4;
-  const int i0 = prefix[b], i1 = prefix[b + 1];
-  auto lse_of = [&](int it) { return a.part_lse[((size_t)it * a.num_kv_heads + h) * a.rows + r]; };
+  // pieces of segment s = b * Hkv + h are the CTAs whose tile slices meet it;
+  // the piece of CTA x sits in slot s + x
+  const int W = a.plan[0];
+  const int* pre = a.plan + 4;
+  const int nb = pre[b + 1] - pre[b];
+  const int seg = b * a.num_kv_heads + h;
+  const int s_first = pre[b] * a.num_kv_heads + h * nb;
+  const int i0 = nb > 0 ? seg + s_first / W : 0;
+  const int i1 = nb > 0 ? seg + (s_first + nb - 1) / W + 1 : 0;
+  auto lse_of = [&](int slot) { return a.part_lse[(size_t)slot * a.rows + r]; };
 
   float m = -INFINITY;
   for (int it = i0 + threadIdx.x; it < i1; it += blockDim.x) m = fmaxf(m, lse_of(it));
@@ -57,7 +64,7 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const Combi
   float wsum = 0.0f;
   if (m != -INFINITY) {
     for (int it = i0 + warp; it < i1; it += kCombineWarps) {
-      const size_t u = ((size_t)it * a.num_kv_heads + h) * a.rows + r;
+      const size_t u = (size_t)it * a.rows + r;
       const float l2 = a.part_lse[u];
       const float w = l2 == -INFINITY ? 0.0f : ptx::fast_exp2(l2 - m);
       wsum += w;

@@ -13,10 +13,9 @@
 // Description: the fold is exact, the normaliser keeps |q*s| <= |q|).
 //
 // Structure (one persistent CTA per SM slot):
-//  * every CTA builds the same split plan from seq_lens in shared memory:
-//    each sequence's key range is cut into chunks of `chunk` keys (a multiple
-//    of the 64-key tile) so that about gridDim.x * kWaves work units exist; a
-//    unit is (sequence, chunk, kv head) and CTA x takes units x, x+grid, ...
+//  * every CTA builds the same split plan from seq_lens in shared memory: the
+//    (sequence, kv head) key ranges laid end to end in 64-key tiles, cut into
+//    one equal slice per CTA; a piece of a range inside a slice is a split;
 //  * one producer warp streams each unit's pages through a ring of shared
 //    memory stages: TMA tensor copies (cp.async.bulk.tensor, 128/64/32-byte
 //    swizzle) of the K and V code rows, the block id taken from the block
@@ -97,6 +96,12 @@ __device__ __forceinline__ uint32_t f8pair(uint32_t w, uint32_t sel) {
   return (y & 0x80008000u) | ((y >> 1) & 0x3F803F80u);
 }
 
+// tanh(x) = 1 - 2 / (e^{2x} + 1), from the definition; absolute error a few
+// 1e-7 (ex2.approx and an approximate divide), saturating to +-1.
+__device__ __forceinline__ float tanh_fast(float x) {
+  return 1.0f - __fdividef(2.0f, ptx::fast_exp2(x * 2.8853900817779268f) + 1.0f);
+}
+
 // Output channel held by accumulator element e of channel tile mt in lane
 // group g (the PV operand permutation chosen for the ldmatrix.trans layout).
 template <int DT>
@@ -152,38 +157,26 @@ __global__ void __launch_bounds__(288, MINB)
   }
 
   // ---------------------------------------------------------------- plan
+  // Segment s = b * Hkv + h is sequence b's key range [lo_b, L_b) for kv head
+  // h: n_b = ceil((L_b - lo_b) / kTile) tiles.  The segments laid end to end
+  // in s order make T tiles, and CTA x takes the contiguous slice
+  // [x W, (x + 1) W) with W = ceil(T / gridDim.x), so every CTA streams the
+  // same number of tiles whatever the length mix.  The piece of segment s in
+  // CTA x's slice writes its partial to slot s + x: distinct for every piece
+  // and contiguous over the pieces of one segment.
   for (int b = tid; b < B; b += blockDim.x) {
     const int raw = a.seq_lens[b];
     if ((raw < 0 || raw > lim) && blockIdx.x == 0) atomicOr(a.err, KVQ_DEVERR_SEQ_LEN);
     int L, lo;
     seq_range(b, L, lo);
-    pl_pre[b] = max(0, L - lo);  // length for now
+    pl_pre[b] = (max(0, L - lo) + kTile - 1) / kTile;  // tiles, for now
   }
   __syncthreads();
   if (warp == 0) {
     const int seg = (B + 31) / 32;
     const int s0 = min(B, lane * seg), s1 = min(B, s0 + seg);
-    long long tot = 0;
-    int mn = 0x7FFFFFFF, mx = 0;
-    for (int b = s0; b < s1; ++b) {
-      tot += pl_pre[b];
-      mn = min(mn, pl_pre[b]);
-      mx = max(mx, pl_pre[b]);
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      tot += __shfl_xor_sync(0xffffffffu, tot, o);
-      mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, o));
-      mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    }
-    // equal lengths split evenly with one unit per CTA; ragged lengths get
-    // kWaves units per CTA so that the shorter ones can balance the longer
-    const long long target = (long long)gridDim.x * (mn == mx ? 1 : kWaves);
-    long long ch = (tot * Hkv + target - 1) / target;
-    ch = (ch + kTile - 1) / kTile * kTile;
-    const int chunk = (int)max((long long)kTile, min(ch, (long long)(1 << 30)));
     int cnt = 0;
-    for (int b = s0; b < s1; ++b) cnt += (pl_pre[b] + chunk - 1) / chunk;
+    for (int b = s0; b < s1; ++b) cnt += pl_pre[b];
     int incl = cnt;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -192,113 +185,133 @@ __global__ void __launch_bounds__(288, MINB)
     }
     int run = incl - cnt;
     for (int b = s0; b < s1; ++b) {
-      const int len = pl_pre[b];
+      const int n = pl_pre[b];
       pl_pre[b] = run;
-      run += (len + chunk - 1) / chunk;
+      run += n;
     }
     if (lane == 31) {
-      int items = incl;
-      if ((long long)items * Hkv > a.units_max) {  // unreachable by construction of `chunk`
-        atomicOr(a.err, KVQ_DEVERR_PLAN);
-        items = a.units_max / Hkv;
-      }
+      const int total = incl * Hkv;
       pl_pre[B] = incl;
-      pl_misc[0] = chunk;
-      pl_misc[1] = items;
+      pl_misc[0] = max(1, (total + (int)gridDim.x - 1) / (int)gridDim.x);
+      pl_misc[1] = total;
     }
   }
   __syncthreads();
-  const int chunk = pl_misc[0];
-  const int total_units = pl_misc[1] * Hkv;
+  const int W = pl_misc[0];
+  const int t_begin = min((int)blockIdx.x * W, pl_misc[1]);
+  const int t_end = min(t_begin + W, pl_misc[1]);
   if (blockIdx.x == 0) {
-    for (int i = tid; i <= B; i += blockDim.x) a.plan[4 + i] = min(pl_pre[i], pl_misc[1]);
+    for (int i = tid; i <= B; i += blockDim.x) a.plan[4 + i] = pl_pre[i];
     if (tid == 0) {
-      a.plan[0] = chunk;
+      a.plan[0] = W;
       a.plan[1] = pl_misc[1];
       a.plan[2] = B;
       a.plan[3] = a.units_max;
     }
   }
 
-  // unit -> (b, h, key range)
-  auto unit_info = [&](int u, int& b, int& h, int& k0, int& k1, int& L) {
-    const int item = u / Hkv;
-    h = u - item * Hkv;
-    int lo = 0, hi = B - 1;  // last b with pre[b] <= item
+  // the piece that starts at global tile gt: sequence, kv head, key range,
+  // partial slot, and the global tile after it
+  auto piece = [&](int gt, int& b, int& h, int& k0, int& k1, int& L, int& slot, int& next) {
+    int lo = 0, hi = B - 1;  // last b with pre[b] * Hkv <= gt (skips empty sequences)
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
-      if (pl_pre[mid] <= item) lo = mid; else hi = mid - 1;
+      if (pl_pre[mid] * Hkv <= gt) lo = mid; else hi = mid - 1;
     }
     b = lo;
+    const int nb = pl_pre[b + 1] - pl_pre[b];
+    const int off = gt - pl_pre[b] * Hkv;
+    h = off / nb;
+    const int t0 = off - h * nb;
+    next = min(gt - t0 + nb, t_end);
     int klo;
     seq_range(b, L, klo);
-    k0 = klo + (item - pl_pre[b]) * chunk;
-    k1 = min(k0 + chunk, L);
+    k0 = klo + t0 * kTile;
+    k1 = min(klo + (t0 + next - gt) * kTile, L);
+    slot = b * Hkv + h + (int)blockIdx.x;
   };
 
   const bool k_row = a.k_mode == KVQ_SCALE_PER_ROW, v_row = a.v_mode == KVQ_SCALE_PER_ROW;
 
   // =============================================================== producer
+  // The whole warp fetches the unit's block ids 32 pages at a time (one
+  // coalesced load per 32 pages) and hands them to lane 0 by shuffles; lane 0
+  // waits for free stages and issues the copies.
   if (warp == n_cw) {
-    if (lane != 0) return;
     const int seg_rows = min(a.block_size, kTile);
     const int n_seg = kTile / seg_rows;
+    const uint32_t S = (uint32_t)a.stages;
     uint32_t it = 0;
-    bool ok = true;
-    for (int u = blockIdx.x; u < total_units; u += gridDim.x) {
-      int b, h, k0, k1, L;
-      unit_info(u, b, h, k0, k1, L);
+    int ok = 1;
+    for (int gt = t_begin, next; gt < t_end; gt = next) {
+      int b, h, k0, k1, L, slot;
+      piece(gt, b, h, k0, k1, L, slot, next);
       const int32_t* bt = a.block_table + (size_t)b * a.max_blocks_per_seq;
+      const int p_last = (k1 - 1) >> a.log2_bs;
+      int base = k0 >> a.log2_bs;
+      int my_id = base + lane <= p_last ? bt[base + lane] : -1;
       for (int key0 = k0; key0 < k1; key0 += kTile, ++it) {
-        const int stage = (int)(it % (uint32_t)a.stages);
-        if (it >= (uint32_t)a.stages && ok) {
-          ok = ptx::mbar_wait_bounded(&bar_empty[stage], ((it / a.stages) - 1) & 1);
+        const int stage = (int)(it % S);
+        if (lane == 0 && it >= S && ok) {
+          ok = ptx::mbar_wait_bounded(&bar_empty[stage], ((it / S) - 1) & 1) ? 1 : 0;
           if (!ok) atomicOr(a.err, KVQ_DEVERR_TIMEOUT);
         }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) {
-          ptx::mbar_arrive(&bar_full[stage]);
+          if (lane == 0) ptx::mbar_arrive(&bar_full[stage]);
           continue;
         }
         int blk[kTile / 16];
         uint32_t bytes = 0;
-        for (int s = 0; s < n_seg; ++s) {
+#pragma unroll
+        for (int s = 0; s < kTile / 16; ++s) {
           blk[s] = -1;
           const int skey = key0 + s * seg_rows;
-          if (skey >= k1) continue;
-          const int id = bt[skey >> a.log2_bs];
+          if (s >= n_seg || skey >= k1) continue;
+          const int page = skey >> a.log2_bs;
+          if (page - base >= 32) {
+            base += 32;
+            my_id = base + lane <= p_last ? bt[base + lane] : -1;
+          }
+          const int id = __shfl_sync(0xffffffffu, my_id, page - base);
           if (id < 0 || id >= a.num_blocks) {
-            atomicOr(a.err, KVQ_DEVERR_BLOCK_ID);
+            if (lane == 0) atomicOr(a.err, KVQ_DEVERR_BLOCK_ID);
             continue;
           }
           blk[s] = id;
           bytes += (uint32_t)seg_rows * (2 * Gm::DP + (k_row ? 4 : 0) + (v_row ? 4 : 0));
         }
-        uint8_t* st = ring + (size_t)stage * Gm::STAGE_STRIDE;
-        ptx::mbar_arrive_expect_tx(&bar_full[stage], bytes);
-        for (int s = 0; s < n_seg; ++s) {
-          if (blk[s] < 0) continue;
-          const int row0 = (key0 + s * seg_rows) & (a.block_size - 1);
+        if (lane == 0) {
+          uint8_t* st = ring + (size_t)stage * Gm::STAGE_STRIDE;
+          ptx::mbar_arrive_expect_tx(&bar_full[stage], bytes);
 #pragma unroll
-          for (int sl = 0; sl < Gm::SLABS; ++sl) {
-            uint8_t* dk = st + sl * (kTile * Gm::SPAN) + s * seg_rows * Gm::SPAN;
-            ptx::tma_load_4d(dk, &tmk, sl * Gm::SPAN, row0, h, blk[s], &bar_full[stage]);
-            ptx::tma_load_4d(dk + Gm::CODE_BYTES, &tmv, sl * Gm::SPAN, row0, h, blk[s], &bar_full[stage]);
+          for (int s = 0; s < kTile / 16; ++s) {
+            if (blk[s] < 0) continue;
+            const int row0 = (key0 + s * seg_rows) & (a.block_size - 1);
+#pragma unroll
+            for (int sl = 0; sl < Gm::SLABS; ++sl) {
+              uint8_t* dk = st + sl * (kTile * Gm::SPAN) + s * seg_rows * Gm::SPAN;
+              ptx::tma_load_4d(dk, &tmk, sl * Gm::SPAN, row0, h, blk[s], &bar_full[stage]);
+              ptx::tma_load_4d(dk + Gm::CODE_BYTES, &tmv, sl * Gm::SPAN, row0, h, blk[s], &bar_full[stage]);
+            }
+            const size_t srow = ((size_t)blk[s] * Hkv + h) * a.block_size + row0;
+            if (k_row)
+              ptx::bulk_load(st + 2 * Gm::CODE_BYTES + s * seg_rows * 4, a.k_scale + srow, seg_rows * 4,
+                             &bar_full[stage]);
+            if (v_row)
+              ptx::bulk_load(st + 2 * Gm::CODE_BYTES + kTile * 4 + s * seg_rows * 4, a.v_scale + srow,
+                             seg_rows * 4, &bar_full[stage]);
           }
-          const size_t srow = ((size_t)blk[s] * Hkv + h) * a.block_size + row0;
-          if (k_row)
-            ptx::bulk_load(st + 2 * Gm::CODE_BYTES + s * seg_rows * 4, a.k_scale + srow, seg_rows * 4,
-                           &bar_full[stage]);
-          if (v_row)
-            ptx::bulk_load(st + 2 * Gm::CODE_BYTES + kTile * 4 + s * seg_rows * 4, a.v_scale + srow,
-                           seg_rows * 4, &bar_full[stage]);
         }
+        __syncwarp();
       }
     }
-    // let every copy this thread issued land before the CTA can exit
-    const uint32_t S = (uint32_t)a.stages;
-    for (uint32_t s = 0; s < S && s < it; ++s) {
-      const uint32_t last = it - 1 - ((it - 1 - s) % S);
-      if (!ptx::mbar_wait_bounded(&bar_full[s], (last / S) & 1)) atomicOr(a.err, KVQ_DEVERR_TIMEOUT);
+    // let every copy this warp issued land before the CTA can exit
+    if (lane == 0) {
+      for (uint32_t s = 0; s < S && s < it; ++s) {
+        const uint32_t last = it - 1 - ((it - 1 - s) % S);
+        if (!ptx::mbar_wait_bounded(&bar_full[s], (last / S) & 1)) atomicOr(a.err, KVQ_DEVERR_TIMEOUT);
+      }
     }
     return;
   }
@@ -317,9 +330,9 @@ __global__ void __launch_bounds__(288, MINB)
   uint32_t it = 0;
   bool ok = true;
 
-  for (int u = blockIdx.x; u < total_units; u += gridDim.x) {
-    int b, h, k0, k1, L;
-    unit_info(u, b, h, k0, k1, L);
+  for (int gt = t_begin, next; gt < t_end; gt = next) {
+    int b, h, k0, k1, L, u;
+    piece(gt, b, h, k0, k1, L, u, next);
 
     // ---- Q prologue: this lane's channels of query row g of the row group
     constexpr int CPL = (DT == KVQ_INT4) ? 8 : 4;  // channels per 16-byte code chunk per lane
@@ -489,7 +502,7 @@ __global__ void __launch_bounds__(288, MINB)
                       (sa[3] + sb[3]) * al1 * ksb};
         if (softcap > 0.0f) {
 #pragma unroll
-          for (int e = 0; e < 4; ++e) x[e] = softcap * tanhf(x[e] * inv_cap) * kLog2e;
+          for (int e = 0; e < 4; ++e) x[e] = softcap * dev::tanh_fast(x[e] * inv_cap) * kLog2e;
         }
         const bool va0 = key_a <= pos0 && (W == 0 || key_a > pos0 - W);
         const bool va1 = key_a <= pos1 && (W == 0 || key_a > pos1 - W);

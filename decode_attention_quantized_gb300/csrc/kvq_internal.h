@@ -15,7 +15,6 @@ namespace kvq {
 
 constexpr int kTile = 64;       // keys per pipeline stage (4 sub-tiles of 16)
 constexpr int kSub = 16;        // keys per MMA sub-tile
-constexpr int kWaves = 2;       // target work units per persistent CTA
 constexpr int kMaxBatch = 1024; // sequences whose split plan fits in shared memory
 constexpr int kMaxStages = 8;
 
@@ -45,10 +44,10 @@ struct DecodeArgs {
   float sm_scale, softcap;
   int window;
   int row_groups, key_warps, stages;
-  int units_max;
-  int* plan;        // workspace: [0] chunk, [1] items, [2] batch, [3] units_max, then prefix[B+1]
-  float* part_lse;  // [units_max, rows]   base-2 log-sum-exp of each split
-  float* part_o;    // [units_max, rows, D] normalized split output
+  int units_max;    // partial slots (grid + batch * Hkv)
+  int* plan;        // workspace: [0] tiles per CTA, [1] total tiles, [2] batch, [3] slots, then tile prefix[B+1]
+  float* part_lse;  // [units_max, rows]   base-2 log-sum-exp of each piece
+  float* part_o;    // [units_max, rows, D] normalized piece output
   unsigned int* err;
 };
 

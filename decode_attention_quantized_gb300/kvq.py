@@ -19,7 +19,7 @@ from .build import LIB_PATH
 
 INT8, FP8_E4M3, INT4 = 1, 2, 3
 PER_ROW, PER_TENSOR, PER_CHANNEL = 1, 2, 3
-DEVERR_SLOT, DEVERR_BLOCK_ID, DEVERR_SEQ_LEN, DEVERR_TIMEOUT, DEVERR_PLAN = 0x1, 0x2, 0x4, 0x8, 0x10
+DEVERR_SLOT, DEVERR_BLOCK_ID, DEVERR_SEQ_LEN, DEVERR_TIMEOUT = 0x1, 0x2, 0x4, 0x8
 STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "workspace too small", 4: "CUDA error",
           5: "device timeout"}
 

@@ -90,7 +90,6 @@ typedef enum {
 #define KVQ_DEVERR_BLOCK_ID 0x2u  /* decode: block_table entry outside [0, num_blocks) */
 #define KVQ_DEVERR_SEQ_LEN 0x4u   /* decode: seq_len < 0, > capacity, or > max_seq_len */
 #define KVQ_DEVERR_TIMEOUT 0x8u   /* a bounded pipeline wait gave up */
-#define KVQ_DEVERR_PLAN 0x10u     /* decode: split plan exceeded the workspace bound (not expected) */
 
 /* The paged cache: one descriptor per layer (kv-quant-attn "Usage": one cache
  * object per layer).  All pointers are device memory owned by the caller.
