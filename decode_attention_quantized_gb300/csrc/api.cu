@@ -97,7 +97,7 @@ kvq_status check_params(const kvq_cache* c, const kvq_decode_params* p) {
 
 // Launch shape of the decode kernel and the workspace it implies.
 struct Plan {
-  int rows, row_groups, key_warps, threads, stages, grid, units_max;
+  int rows, row_groups, key_warps, nt, threads, stages, grid, units_max;
   size_t smem, ws_plan, ws_lse, ws_o, ws_total;
 };
 
@@ -108,19 +108,22 @@ size_t stage_stride(const kvq_cache* c) {
   return (2 * code + 2 * kTile * 4 + 1023) / 1024 * 1024;
 }
 
-size_t fixed_smem(const kvq_cache* c, int row_groups, int key_warps, int batch, int stages) {
+size_t fixed_smem(const kvq_cache* c, int row_groups, int key_warps, int nt, int batch, int stages) {
   size_t s = 1024;  // alignment slack of the ring
-  if (key_warps > 1) s += (size_t)row_groups * (c->head_dim / 16 * 4 + 4) * 32 * 4;  // merge slot per row group
+  if (nt > 0)  // wide layout: P buffer, row maxima / sums, Q operand, logit factors
+    s += (size_t)(16 * nt * 32 + 2 * 4 * 16 * nt + 32 + 16 * nt * (c->head_dim / 2) + (16 * nt + 31) / 32 * 32) * 4;
+  else if (key_warps > 1)
+    s += (size_t)row_groups * (c->head_dim / 16 * 4 + 4) * 32 * 4;  // merge slot per row group
   s += ((size_t)batch + 5 + ((batch + 5) & 1)) * 4;                                  // split plan
   s += (size_t)stages * 2 * 8;                                                       // mbarriers
   return s;
 }
 
-cudaError_t occupancy(const kvq_cache* c, int threads, size_t smem, int* n) {
+cudaError_t occupancy(const kvq_cache* c, int nt, int threads, size_t smem, int* n) {
   switch (c->dtype) {
-    case KVQ_INT8: return occupancy_decode_int8(c->head_dim, threads, smem, n);
-    case KVQ_FP8_E4M3: return occupancy_decode_fp8(c->head_dim, threads, smem, n);
-    default: return occupancy_decode_int4(c->head_dim, threads, smem, n);
+    case KVQ_INT8: return occupancy_decode_int8(c->head_dim, nt, threads, smem, n);
+    case KVQ_FP8_E4M3: return occupancy_decode_fp8(c->head_dim, nt, threads, smem, n);
+    default: return occupancy_decode_int4(c->head_dim, nt, threads, smem, n);
   }
 }
 
@@ -130,6 +133,14 @@ kvq_status make_plan_uncached(const kvq_cache* c, const kvq_decode_params* p, co
   P.rows = G * p->q_tokens;
   P.row_groups = (P.rows + 7) / 8;
   P.key_warps = P.row_groups <= 2 ? 4 : (P.row_groups <= 4 ? 2 : 1);
+  // 17..48 rows (e.g. drafts x GQA group): the wide layout, 4 key quarters x 2
+  // row halves of nt n-tiles, when a channel quarter spans >= 2 code chunks
+  const bool wide_fits = c->dtype == KVQ_INT4 ? c->head_dim == 256 : c->head_dim >= 128;
+  P.nt = (wide_fits && P.row_groups >= 3 && P.row_groups <= 6) ? (P.row_groups + 1) / 2 : 0;
+  if (P.nt > 0) {
+    P.row_groups = 2;
+    P.key_warps = 4;
+  }
   const int n_cw = P.row_groups * P.key_warps;
   P.threads = 32 * (n_cw + 1);
   const int B = p->batch > 0 ? p->batch : 1;
@@ -140,14 +151,14 @@ kvq_status make_plan_uncached(const kvq_cache* c, const kvq_decode_params* p, co
   for (int target : {4, 3, 2, 1}) {
     // per-SM shared memory is 228 KiB with 1 KiB reserved per resident CTA
     const size_t budget = (size_t)228 * 1024 / target - 1024;
-    const size_t fixed = fixed_smem(c, P.row_groups, P.key_warps, B, 0);
+    const size_t fixed = fixed_smem(c, P.row_groups, P.key_warps, P.nt, B, 0);
     const int min_stages = target > 1 ? 3 : 2;
     if (fixed + (size_t)min_stages * (stride + 16) > budget) continue;
     int stages = (int)((budget - fixed) / (stride + 16));
     stages = stages > kMaxStages ? kMaxStages : stages;
-    const size_t smem = fixed_smem(c, P.row_groups, P.key_warps, B, stages) + (size_t)stages * stride;
+    const size_t smem = fixed_smem(c, P.row_groups, P.key_warps, P.nt, B, stages) + (size_t)stages * stride;
     int n = 0;
-    if (occupancy(c, P.threads, smem, &n) != cudaSuccess) return KVQ_ERR_CUDA;
+    if (occupancy(c, P.nt, P.threads, smem, &n) != cudaSuccess) return KVQ_ERR_CUDA;
     if (n >= target) {
       occ = target;
       P.stages = stages;
@@ -355,9 +366,9 @@ KVQ_API kvq_status kvq_decode(const kvq_cache* cache, const kvq_decode_params* p
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e;
   switch (cache->dtype) {
-    case KVQ_INT8: e = launch_decode_int8(cache->head_dim, tk, tv, a, P.grid, P.threads, P.smem, st); break;
-    case KVQ_FP8_E4M3: e = launch_decode_fp8(cache->head_dim, tk, tv, a, P.grid, P.threads, P.smem, st); break;
-    default: e = launch_decode_int4(cache->head_dim, tk, tv, a, P.grid, P.threads, P.smem, st); break;
+    case KVQ_INT8: e = launch_decode_int8(cache->head_dim, P.nt, tk, tv, a, P.grid, P.threads, P.smem, st); break;
+    case KVQ_FP8_E4M3: e = launch_decode_fp8(cache->head_dim, P.nt, tk, tv, a, P.grid, P.threads, P.smem, st); break;
+    default: e = launch_decode_int4(cache->head_dim, P.nt, tk, tv, a, P.grid, P.threads, P.smem, st); break;
   }
   return from_cuda(e);
 }

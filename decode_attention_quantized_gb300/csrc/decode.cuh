@@ -34,6 +34,8 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <type_traits>
+
 #include "kvq_internal.h"
 #include "ptx.cuh"
 
@@ -112,9 +114,105 @@ __device__ __forceinline__ int out_channel(int mt, int e, int g) {
     return 16 * mt + 2 * g + (e >> 1);
 }
 
+// Q operand of one query row rq (of the (b, h) work piece) for lane group c:
+// the lane's channels in the MMA B-fragment permutation, per-channel K scale
+// folded in under a power-of-two normaliser (|q * s| <= |q|), the row then
+// normalised by the power of two just above its max so the f16 operand keeps
+// its full mantissa.  Returns the logit factor for the row (sm_scale, tensor
+// scale, e4m3 2^8, both powers of two; times log2 e when no softcap follows),
+// clamped to FLT_MAX so zero codes under a huge scale stay zero.  Rows past
+// a.rows get q = 0.  Every lane of the warp must call it.
+template <int DT, int D>
+__device__ __forceinline__ float q_prologue(const DecodeArgs& a, int rq, int b, int h, int c,
+                                            uint32_t (&qf)[D / 16][2]) {
+  constexpr float kLog2e = 1.4426950408889634f;
+  constexpr int CPL = (DT == KVQ_INT4) ? 8 : 4;  // channels per 16-byte code chunk per lane
+  constexpr int NQC = D / (4 * CPL);             // code chunks per row
+  const int G = a.group, T = a.q_tokens, Hq = a.num_q_heads;
+  const bool qvalid = rq < a.rows;
+  const int tq = qvalid ? rq / G : 0, gq = qvalid ? rq % G : 0;
+  const uint16_t* qp = a.q + (((size_t)b * T + tq) * Hq + (size_t)h * G + gq) * D;
+  float qv[NQC][CPL];
+#pragma unroll
+  for (int j = 0; j < NQC; ++j) {
+    const int ch0 = j * 4 * CPL + c * CPL;
+    if constexpr (CPL == 8) {
+      const uint4 w = qvalid ? *reinterpret_cast<const uint4*>(qp + ch0) : make_uint4(0, 0, 0, 0);
+      const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        qv[j][2 * i] = __uint_as_float(ww[i] << 16);
+        qv[j][2 * i + 1] = __uint_as_float(ww[i] & 0xFFFF0000u);
+      }
+    } else {
+      const uint2 w = qvalid ? *reinterpret_cast<const uint2*>(qp + ch0) : make_uint2(0, 0);
+      qv[j][0] = __uint_as_float(w.x << 16);
+      qv[j][1] = __uint_as_float(w.x & 0xFFFF0000u);
+      qv[j][2] = __uint_as_float(w.y << 16);
+      qv[j][3] = __uint_as_float(w.y & 0xFFFF0000u);
+    }
+  }
+  int e_tot = 0;
+  if (a.k_mode == KVQ_SCALE_PER_CHANNEL) {
+    const float* ks = a.k_scale + (size_t)h * D;
+    float km = 0.0f;
+#pragma unroll
+    for (int j = 0; j < NQC; ++j)
+#pragma unroll
+      for (int i = 0; i < CPL; ++i) km = fmaxf(km, fabsf(ks[j * 4 * CPL + c * CPL + i]));
+    km = fmaxf(km, __shfl_xor_sync(0xffffffffu, km, 1));
+    km = fmaxf(km, __shfl_xor_sync(0xffffffffu, km, 2));
+    const int ek = km > 0.0f ? min(126, max(-126, ceil_log2(km))) : 0;
+    const float sk = pow2i(-ek);
+#pragma unroll
+    for (int j = 0; j < NQC; ++j)
+#pragma unroll
+      for (int i = 0; i < CPL; ++i) qv[j][i] *= ks[j * 4 * CPL + c * CPL + i] * sk;
+    e_tot += ek;
+  }
+  float qm = 0.0f;
+#pragma unroll
+  for (int j = 0; j < NQC; ++j)
+#pragma unroll
+    for (int i = 0; i < CPL; ++i) qm = fmaxf(qm, fabsf(qv[j][i]));
+  qm = fmaxf(qm, __shfl_xor_sync(0xffffffffu, qm, 1));
+  qm = fmaxf(qm, __shfl_xor_sync(0xffffffffu, qm, 2));
+  const int eq = qm > 0.0f ? min(126, max(-126, ceil_log2(qm))) : 0;
+  const float sq = pow2i(-eq);
+  e_tot += eq;
+#pragma unroll
+  for (int j = 0; j < NQC; ++j) {
+    if constexpr (DT == KVQ_INT4) {
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+        qf[2 * j + t][0] = pack_h2(qv[j][2 * t] * sq, qv[j][2 * t + 4] * sq);
+        qf[2 * j + t][1] = pack_h2(qv[j][2 * t + 1] * sq, qv[j][2 * t + 5] * sq);
+      }
+    } else {
+      qf[j][0] = pack_h2(qv[j][0] * sq, qv[j][1] * sq);
+      qf[j][1] = pack_h2(qv[j][2] * sq, qv[j][3] * sq);
+    }
+  }
+  float base = a.sm_scale;
+  if (a.k_mode == KVQ_SCALE_PER_TENSOR) base *= a.k_scale[0];
+  if constexpr (DT == KVQ_FP8_E4M3) base *= 256.0f;
+  float alpha = ldexpf(base, e_tot);
+  if (a.softcap <= 0.0f) alpha *= kLog2e;
+  return fminf(alpha, 3.4028234e38f);
+}
+
 }  // namespace dev
 
-template <int DT, int D, int MINB>
+// Shared floats of the wide consumer layout with NT n-tiles per row half: the
+// P buffer ([16 NT rows][64 keys] f16 = 16 NT x 32 floats), per-quarter row
+// maxima and row sums ([4][16 NT] each), per-quarter V-scale maxima (+ pad to
+// 32), the Q operand ([16 NT rows][D] f16) and the rows' logit factors (+ pad).
+template <int NT, int D>
+__host__ __device__ constexpr int wide_scratch_floats() {
+  return NT > 0 ? 16 * NT * 32 + 2 * 4 * 16 * NT + 32 + 16 * NT * (D / 2) + ((16 * NT + 31) / 32) * 32 : 0;
+}
+
+template <int DT, int D, int MINB, int NT>
 __global__ void __launch_bounds__(288, MINB)
     decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                   const DecodeArgs a) {
@@ -127,7 +225,8 @@ __global__ void __launch_bounds__(288, MINB)
   const int n_cw = a.row_groups * a.key_warps;
   constexpr int kScrPerRg = (Gm::NMT * 4 + 4) * 32;  // floats: accumulators + (m, l) of one warp, [elem][lane]
   float* scr = reinterpret_cast<float*>(ring + (size_t)a.stages * Gm::STAGE_STRIDE);
-  const int scr_floats = a.key_warps > 1 ? a.row_groups * kScrPerRg : 0;
+  const int scr_floats =
+      NT > 0 ? wide_scratch_floats<NT, D>() : (a.key_warps > 1 ? a.row_groups * kScrPerRg : 0);
   int* pl_pre = reinterpret_cast<int*>(scr + scr_floats);  // [B + 1]
   int* pl_misc = pl_pre + a.batch + 1;                     // [4]
   uint64_t* bar_full = reinterpret_cast<uint64_t*>(pl_misc + 4 + ((a.batch + 5) & 1));
@@ -316,7 +415,393 @@ __global__ void __launch_bounds__(288, MINB)
     return;
   }
 
-  // =============================================================== consumers
+  if constexpr (NT > 0) {
+    // ======================================================= wide consumers
+    // For many query rows (17..48: drafts x GQA group).  8 warps = 4 key
+    // quarters kq x 2 row halves rh of NT x 8 rows.  QK: warp (kq, rh) scores
+    // keys [16 kq, 16 kq + 16) of each tile against its rows (each code is
+    // converted by 2 warps, not by every row group); the per-row tile maxima
+    // meet in shared memory so every warp applies the same running maximum;
+    // P goes to a swizzled shared buffer; PV: warp (kq, rh) accumulates
+    // channel quarter kq of its rows over all 64 keys.  The warps' outputs are
+    // disjoint, so the end of a piece only sums the row sums.
+    constexpr int RW = NT * 8, ROWS = 2 * RW;
+    constexpr int QCH = Gm::NCH / 4;                     // code chunks of a channel quarter
+    constexpr int MTW = (DT == KVQ_INT4 ? 2 : 1) * QCH;  // 16-channel tiles of a quarter
+    float* s_max = scr + ROWS * 32;                      // [4][ROWS]
+    float* s_l = s_max + 4 * ROWS;                       // [4][ROWS]
+    float* s_vmax = s_l + 4 * ROWS;                      // [4]
+    const uint32_t p_base = ptx::smem_u32(scr);          // P: [ROWS][64 keys] f16, 128-byte rows
+    float* s_q = s_vmax + 32;                            // Q: [ROWS][D] f16 in MMA k-slot order
+    const uint32_t q_base = ptx::smem_u32(s_q);
+    float* s_alpha = s_q + ROWS * (D / 2);               // [ROWS] logit factors
+    const int rh = warp & 1, kq = warp >> 1;
+    const int g = lane >> 2, c = lane & 3;
+    const int G = a.group, W = a.window;
+    const float softcap = a.softcap;
+    const float inv_cap = softcap > 0.0f ? 1.0f / softcap : 0.0f;
+    const int ld_key = ((lane >> 3) & 1) * 8 + (lane & 7);
+    const int ld_chunk = lane >> 4;
+    // byte offset of P[row][key]: the 16-byte chunk index XOR (row & 7)
+    auto p_off = [](int row, int key) -> uint32_t {
+      return (uint32_t)(row * 128 + ((((key >> 3) ^ row) & 7) << 4) + (key & 7) * 2);
+    };
+    // byte offset of Q[row][k] (k = 16 * k-step + slot): 2D-byte rows, the
+    // low three bits of the 16-byte chunk index XOR (row & 7)
+    auto q_off = [](int row, int k) -> uint32_t {
+      return (uint32_t)(row * 2 * D + ((((k >> 3) & ~7) | (((k >> 3) ^ row) & 7)) << 4) + (k & 7) * 2);
+    };
+    uint32_t it = 0;
+    bool ok = true;
+    for (int gt = t_begin, next; gt < t_end; gt = next) {
+      int b, h, k0, k1, L, u;
+      piece(gt, b, h, k0, k1, L, u, next);
+      // Q of n-tile kq of this half (warps kq < NT), stored in k-slot order so
+      // that ldmatrix yields the B fragments; the rows' logit factors beside it
+      if (kq < NT) {
+        uint32_t qf[Gm::NMT][2];
+        const int row = rh * RW + kq * 8 + g;
+        const float ag = dev::q_prologue<DT, D>(a, row, b, h, c, qf);
+#pragma unroll
+        for (int ks = 0; ks < Gm::NMT; ++ks) {
+          ptx::st_shared_u32(q_base + q_off(row, ks * 16 + 2 * c), qf[ks][0]);
+          ptx::st_shared_u32(q_base + q_off(row, ks * 16 + 8 + 2 * c), qf[ks][1]);
+        }
+        if (c == 0) s_alpha[row] = ag;
+      }
+      ptx::named_bar_sync(1, 8 * 32);
+      float al[NT][2], m[NT][2], l[NT][2];
+      int pos[NT][2];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          const int r = rh * RW + nt * 8 + 2 * c + i;
+          al[nt][i] = s_alpha[r];
+          pos[nt][i] = r < a.rows ? L - T + r / G : -1;
+          m[nt][i] = -INFINITY;
+          l[nt][i] = 0.0f;
+        }
+      }
+      int F = v_row ? -126 : 0;  // V-scale normaliser exponent, the same in every warp
+      float acc[MTW][NT][4];
+#pragma unroll
+      for (int mt = 0; mt < MTW; ++mt)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) acc[mt][nt][0] = acc[mt][nt][1] = acc[mt][nt][2] = acc[mt][nt][3] = 0.0f;
+
+      for (int key0 = k0; key0 < k1; key0 += kTile, ++it) {
+        const int stage = (int)(it % (uint32_t)a.stages);
+        if (ok) {
+          ok = ptx::mbar_wait_bounded(&bar_full[stage], (it / a.stages) & 1);
+          if (!ok) atomicOr(a.err, KVQ_DEVERR_TIMEOUT);
+        }
+        const uint8_t* st = ring + (size_t)stage * Gm::STAGE_STRIDE;
+        const uint32_t sk_base = ptx::smem_u32(st);
+        const uint32_t sv_base = sk_base + Gm::CODE_BYTES;
+        const float* ks_row = reinterpret_cast<const float*>(st + 2 * Gm::CODE_BYTES);
+        const float* vs_row = ks_row + kTile;
+
+        // ---- phase A: scores of this warp's 16 keys x NT n-tiles of rows
+        const int kb = key0 + kq * kSub;
+        const bool active = ok && kb < k1;
+        const int key_a = kb + g, key_b = key_a + 8;
+        float x[NT][4];
+        float vpa = 0.0f, vpb = 0.0f;
+        if (active) {
+          float sacc[NT][4];
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) sacc[nt][0] = sacc[nt][1] = sacc[nt][2] = sacc[nt][3] = 0.0f;
+          const uint32_t row_off = (uint32_t)(kq * kSub + ld_key) * Gm::SPAN;
+          // B fragments of k-step ks for every n-tile of this half, from Q
+          auto qfrag = [&](int ks, uint32_t (&bq)[NT][2]) {
+            const int mi = lane >> 3;
+#pragma unroll
+            for (int np = 0; np < NT / 2; ++np) {
+              const int row = rh * RW + (2 * np + (mi >> 1)) * 8 + (lane & 7);
+              uint32_t R[4];
+              ptx::ldmatrix_x4(R, q_base + q_off(row, ks * 16 + (mi & 1) * 8));
+              bq[2 * np][0] = R[0];
+              bq[2 * np][1] = R[1];
+              bq[2 * np + 1][0] = R[2];
+              bq[2 * np + 1][1] = R[3];
+            }
+            if constexpr (NT % 2 == 1) {
+              const int row = rh * RW + (NT - 1) * 8 + (lane & 7);
+              uint32_t R[2];
+              ptx::ldmatrix_x2(R, q_base + q_off(row, ks * 16 + (mi & 1) * 8));
+              bq[NT - 1][0] = R[0];
+              bq[NT - 1][1] = R[1];
+            }
+          };
+#pragma unroll
+          for (int kk = 0; kk < Gm::NCH / 2; ++kk) {
+            const uint32_t byte = (uint32_t)(2 * kk + ld_chunk) * 16;
+            const uint32_t addr =
+                sk_base + (byte / Gm::SPAN) * (kTile * Gm::SPAN) + dev::swz<Gm::SPAN>(row_off + byte % Gm::SPAN);
+            uint32_t R[4];
+            ptx::ldmatrix_x4(R, addr);
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2) {
+              const int j = 2 * kk + h2;
+              const uint32_t wl = R[2 * h2], wh = R[2 * h2 + 1];
+              if constexpr (DT == KVQ_INT4) {
+                const uint32_t xl = wl ^ 0x88888888u, xh = wh ^ 0x88888888u;
+#pragma unroll
+                for (int t = 0; t < 2; ++t) {
+                  const uint32_t A[4] = {dev::i4pair(xl, 8 * t), dev::i4pair(xh, 8 * t),
+                                         dev::i4pair(xl, 8 * t + 4), dev::i4pair(xh, 8 * t + 4)};
+                  uint32_t bq[NT][2];
+                  qfrag(2 * j + t, bq);
+#pragma unroll
+                  for (int nt = 0; nt < NT; ++nt) ptx::mma_16816(sacc[nt], A, bq[nt][0], bq[nt][1]);
+                }
+              } else {
+                uint32_t A[4];
+                if constexpr (DT == KVQ_INT8) {
+                  const uint32_t xl = wl ^ 0x80808080u, xh = wh ^ 0x80808080u;
+                  A[0] = dev::i8pair(xl, 0x4140u);
+                  A[1] = dev::i8pair(xh, 0x4140u);
+                  A[2] = dev::i8pair(xl, 0x4342u);
+                  A[3] = dev::i8pair(xh, 0x4342u);
+                } else {
+                  A[0] = dev::f8pair(wl, 0x1404u);
+                  A[1] = dev::f8pair(wh, 0x1404u);
+                  A[2] = dev::f8pair(wl, 0x3424u);
+                  A[3] = dev::f8pair(wh, 0x3424u);
+                }
+                uint32_t bq[NT][2];
+                qfrag(j, bq);
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) ptx::mma_16816(sacc[nt], A, bq[nt][0], bq[nt][1]);
+              }
+            }
+          }
+          float ksa = 1.0f, ksb = 1.0f;
+          if (k_row) {
+            ksa = ks_row[kq * kSub + g];
+            ksb = ks_row[kq * kSub + g + 8];
+          }
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            x[nt][0] = sacc[nt][0] * al[nt][0] * ksa;
+            x[nt][1] = sacc[nt][1] * al[nt][1] * ksa;
+            x[nt][2] = sacc[nt][2] * al[nt][0] * ksb;
+            x[nt][3] = sacc[nt][3] * al[nt][1] * ksb;
+            if (softcap > 0.0f) {
+#pragma unroll
+              for (int e = 0; e < 4; ++e) x[nt][e] = softcap * dev::tanh_fast(x[nt][e] * inv_cap) * kLog2e;
+            }
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int key = e < 2 ? key_a : key_b, p = pos[nt][e & 1];
+              if (!(key <= p && (W == 0 || key > p - W))) x[nt][e] = -INFINITY;
+            }
+          }
+          if (v_row) {
+            vpa = key_a < L ? vs_row[kq * kSub + g] : 0.0f;
+            vpb = key_b < L ? vs_row[kq * kSub + g + 8] : 0.0f;
+          }
+        } else {
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) x[nt][0] = x[nt][1] = x[nt][2] = x[nt][3] = -INFINITY;
+        }
+        // this warp's per-row maxima over its 16 keys, and its V-scale maximum
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+          for (int i = 0; i < 2; ++i) {
+            float t = fmaxf(x[nt][i], x[nt][i + 2]);
+#pragma unroll
+            for (int o = 4; o < 32; o <<= 1) t = fmaxf(t, __shfl_xor_sync(0xffffffffu, t, o));
+            if (g == 0) s_max[kq * ROWS + rh * RW + nt * 8 + 2 * c + i] = t;
+          }
+        }
+        if (v_row) {
+          float vm = fmaxf(vpa, vpb);
+#pragma unroll
+          for (int o = 4; o < 32; o <<= 1) vm = fmaxf(vm, __shfl_xor_sync(0xffffffffu, vm, o));
+          if (rh == 0 && lane == 0) s_vmax[kq] = vm;
+        }
+        ptx::named_bar_sync(1, 8 * 32);
+
+        // ---- phase B: the running maximum of every row over the 4 quarters
+        float mu[NT][2], corr[NT][2];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+          for (int i = 0; i < 2; ++i) {
+            const int row = rh * RW + nt * 8 + 2 * c + i;
+            float tm = s_max[row];
+#pragma unroll
+            for (int q = 1; q < 4; ++q) tm = fmaxf(tm, s_max[q * ROWS + row]);
+            const float mn = fmaxf(m[nt][i], tm);
+            mu[nt][i] = mn == -INFINITY ? 0.0f : mn;
+            corr[nt][i] = ptx::fast_exp2(m[nt][i] - mu[nt][i]);
+            m[nt][i] = mn;
+          }
+        }
+        float fs = 1.0f, inv = 1.0f;
+        if (v_row) {
+          const float vm = fmaxf(fmaxf(s_vmax[0], s_vmax[1]), fmaxf(s_vmax[2], s_vmax[3]));
+          if (vm > 0.0f) {
+            const int fn = min(126, max(-126, dev::ceil_log2(vm)));
+            if (fn > F) {
+              fs = (F - fn < -126) ? 0.0f : dev::pow2i(F - fn);
+              F = fn;
+            }
+          }
+          inv = dev::pow2i(-F);
+        }
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          const float p0 = ptx::fast_exp2(x[nt][0] - mu[nt][0]), p1 = ptx::fast_exp2(x[nt][1] - mu[nt][1]);
+          const float p2 = ptx::fast_exp2(x[nt][2] - mu[nt][0]), p3 = ptx::fast_exp2(x[nt][3] - mu[nt][1]);
+          l[nt][0] = l[nt][0] * corr[nt][0] + p0 + p2;
+          l[nt][1] = l[nt][1] * corr[nt][1] + p1 + p3;
+          if (active) {
+            const float va = v_row ? vpa * inv : 1.0f, vb = v_row ? vpb * inv : 1.0f;
+            // (keys x rows) -> (row g; keys 2c, 2c+1) of each 8-key half
+            const uint32_t y0 = ptx::movmatrix_trans(dev::pack_h2(p0 * va, p1 * va));
+            const uint32_t y1 = ptx::movmatrix_trans(dev::pack_h2(p2 * vb, p3 * vb));
+            const int row = rh * RW + nt * 8 + g;
+            ptx::st_shared_u32(p_base + p_off(row, kq * kSub + 2 * c), y0);
+            ptx::st_shared_u32(p_base + p_off(row, kq * kSub + 8 + 2 * c), y1);
+          }
+        }
+        {
+          bool one = fs == 1.0f;
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) one = one && corr[nt][0] == 1.0f && corr[nt][1] == 1.0f;
+          if (!__all_sync(0xffffffffu, one)) {
+#pragma unroll
+            for (int mt = 0; mt < MTW; ++mt)
+#pragma unroll
+              for (int nt = 0; nt < NT; ++nt) {
+                acc[mt][nt][0] *= corr[nt][0] * fs;
+                acc[mt][nt][1] *= corr[nt][1] * fs;
+                acc[mt][nt][2] *= corr[nt][0] * fs;
+                acc[mt][nt][3] *= corr[nt][1] * fs;
+              }
+          }
+        }
+        ptx::named_bar_sync(1, 8 * 32);
+
+        // ---- phase C: channel quarter kq of this half's rows over the tile
+        for (int kg = 0; ok && kg < kTile / kSub; ++kg) {
+          if (key0 + kg * kSub >= k1) break;  // that quarter wrote no P this tile
+          uint32_t pb[NT][2];
+          {
+            const int mi = lane >> 3;  // x4: (n-tile pair, key half)
+#pragma unroll
+            for (int np = 0; np < NT / 2; ++np) {
+              const int row = rh * RW + (2 * np + (mi >> 1)) * 8 + (lane & 7);
+              uint32_t R[4];
+              ptx::ldmatrix_x4(R, p_base + p_off(row, kg * kSub + (mi & 1) * 8));
+              pb[2 * np][0] = R[0];
+              pb[2 * np][1] = R[1];
+              pb[2 * np + 1][0] = R[2];
+              pb[2 * np + 1][1] = R[3];
+            }
+            if constexpr (NT % 2 == 1) {
+              const int row = rh * RW + (NT - 1) * 8 + (lane & 7);
+              uint32_t R[2];
+              ptx::ldmatrix_x2(R, p_base + p_off(row, kg * kSub + (mi & 1) * 8));
+              pb[NT - 1][0] = R[0];
+              pb[NT - 1][1] = R[1];
+            }
+          }
+          const uint32_t vrow_off = (uint32_t)(kg * kSub + ld_key) * Gm::SPAN;
+#pragma unroll
+          for (int jj = 0; jj < QCH / 2; ++jj) {
+            const uint32_t byte = (uint32_t)(QCH * kq + 2 * jj + ld_chunk) * 16;
+            const uint32_t addr =
+                sv_base + (byte / Gm::SPAN) * (kTile * Gm::SPAN) + dev::swz<Gm::SPAN>(vrow_off + byte % Gm::SPAN);
+            uint32_t R[4];
+            ptx::ldmatrix_x4_trans(R, addr);
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2) {
+              const int jl = 2 * jj + h2;
+              const uint32_t wl = R[2 * h2], wh = R[2 * h2 + 1];
+              if constexpr (DT == KVQ_INT4) {
+                const uint32_t xl = wl ^ 0x88888888u, xh = wh ^ 0x88888888u;
+#pragma unroll
+                for (int t = 0; t < 2; ++t) {
+                  const uint32_t A[4] = {dev::i4pair(xl, 8 * t), dev::i4pair(xl, 8 * t + 4),
+                                         dev::i4pair(xh, 8 * t), dev::i4pair(xh, 8 * t + 4)};
+#pragma unroll
+                  for (int nt = 0; nt < NT; ++nt) ptx::mma_16816(acc[2 * jl + t][nt], A, pb[nt][0], pb[nt][1]);
+                }
+              } else {
+                uint32_t A[4];
+                if constexpr (DT == KVQ_INT8) {
+                  const uint32_t xl = wl ^ 0x80808080u, xh = wh ^ 0x80808080u;
+                  A[0] = dev::i8pair(xl, 0x4240u);
+                  A[1] = dev::i8pair(xl, 0x4341u);
+                  A[2] = dev::i8pair(xh, 0x4240u);
+                  A[3] = dev::i8pair(xh, 0x4341u);
+                } else {
+                  A[0] = dev::f8pair(wl, 0x2404u);
+                  A[1] = dev::f8pair(wl, 0x3414u);
+                  A[2] = dev::f8pair(wh, 0x2404u);
+                  A[3] = dev::f8pair(wh, 0x3414u);
+                }
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) ptx::mma_16816(acc[jl][nt], A, pb[nt][0], pb[nt][1]);
+              }
+            }
+          }
+        }
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&bar_empty[stage]);
+      }
+
+      // ---- piece end: row sums over the 4 quarters, then each warp writes its
+      // (rows, channel quarter) block of the normalized partial
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          float v = l[nt][i];
+#pragma unroll
+          for (int o = 4; o < 32; o <<= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+          if (g == 0) s_l[kq * ROWS + rh * RW + nt * 8 + 2 * c + i] = v;
+        }
+      ptx::named_bar_sync(1, 8 * 32);
+      float to_true = v_row ? dev::pow2i(F) : 1.0f;
+      if constexpr (DT == KVQ_FP8_E4M3) to_true *= 256.0f;
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        const int r0 = rh * RW + nt * 8 + 2 * c, r1 = r0 + 1;
+        float lt[2];
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          const int row = r0 + i;
+          lt[i] = s_l[row] + s_l[ROWS + row];
+          lt[i] += s_l[2 * ROWS + row];
+          lt[i] += s_l[3 * ROWS + row];
+        }
+        const float f0 = lt[0] > 0.0f ? to_true / lt[0] : 0.0f, f1 = lt[1] > 0.0f ? to_true / lt[1] : 0.0f;
+        float* o0 = a.part_o + ((size_t)u * a.rows + r0) * D;
+        float* o1 = o0 + D;
+#pragma unroll
+        for (int mt = 0; mt < MTW; ++mt) {
+          const int mtg = (DT == KVQ_INT4 ? 2 * QCH * kq : QCH * kq) + mt;
+          const int ch = dev::out_channel<DT>(mtg, 0, g);
+          if (r0 < a.rows) *reinterpret_cast<float2*>(o0 + ch) = make_float2(acc[mt][nt][0] * f0, acc[mt][nt][2] * f0);
+          if (r1 < a.rows) *reinterpret_cast<float2*>(o1 + ch) = make_float2(acc[mt][nt][1] * f1, acc[mt][nt][3] * f1);
+        }
+        if (kq == 0 && g == 0) {
+          if (r0 < a.rows) a.part_lse[(size_t)u * a.rows + r0] = lt[0] > 0.0f ? m[nt][0] + ptx::fast_log2(lt[0]) : -INFINITY;
+          if (r1 < a.rows) a.part_lse[(size_t)u * a.rows + r1] = lt[1] > 0.0f ? m[nt][1] + ptx::fast_log2(lt[1]) : -INFINITY;
+        }
+      }
+      ptx::named_bar_sync(1, 8 * 32);
+    }
+    return;
+  }
+
+  // ============================================ consumers, grouped layout
   const int cw = warp;
   const int rg = cw % a.row_groups, kw = cw / a.row_groups;
   const int g = lane >> 2, c = lane & 3;
@@ -335,87 +820,8 @@ __global__ void __launch_bounds__(288, MINB)
     piece(gt, b, h, k0, k1, L, u, next);
 
     // ---- Q prologue: this lane's channels of query row g of the row group
-    constexpr int CPL = (DT == KVQ_INT4) ? 8 : 4;  // channels per 16-byte code chunk per lane
-    constexpr int NQC = D / (4 * CPL);             // code chunks per row
     uint32_t qf[Gm::NMT][2];
-    float alpha_g;
-    {
-      const int rq = rg * 8 + g;
-      const bool qvalid = rq < a.rows;
-      const int tq = qvalid ? rq / G : 0, gq = qvalid ? rq % G : 0;
-      const uint16_t* qp = a.q + (((size_t)b * T + tq) * Hq + (size_t)h * G + gq) * D;
-      float qv[NQC][CPL];
-#pragma unroll
-      for (int j = 0; j < NQC; ++j) {
-        const int ch0 = j * 4 * CPL + c * CPL;
-        if constexpr (CPL == 8) {
-          const uint4 w = qvalid ? *reinterpret_cast<const uint4*>(qp + ch0) : make_uint4(0, 0, 0, 0);
-          const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            qv[j][2 * i] = __uint_as_float(ww[i] << 16);
-            qv[j][2 * i + 1] = __uint_as_float(ww[i] & 0xFFFF0000u);
-          }
-        } else {
-          const uint2 w = qvalid ? *reinterpret_cast<const uint2*>(qp + ch0) : make_uint2(0, 0);
-          qv[j][0] = __uint_as_float(w.x << 16);
-          qv[j][1] = __uint_as_float(w.x & 0xFFFF0000u);
-          qv[j][2] = __uint_as_float(w.y << 16);
-          qv[j][3] = __uint_as_float(w.y & 0xFFFF0000u);
-        }
-      }
-      int e_tot = 0;
-      if (a.k_mode == KVQ_SCALE_PER_CHANNEL) {
-        // fold the K channel scale into q, normalised by the power of two
-        // just above max|k_scale| so the product cannot overflow
-        const float* ks = a.k_scale + (size_t)h * D;
-        float km = 0.0f;
-#pragma unroll
-        for (int j = 0; j < NQC; ++j)
-#pragma unroll
-          for (int i = 0; i < CPL; ++i) km = fmaxf(km, fabsf(ks[j * 4 * CPL + c * CPL + i]));
-        km = fmaxf(km, __shfl_xor_sync(0xffffffffu, km, 1));
-        km = fmaxf(km, __shfl_xor_sync(0xffffffffu, km, 2));
-        const int ek = km > 0.0f ? min(126, max(-126, dev::ceil_log2(km))) : 0;
-        const float sk = dev::pow2i(-ek);
-#pragma unroll
-        for (int j = 0; j < NQC; ++j)
-#pragma unroll
-          for (int i = 0; i < CPL; ++i) qv[j][i] *= ks[j * 4 * CPL + c * CPL + i] * sk;
-        e_tot += ek;
-      }
-      float qm = 0.0f;
-#pragma unroll
-      for (int j = 0; j < NQC; ++j)
-#pragma unroll
-        for (int i = 0; i < CPL; ++i) qm = fmaxf(qm, fabsf(qv[j][i]));
-      qm = fmaxf(qm, __shfl_xor_sync(0xffffffffu, qm, 1));
-      qm = fmaxf(qm, __shfl_xor_sync(0xffffffffu, qm, 2));
-      const int eq = qm > 0.0f ? min(126, max(-126, dev::ceil_log2(qm))) : 0;
-      const float sq = dev::pow2i(-eq);
-      e_tot += eq;
-#pragma unroll
-      for (int j = 0; j < NQC; ++j) {
-        if constexpr (DT == KVQ_INT4) {
-#pragma unroll
-          for (int t = 0; t < 2; ++t) {
-            qf[2 * j + t][0] = dev::pack_h2(qv[j][2 * t] * sq, qv[j][2 * t + 4] * sq);
-            qf[2 * j + t][1] = dev::pack_h2(qv[j][2 * t + 1] * sq, qv[j][2 * t + 5] * sq);
-          }
-        } else {
-          qf[j][0] = dev::pack_h2(qv[j][0] * sq, qv[j][1] * sq);
-          qf[j][1] = dev::pack_h2(qv[j][2] * sq, qv[j][3] * sq);
-        }
-      }
-      float base = a.sm_scale;
-      if (a.k_mode == KVQ_SCALE_PER_TENSOR) base *= a.k_scale[0];
-      if constexpr (DT == KVQ_FP8_E4M3) base *= 256.0f;
-      alpha_g = ldexpf(base, e_tot);
-      if (softcap <= 0.0f) alpha_g *= kLog2e;
-      // a scale beyond fp32 (e.g. a channel scale near FLT_MAX) stays finite,
-      // so an all-zero code row still gives a zero logit instead of inf * 0
-      alpha_g = fminf(alpha_g, 3.4028234e38f);
-    }
+    const float alpha_g = dev::q_prologue<DT, D>(a, rg * 8 + g, b, h, c, qf);
     const int r0 = rg * 8 + 2 * c, r1 = r0 + 1;
     const float al0 = __shfl_sync(0xffffffffu, alpha_g, (2 * c) * 4);
     const float al1 = __shfl_sync(0xffffffffu, alpha_g, (2 * c + 1) * 4);
@@ -675,7 +1081,7 @@ __global__ void __launch_bounds__(288, MINB)
 // Raises (never lowers) the kernel's dynamic shared-memory limit on the
 // current device; shared by the occupancy query and the launch so that a
 // query for a small plan cannot undercut a larger plan launched later.
-template <int DT, int D, int MINB>
+template <int DT, int D, int MINB, int NT>
 cudaError_t ensure_smem(size_t smem) {
   static int smem_set[64] = {};
   int dev = 0;
@@ -683,46 +1089,64 @@ cudaError_t ensure_smem(size_t smem) {
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (smem_set[dev] < (int)smem) {
-    e = cudaFuncSetAttribute(decode_kernel<DT, D, MINB>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    e = cudaFuncSetAttribute(decode_kernel<DT, D, MINB, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem);
     if (e != cudaSuccess) return e;
     smem_set[dev] = (int)smem;
   }
   return cudaSuccess;
 }
 
-template <int DT, int D, int MINB>
+template <int DT, int D, int MINB, int NT>
 cudaError_t launch_decode_d(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeArgs& a, int grid,
                             int threads, size_t smem, cudaStream_t stream) {
-  cudaError_t e = ensure_smem<DT, D, MINB>(smem);
+  cudaError_t e = ensure_smem<DT, D, MINB, NT>(smem);
   if (e != cudaSuccess) return e;
-  decode_kernel<DT, D, MINB><<<grid, threads, smem, stream>>>(tk, tv, a);
+  decode_kernel<DT, D, MINB, NT><<<grid, threads, smem, stream>>>(tk, tv, a);
   return cudaGetLastError();
 }
 
-template <int DT, int D, int MINB>
+template <int DT, int D, int MINB, int NT>
 cudaError_t occupancy_decode_d(int threads, size_t smem, int* blocks_per_sm) {
-  cudaError_t e = ensure_smem<DT, D, MINB>(smem);
+  cudaError_t e = ensure_smem<DT, D, MINB, NT>(smem);
   if (e != cudaSuccess) return e;
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, decode_kernel<DT, D, MINB>, threads, smem);
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, decode_kernel<DT, D, MINB, NT>, threads,
+                                                       smem);
 }
 
-template <int DT>
-cudaError_t launch_decode_t(int head_dim, const CUtensorMap& tk, const CUtensorMap& tv, const DecodeArgs& a,
-                            int grid, int threads, size_t smem, cudaStream_t stream) {
-  switch (head_dim) {
-    case 64: return launch_decode_d<DT, 64, 2>(tk, tv, a, grid, threads, smem, stream);
-    case 128: return launch_decode_d<DT, 128, 2>(tk, tv, a, grid, threads, smem, stream);
-    case 256: return launch_decode_d<DT, 256, 1>(tk, tv, a, grid, threads, smem, stream);
-    default: return cudaErrorInvalidValue;
-  }
-}
+// The wide layout needs a channel quarter of at least two 16-byte code chunks.
+template <int DT, int D>
+constexpr bool wide_ok() { return Geo<DT, D>::NCH >= 8; }
 
-template <int DT>
-cudaError_t occupancy_decode_t(int head_dim, int threads, size_t smem, int* blocks_per_sm) {
+template <int D_, int MINB_, int NT_>
+struct KernelCfg {
+  static constexpr int d = D_, minb = MINB_, nt = NT_;
+};
+
+// Dispatch on head_dim and on nt (0: grouped layout; 2, 3: wide layout).
+template <int DT, bool Query>
+cudaError_t dispatch_decode(int head_dim, int nt, const CUtensorMap* tk, const CUtensorMap* tv, const DecodeArgs* a,
+                            int grid, int threads, size_t smem, cudaStream_t stream, int* blocks_per_sm) {
+  auto go = [&](auto cfg) -> cudaError_t {
+    using K = decltype(cfg);
+    if constexpr (Query)
+      return occupancy_decode_d<DT, K::d, K::minb, K::nt>(threads, smem, blocks_per_sm);
+    else
+      return launch_decode_d<DT, K::d, K::minb, K::nt>(*tk, *tv, *a, grid, threads, smem, stream);
+  };
+  auto by_nt = [&](auto dtag) -> cudaError_t {
+    constexpr int d = decltype(dtag)::value;
+    if (nt == 0) return go(KernelCfg<d, d == 256 ? 1 : 2, 0>{});
+    if constexpr (wide_ok<DT, d>()) {
+      if (nt == 2) return go(KernelCfg<d, 1, 2>{});
+      if (nt == 3) return go(KernelCfg<d, 1, 3>{});
+    }
+    return cudaErrorInvalidValue;
+  };
   switch (head_dim) {
-    case 64: return occupancy_decode_d<DT, 64, 2>(threads, smem, blocks_per_sm);
-    case 128: return occupancy_decode_d<DT, 128, 2>(threads, smem, blocks_per_sm);
-    case 256: return occupancy_decode_d<DT, 256, 1>(threads, smem, blocks_per_sm);
+    case 64: return by_nt(std::integral_constant<int, 64>{});
+    case 128: return by_nt(std::integral_constant<int, 128>{});
+    case 256: return by_nt(std::integral_constant<int, 256>{});
     default: return cudaErrorInvalidValue;
   }
 }

@@ -1,17 +1,18 @@
 // decode_fp8.cu -- instantiates the split-KV decode kernel for fp8 cache codes
-// (head_dim 64, 128, 256).  One translation unit per element type keeps the
-// build parallel.
+// (head_dim 64, 128, 256; grouped and, where it applies, wide consumer
+// layouts).  One translation unit per element type keeps the build parallel.
 #include "decode.cuh"
 
 namespace kvq {
 
-cudaError_t launch_decode_fp8(int head_dim, const CUtensorMap& tk, const CUtensorMap& tv, const DecodeArgs& a,
-                             int grid, int threads, size_t smem, cudaStream_t stream) {
-  return launch_decode_t<KVQ_FP8_E4M3>(head_dim, tk, tv, a, grid, threads, smem, stream);
+cudaError_t launch_decode_fp8(int head_dim, int nt, const CUtensorMap& tk, const CUtensorMap& tv,
+                             const DecodeArgs& a, int grid, int threads, size_t smem, cudaStream_t stream) {
+  return dispatch_decode<KVQ_FP8_E4M3, false>(head_dim, nt, &tk, &tv, &a, grid, threads, smem, stream, nullptr);
 }
 
-cudaError_t occupancy_decode_fp8(int head_dim, int threads, size_t smem, int* blocks_per_sm) {
-  return occupancy_decode_t<KVQ_FP8_E4M3>(head_dim, threads, smem, blocks_per_sm);
+cudaError_t occupancy_decode_fp8(int head_dim, int nt, int threads, size_t smem, int* blocks_per_sm) {
+  return dispatch_decode<KVQ_FP8_E4M3, true>(head_dim, nt, nullptr, nullptr, nullptr, 0, threads, smem, nullptr,
+                                   blocks_per_sm);
 }
 
 }  // namespace kvq

@@ -65,15 +65,15 @@ struct CombineArgs {
 
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t stream);
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t stream);
-cudaError_t launch_decode_int8(int head_dim, const CUtensorMap& tk, const CUtensorMap& tv, const DecodeArgs& a,
-                               int grid, int threads, size_t smem, cudaStream_t stream);
-cudaError_t launch_decode_fp8(int head_dim, const CUtensorMap& tk, const CUtensorMap& tv, const DecodeArgs& a,
-                              int grid, int threads, size_t smem, cudaStream_t stream);
-cudaError_t launch_decode_int4(int head_dim, const CUtensorMap& tk, const CUtensorMap& tv, const DecodeArgs& a,
-                               int grid, int threads, size_t smem, cudaStream_t stream);
+cudaError_t launch_decode_int8(int head_dim, int nt, const CUtensorMap& tk, const CUtensorMap& tv,
+                               const DecodeArgs& a, int grid, int threads, size_t smem, cudaStream_t stream);
+cudaError_t launch_decode_fp8(int head_dim, int nt, const CUtensorMap& tk, const CUtensorMap& tv,
+                               const DecodeArgs& a, int grid, int threads, size_t smem, cudaStream_t stream);
+cudaError_t launch_decode_int4(int head_dim, int nt, const CUtensorMap& tk, const CUtensorMap& tv,
+                               const DecodeArgs& a, int grid, int threads, size_t smem, cudaStream_t stream);
 
-cudaError_t occupancy_decode_int8(int head_dim, int threads, size_t smem, int* blocks_per_sm);
-cudaError_t occupancy_decode_fp8(int head_dim, int threads, size_t smem, int* blocks_per_sm);
-cudaError_t occupancy_decode_int4(int head_dim, int threads, size_t smem, int* blocks_per_sm);
+cudaError_t occupancy_decode_int8(int head_dim, int nt, int threads, size_t smem, int* blocks_per_sm);
+cudaError_t occupancy_decode_fp8(int head_dim, int nt, int threads, size_t smem, int* blocks_per_sm);
+cudaError_t occupancy_decode_int4(int head_dim, int nt, int threads, size_t smem, int* blocks_per_sm);
 
 }  // namespace kvq

@@ -170,3 +170,30 @@ def test_bad_block_id_and_seq_len_are_flagged_not_faulted(lib):
     out, _ = kvq.decode_step(gw.cache, params, q, gw.block_table, gw.seq_lens, bufs)
     torch.cuda.synchronize()
     assert torch.isfinite(out.float()).all()
+
+
+WIDE = [
+    # dtype, D, G, T, k_mode, v_mode, softcap, window, sink   (rows = G*T in 17..48)
+    (kvq.INT8, 128, 3, 6, kvq.PER_ROW, kvq.PER_ROW, 0.0, 0, False),
+    (kvq.FP8_E4M3, 256, 4, 7, kvq.PER_TENSOR, kvq.PER_TENSOR, 20.0, 0, False),
+    (kvq.INT4, 256, 5, 7, kvq.PER_ROW, kvq.PER_ROW, 0.0, 0, True),
+    (kvq.INT8, 256, 8, 5, kvq.PER_CHANNEL, kvq.PER_ROW, 0.0, 100, True),
+    (kvq.INT4, 256, 6, 8, kvq.PER_CHANNEL, kvq.PER_CHANNEL, 0.0, 0, False),
+    (kvq.FP8_E4M3, 128, 8, 6, kvq.PER_ROW, kvq.PER_TENSOR, 0.0, 37, True),
+]
+
+
+@pytest.mark.parametrize("case", WIDE, ids=lambda c: f"dt{c[0]}-D{c[1]}-rows{c[2] * c[3]}")
+def test_many_query_rows_layout(lib, orc, case):
+    """17..48 query rows per kv head (drafts x GQA group) take the layout in
+    which four key quarters share each tile's row maxima and P."""
+    dt, D, G, T, km, vm, cap, W, sink = case
+    Hkv, bs = 2, 32
+    L = np.array([300, T - 2, 129, 64, 1], np.int32)
+    mb = 10
+    w = synth.Workload("wide", dt, km, vm, len(L), G * Hkv, Hkv, D, T, bs, L,
+                       np.random.default_rng(G * T).permutation(len(L) * mb).astype(np.int32).reshape(len(L), mb),
+                       len(L) * mb, softcap=cap, use_sink=sink, k_channel_lognormal=0.5, seed=G * 100 + T)
+    run_case(orc, w)
+    if W:
+        run_case(orc, w, window=W, check_cache=False)
