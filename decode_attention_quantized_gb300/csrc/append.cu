@@ -11,6 +11,7 @@
 #include <cuda_fp8.h>
 
 #include "kvq_internal.h"
+#include "ptx.cuh"
 
 namespace kvq {
 namespace {
@@ -57,6 +58,8 @@ __device__ __forceinline__ void store_bytes(uint8_t* dst, const uint8_t (&b)[NB]
 template <int D>
 __global__ void __launch_bounds__(256) append_kernel(const AppendArgs a) {
   constexpr int E = D / 32;  // channels per lane
+  ptx::griddep_wait();
+  ptx::griddep_launch_dependents();
   const int wg = (int)((blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5);
   const int lane = threadIdx.x & 31;
   if (wg >= a.n_tokens * a.num_kv_heads * 2) return;
@@ -136,12 +139,11 @@ cudaError_t launch_append(const AppendArgs& a, cudaStream_t stream) {
   const long long warps = (long long)a.n_tokens * a.num_kv_heads * 2;
   const unsigned blocks = (unsigned)((warps + 7) / 8);
   switch (a.head_dim) {
-    case 64: append_kernel<64><<<blocks, 256, 0, stream>>>(a); break;
-    case 128: append_kernel<128><<<blocks, 256, 0, stream>>>(a); break;
-    case 256: append_kernel<256><<<blocks, 256, 0, stream>>>(a); break;
+    case 64: return launch_pdl(append_kernel<64>, blocks, 256, 0, stream, a);
+    case 128: return launch_pdl(append_kernel<128>, blocks, 256, 0, stream, a);
+    case 256: return launch_pdl(append_kernel<256>, blocks, 256, 0, stream, a);
     default: return cudaErrorInvalidValue;
   }
-  return cudaGetLastError();
 }
 
 }  // namespace kvq

@@ -29,6 +29,8 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const Combi
   __shared__ float s_acc[kCombineWarps][D];
   __shared__ float s_w[kCombineWarps];
   __shared__ float s_m[kCombineWarps];
+  ptx::griddep_wait();
+  ptx::griddep_launch_dependents();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int row_id = blockIdx.x;
   const int hq = row_id % a.num_q_heads;
@@ -147,12 +149,11 @@ cudaError_t launch_combine(const CombineArgs& a, cudaStream_t stream) {
   const unsigned blocks = (unsigned)((long long)a.batch * a.q_tokens * a.num_q_heads);
   constexpr int threads = kCombineWarps * 32;
   switch (a.head_dim) {
-    case 64: combine_kernel<64><<<blocks, threads, 0, stream>>>(a); break;
-    case 128: combine_kernel<128><<<blocks, threads, 0, stream>>>(a); break;
-    case 256: combine_kernel<256><<<blocks, threads, 0, stream>>>(a); break;
+    case 64: return launch_pdl(combine_kernel<64>, blocks, threads, 0, stream, a);
+    case 128: return launch_pdl(combine_kernel<128>, blocks, threads, 0, stream, a);
+    case 256: return launch_pdl(combine_kernel<256>, blocks, threads, 0, stream, a);
     default: return cudaErrorInvalidValue;
   }
-  return cudaGetLastError();
 }
 
 }  // namespace kvq

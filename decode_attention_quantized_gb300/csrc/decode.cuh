@@ -104,6 +104,40 @@ __device__ __forceinline__ float tanh_fast(float x) {
   return 1.0f - __fdividef(2.0f, ptx::fast_exp2(x * 2.8853900817779268f) + 1.0f);
 }
 
+// Exact e4m3x2 -> f16x2 (hardware conversion; the low byte goes to the low
+// half).  Used for K only: a stale e4m3 NaN byte under a masked key can then
+// only poison that key's own score, which the mask replaces.
+__device__ __forceinline__ uint32_t e4m3x2_f16x2(uint16_t v) {
+  uint32_t d;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(d) : "h"(v));
+  return d;
+}
+
+// A fragment (keys x k-slots) of k-step t of a 16-byte code chunk for QK,
+// from the ldmatrix words of keys g (wl) and g + 8 (wh), every code converted
+// exactly (a zero code must give an exactly zero product whatever the scale).
+template <int DT>
+__device__ __forceinline__ void k_frag(uint32_t wl, uint32_t wh, int t, uint32_t (&A)[4]) {
+  if constexpr (DT == KVQ_INT4) {
+    const uint32_t xl = wl ^ 0x88888888u, xh = wh ^ 0x88888888u;
+    A[0] = i4pair(xl, 8 * t);
+    A[1] = i4pair(xh, 8 * t);
+    A[2] = i4pair(xl, 8 * t + 4);
+    A[3] = i4pair(xh, 8 * t + 4);
+  } else if constexpr (DT == KVQ_INT8) {
+    const uint32_t xl = wl ^ 0x80808080u, xh = wh ^ 0x80808080u;
+    A[0] = i8pair(xl, 0x4140u);
+    A[1] = i8pair(xh, 0x4140u);
+    A[2] = i8pair(xl, 0x4342u);
+    A[3] = i8pair(xh, 0x4342u);
+  } else {
+    A[0] = e4m3x2_f16x2((uint16_t)(wl & 0xFFFFu));
+    A[1] = e4m3x2_f16x2((uint16_t)(wh & 0xFFFFu));
+    A[2] = e4m3x2_f16x2((uint16_t)(wl >> 16));
+    A[3] = e4m3x2_f16x2((uint16_t)(wh >> 16));
+  }
+}
+
 // Output channel held by accumulator element e of channel tile mt in lane
 // group g (the PV operand permutation chosen for the ldmatrix.trans layout).
 template <int DT>
@@ -119,7 +153,7 @@ __device__ __forceinline__ int out_channel(int mt, int e, int g) {
 // folded in under a power-of-two normaliser (|q * s| <= |q|), the row then
 // normalised by the power of two just above its max so the f16 operand keeps
 // its full mantissa.  Returns the logit factor for the row (sm_scale, tensor
-// scale, e4m3 2^8, both powers of two; times log2 e when no softcap follows),
+// scale, both powers of two; times log2 e when no softcap follows),
 // clamped to FLT_MAX so zero codes under a huge scale stay zero.  Rows past
 // a.rows get q = 0.  Every lane of the warp must call it.
 template <int DT, int D>
@@ -195,7 +229,6 @@ __device__ __forceinline__ float q_prologue(const DecodeArgs& a, int rq, int b, 
   }
   float base = a.sm_scale;
   if (a.k_mode == KVQ_SCALE_PER_TENSOR) base *= a.k_scale[0];
-  if constexpr (DT == KVQ_FP8_E4M3) base *= 256.0f;
   float alpha = ldexpf(base, e_tot);
   if (a.softcap <= 0.0f) alpha *= kLog2e;
   return fminf(alpha, 3.4028234e38f);
@@ -254,6 +287,9 @@ __global__ void __launch_bounds__(288, MINB)
     }
     ptx::fence_mbar_init();
   }
+  // everything above touched only shared memory; inputs may still be in
+  // flight from the previous kernel on the stream
+  ptx::griddep_wait();
 
   // ---------------------------------------------------------------- plan
   // Segment s = b * Hkv + h is sequence b's key range [lo_b, L_b) for kv head
@@ -296,6 +332,8 @@ __global__ void __launch_bounds__(288, MINB)
     }
   }
   __syncthreads();
+  // the combine may be scheduled now; it waits for this grid to complete
+  ptx::griddep_launch_dependents();
   const int W = pl_misc[0];
   const int t_begin = min((int)blockIdx.x * W, pl_misc[1]);
   const int t_end = min(t_begin + W, pl_misc[1]);
@@ -546,11 +584,10 @@ __global__ void __launch_bounds__(288, MINB)
               const int j = 2 * kk + h2;
               const uint32_t wl = R[2 * h2], wh = R[2 * h2 + 1];
               if constexpr (DT == KVQ_INT4) {
-                const uint32_t xl = wl ^ 0x88888888u, xh = wh ^ 0x88888888u;
 #pragma unroll
                 for (int t = 0; t < 2; ++t) {
-                  const uint32_t A[4] = {dev::i4pair(xl, 8 * t), dev::i4pair(xh, 8 * t),
-                                         dev::i4pair(xl, 8 * t + 4), dev::i4pair(xh, 8 * t + 4)};
+                  uint32_t A[4];
+                  dev::k_frag<DT>(wl, wh, t, A);
                   uint32_t bq[NT][2];
                   qfrag(2 * j + t, bq);
 #pragma unroll
@@ -558,18 +595,7 @@ __global__ void __launch_bounds__(288, MINB)
                 }
               } else {
                 uint32_t A[4];
-                if constexpr (DT == KVQ_INT8) {
-                  const uint32_t xl = wl ^ 0x80808080u, xh = wh ^ 0x80808080u;
-                  A[0] = dev::i8pair(xl, 0x4140u);
-                  A[1] = dev::i8pair(xh, 0x4140u);
-                  A[2] = dev::i8pair(xl, 0x4342u);
-                  A[3] = dev::i8pair(xh, 0x4342u);
-                } else {
-                  A[0] = dev::f8pair(wl, 0x1404u);
-                  A[1] = dev::f8pair(wh, 0x1404u);
-                  A[2] = dev::f8pair(wl, 0x3424u);
-                  A[3] = dev::f8pair(wh, 0x3424u);
-                }
+                dev::k_frag<DT>(wl, wh, 0, A);
                 uint32_t bq[NT][2];
                 qfrag(j, bq);
 #pragma unroll
@@ -865,11 +891,10 @@ __global__ void __launch_bounds__(288, MINB)
             const int j = 2 * kk + h2;
             const uint32_t wl = R[2 * h2], wh = R[2 * h2 + 1];
             if constexpr (DT == KVQ_INT4) {
-              const uint32_t xl = wl ^ 0x88888888u, xh = wh ^ 0x88888888u;
 #pragma unroll
               for (int t = 0; t < 2; ++t) {
-                const uint32_t A[4] = {dev::i4pair(xl, 8 * t), dev::i4pair(xh, 8 * t), dev::i4pair(xl, 8 * t + 4),
-                                       dev::i4pair(xh, 8 * t + 4)};
+                uint32_t A[4];
+                dev::k_frag<DT>(wl, wh, t, A);
                 if (t == 0)
                   ptx::mma_16816(sa, A, qf[2 * j + t][0], qf[2 * j + t][1]);
                 else
@@ -877,18 +902,7 @@ __global__ void __launch_bounds__(288, MINB)
               }
             } else {
               uint32_t A[4];
-              if constexpr (DT == KVQ_INT8) {
-                const uint32_t xl = wl ^ 0x80808080u, xh = wh ^ 0x80808080u;
-                A[0] = dev::i8pair(xl, 0x4140u);
-                A[1] = dev::i8pair(xh, 0x4140u);
-                A[2] = dev::i8pair(xl, 0x4342u);
-                A[3] = dev::i8pair(xh, 0x4342u);
-              } else {
-                A[0] = dev::f8pair(wl, 0x1404u);
-                A[1] = dev::f8pair(wh, 0x1404u);
-                A[2] = dev::f8pair(wl, 0x3424u);
-                A[3] = dev::f8pair(wh, 0x3424u);
-              }
+              dev::k_frag<DT>(wl, wh, 0, A);
               if (h2 == 0)
                 ptx::mma_16816(sa, A, qf[j][0], qf[j][1]);
               else
@@ -1102,8 +1116,7 @@ cudaError_t launch_decode_d(const CUtensorMap& tk, const CUtensorMap& tv, const 
                             int threads, size_t smem, cudaStream_t stream) {
   cudaError_t e = ensure_smem<DT, D, MINB, NT>(smem);
   if (e != cudaSuccess) return e;
-  decode_kernel<DT, D, MINB, NT><<<grid, threads, smem, stream>>>(tk, tv, a);
-  return cudaGetLastError();
+  return launch_pdl(decode_kernel<DT, D, MINB, NT>, grid, threads, smem, stream, tk, tv, a);
 }
 
 template <int DT, int D, int MINB, int NT>

@@ -8,6 +8,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <utility>
 
 #include "kvq.h"
 
@@ -62,6 +63,25 @@ struct CombineArgs {
   float* lse_out;          // [B, T, Hq] or null
   int batch, q_tokens, num_q_heads, num_kv_heads, group, rows, head_dim;
 };
+
+// Launches a kernel with programmatic stream serialization: it may start while
+// the previous kernel on the stream finishes, and every kvq kernel waits
+// (griddepcontrol.wait) before its first global-memory access.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t stream);
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t stream);

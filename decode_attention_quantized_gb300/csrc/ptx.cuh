@@ -146,6 +146,13 @@ __device__ __forceinline__ float fast_log2(float x) {
   return y;
 }
 
+// Programmatic dependent launch: wait until the preceding grid on the stream
+// has completed and its memory is visible; allow the next grid to launch.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
