@@ -2,6 +2,7 @@
 // TMA descriptor encoding and kernel launches.  No allocation, no host sync
 // (except kvq_get_device_error, which says so), no device data read back.
 #include <cmath>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
@@ -97,7 +98,7 @@ kvq_status check_params(const kvq_cache* c, const kvq_decode_params* p) {
 
 // Launch shape of the decode kernel and the workspace it implies.
 struct Plan {
-  int rows, row_groups, key_warps, nt, threads, stages, grid, units_max;
+  int rows, row_groups, key_warps, nt, tc_nr, threads, stages, grid, units_max;
   size_t smem, ws_plan, ws_lse, ws_o, ws_total;
 };
 
@@ -127,10 +128,57 @@ cudaError_t occupancy(const kvq_cache* c, int nt, int threads, size_t smem, int*
   }
 }
 
+// The tensor-memory kernel takes 17..48 query rows per kv head at head_dim
+// 256 and 17..64 at head_dim 128 (its TMEM columns bound rows x head_dim);
+// KVQ_NO_TC=1 in the environment keeps such shapes on the mma.sync layouts.
+int tc_rows(const kvq_cache* c, int rows) {
+  const char* off = std::getenv("KVQ_NO_TC");
+  if (off && off[0] == '1') return 0;
+  if (rows < 17) return 0;
+  if (c->head_dim == 256 && rows <= 48) return rows <= 32 ? 32 : 48;
+  if (c->head_dim == 128 && rows <= 64) return rows <= 32 ? 32 : (rows <= 48 ? 48 : 64);
+  return 0;
+}
+
+kvq_status make_plan_tc(const kvq_cache* c, const kvq_decode_params* p, const DeviceInfo& dev, Plan* P) {
+  const int B = p->batch > 0 ? p->batch : 1;
+  const int dp = row_bytes(c);
+  constexpr size_t kMaxSmem = 227 * 1024;  // per CTA
+  int stages = 0;
+  for (int s = kMaxStages; s >= 2 && stages == 0; --s)
+    if ((size_t)tc_smem_layout(c->head_dim, dp, P->tc_nr, s, B).total + 1024 <= kMaxSmem) stages = s;
+  if (stages == 0) return KVQ_ERR_UNSUPPORTED;
+  P->stages = stages;
+  P->smem = (size_t)tc_smem_layout(c->head_dim, dp, P->tc_nr, stages, B).total + 1024;
+  P->threads = kTcWarps * 32;
+  P->row_groups = 0;
+  P->key_warps = 0;
+  P->nt = 0;
+  const long long cap = (long long)p->max_blocks_per_seq * c->block_size;
+  const long long maxlen = (p->max_seq_len > 0 && p->max_seq_len < cap) ? p->max_seq_len : cap;
+  long long grid = dev.sms;  // one CTA per SM: it holds all of the SM's tensor memory
+  const long long useful = (long long)B * c->num_kv_heads * ((maxlen + kTcKeys - 1) / kTcKeys + 1);
+  if (grid > useful) grid = useful;
+  P->grid = (int)(grid < 1 ? 1 : grid);
+  return KVQ_OK;
+}
+
 kvq_status make_plan_uncached(const kvq_cache* c, const kvq_decode_params* p, const DeviceInfo& dev, Plan* out) {
   Plan P{};
   const int G = p->num_q_heads / c->num_kv_heads;
   P.rows = G * p->q_tokens;
+  P.tc_nr = tc_rows(c, P.rows);
+  if (P.tc_nr) {
+    if (kvq_status s = make_plan_tc(c, p, dev, &P)) return s;
+    const int B = p->batch > 0 ? p->batch : 1;
+    P.units_max = P.grid + B * c->num_kv_heads;
+    P.ws_plan = align256((size_t)(4 + B + 1) * 4);
+    P.ws_lse = align256((size_t)P.units_max * P.rows * 4);
+    P.ws_o = (size_t)P.units_max * P.rows * c->head_dim * 4;
+    P.ws_total = P.ws_plan + P.ws_lse + P.ws_o;
+    *out = P;
+    return KVQ_OK;
+  }
   P.row_groups = (P.rows + 7) / 8;
   P.key_warps = P.row_groups <= 2 ? 4 : (P.row_groups <= 4 ? 2 : 1);
   // 17..48 rows (e.g. drafts x GQA group): the wide layout, 4 key quarters x 2
@@ -365,10 +413,18 @@ KVQ_API kvq_status kvq_decode(const kvq_cache* cache, const kvq_decode_params* p
 
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e;
-  switch (cache->dtype) {
-    case KVQ_INT8: e = launch_decode_int8(cache->head_dim, P.nt, tk, tv, a, P.grid, P.threads, P.smem, st); break;
-    case KVQ_FP8_E4M3: e = launch_decode_fp8(cache->head_dim, P.nt, tk, tv, a, P.grid, P.threads, P.smem, st); break;
-    default: e = launch_decode_int4(cache->head_dim, P.nt, tk, tv, a, P.grid, P.threads, P.smem, st); break;
+  if (P.tc_nr) {
+    switch (cache->dtype) {
+      case KVQ_INT8: e = launch_decode_tc_int8(cache->head_dim, P.tc_nr, tk, tv, a, P.grid, P.smem, st); break;
+      case KVQ_FP8_E4M3: e = launch_decode_tc_fp8(cache->head_dim, P.tc_nr, tk, tv, a, P.grid, P.smem, st); break;
+      default: e = launch_decode_tc_int4(cache->head_dim, P.tc_nr, tk, tv, a, P.grid, P.smem, st); break;
+    }
+  } else {
+    switch (cache->dtype) {
+      case KVQ_INT8: e = launch_decode_int8(cache->head_dim, P.nt, tk, tv, a, P.grid, P.threads, P.smem, st); break;
+      case KVQ_FP8_E4M3: e = launch_decode_fp8(cache->head_dim, P.nt, tk, tv, a, P.grid, P.threads, P.smem, st); break;
+      default: e = launch_decode_int4(cache->head_dim, P.nt, tk, tv, a, P.grid, P.threads, P.smem, st); break;
+    }
   }
   return from_cuda(e);
 }

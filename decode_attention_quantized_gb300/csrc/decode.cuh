@@ -37,31 +37,12 @@
 #include <type_traits>
 
 #include "kvq_internal.h"
+#include "pipeline.cuh"
 #include "ptx.cuh"
 
 namespace kvq {
 
-constexpr int round_up_c(int x, int m) { return (x + m - 1) / m * m; }
-
-template <int DT, int D>
-struct Geo {
-  static constexpr int DP = DT == KVQ_INT4 ? D / 2 : D;  // bytes per cached row
-  static constexpr int SPAN = DP >= 128 ? 128 : DP;      // TMA box inner bytes = swizzle span
-  static constexpr int SLABS = DP / SPAN;                // column slabs per row
-  static constexpr int NCH = DP / 16;                    // 16-byte chunks per row
-  static constexpr int NMT = D / 16;                     // 16-channel MMA tiles
-  static constexpr int CODE_BYTES = kTile * DP;          // one side of one stage
-  static constexpr int STAGE_STRIDE = round_up_c(2 * CODE_BYTES + 2 * kTile * 4, 1024);
-};
-
 namespace dev {
-
-// byte offset o inside a slab of SPAN-byte rows -> swizzled offset written by
-// the TMA unit (16-byte granule index XOR row-group bits 7.., period 8 rows).
-template <int SPAN>
-__device__ __forceinline__ uint32_t swz(uint32_t o) {
-  return o ^ (((o >> 7) & (SPAN / 16 - 1)) << 4);
-}
 
 // Smallest e with 2^e >= x for finite x > 0 (read off the IEEE fields).
 __device__ __forceinline__ int ceil_log2(float x) {
@@ -266,19 +247,7 @@ __global__ void __launch_bounds__(288, MINB)
   uint64_t* bar_empty = bar_full + a.stages;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int B = a.batch, T = a.q_tokens, Hkv = a.num_kv_heads;
-  const int cap = a.max_blocks_per_seq * a.block_size;
-  const int lim = (a.max_seq_len > 0 && a.max_seq_len < cap) ? a.max_seq_len : cap;
-
-  // key range [lo, L) of sequence b: L clamped to the capacity bound, lo the
-  // first key any query row sees (window) rounded down to the tile
-  auto seq_range = [&](int b, int& L, int& lo) {
-    L = a.seq_lens[b];
-    L = L < 0 ? 0 : (L > lim ? lim : L);
-    lo = 0;
-    if (a.window > 0) lo = max(0, L - T - a.window + 1);
-    lo &= ~(kTile - 1);
-  };
+  const int T = a.q_tokens;
 
   if (tid == 0) {
     for (int s = 0; s < a.stages; ++s) {
@@ -290,166 +259,17 @@ __global__ void __launch_bounds__(288, MINB)
   // everything above touched only shared memory; inputs may still be in
   // flight from the previous kernel on the stream
   ptx::griddep_wait();
-
-  // ---------------------------------------------------------------- plan
-  // Segment s = b * Hkv + h is sequence b's key range [lo_b, L_b) for kv head
-  // h: n_b = ceil((L_b - lo_b) / kTile) tiles.  The segments laid end to end
-  // in s order make T tiles, and CTA x takes the contiguous slice
-  // [x W, (x + 1) W) with W = ceil(T / gridDim.x), so every CTA streams the
-  // same number of tiles whatever the length mix.  The piece of segment s in
-  // CTA x's slice writes its partial to slot s + x: distinct for every piece
-  // and contiguous over the pieces of one segment.
-  for (int b = tid; b < B; b += blockDim.x) {
-    const int raw = a.seq_lens[b];
-    if ((raw < 0 || raw > lim) && blockIdx.x == 0) atomicOr(a.err, KVQ_DEVERR_SEQ_LEN);
-    int L, lo;
-    seq_range(b, L, lo);
-    pl_pre[b] = (max(0, L - lo) + kTile - 1) / kTile;  // tiles, for now
-  }
-  __syncthreads();
-  if (warp == 0) {
-    const int seg = (B + 31) / 32;
-    const int s0 = min(B, lane * seg), s1 = min(B, s0 + seg);
-    int cnt = 0;
-    for (int b = s0; b < s1; ++b) cnt += pl_pre[b];
-    int incl = cnt;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += y;
-    }
-    int run = incl - cnt;
-    for (int b = s0; b < s1; ++b) {
-      const int n = pl_pre[b];
-      pl_pre[b] = run;
-      run += n;
-    }
-    if (lane == 31) {
-      const int total = incl * Hkv;
-      pl_pre[B] = incl;
-      pl_misc[0] = max(1, (total + (int)gridDim.x - 1) / (int)gridDim.x);
-      pl_misc[1] = total;
-    }
-  }
-  __syncthreads();
-  // the combine may be scheduled now; it waits for this grid to complete
-  ptx::griddep_launch_dependents();
-  const int W = pl_misc[0];
-  const int t_begin = min((int)blockIdx.x * W, pl_misc[1]);
-  const int t_end = min(t_begin + W, pl_misc[1]);
-  if (blockIdx.x == 0) {
-    for (int i = tid; i <= B; i += blockDim.x) a.plan[4 + i] = pl_pre[i];
-    if (tid == 0) {
-      a.plan[0] = W;
-      a.plan[1] = pl_misc[1];
-      a.plan[2] = B;
-      a.plan[3] = a.units_max;
-    }
-  }
-
-  // the piece that starts at global tile gt: sequence, kv head, key range,
-  // partial slot, and the global tile after it
+  const Slice<kTile> sp = build_slice<kTile>(a, pl_pre, pl_misc);
+  const int t_begin = sp.t_begin, t_end = sp.t_end;
   auto piece = [&](int gt, int& b, int& h, int& k0, int& k1, int& L, int& slot, int& next) {
-    int lo = 0, hi = B - 1;  // last b with pre[b] * Hkv <= gt (skips empty sequences)
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (pl_pre[mid] * Hkv <= gt) lo = mid; else hi = mid - 1;
-    }
-    b = lo;
-    const int nb = pl_pre[b + 1] - pl_pre[b];
-    const int off = gt - pl_pre[b] * Hkv;
-    h = off / nb;
-    const int t0 = off - h * nb;
-    next = min(gt - t0 + nb, t_end);
-    int klo;
-    seq_range(b, L, klo);
-    k0 = klo + t0 * kTile;
-    k1 = min(klo + (t0 + next - gt) * kTile, L);
-    slot = b * Hkv + h + (int)blockIdx.x;
+    sp.piece(a, gt, b, h, k0, k1, L, slot, next);
   };
 
   const bool k_row = a.k_mode == KVQ_SCALE_PER_ROW, v_row = a.v_mode == KVQ_SCALE_PER_ROW;
 
   // =============================================================== producer
-  // The whole warp fetches the unit's block ids 32 pages at a time (one
-  // coalesced load per 32 pages) and hands them to lane 0 by shuffles; lane 0
-  // waits for free stages and issues the copies.
   if (warp == n_cw) {
-    const int seg_rows = min(a.block_size, kTile);
-    const int n_seg = kTile / seg_rows;
-    const uint32_t S = (uint32_t)a.stages;
-    uint32_t it = 0;
-    int ok = 1;
-    for (int gt = t_begin, next; gt < t_end; gt = next) {
-      int b, h, k0, k1, L, slot;
-      piece(gt, b, h, k0, k1, L, slot, next);
-      const int32_t* bt = a.block_table + (size_t)b * a.max_blocks_per_seq;
-      const int p_last = (k1 - 1) >> a.log2_bs;
-      int base = k0 >> a.log2_bs;
-      int my_id = base + lane <= p_last ? bt[base + lane] : -1;
-      for (int key0 = k0; key0 < k1; key0 += kTile, ++it) {
-        const int stage = (int)(it % S);
-        if (lane == 0 && it >= S && ok) {
-          ok = ptx::mbar_wait_bounded(&bar_empty[stage], ((it / S) - 1) & 1) ? 1 : 0;
-          if (!ok) atomicOr(a.err, KVQ_DEVERR_TIMEOUT);
-        }
-        ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (!ok) {
-          if (lane == 0) ptx::mbar_arrive(&bar_full[stage]);
-          continue;
-        }
-        int blk[kTile / 16];
-        uint32_t bytes = 0;
-#pragma unroll
-        for (int s = 0; s < kTile / 16; ++s) {
-          blk[s] = -1;
-          const int skey = key0 + s * seg_rows;
-          if (s >= n_seg || skey >= k1) continue;
-          const int page = skey >> a.log2_bs;
-          if (page - base >= 32) {
-            base += 32;
-            my_id = base + lane <= p_last ? bt[base + lane] : -1;
-          }
-          const int id = __shfl_sync(0xffffffffu, my_id, page - base);
-          if (id < 0 || id >= a.num_blocks) {
-            if (lane == 0) atomicOr(a.err, KVQ_DEVERR_BLOCK_ID);
-            continue;
-          }
-          blk[s] = id;
-          bytes += (uint32_t)seg_rows * (2 * Gm::DP + (k_row ? 4 : 0) + (v_row ? 4 : 0));
-        }
-        if (lane == 0) {
-          uint8_t* st = ring + (size_t)stage * Gm::STAGE_STRIDE;
-          ptx::mbar_arrive_expect_tx(&bar_full[stage], bytes);
-#pragma unroll
-          for (int s = 0; s < kTile / 16; ++s) {
-            if (blk[s] < 0) continue;
-            const int row0 = (key0 + s * seg_rows) & (a.block_size - 1);
-#pragma unroll
-            for (int sl = 0; sl < Gm::SLABS; ++sl) {
-              uint8_t* dk = st + sl * (kTile * Gm::SPAN) + s * seg_rows * Gm::SPAN;
-              ptx::tma_load_4d(dk, &tmk, sl * Gm::SPAN, row0, h, blk[s], &bar_full[stage]);
-              ptx::tma_load_4d(dk + Gm::CODE_BYTES, &tmv, sl * Gm::SPAN, row0, h, blk[s], &bar_full[stage]);
-            }
-            const size_t srow = ((size_t)blk[s] * Hkv + h) * a.block_size + row0;
-            if (k_row)
-              ptx::bulk_load(st + 2 * Gm::CODE_BYTES + s * seg_rows * 4, a.k_scale + srow, seg_rows * 4,
-                             &bar_full[stage]);
-            if (v_row)
-              ptx::bulk_load(st + 2 * Gm::CODE_BYTES + kTile * 4 + s * seg_rows * 4, a.v_scale + srow,
-                             seg_rows * 4, &bar_full[stage]);
-          }
-        }
-        __syncwarp();
-      }
-    }
-    // let every copy this warp issued land before the CTA can exit
-    if (lane == 0) {
-      for (uint32_t s = 0; s < S && s < it; ++s) {
-        const uint32_t last = it - 1 - ((it - 1 - s) % S);
-        if (!ptx::mbar_wait_bounded(&bar_full[s], (last / S) & 1)) atomicOr(a.err, KVQ_DEVERR_TIMEOUT);
-      }
-    }
+    produce<Gm>(a, sp, &tmk, &tmv, ring, bar_full, bar_empty);
     return;
   }
 

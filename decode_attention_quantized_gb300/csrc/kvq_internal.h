@@ -64,6 +64,37 @@ struct CombineArgs {
   int batch, q_tokens, num_q_heads, num_kv_heads, group, rows, head_dim;
 };
 
+// The tensor-memory decode kernel (many query rows per kv head): 128 keys per
+// stage and per MMA tile, 14 warps, and its shared-memory layout (byte offsets
+// from the 1024-aligned base; the host adds 1024 bytes of alignment slack).
+constexpr int kTcKeys = 128;
+constexpr int kTcWarps = 14;
+
+struct TcSmem {
+  int ring, q, p, scr, pre, bars, slot, total;
+};
+
+__host__ __device__ constexpr int tc_stage_stride(int row_bytes) {
+  return (2 * kTcKeys * row_bytes + 2 * kTcKeys * 4 + 1023) / 1024 * 1024;
+}
+
+// ring: stages x stage stride; q: [D/64 slabs][nr rows][128 B] f16; p: two
+// [2 slabs][nr rows][128 B] f16 buffers; scr: row factors, positions and the
+// per-warp row maxima / reference maxima / rescale factors; pre: split plan;
+// bars: mbarriers; slot: TMEM address + abort flag.
+__host__ __device__ constexpr TcSmem tc_smem_layout(int head_dim, int row_bytes, int nr, int stages, int batch) {
+  TcSmem s{};
+  s.ring = 0;
+  s.q = stages * tc_stage_stride(row_bytes);
+  s.p = s.q + nr * 2 * head_dim;
+  s.scr = s.p + 2 * nr * 2 * kTcKeys;
+  s.pre = s.scr + (2 * nr + 3 * 4 * nr + 16) * 4;
+  s.bars = (s.pre + (batch + 5) * 4 + 7) / 8 * 8;
+  s.slot = s.bars + (2 * stages + 16) * 8;
+  s.total = s.slot + 16;
+  return s;
+}
+
 // Launches a kernel with programmatic stream serialization: it may start while
 // the previous kernel on the stream finishes, and every kvq kernel waits
 // (griddepcontrol.wait) before its first global-memory access.
@@ -91,6 +122,14 @@ cudaError_t launch_decode_fp8(int head_dim, int nt, const CUtensorMap& tk, const
                                const DecodeArgs& a, int grid, int threads, size_t smem, cudaStream_t stream);
 cudaError_t launch_decode_int4(int head_dim, int nt, const CUtensorMap& tk, const CUtensorMap& tv,
                                const DecodeArgs& a, int grid, int threads, size_t smem, cudaStream_t stream);
+
+// Tensor-memory layout for nr padded query rows (32, 48; 64 with head_dim 128).
+cudaError_t launch_decode_tc_int8(int head_dim, int nr, const CUtensorMap& tk, const CUtensorMap& tv,
+                                  const DecodeArgs& a, int grid, size_t smem, cudaStream_t stream);
+cudaError_t launch_decode_tc_fp8(int head_dim, int nr, const CUtensorMap& tk, const CUtensorMap& tv,
+                                 const DecodeArgs& a, int grid, size_t smem, cudaStream_t stream);
+cudaError_t launch_decode_tc_int4(int head_dim, int nr, const CUtensorMap& tk, const CUtensorMap& tv,
+                                  const DecodeArgs& a, int grid, size_t smem, cudaStream_t stream);
 
 cudaError_t occupancy_decode_int8(int head_dim, int nt, int threads, size_t smem, int* blocks_per_sm);
 cudaError_t occupancy_decode_fp8(int head_dim, int nt, int threads, size_t smem, int* blocks_per_sm);

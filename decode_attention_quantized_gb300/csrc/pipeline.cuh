@@ -1,0 +1,239 @@
+// pipeline.cuh -- the parts every decode kernel shares: the geometry of a
+// shared-memory stage of quantized code rows, the tile-balanced split plan
+// that each CTA builds from seq_lens, the walk over the pieces of a CTA's
+// slice, and the producer warp that streams code pages through a ring of
+// mbarrier-guarded stages with TMA.
+//
+// Split-KV over a paged cache: PagedAttention paged decode (onnxruntime PR
+// #29912, Summary of Changes: split-KV, block-table aware); one block owns a
+// (batch, kv head) key range and partials are merged in a fixed order
+// (kv-quant-attn page, section "Method").
+#pragma once
+
+#include "kvq_internal.h"
+#include "ptx.cuh"
+
+namespace kvq {
+
+constexpr int round_up_c(int x, int m) { return (x + m - 1) / m * m; }
+
+// One stage holds KT keys: the K code rows, then the V code rows, each as
+// SLABS column slabs of [KT rows][SPAN bytes] in the TMA swizzle, then KT K
+// scales and KT V scales (fp32, per-row mode only).
+template <int DT, int D, int KT = kTile>
+struct Geo {
+  static constexpr int DP = DT == KVQ_INT4 ? D / 2 : D;  // bytes per cached row
+  static constexpr int SPAN = DP >= 128 ? 128 : DP;      // TMA box inner bytes = swizzle span
+  static constexpr int SLABS = DP / SPAN;                // column slabs per row
+  static constexpr int NCH = DP / 16;                    // 16-byte chunks per row
+  static constexpr int NMT = D / 16;                     // 16-channel MMA tiles
+  static constexpr int KEYS = KT;                        // keys per stage
+  static constexpr int CODE_BYTES = KT * DP;             // one side of one stage
+  static constexpr int STAGE_STRIDE = round_up_c(2 * CODE_BYTES + 2 * KT * 4, 1024);
+};
+
+namespace dev {
+
+// byte offset o inside a slab of SPAN-byte rows -> swizzled offset written by
+// the TMA unit (16-byte granule index XOR row-group bits 7.., period 8 rows).
+template <int SPAN>
+__device__ __forceinline__ uint32_t swz(uint32_t o) {
+  return o ^ (((o >> 7) & (SPAN / 16 - 1)) << 4);
+}
+
+}  // namespace dev
+
+// The split plan.  Segment s = b * Hkv + h is sequence b's key range
+// [lo_b, L_b) for kv head h: n_b = ceil((L_b - lo_b) / KT) tiles.  The
+// segments laid end to end in s order make `total` tiles, and CTA x takes the
+// contiguous slice [x W, (x + 1) W) with W = ceil(total / gridDim.x), so
+// every CTA streams the same number of tiles whatever the length mix.  The
+// piece of segment s in CTA x's slice writes its partial to slot s + x:
+// distinct for every piece and contiguous over the pieces of one segment
+// (the combine walks them in that order).
+template <int KT>
+struct Slice {
+  const int* pre;  // shared [B + 1]: tile prefix over sequences
+  int lim, t_begin, t_end;
+
+  // key range [lo, L) of sequence b: L clamped to the capacity bound, lo the
+  // first key any query row sees (window) rounded down to the tile
+  __device__ __forceinline__ void seq_range(const DecodeArgs& a, int b, int& L, int& lo) const {
+    L = a.seq_lens[b];
+    L = L < 0 ? 0 : (L > lim ? lim : L);
+    lo = 0;
+    if (a.window > 0) lo = max(0, L - a.q_tokens - a.window + 1);
+    lo &= ~(KT - 1);
+  }
+
+  // the piece that starts at global tile gt: sequence, kv head, key range
+  // [k0, k1), sequence length, partial slot, and the global tile after it
+  __device__ __forceinline__ void piece(const DecodeArgs& a, int gt, int& b, int& h, int& k0, int& k1, int& L,
+                                        int& slot, int& next) const {
+    const int Hkv = a.num_kv_heads;
+    int lo = 0, hi = a.batch - 1;  // last b with pre[b] * Hkv <= gt (skips empty sequences)
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (pre[mid] * Hkv <= gt) lo = mid; else hi = mid - 1;
+    }
+    b = lo;
+    const int nb = pre[b + 1] - pre[b];
+    const int off = gt - pre[b] * Hkv;
+    h = off / nb;
+    const int t0 = off - h * nb;
+    next = min(gt - t0 + nb, t_end);
+    int klo;
+    seq_range(a, b, L, klo);
+    k0 = klo + t0 * KT;
+    k1 = min(klo + (t0 + next - gt) * KT, L);
+    slot = b * Hkv + h + (int)blockIdx.x;
+  }
+};
+
+// Builds the plan in shared memory (pl_pre [B + 1], pl_misc [4]); every
+// thread of the CTA calls it after griddep_wait.  CTA 0 also publishes it to
+// the workspace for the combine.  Flags seq_lens outside [0, capacity].
+template <int KT>
+__device__ Slice<KT> build_slice(const DecodeArgs& a, int* pl_pre, int* pl_misc) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int B = a.batch, Hkv = a.num_kv_heads;
+  const int cap = a.max_blocks_per_seq * a.block_size;
+  Slice<KT> sp;
+  sp.pre = pl_pre;
+  sp.lim = (a.max_seq_len > 0 && a.max_seq_len < cap) ? a.max_seq_len : cap;
+  for (int b = tid; b < B; b += blockDim.x) {
+    const int raw = a.seq_lens[b];
+    if ((raw < 0 || raw > sp.lim) && blockIdx.x == 0) atomicOr(a.err, KVQ_DEVERR_SEQ_LEN);
+    int L, lo;
+    sp.seq_range(a, b, L, lo);
+    pl_pre[b] = (max(0, L - lo) + KT - 1) / KT;  // tiles, for now
+  }
+  __syncthreads();
+  if (warp == 0) {
+    const int seg = (B + 31) / 32;
+    const int s0 = min(B, lane * seg), s1 = min(B, s0 + seg);
+    int cnt = 0;
+    for (int b = s0; b < s1; ++b) cnt += pl_pre[b];
+    int incl = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    int run = incl - cnt;
+    for (int b = s0; b < s1; ++b) {
+      const int n = pl_pre[b];
+      pl_pre[b] = run;
+      run += n;
+    }
+    if (lane == 31) {
+      const int total = incl * Hkv;
+      pl_pre[B] = incl;
+      pl_misc[0] = max(1, (total + (int)gridDim.x - 1) / (int)gridDim.x);
+      pl_misc[1] = total;
+    }
+  }
+  __syncthreads();
+  // the combine may be scheduled now; it waits for this grid to complete
+  ptx::griddep_launch_dependents();
+  const int W = pl_misc[0];
+  sp.t_begin = min((int)blockIdx.x * W, pl_misc[1]);
+  sp.t_end = min(sp.t_begin + W, pl_misc[1]);
+  if (blockIdx.x == 0) {
+    for (int i = tid; i <= B; i += blockDim.x) a.plan[4 + i] = pl_pre[i];
+    if (tid == 0) {
+      a.plan[0] = W;
+      a.plan[1] = pl_misc[1];
+      a.plan[2] = B;
+      a.plan[3] = a.units_max;
+    }
+  }
+  return sp;
+}
+
+// The producer warp.  The whole warp fetches a piece's block ids 32 pages at
+// a time (one coalesced load per 32 pages) and hands them to lane 0 by
+// shuffles; lane 0 waits for a free stage, then for each page segment of the
+// stage adds the segment's bytes to the stage's transaction count and issues
+// one TMA tensor copy per (slab, side) with the block id as the outer
+// coordinate, plus 1-D bulk copies of the per-row scales; its single arrival
+// after the last segment lets the phase complete.  A block id outside
+// [0, num_blocks) is flagged and its rows are not loaded.  Returns after
+// every copy it issued has landed, so the CTA never exits with a copy in
+// flight.  The segment loop is not unrolled: the producer shares its
+// scheduler with compute warps, and a small loop keeps their instruction
+// footprint small.
+template <class Gm>
+__device__ void produce(const DecodeArgs& a, const Slice<Gm::KEYS>& sp, const CUtensorMap* tmk,
+                        const CUtensorMap* tmv, uint8_t* ring, uint64_t* bar_full, uint64_t* bar_empty) {
+  constexpr int KT = Gm::KEYS;
+  const int lane = threadIdx.x & 31;
+  const bool k_row = a.k_mode == KVQ_SCALE_PER_ROW, v_row = a.v_mode == KVQ_SCALE_PER_ROW;
+  const int Hkv = a.num_kv_heads;
+  const int seg_rows = min(a.block_size, kTile);  // rows of one TMA box
+  const uint32_t seg_bytes = (uint32_t)seg_rows * (2 * Gm::DP + (k_row ? 4 : 0) + (v_row ? 4 : 0));
+  const uint32_t S = (uint32_t)a.stages;
+  uint32_t it = 0;
+  int ok = 1;
+  for (int gt = sp.t_begin, next; gt < sp.t_end; gt = next) {
+    int b, h, k0, k1, L, slot;
+    sp.piece(a, gt, b, h, k0, k1, L, slot, next);
+    const int32_t* bt = a.block_table + (size_t)b * a.max_blocks_per_seq;
+    const int p_last = (k1 - 1) >> a.log2_bs;
+    int base = k0 >> a.log2_bs;
+    int my_id = base + lane <= p_last ? bt[base + lane] : -1;
+    for (int key0 = k0; key0 < k1; key0 += KT, ++it) {
+      const int stage = (int)(it % S);
+      if (lane == 0 && it >= S && ok) {
+        ok = ptx::mbar_wait_bounded(&bar_empty[stage], ((it / S) - 1) & 1) ? 1 : 0;
+        if (!ok) atomicOr(a.err, KVQ_DEVERR_TIMEOUT);
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      uint8_t* st = ring + (size_t)stage * Gm::STAGE_STRIDE;
+      const int kend = ok ? min(key0 + KT, k1) : key0;  // nothing is loaded after a timeout
+#pragma unroll 1
+      for (int skey = key0; skey < kend; skey += seg_rows) {
+        const int page = skey >> a.log2_bs;
+        if (page - base >= 32) {
+          base += 32;
+          my_id = base + lane <= p_last ? bt[base + lane] : -1;
+        }
+        const int id = __shfl_sync(0xffffffffu, my_id, page - base);
+        if (lane == 0) {
+          if (id < 0 || id >= a.num_blocks) {
+            atomicOr(a.err, KVQ_DEVERR_BLOCK_ID);
+          } else {
+            const int s = (skey - key0) / seg_rows;
+            const int row0 = skey & (a.block_size - 1);
+            ptx::mbar_expect_tx(&bar_full[stage], seg_bytes);
+#pragma unroll
+            for (int sl = 0; sl < Gm::SLABS; ++sl) {
+              uint8_t* dk = st + sl * (KT * Gm::SPAN) + s * seg_rows * Gm::SPAN;
+              ptx::tma_load_4d(dk, tmk, sl * Gm::SPAN, row0, h, id, &bar_full[stage]);
+              ptx::tma_load_4d(dk + Gm::CODE_BYTES, tmv, sl * Gm::SPAN, row0, h, id, &bar_full[stage]);
+            }
+            const size_t srow = ((size_t)id * Hkv + h) * a.block_size + row0;
+            if (k_row)
+              ptx::bulk_load(st + 2 * Gm::CODE_BYTES + s * seg_rows * 4, a.k_scale + srow, seg_rows * 4,
+                             &bar_full[stage]);
+            if (v_row)
+              ptx::bulk_load(st + 2 * Gm::CODE_BYTES + KT * 4 + s * seg_rows * 4, a.v_scale + srow, seg_rows * 4,
+                             &bar_full[stage]);
+          }
+        }
+      }
+      if (lane == 0) ptx::mbar_arrive(&bar_full[stage]);
+      __syncwarp();
+    }
+  }
+  // let every copy this warp issued land before the CTA can exit
+  if (lane == 0) {
+    for (uint32_t s = 0; s < S && s < it; ++s) {
+      const uint32_t last = it - 1 - ((it - 1 - s) % S);
+      if (!ptx::mbar_wait_bounded(&bar_full[s], (last / S) & 1)) atomicOr(a.err, KVQ_DEVERR_TIMEOUT);
+    }
+  }
+  __syncwarp();
+}
+
+}  // namespace kvq

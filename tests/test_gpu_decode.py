@@ -23,13 +23,15 @@ def lib():
     return kvq.load()
 
 
-def run_case(orc, w, *, window=0, gen="cpu", step=0, check_cache=True, max_seq_len=None):
+def run_case(orc, w, *, window=0, gen="cpu", step=0, check_cache=True, max_seq_len=None, q_scale=1.0):
     gw = GpuWorkload(w, gen_device=gen)
     gw.fill_history()
     k_new, v_new, slots = gw.new_tokens()
     params = gw.params(window=window, max_seq_len=max_seq_len)
     bufs = gw.buffers(params)
     q = w.q(gen, step).to("cuda")
+    if q_scale != 1.0:
+        q = (q.float() * q_scale).to(q.dtype)
     out, lse = gw.step(q, k_new, v_new, slots, params, bufs)
     torch.cuda.synchronize()
     assert kvq.kvq_get_device_error(clear=True) == 0
@@ -197,3 +199,40 @@ def test_many_query_rows_layout(lib, orc, case):
     run_case(orc, w)
     if W:
         run_case(orc, w, window=W, check_cache=False)
+
+
+TC = [
+    # dtype, D, G, T, k_mode, v_mode, softcap, window, sink, q_scale
+    # (rows = G*T in 17..48 at D 256, 17..64 at D 128: the tensor-memory layout)
+    (kvq.INT4, 256, 6, 8, kvq.PER_CHANNEL, kvq.PER_CHANNEL, 0.0, 0, False, 1.0),
+    (kvq.INT4, 256, 4, 5, kvq.PER_ROW, kvq.PER_ROW, 0.0, 0, True, 6.0),
+    (kvq.INT8, 256, 8, 6, kvq.PER_ROW, kvq.PER_ROW, 0.0, 0, False, 1.0),
+    (kvq.FP8_E4M3, 256, 6, 6, kvq.PER_TENSOR, kvq.PER_ROW, 30.0, 0, False, 6.0),
+    (kvq.INT8, 128, 8, 8, kvq.PER_CHANNEL, kvq.PER_TENSOR, 0.0, 200, True, 1.0),
+    (kvq.FP8_E4M3, 128, 7, 7, kvq.PER_ROW, kvq.PER_TENSOR, 0.0, 0, True, 1.0),
+    (kvq.INT4, 128, 5, 8, kvq.PER_ROW, kvq.PER_CHANNEL, 0.0, 0, False, 8.0),
+    (kvq.INT8, 128, 3, 6, kvq.PER_ROW, kvq.PER_ROW, 0.0, 0, False, 1.0),
+    (kvq.FP8_E4M3, 256, 8, 4, kvq.PER_CHANNEL, kvq.PER_CHANNEL, 0.0, 0, False, 1.0),
+]
+
+
+@pytest.mark.parametrize("case", TC, ids=lambda c: f"dt{c[0]}-D{c[1]}-rows{c[2] * c[3]}-km{c[4]}vm{c[5]}")
+def test_tensor_memory_layout(lib, orc, case):
+    """17..64 query rows per kv head on the tcgen05 path: every code type,
+    scale mode and head size it takes, ragged lengths over several 128-key
+    tiles and pieces, softcap / window / sink; q_scale > 1 sharpens the
+    logits so that row maxima move by more than 2^8 between tiles (the lazy
+    rescale of O and l).  Repeated decodes are bitwise identical."""
+    dt, D, G, T, km, vm, cap, W, sink, qs = case
+    Hkv, bs = 2, 32
+    L = np.array([1500, T - 1, 129, 128, 1, 700], np.int32)
+    mb = 48
+    w = synth.Workload("tc", dt, km, vm, len(L), G * Hkv, Hkv, D, T, bs, L,
+                       np.random.default_rng(G * T + D).permutation(len(L) * mb).astype(np.int32).reshape(len(L), mb),
+                       len(L) * mb, softcap=cap, use_sink=sink, k_channel_lognormal=0.5, seed=G * 100 + T + D)
+    gw, params, bufs, q, _ = run_case(orc, w, q_scale=qs)
+    ref = bufs.out.clone()
+    kvq.decode_step(gw.cache, params, q, gw.block_table, gw.seq_lens, bufs, gw.head_sink)
+    assert torch.equal(bufs.out, ref)
+    if W:
+        run_case(orc, w, window=W, check_cache=False, q_scale=qs)
