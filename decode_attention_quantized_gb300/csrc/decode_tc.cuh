@@ -18,21 +18,24 @@
 // PV product uses; a per-row V scale is folded into V^T (with a power-of-two
 // normaliser), so P holds plain softmax weights.
 //
-// Warp roles (10 warps):
-//   0-3  softmax: S^T out of TMEM (one key per thread, two passes over
-//        16-column chunks: row maxima, then P), scale / softcap / mask, P
-//        into shared memory, rescale of O when a row maximum moved; also the
-//        Q prologue of each piece and the epilogue (O / l out of TMEM,
-//        partial to the workspace)
-//   4-7  dequant: one key row per thread -> f16 K columns in TMEM, then
-//        ldmatrix.trans fragments -> V^T in TMEM (16x256b stores)
-//   8    TMA producer of the code stages (shared with decode.cuh)
-//   9    TMEM allocation; lane 0 issues every tcgen05.mma and commit
-// S^T is double-buffered in TMEM, so QK^T of the next tile runs while the
-// softmax warps work on the current one.  The softmax keeps a lazy reference
-// maximum per row: P = exp2(x - mu) with mu moved (and O, l rescaled) only
-// when a row maximum exceeds it by more than 8 (P <= 2^8 in f16, fp32
-// accumulators).
+// Warp roles (15 warps):
+//   0-3   softmax: S^T of a tile out of TMEM in one round trip (one key per
+//         thread), scale / softcap / mask, P into shared memory; exact row
+//         maxima (and a rescale of O, l) only when a logit exceeds its row's
+//         reference maximum by more than 8 (P <= 2^8 in f16, fp32
+//         accumulators); also the Q prologue and the epilogue of each piece
+//   4-7   K dequant: one key row per thread -> f16 K columns in TMEM, in two
+//         channel halves, each released by its half of QK^T
+//   8-11  V dequant: ldmatrix.trans fragments -> V^T in TMEM (16x256b
+//         stores), per 128-channel half; a per-row V scale is folded in
+//   12    TMA producer of the code stages (shared with decode.cuh)
+//   13    TMEM allocation; issues QK^T into a double-buffered S^T
+//   14    issues PV and the row sums
+// MMAs are issued by an elected lane of a converged warp, four k-steps per
+// asm block; bounded waits poll once inline and loop out of line.  The
+// code is kept compact (rolled loops where registers allow): fifteen
+// warps on four schedulers run six different loops, and a kernel whose
+// hot code outgrows the instruction caches stalls on instruction fetch.
 #pragma once
 
 #include "decode.cuh"
@@ -211,7 +214,7 @@ __global__ void __launch_bounds__(kTcWarps * 32, 1)
   using C = TcCfg<DT, D, NR>;
   using Gm = typename C::Gm;
   constexpr int KT = kTcKeys;
-  constexpr int kSoftmax = 0, kDqK = 4, kDqV = 8, kProducer = 12, kMma = 13;
+  constexpr int kSoftmax = 0, kDqK = 4, kDqV = 8, kProducer = 12, kMma = 13, kMmaPv = 14;
   constexpr int NKS = D / 16;  // k-steps of QK^T; the K tile is freed in two channel halves
   constexpr float kLog2e = 1.4426950408889634f;
   extern __shared__ __align__(16) uint8_t smem_raw[];
@@ -434,101 +437,77 @@ __global__ void __launch_bounds__(kTcWarps * 32, 1)
         if (lane == 0) ptx::mbar_arrive(&bar_empty[stage]);
       }
     }
-  } else if (warp == kMma) {
+  } else if (warp == kMma || warp == kMmaPv) {
     // ================================================================ MMA
-    // The whole warp runs this loop (waits included) and stays converged;
-    // one elected lane issues every MMA and commit.  Step j issues QK^T of
-    // tile j (if any) and then PV of tile j - 1 (if any), so the next scores
-    // are computed while the softmax warps work on the current ones; each
-    // operand half is released as soon as the MMAs that read it complete.
-    // MMA runs are 4 k-steps (one 128-byte swizzle row) per loop trip: the
-    // descriptors advance by a 32-bit add, and the loops stay small.
+    // Two issuing warps on different schedulers: warp kMma issues QK^T of
+    // every tile, warp kMmaPv its PV and row sums (their TMEM regions and
+    // shared operands are disjoint; the softmax orders the two).  Each warp
+    // runs its loop whole and converged; one elected lane issues every MMA
+    // and commit.  Runs of 4 k-steps (one 128-byte swizzle row of B) are one
+    // asm block; each operand half is released as soon as the MMAs that
+    // read it complete.
     constexpr uint32_t idesc = ptx::idesc_f16_f32(128, NR);
     const uint64_t q_desc = ptx::smem_desc_sw128(ptx::smem_u32(q_s));
     const uint32_t q_lo = (uint32_t)q_desc, d_hi = (uint32_t)(q_desc >> 32);
     const uint32_t p_lo = (uint32_t)ptx::smem_desc_sw128(ptx::smem_u32(p_s));
     constexpr uint32_t kSlabDesc = (NR * 128) >> 4;  // descriptor step between 64-element K slabs
-    // 4 k-steps of D (+)= A * B^T over one 128-byte row of B (64 K elements);
-    // A advances a_step columns per k-step (0: the same 16 columns each
-    // time, the ones of the row sums); accumulate unless acc0 == 0
-    auto mma4 = [&](uint32_t d, uint32_t a_col, uint32_t a_step, uint32_t b_lo, uint32_t acc0) {
-      ptx::mma_f16_ts(d, a_col, b_lo, d_hi, idesc, acc0);
-      ptx::mma_f16_ts(d, a_col + a_step, b_lo + 2, d_hi, idesc, 1u);
-      ptx::mma_f16_ts(d, a_col + 2 * a_step, b_lo + 4, d_hi, idesc, 1u);
-      ptx::mma_f16_ts(d, a_col + 3 * a_step, b_lo + 6, d_hi, idesc, 1u);
-    };
-    uint32_t it = 0, prev = 0;
-    bool have_prev = false, prev_first = false;
-    int pc = 0, gt = sp.t_begin, next = 0, k0 = 0, k1 = 0, key0 = 0;
-    if (gt < sp.t_end) {
-      int b, h, L, u;
+    const bool qk_warp = warp == kMma;
+    uint32_t it = 0;
+    int pc = 0;
+    for (int gt = sp.t_begin, next; gt < sp.t_end; gt = next, ++pc) {
+      int b, h, k0, k1, L, u;
       sp.piece(a, gt, b, h, k0, k1, L, u, next);
-      key0 = k0;
-    }
-    while (have_prev || gt < sp.t_end) {
-      if (gt < sp.t_end) {
-        // ---- QK^T of tile `it` (two channel halves, each committed)
+      for (int key0 = k0; key0 < k1; key0 += KT, ++it) {
         const bool first = key0 == k0;
-        if (first) wait(b_qfull, pc & 1);
-        if (it >= 2) wait(&b_sfree[it & 1], ((it - 2) >> 1) & 1);  // the softmax is done with this S buffer
-        const uint32_t s_col = tmem + C::S_COL + (it & 1) * NR;
+        if (qk_warp) {
+          // ---- QK^T of tile `it` (two channel halves, each committed)
+          if (first) wait(b_qfull, pc & 1);
+          if (it >= 2) wait(&b_sfree[it & 1], ((it - 2) >> 1) & 1);  // the softmax is done with this S buffer
+          const uint32_t s_col = tmem + C::S_COL + (it & 1) * NR;
 #pragma unroll 1
-        for (int half = 0; half < 2; ++half) {
-          wait(&b_kfull[half], it & 1);
+          for (int half = 0; half < 2; ++half) {
+            wait(&b_kfull[half], it & 1);
+            __syncwarp();
+            ptx::tc_fence_after();
+#pragma unroll 1
+            for (int sl = half * (D / 128); sl < (half + 1) * (D / 128); ++sl)
+              ptx::mma_f16_ts_x4(s_col, tmem + C::K_COL + 32 * sl, 8, q_lo + sl * kSlabDesc, d_hi, idesc,
+                                 sl > 0 ? 1u : 0u);
+            ptx::mma_commit(half == 0 ? b_kh0 : &b_qk[it & 1]);
+          }
+        } else {
+          // ---- PV and row sums of tile `it`.  A piece's first PV overwrites
+          // O and l: the softmax warps read the previous piece's out before
+          // they release that tile's P buffer.
+          wait(&b_pfull[it & 1], (it >> 1) & 1);
           __syncwarp();
           ptx::tc_fence_after();
-#pragma unroll 1
-          for (int sl = half * (D / 128); sl < (half + 1) * (D / 128); ++sl)
-            mma4(s_col, tmem + C::K_COL + 32 * sl, 8, q_lo + sl * kSlabDesc, sl > 0 ? 1u : 0u);
-          ptx::mma_commit(half == 0 ? b_kh0 : &b_qk[it & 1]);
-        }
-      }
-      if (have_prev) {
-        // ---- PV and row sums of tile `prev`
-        const uint32_t t = prev;
-        wait(&b_pfull[t & 1], (t >> 1) & 1);
-        __syncwarp();
-        ptx::tc_fence_after();
-        const uint32_t pb = p_lo + (t & 1) * (C::P_BYTES >> 4);
-        const uint32_t acc0 = prev_first ? 0u : 1u;
-        // (a piece's first PV overwrites O and l: the softmax warps read the
-        // previous piece's out before they release that tile's P buffer)
-#pragma unroll 1
-        for (int sl = 0; sl < 2; ++sl) mma4(tmem + C::L_COL, tmem + C::ONE_COL, 0, pb + sl * kSlabDesc, sl ? 1u : acc0);
-#pragma unroll 1
-        for (int hh = 0; hh < C::NH; ++hh) {
-          wait(&b_vfull[hh], t & 1);
-          __syncwarp();
-          ptx::tc_fence_after();
+          const uint32_t pb = p_lo + (it & 1) * (C::P_BYTES >> 4);
+          const uint32_t acc0 = first ? 0u : 1u;
 #pragma unroll 1
           for (int sl = 0; sl < 2; ++sl)
-            mma4(tmem + C::O_COL + hh * NR, tmem + C::V_COL + 64 * hh + 32 * sl, 8, pb + sl * kSlabDesc, sl ? 1u : acc0);
-          ptx::mma_commit(&b_vh[hh]);
-        }
-        ptx::mma_commit(&b_pv[t & 1]);
-        have_prev = false;
-      }
-      if (gt < sp.t_end) {
-        have_prev = true;
-        prev = it;
-        prev_first = key0 == k0;
-        ++it;
-        key0 += KT;
-        if (key0 >= k1) {  // next piece
-          gt = next;
-          ++pc;
-          if (gt < sp.t_end) {
-            int b, h, L, u;
-            sp.piece(a, gt, b, h, k0, k1, L, u, next);
-            key0 = k0;
+            ptx::mma_f16_ts_x4(tmem + C::L_COL, tmem + C::ONE_COL, 0, pb + sl * kSlabDesc, d_hi, idesc,
+                               sl ? 1u : acc0);
+#pragma unroll 1
+          for (int hh = 0; hh < C::NH; ++hh) {
+            wait(&b_vfull[hh], it & 1);
+            __syncwarp();
+            ptx::tc_fence_after();
+#pragma unroll 1
+            for (int sl = 0; sl < 2; ++sl)
+              ptx::mma_f16_ts_x4(tmem + C::O_COL + hh * NR, tmem + C::V_COL + 64 * hh + 32 * sl, 8,
+                                 pb + sl * kSlabDesc, d_hi, idesc, sl ? 1u : acc0);
+            ptx::mma_commit(&b_vh[hh]);
           }
+          ptx::mma_commit(&b_pv[it & 1]);
         }
       }
     }
     if (it > 0) {
-      // every MMA has completed before TMEM can be released
+      // every MMA this warp issued has completed before TMEM can be released
       const uint32_t last = it - 1;
-      if (!ptx::mbar_wait_bounded(&b_pv[last & 1], (last >> 1) & 1) && lane == 0) atomicOr(a.err, KVQ_DEVERR_TIMEOUT);
+      uint64_t* done = qk_warp ? &b_qk[last & 1] : &b_pv[last & 1];
+      if (!ptx::mbar_wait_bounded(done, (last >> 1) & 1) && lane == 0) atomicOr(a.err, KVQ_DEVERR_TIMEOUT);
     }
     __syncwarp();
   } else {

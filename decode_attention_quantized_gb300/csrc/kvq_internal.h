@@ -65,10 +65,10 @@ struct CombineArgs {
 };
 
 // The tensor-memory decode kernel (many query rows per kv head): 128 keys per
-// stage and per MMA tile, 14 warps, and its shared-memory layout (byte offsets
+// stage and per MMA tile, 15 warps, and its shared-memory layout (byte offsets
 // from the 1024-aligned base; the host adds 1024 bytes of alignment slack).
 constexpr int kTcKeys = 128;
-constexpr int kTcWarps = 14;
+constexpr int kTcWarps = 15;
 
 struct TcSmem {
   int ring, q, p, scr, pre, bars, slot, total;

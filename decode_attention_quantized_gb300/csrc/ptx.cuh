@@ -270,6 +270,27 @@ __device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uin
       : "memory");
 }
 
+// Four consecutive k-steps of D (+)= A[tmem] * B[smem]^T in one block: one
+// elect.sync, A at a_tmem + j * a_step, B descriptor low half b_lo + 2 j
+// (one 32-byte step of a 128-byte swizzle row), the first step accumulating
+// unless accumulate == 0.  Called by a whole converged warp.
+__device__ __forceinline__ void mma_f16_ts_x4(uint32_t d_tmem, uint32_t a_tmem, uint32_t a_step, uint32_t b_lo,
+                                              uint32_t b_hi, uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, t, e;\n\t.reg .b32 a1, a2, a3, l1, l2, l3;\n\t.reg .b64 b0, b1, b2, b3;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\tsetp.ne.b32 t, %5, 0;\n\t"
+      "add.u32 a1, %1, %2;\n\tadd.u32 a2, a1, %2;\n\tadd.u32 a3, a2, %2;\n\t"
+      "add.u32 l1, %3, 2;\n\tadd.u32 l2, %3, 4;\n\tadd.u32 l3, %3, 6;\n\t"
+      "mov.b64 b0, {%3, %4};\n\tmov.b64 b1, {l1, %4};\n\tmov.b64 b2, {l2, %4};\n\tmov.b64 b3, {l3, %4};\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], b0, %5, p;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a1], b1, %5, t;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a2], b2, %5, t;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a3], b3, %5, t;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "r"(a_step), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Arrive on an mbarrier once every tcgen05.mma issued so far by the elected
 // lane has completed (called by the whole warp, like mma_f16_ts).
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
