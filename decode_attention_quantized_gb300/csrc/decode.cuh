@@ -256,9 +256,11 @@ __global__ void __launch_bounds__(288, MINB)
     }
     ptx::fence_mbar_init();
   }
-  // everything above touched only shared memory; inputs may still be in
-  // flight from the previous kernel on the stream
-  ptx::griddep_wait();
+  // Only inputs that no kvq kernel writes (seq_lens, block table, q, static
+  // scales) are read before the wait on the preceding grid on the stream:
+  // the producer waits before its first cache read and the consumers before
+  // their first workspace write, so the plan, the first block ids and the Q
+  // prologue overlap that grid's tail.
   const Slice<kTile> sp = build_slice<kTile>(a, pl_pre, pl_misc);
   const int t_begin = sp.t_begin, t_end = sp.t_end;
   auto piece = [&](int gt, int& b, int& h, int& k0, int& k1, int& L, int& slot, int& next) {
@@ -269,7 +271,7 @@ __global__ void __launch_bounds__(288, MINB)
 
   // =============================================================== producer
   if (warp == n_cw) {
-    produce<Gm>(a, sp, &tmk, &tmv, ring, bar_full, bar_empty);
+    produce<Gm>(a, sp, &tmk, &tmv, ring, bar_full, bar_empty, pl_pre, pl_misc);
     return;
   }
 
@@ -327,6 +329,7 @@ __global__ void __launch_bounds__(288, MINB)
         }
         if (c == 0) s_alpha[row] = ag;
       }
+      ptx::griddep_wait();  // before the first workspace write (no-op after the first)
       ptx::named_bar_sync(1, 8 * 32);
       float al[NT][2], m[NT][2], l[NT][2];
       int pos[NT][2];
@@ -668,6 +671,7 @@ __global__ void __launch_bounds__(288, MINB)
     // ---- Q prologue: this lane's channels of query row g of the row group
     uint32_t qf[Gm::NMT][2];
     const float alpha_g = dev::q_prologue<DT, D>(a, rg * 8 + g, b, h, c, qf);
+    ptx::griddep_wait();  // before the first workspace write (no-op after the first)
     const int r0 = rg * 8 + 2 * c, r1 = r0 + 1;
     const float al0 = __shfl_sync(0xffffffffu, alpha_g, (2 * c) * 4);
     const float al1 = __shfl_sync(0xffffffffu, alpha_g, (2 * c + 1) * 4);

@@ -270,9 +270,12 @@ __global__ void __launch_bounds__(kTcWarps * 32, 1)
     ptx::tmem_alloc(tmem_slot, C::TMEM_COLS);
     ptx::tc_fence_before();
   }
-  // everything above touched only shared memory and TMEM; inputs may still
-  // be in flight from the previous kernel on the stream
-  ptx::griddep_wait();
+  // Only inputs that no kvq kernel writes (seq_lens, block table, q, static
+  // scales) are read before the wait on the preceding grid on the stream:
+  // the producer waits before its first cache read, the softmax warps before
+  // their first workspace write (the other roles touch only shared memory and
+  // TMEM), so the plan, the first block ids and the Q prologue overlap that
+  // grid's tail.
   const Slice<KT> sp = build_slice<KT>(a, pl_pre, pl_misc);
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
@@ -287,7 +290,7 @@ __global__ void __launch_bounds__(kTcWarps * 32, 1)
 
   if (warp == kProducer) {
     // ============================================================ producer
-    produce<Gm>(a, sp, &tmk, &tmv, ring, bar_full, bar_empty);
+    produce<Gm>(a, sp, &tmk, &tmv, ring, bar_full, bar_empty, pl_pre, pl_misc);
   } else if (warp >= kDqK && warp < kDqK + 4) {
     // ========================================================== K dequant
     // thread = key 32 q + lane of the tile = TMEM lane of the K operand; the
@@ -674,6 +677,7 @@ __global__ void __launch_bounds__(kTcWarps * 32, 1)
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(b_qfull);
       }
+      ptx::griddep_wait();  // before the first workspace write (no-op after the first)
       if (pc > 0) epilogue(e_u, e_last, e_mu0, e_mu1, e_F);
       if (!more) break;
       ptx::named_bar_sync(1, 128);  // this piece's row factors are visible

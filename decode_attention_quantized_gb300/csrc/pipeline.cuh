@@ -91,8 +91,10 @@ struct Slice {
 };
 
 // Builds the plan in shared memory (pl_pre [B + 1], pl_misc [4]); every
-// thread of the CTA calls it after griddep_wait.  CTA 0 also publishes it to
-// the workspace for the combine.  Flags seq_lens outside [0, capacity].
+// thread of the CTA calls it.  It reads only seq_lens, which no kvq kernel
+// writes, so it runs before the wait on the preceding grid; the producer
+// publishes the plan to the workspace after that wait (publish_slice).
+// Flags seq_lens outside [0, capacity].
 template <int KT>
 __device__ Slice<KT> build_slice(const DecodeArgs& a, int* pl_pre, int* pl_misc) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -139,21 +141,29 @@ __device__ Slice<KT> build_slice(const DecodeArgs& a, int* pl_pre, int* pl_misc)
   const int W = pl_misc[0];
   sp.t_begin = min((int)blockIdx.x * W, pl_misc[1]);
   sp.t_end = min(sp.t_begin + W, pl_misc[1]);
-  if (blockIdx.x == 0) {
-    for (int i = tid; i <= B; i += blockDim.x) a.plan[4 + i] = pl_pre[i];
-    if (tid == 0) {
-      a.plan[0] = W;
-      a.plan[1] = pl_misc[1];
-      a.plan[2] = B;
-      a.plan[3] = a.units_max;
-    }
-  }
   return sp;
+}
+
+// CTA 0 copies the plan into the workspace for the combine (one warp, after
+// the wait on the preceding grid: that grid may still read the workspace).
+__device__ __forceinline__ void publish_slice(const DecodeArgs& a, const int* pl_pre, const int* pl_misc) {
+  if (blockIdx.x != 0) return;
+  const int lane = threadIdx.x & 31;
+  for (int i = lane; i <= a.batch; i += 32) a.plan[4 + i] = pl_pre[i];
+  if (lane == 0) {
+    a.plan[0] = pl_misc[0];
+    a.plan[1] = pl_misc[1];
+    a.plan[2] = a.batch;
+    a.plan[3] = a.units_max;
+  }
 }
 
 // The producer warp.  The whole warp fetches a piece's block ids 32 pages at
 // a time (one coalesced load per 32 pages) and hands them to lane 0 by
-// shuffles; lane 0 waits for a free stage, then for each page segment of the
+// shuffles.  The first piece's ids are read before the wait on the preceding
+// grid (no kvq kernel writes the block table); the cache is read, and the
+// plan published, only after it.  Lane 0 waits for a free stage, then for
+// each page segment of the
 // stage adds the segment's bytes to the stage's transaction count and issues
 // one TMA tensor copy per (slab, side) with the block id as the outer
 // coordinate, plus 1-D bulk copies of the per-row scales; its single arrival
@@ -165,9 +175,17 @@ __device__ Slice<KT> build_slice(const DecodeArgs& a, int* pl_pre, int* pl_misc)
 // footprint small.
 template <class Gm>
 __device__ void produce(const DecodeArgs& a, const Slice<Gm::KEYS>& sp, const CUtensorMap* tmk,
-                        const CUtensorMap* tmv, uint8_t* ring, uint64_t* bar_full, uint64_t* bar_empty) {
+                        const CUtensorMap* tmv, uint8_t* ring, uint64_t* bar_full, uint64_t* bar_empty,
+                        const int* pl_pre, const int* pl_misc) {
   constexpr int KT = Gm::KEYS;
   const int lane = threadIdx.x & 31;
+  bool waited = false;
+  auto gate = [&]() {
+    if (waited) return;
+    ptx::griddep_wait();
+    publish_slice(a, pl_pre, pl_misc);
+    waited = true;
+  };
   const bool k_row = a.k_mode == KVQ_SCALE_PER_ROW, v_row = a.v_mode == KVQ_SCALE_PER_ROW;
   const int Hkv = a.num_kv_heads;
   const int seg_rows = min(a.block_size, kTile);  // rows of one TMA box
@@ -182,6 +200,7 @@ __device__ void produce(const DecodeArgs& a, const Slice<Gm::KEYS>& sp, const CU
     const int p_last = (k1 - 1) >> a.log2_bs;
     int base = k0 >> a.log2_bs;
     int my_id = base + lane <= p_last ? bt[base + lane] : -1;
+    gate();
     for (int key0 = k0; key0 < k1; key0 += KT, ++it) {
       const int stage = (int)(it % S);
       if (lane == 0 && it >= S && ok) {
@@ -226,6 +245,7 @@ __device__ void produce(const DecodeArgs& a, const Slice<Gm::KEYS>& sp, const CU
       __syncwarp();
     }
   }
+  gate();  // (an empty slice still publishes the plan from CTA 0)
   // let every copy this warp issued land before the CTA can exit
   if (lane == 0) {
     for (uint32_t s = 0; s < S && s < it; ++s) {

@@ -159,7 +159,15 @@ KVQ_API kvq_status kvq_decode_workspace_size(const kvq_cache* cache,
  * kvq_decode_workspace_size bytes, 256-byte aligned).  The result is
  * completed by kvq_combine with the same cache, params and workspace on the
  * same stream.  Per query row, logits are sm_scale * <q, k_j>, capped by
- * softcap, masked to keys j <= pos (and j > pos - window when set). */
+ * softcap, masked to keys j <= pos (and j > pos - window when set).
+ * The kvq kernels let the next kernel on the stream start early
+ * (programmatic dependent launch).  kvq_decode reads q, block_table,
+ * seq_lens and the static (PER_TENSOR / PER_CHANNEL) scales before it waits
+ * for the kernel launched just before it on the stream to finish, and reads
+ * the cache and writes the workspace only after that wait: q, block_table,
+ * seq_lens and those scales must therefore not be outputs of that preceding
+ * kvq kernel (kvq_combine's out or lse_out).  Outputs of any other kernel
+ * are safe: such a kernel completes before kvq_decode starts. */
 KVQ_API kvq_status kvq_decode(const kvq_cache* cache, const kvq_decode_params* params,
                               const void* q, const int32_t* block_table,
                               const int32_t* seq_lens, void* workspace,
