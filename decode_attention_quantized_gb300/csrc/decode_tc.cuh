@@ -543,39 +543,39 @@ __global__ void __launch_bounds__(kTcWarps * 32, 1)
     constexpr int LPR = D / 8, RPP = 32 / LPR, NQR = NR / (4 * RPP);
     const int rsub = lane / LPR, cl = lane % LPR;
 
-    // Epilogue of a piece: O and row sums out of TMEM (16 rows at a time),
-    // the normalized partial and its base-2 log-sum-exp to the workspace.
+    // Epilogue of a piece: O and row sums out of TMEM 16 rows at a time, the
+    // normalized partial and its base-2 log-sum-exp to the workspace.  Run
+    // once per piece, so kept small (its code is cold by then).
     auto epilogue = [&](int u, uint32_t last, float m0, float m1, int F) {
       wait(&b_pv[last & 1], (last >> 1) & 1);
       ptx::tc_fence_after();
       float to_true = v_row ? dev::pow2i(F) : 1.0f;
       if constexpr (DT == KVQ_FP8_E4M3) to_true *= 256.0f;
+      float* lse = a.part_lse + (size_t)u * rows;
 #pragma unroll 1
-      for (int r0 = 0; r0 < NR; r0 += 16) {
-        float l16[16], inv[16];
-        dev::tmem_ld_cols<16>(t_lane + C::L_COL + r0, l16);
+      for (int r0 = 0; r0 < rows; r0 += 16) {
+        float inv[16];  // the row sums l, turned into the output factors in place
+        dev::tmem_ld_cols<16>(t_lane + C::L_COL + r0, inv);
+        // every lane holds all 16 sums; lane j + (r0 & 31) takes row r0 + j's
+        const int j = lane - (r0 & 31);
+        float lj = 0.0f;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) inv[i] = l16[i] > 0.0f ? to_true * __frcp_rn(l16[i]) : 0.0f;
-#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          lj = j == i ? inv[i] : lj;
+          inv[i] = inv[i] > 0.0f ? to_true * ptx::fast_rcp(inv[i]) : 0.0f;
+        }
+        if (q == 0 && j >= 0 && j < 16 && r0 + j < rows)
+          lse[r0 + j] = lj > 0.0f ? (r0 + j < 32 ? m0 : m1) + ptx::fast_log2(lj) : -INFINITY;
+#pragma unroll 1
         for (int hh = 0; hh < C::NH; ++hh) {
-          float o16[16];
-          dev::tmem_ld_cols<16>(t_lane + C::O_COL + hh * NR + r0, o16);
+          float o[16];
+          dev::tmem_ld_cols<16>(t_lane + C::O_COL + hh * NR + r0, o);
           const int ch = dev::tc_out_channel<DT>(hh, q, lane);
           const float cf = (ch & 1) ? dev::odd_channel_factor<DT>() : 1.0f;
           float* dst = a.part_o + ((size_t)u * rows + r0) * D + ch;
 #pragma unroll
           for (int i = 0; i < 16; ++i)
-            if (r0 + i < rows) dst[(size_t)i * D] = o16[i] * inv[i] * cf;
-        }
-        if (q == 0) {
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const int r = r0 + i;
-            if (r < rows && (r & 31) == lane) {
-              const float mu = r < 32 ? m0 : m1;
-              a.part_lse[(size_t)u * rows + r] = l16[i] > 0.0f ? mu + ptx::fast_log2(l16[i]) : -INFINITY;
-            }
-          }
+            if (r0 + i < rows) dst[(size_t)i * D] = o[i] * inv[i] * cf;
         }
       }
       ptx::tc_fence_before();
@@ -597,7 +597,7 @@ __global__ void __launch_bounds__(kTcWarps * 32, 1)
       // QK^T, so the buffer is free): per-channel K scale folded in under a
       // power-of-two normaliser, each row normalised by the power of two just
       // above its maximum, f16 in the MMA's K order, 128-byte swizzle.  Rows
-      // are taken one per loop trip with the next row's load in flight.
+      // are taken one per loop trip with the next three rows' loads in flight.
       if (more) {
         const bool kc = a.k_mode == KVQ_SCALE_PER_CHANNEL;
         auto q_row = [&](int i) -> uint4 {
@@ -606,7 +606,7 @@ __global__ void __launch_bounds__(kTcWarps * 32, 1)
                                 a.q + (((size_t)b * T + r / G) * Hq + (size_t)h * G + r % G) * D + 8 * cl))
                           : make_uint4(0, 0, 0, 0);
         };
-        uint4 raw = q_row(0);
+        uint4 ra = q_row(0), rb = q_row(1), rc = q_row(2);  // three row loads in flight
         float ksv[8];
         int ek = 0;
         if (kc) {
@@ -630,8 +630,10 @@ __global__ void __launch_bounds__(kTcWarps * 32, 1)
 #pragma unroll 1
         for (int i = 0; i < NQR; ++i) {
           const int r = (q + 4 * i) * RPP + rsub;
-          const uint4 cur = raw;
-          if (i + 1 < NQR) raw = q_row(i + 1);
+          const uint4 cur = ra;
+          ra = rb;
+          rb = rc;
+          if (i + 3 < NQR) rc = q_row(i + 3);
           float qv[8];
           const uint32_t ww[4] = {cur.x, cur.y, cur.z, cur.w};
 #pragma unroll

@@ -20,13 +20,14 @@ constexpr int round_up_c(int x, int m) { return (x + m - 1) / m * m; }
 // One stage holds KT keys: the K code rows, then the V code rows, each as
 // SLABS column slabs of [KT rows][SPAN bytes] in the TMA swizzle, then KT K
 // scales and KT V scales (fp32, per-row mode only).
-template <int DT, int D, int KT = kTile>
+template <int DT, int D_, int KT = kTile>
 struct Geo {
-  static constexpr int DP = DT == KVQ_INT4 ? D / 2 : D;  // bytes per cached row
+  static constexpr int D = D_;
+  static constexpr int DP = DT == KVQ_INT4 ? D_ / 2 : D_;  // bytes per cached row
   static constexpr int SPAN = DP >= 128 ? 128 : DP;      // TMA box inner bytes = swizzle span
   static constexpr int SLABS = DP / SPAN;                // column slabs per row
   static constexpr int NCH = DP / 16;                    // 16-byte chunks per row
-  static constexpr int NMT = D / 16;                     // 16-channel MMA tiles
+  static constexpr int NMT = D_ / 16;                      // 16-channel MMA tiles
   static constexpr int KEYS = KT;                        // keys per stage
   static constexpr int CODE_BYTES = KT * DP;             // one side of one stage
   static constexpr int STAGE_STRIDE = round_up_c(2 * CODE_BYTES + 2 * KT * 4, 1024);
@@ -201,6 +202,16 @@ __device__ void produce(const DecodeArgs& a, const Slice<Gm::KEYS>& sp, const CU
     int base = k0 >> a.log2_bs;
     int my_id = base + lane <= p_last ? bt[base + lane] : -1;
     gate();
+    if (gt != sp.t_begin) {
+      // the consumers read this piece's query rows once the previous piece
+      // ends; the producer runs a ring ahead of them, so it pulls those rows
+      // into L2 now (G heads of one kv head are contiguous per token)
+      const int lines = a.group * Gm::D * 2 / 128;
+      for (int i = lane; i < a.q_tokens * lines; i += 32) {
+        const int t = i / lines, c = i - t * lines;
+        ptx::prefetch_l2(a.q + (((size_t)b * a.q_tokens + t) * a.num_q_heads + (size_t)h * a.group) * Gm::D + c * 64);
+      }
+    }
     for (int key0 = k0; key0 < k1; key0 += KT, ++it) {
       const int stage = (int)(it % S);
       if (lane == 0 && it >= S && ok) {

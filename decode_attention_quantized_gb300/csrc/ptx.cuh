@@ -157,6 +157,14 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
+// 1 / x by the SFU's approximate reciprocal (within 1 ulp per the PTX ISA;
+// flushes subnormal inputs and results to zero).
+__device__ __forceinline__ float fast_rcp(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 __device__ __forceinline__ float fast_log2(float x) {
   float y;
   asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -179,6 +187,11 @@ __device__ __forceinline__ float redux_max(float x) {
   float y;
   asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(y) : "f"(x));
   return y;
+}
+
+// Pulls the 128-byte line holding `p` into L2.
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(p));
 }
 
 // Makes this thread's generic-proxy shared-memory writes visible to the async
