@@ -271,7 +271,7 @@ __global__ void __launch_bounds__(288, MINB)
 
   // =============================================================== producer
   if (warp == n_cw) {
-    produce<Gm>(a, sp, &tmk, &tmv, ring, bar_full, bar_empty, pl_pre, pl_misc);
+    produce<Gm, true>(a, sp, &tmk, &tmv, ring, bar_full, bar_empty, pl_pre, pl_misc);
     return;
   }
 
@@ -354,7 +354,7 @@ __global__ void __launch_bounds__(288, MINB)
       for (int key0 = k0; key0 < k1; key0 += kTile, ++it) {
         const int stage = (int)(it % (uint32_t)a.stages);
         if (ok) {
-          ok = ptx::mbar_wait_bounded(&bar_full[stage], (it / a.stages) & 1);
+          ok = ptx::mbar_wait_bounded_inl(&bar_full[stage], (it / a.stages) & 1);
           if (!ok) atomicOr(a.err, KVQ_DEVERR_TIMEOUT);
         }
         const uint8_t* st = ring + (size_t)stage * Gm::STAGE_STRIDE;
@@ -688,7 +688,7 @@ __global__ void __launch_bounds__(288, MINB)
     for (int key0 = k0; key0 < k1; key0 += kTile, ++it) {
       const int stage = (int)(it % (uint32_t)a.stages);
       if (ok) {
-        ok = ptx::mbar_wait_bounded(&bar_full[stage], (it / a.stages) & 1);
+        ok = ptx::mbar_wait_bounded_inl(&bar_full[stage], (it / a.stages) & 1);
         if (!ok) atomicOr(a.err, KVQ_DEVERR_TIMEOUT);
       }
       const uint8_t* st = ring + (size_t)stage * Gm::STAGE_STRIDE;

@@ -290,7 +290,7 @@ __global__ void __launch_bounds__(kTcWarps * 32, 1)
 
   if (warp == kProducer) {
     // ============================================================ producer
-    produce<Gm>(a, sp, &tmk, &tmv, ring, bar_full, bar_empty, pl_pre, pl_misc);
+    produce<Gm, false>(a, sp, &tmk, &tmv, ring, bar_full, bar_empty, pl_pre, pl_misc);
   } else if (warp >= kDqK && warp < kDqK + 4) {
     // ========================================================== K dequant
     // thread = key 32 q + lane of the tile = TMEM lane of the K operand; the

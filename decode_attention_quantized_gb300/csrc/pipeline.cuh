@@ -163,18 +163,20 @@ __device__ __forceinline__ void publish_slice(const DecodeArgs& a, const int* pl
 // a time (one coalesced load per 32 pages) and hands them to lane 0 by
 // shuffles.  The first piece's ids are read before the wait on the preceding
 // grid (no kvq kernel writes the block table); the cache is read, and the
-// plan published, only after it.  Lane 0 waits for a free stage, then for
-// each page segment of the
-// stage adds the segment's bytes to the stage's transaction count and issues
-// one TMA tensor copy per (slab, side) with the block id as the outer
-// coordinate, plus 1-D bulk copies of the per-row scales; its single arrival
-// after the last segment lets the phase complete.  A block id outside
+// plan published, only after it.  Lane 0 waits for a free stage and issues,
+// per page segment of the stage, one TMA tensor copy per (slab, side) with
+// the block id as the outer coordinate, plus 1-D bulk copies of the per-row
+// scales.  kBurst: the whole stage's block ids are resolved first and its
+// copies go out in one unrolled burst under a single expect-tx arrival (the
+// mma.sync kernel, whose stages of small pages want a short issue path).
+// Otherwise the segment loop stays rolled, each segment adding its bytes to
+// the transaction count, with one arrival after the last (the tensor-memory
+// kernel, whose fifteen warps share four schedulers and which stalls on
+// instruction fetch when its code grows).  A block id outside
 // [0, num_blocks) is flagged and its rows are not loaded.  Returns after
 // every copy it issued has landed, so the CTA never exits with a copy in
-// flight.  The segment loop is not unrolled: the producer shares its
-// scheduler with compute warps, and a small loop keeps their instruction
-// footprint small.
-template <class Gm>
+// flight.
+template <class Gm, bool kBurst>
 __device__ void produce(const DecodeArgs& a, const Slice<Gm::KEYS>& sp, const CUtensorMap* tmk,
                         const CUtensorMap* tmv, uint8_t* ring, uint64_t* bar_full, uint64_t* bar_empty,
                         const int* pl_pre, const int* pl_misc) {
@@ -215,34 +217,49 @@ __device__ void produce(const DecodeArgs& a, const Slice<Gm::KEYS>& sp, const CU
     for (int key0 = k0; key0 < k1; key0 += KT, ++it) {
       const int stage = (int)(it % S);
       if (lane == 0 && it >= S && ok) {
-        ok = ptx::mbar_wait_bounded(&bar_empty[stage], ((it / S) - 1) & 1) ? 1 : 0;
+        ok = (kBurst ? ptx::mbar_wait_bounded_inl(&bar_empty[stage], ((it / S) - 1) & 1)
+                     : ptx::mbar_wait_bounded(&bar_empty[stage], ((it / S) - 1) & 1)) ? 1 : 0;
         if (!ok) atomicOr(a.err, KVQ_DEVERR_TIMEOUT);
       }
       ok = __shfl_sync(0xffffffffu, ok, 0);
       uint8_t* st = ring + (size_t)stage * Gm::STAGE_STRIDE;
       const int kend = ok ? min(key0 + KT, k1) : key0;  // nothing is loaded after a timeout
-#pragma unroll 1
-      for (int skey = key0; skey < kend; skey += seg_rows) {
-        const int page = skey >> a.log2_bs;
-        if (page - base >= 32) {
-          base += 32;
-          my_id = base + lane <= p_last ? bt[base + lane] : -1;
-        }
-        const int id = __shfl_sync(0xffffffffu, my_id, page - base);
-        if (lane == 0) {
+      if constexpr (kBurst) {
+        // the stage's block ids first (whole warp), then one burst of copies
+        // from lane 0 under a single expect-tx arrival
+        int blk[KT / 16];
+        uint32_t bytes = 0;
+  #pragma unroll
+        for (int s = 0; s < KT / 16; ++s) {
+          blk[s] = -1;
+          const int skey = key0 + s * seg_rows;
+          if (skey >= kend) continue;
+          const int page = skey >> a.log2_bs;
+          if (page - base >= 32) {
+            base += 32;
+            my_id = base + lane <= p_last ? bt[base + lane] : -1;
+          }
+          const int id = __shfl_sync(0xffffffffu, my_id, page - base);
           if (id < 0 || id >= a.num_blocks) {
-            atomicOr(a.err, KVQ_DEVERR_BLOCK_ID);
-          } else {
-            const int s = (skey - key0) / seg_rows;
-            const int row0 = skey & (a.block_size - 1);
-            ptx::mbar_expect_tx(&bar_full[stage], seg_bytes);
-#pragma unroll
+            if (lane == 0) atomicOr(a.err, KVQ_DEVERR_BLOCK_ID);
+            continue;
+          }
+          blk[s] = id;
+          bytes += seg_bytes;
+        }
+        if (lane == 0) {
+          ptx::mbar_arrive_expect_tx(&bar_full[stage], bytes);
+  #pragma unroll
+          for (int s = 0; s < KT / 16; ++s) {
+            if (blk[s] < 0) continue;
+            const int row0 = (key0 + s * seg_rows) & (a.block_size - 1);
+  #pragma unroll
             for (int sl = 0; sl < Gm::SLABS; ++sl) {
               uint8_t* dk = st + sl * (KT * Gm::SPAN) + s * seg_rows * Gm::SPAN;
-              ptx::tma_load_4d(dk, tmk, sl * Gm::SPAN, row0, h, id, &bar_full[stage]);
-              ptx::tma_load_4d(dk + Gm::CODE_BYTES, tmv, sl * Gm::SPAN, row0, h, id, &bar_full[stage]);
+              ptx::tma_load_4d(dk, tmk, sl * Gm::SPAN, row0, h, blk[s], &bar_full[stage]);
+              ptx::tma_load_4d(dk + Gm::CODE_BYTES, tmv, sl * Gm::SPAN, row0, h, blk[s], &bar_full[stage]);
             }
-            const size_t srow = ((size_t)id * Hkv + h) * a.block_size + row0;
+            const size_t srow = ((size_t)blk[s] * Hkv + h) * a.block_size + row0;
             if (k_row)
               ptx::bulk_load(st + 2 * Gm::CODE_BYTES + s * seg_rows * 4, a.k_scale + srow, seg_rows * 4,
                              &bar_full[stage]);
@@ -251,8 +268,40 @@ __device__ void produce(const DecodeArgs& a, const Slice<Gm::KEYS>& sp, const CU
                              &bar_full[stage]);
           }
         }
+      } else {
+#pragma unroll 1
+        for (int skey = key0; skey < kend; skey += seg_rows) {
+          const int page = skey >> a.log2_bs;
+          if (page - base >= 32) {
+            base += 32;
+            my_id = base + lane <= p_last ? bt[base + lane] : -1;
+          }
+          const int id = __shfl_sync(0xffffffffu, my_id, page - base);
+          if (lane == 0) {
+            if (id < 0 || id >= a.num_blocks) {
+              atomicOr(a.err, KVQ_DEVERR_BLOCK_ID);
+            } else {
+              const int s = (skey - key0) / seg_rows;
+              const int row0 = skey & (a.block_size - 1);
+              ptx::mbar_expect_tx(&bar_full[stage], seg_bytes);
+#pragma unroll
+              for (int sl = 0; sl < Gm::SLABS; ++sl) {
+                uint8_t* dk = st + sl * (KT * Gm::SPAN) + s * seg_rows * Gm::SPAN;
+                ptx::tma_load_4d(dk, tmk, sl * Gm::SPAN, row0, h, id, &bar_full[stage]);
+                ptx::tma_load_4d(dk + Gm::CODE_BYTES, tmv, sl * Gm::SPAN, row0, h, id, &bar_full[stage]);
+              }
+              const size_t srow = ((size_t)id * Hkv + h) * a.block_size + row0;
+              if (k_row)
+                ptx::bulk_load(st + 2 * Gm::CODE_BYTES + s * seg_rows * 4, a.k_scale + srow, seg_rows * 4,
+                               &bar_full[stage]);
+              if (v_row)
+                ptx::bulk_load(st + 2 * Gm::CODE_BYTES + KT * 4 + s * seg_rows * 4, a.v_scale + srow,
+                               seg_rows * 4, &bar_full[stage]);
+            }
+          }
+        }
+        if (lane == 0) ptx::mbar_arrive(&bar_full[stage]);
       }
-      if (lane == 0) ptx::mbar_arrive(&bar_full[stage]);
       __syncwarp();
     }
   }

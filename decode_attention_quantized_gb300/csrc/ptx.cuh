@@ -76,6 +76,19 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
   return mbar_wait_slow(bar, parity);
 }
 
+// The same bounded wait with the polling loop inlined: for kernels with few
+// wait sites, where a call (and the register saves around it) on the hot
+// path costs more than the code it saves.
+__device__ __forceinline__ bool mbar_wait_bounded_inl(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t i = 0; i < (1u << 24); ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 255u) == 255u && globaltimer_ns() - t0 > 1500000000ull) return false;
+  }
+  return false;
+}
+
 // ---------------------------------------------------------------------- TMA
 // 4-D tiled tensor load into shared memory, completion counted on `bar`.
 __device__ __forceinline__ void tma_load_4d(void* dst, const void* tmap, int x, int y, int z, int w,
