@@ -52,6 +52,14 @@ __device__ __forceinline__ int ceil_log2(float x) {
   return e;
 }
 
+// r / G for 0 <= r < 2^16 and 1 <= G <= 64, given inv = fl(1/G): without an
+// integer divide (a long dependent sequence on this GPU).  (r + 0.5) / G is at
+// least 0.5 / G >= 2^-7 away from an integer, while the two roundings below
+// move it by at most (r + 0.5) / G * 2^-23 < 2^-7, so the floor is exact.
+__device__ __forceinline__ int div_small(int r, float inv) {
+  return (int)(((float)r + 0.5f) * inv);
+}
+
 // 2^e for e in [-126, 127], exact.
 __device__ __forceinline__ float pow2i(int e) { return __uint_as_float((uint32_t)(e + 127) << 23); }
 
@@ -145,7 +153,7 @@ __device__ __forceinline__ float q_prologue(const DecodeArgs& a, int rq, int b, 
   constexpr int NQC = D / (4 * CPL);             // code chunks per row
   const int G = a.group, T = a.q_tokens, Hq = a.num_q_heads;
   const bool qvalid = rq < a.rows;
-  const int tq = qvalid ? rq / G : 0, gq = qvalid ? rq % G : 0;
+  const int tq = qvalid ? div_small(rq, __frcp_rn((float)G)) : 0, gq = qvalid ? rq - tq * G : 0;
   const uint16_t* qp = a.q + (((size_t)b * T + tq) * Hq + (size_t)h * G + gq) * D;
   float qv[NQC][CPL];
 #pragma unroll
@@ -298,6 +306,7 @@ __global__ void __launch_bounds__(288, MINB)
     const int rh = warp & 1, kq = warp >> 1;
     const int g = lane >> 2, c = lane & 3;
     const int G = a.group, W = a.window;
+    const float inv_g = __frcp_rn((float)G);  // r / G by dev::div_small
     const float softcap = a.softcap;
     const float inv_cap = softcap > 0.0f ? 1.0f / softcap : 0.0f;
     const int ld_key = ((lane >> 3) & 1) * 8 + (lane & 7);
@@ -339,7 +348,7 @@ __global__ void __launch_bounds__(288, MINB)
         for (int i = 0; i < 2; ++i) {
           const int r = rh * RW + nt * 8 + 2 * c + i;
           al[nt][i] = s_alpha[r];
-          pos[nt][i] = r < a.rows ? L - T + r / G : -1;
+          pos[nt][i] = r < a.rows ? L - T + dev::div_small(r, inv_g) : -1;
           m[nt][i] = -INFINITY;
           l[nt][i] = 0.0f;
         }
@@ -675,8 +684,9 @@ __global__ void __launch_bounds__(288, MINB)
     const int r0 = rg * 8 + 2 * c, r1 = r0 + 1;
     const float al0 = __shfl_sync(0xffffffffu, alpha_g, (2 * c) * 4);
     const float al1 = __shfl_sync(0xffffffffu, alpha_g, (2 * c + 1) * 4);
-    const int pos0 = r0 < a.rows ? L - T + r0 / G : -1;
-    const int pos1 = r1 < a.rows ? L - T + r1 / G : -1;
+    const float inv_g = __frcp_rn((float)G);
+    const int pos0 = r0 < a.rows ? L - T + dev::div_small(r0, inv_g) : -1;
+    const int pos1 = r1 < a.rows ? L - T + dev::div_small(r1, inv_g) : -1;
     const int W = a.window;
 
     float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.0f, l1 = 0.0f;

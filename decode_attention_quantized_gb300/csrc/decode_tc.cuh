@@ -519,6 +519,7 @@ __global__ void __launch_bounds__(kTcWarps * 32, 1)
     const int kk = 32 * q + lane;  // tile-local key of this thread = TMEM lane of S^T
     const uint32_t t_lane = tmem + ((uint32_t)(32 * q) << 16);
     const int G = a.group, T = a.q_tokens, Hq = a.num_q_heads, W = a.window, rows = a.rows;
+    const float inv_g = __frcp_rn((float)G);  // r / G by dev::div_small
     const float softcap = a.softcap;
     const float inv_cap = softcap > 0.0f ? 1.0f / softcap : 0.0f;
     // where this key's P goes in a P buffer: slab of 64 K indices, 16-byte
@@ -543,7 +544,8 @@ __global__ void __launch_bounds__(kTcWarps * 32, 1)
     constexpr int LPR = D / 8, RPP = 32 / LPR, NQR = NR / (4 * RPP);
     const int rsub = lane / LPR, cl = lane % LPR;
 
-    // Epilogue of a piece: O and row sums out of TMEM 16 rows at a time, the
+    // Epilogue of a piece: O and row sums out of TMEM 16 rows at a time (the
+    // sums and both O channel halves of a chunk in one TMEM round trip), the
     // normalized partial and its base-2 log-sum-exp to the workspace.  Run
     // once per piece, so kept small (its code is cold by then).
     auto epilogue = [&](int u, uint32_t last, float m0, float m1, int F) {
@@ -554,28 +556,33 @@ __global__ void __launch_bounds__(kTcWarps * 32, 1)
       float* lse = a.part_lse + (size_t)u * rows;
 #pragma unroll 1
       for (int r0 = 0; r0 < rows; r0 += 16) {
-        float inv[16];  // the row sums l, turned into the output factors in place
-        dev::tmem_ld_cols<16>(t_lane + C::L_COL + r0, inv);
+        uint32_t lu[16], ou[C::NH][16];
+        ptx::tmem_ld16(t_lane + C::L_COL + r0, lu);
+#pragma unroll
+        for (int hh = 0; hh < C::NH; ++hh) ptx::tmem_ld16(t_lane + C::O_COL + hh * NR + r0, ou[hh]);
+        ptx::tmem_wait_ld();
         // every lane holds all 16 sums; lane j + (r0 & 31) takes row r0 + j's
         const int j = lane - (r0 & 31);
-        float lj = 0.0f;
+        float lj = 0.0f, inv[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          lj = j == i ? inv[i] : lj;
-          inv[i] = inv[i] > 0.0f ? to_true * ptx::fast_rcp(inv[i]) : 0.0f;
+          asm volatile("" : "+r"(lu[i]));
+          const float l = __uint_as_float(lu[i]);
+          lj = j == i ? l : lj;
+          inv[i] = l > 0.0f ? to_true * ptx::fast_rcp(l) : 0.0f;
         }
         if (q == 0 && j >= 0 && j < 16 && r0 + j < rows)
           lse[r0 + j] = lj > 0.0f ? (r0 + j < 32 ? m0 : m1) + ptx::fast_log2(lj) : -INFINITY;
-#pragma unroll 1
+#pragma unroll
         for (int hh = 0; hh < C::NH; ++hh) {
-          float o[16];
-          dev::tmem_ld_cols<16>(t_lane + C::O_COL + hh * NR + r0, o);
           const int ch = dev::tc_out_channel<DT>(hh, q, lane);
           const float cf = (ch & 1) ? dev::odd_channel_factor<DT>() : 1.0f;
           float* dst = a.part_o + ((size_t)u * rows + r0) * D + ch;
 #pragma unroll
-          for (int i = 0; i < 16; ++i)
-            if (r0 + i < rows) dst[(size_t)i * D] = o[i] * inv[i] * cf;
+          for (int i = 0; i < 16; ++i) {
+            asm volatile("" : "+r"(ou[hh][i]));
+            if (r0 + i < rows) dst[(size_t)i * D] = __uint_as_float(ou[hh][i]) * inv[i] * cf;
+          }
         }
       }
       ptx::tc_fence_before();
@@ -596,17 +603,19 @@ __global__ void __launch_bounds__(kTcWarps * 32, 1)
       // ---- Q of this piece (this warp waited for the previous piece's last
       // QK^T, so the buffer is free): per-channel K scale folded in under a
       // power-of-two normaliser, each row normalised by the power of two just
-      // above its maximum, f16 in the MMA's K order, 128-byte swizzle.  Rows
-      // are taken one per loop trip with the next three rows' loads in flight.
+      // above its maximum, f16 in the MMA's K order, 128-byte swizzle.  Every
+      // row this thread converts is loaded first (one round trip), and the
+      // rows are converted with their reductions interleaved.
       if (more) {
         const bool kc = a.k_mode == KVQ_SCALE_PER_CHANNEL;
-        auto q_row = [&](int i) -> uint4 {
+        uint4 raw[NQR];
+#pragma unroll
+        for (int i = 0; i < NQR; ++i) {
           const int r = (q + 4 * i) * RPP + rsub;
-          return r < rows ? __ldg(reinterpret_cast<const uint4*>(
-                                a.q + (((size_t)b * T + r / G) * Hq + (size_t)h * G + r % G) * D + 8 * cl))
-                          : make_uint4(0, 0, 0, 0);
-        };
-        uint4 ra = q_row(0), rb = q_row(1), rc = q_row(2);  // three row loads in flight
+          const int t = dev::div_small(r, inv_g);
+          raw[i] = r < rows ? ptx::ldg_nc_v4(a.q + (((size_t)b * T + t) * Hq + (size_t)h * G + r - t * G) * D + 8 * cl)
+                            : make_uint4(0, 0, 0, 0);
+        }
         float ksv[8];
         int ek = 0;
         if (kc) {
@@ -627,15 +636,11 @@ __global__ void __launch_bounds__(kTcWarps * 32, 1)
         float base = a.sm_scale;
         if (a.k_mode == KVQ_SCALE_PER_TENSOR) base *= a.k_scale[0];
         if (softcap <= 0.0f) base *= kLog2e;
-#pragma unroll 1
+#pragma unroll
         for (int i = 0; i < NQR; ++i) {
           const int r = (q + 4 * i) * RPP + rsub;
-          const uint4 cur = ra;
-          ra = rb;
-          rb = rc;
-          if (i + 3 < NQR) rc = q_row(i + 3);
           float qv[8];
-          const uint32_t ww[4] = {cur.x, cur.y, cur.z, cur.w};
+          const uint32_t ww[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
             qv[2 * j] = __uint_as_float(ww[j] << 16);
@@ -648,8 +653,12 @@ __global__ void __launch_bounds__(kTcWarps * 32, 1)
           float qm = 0.0f;
 #pragma unroll
           for (int j = 0; j < 8; ++j) qm = fmaxf(qm, fabsf(qv[j]));
+          if constexpr (LPR == 32) {
+            qm = ptx::redux_max(qm);  // one row per warp
+          } else {
 #pragma unroll
-          for (int o = 1; o < LPR; o <<= 1) qm = fmaxf(qm, __shfl_xor_sync(0xffffffffu, qm, o));
+            for (int o = 1; o < LPR; o <<= 1) qm = fmaxf(qm, __shfl_xor_sync(0xffffffffu, qm, o));
+          }
           const int eq = qm > 0.0f ? min(126, max(-126, dev::ceil_log2(qm))) : 0;
           const float sq = dev::pow2i(-eq);
           uint32_t w[4];
@@ -672,7 +681,7 @@ __global__ void __launch_bounds__(kTcWarps * 32, 1)
             const float al = fmaxf(fminf(base * dev::pow2i(e1) * dev::pow2i(e - e1), 3.4028234e38f), 1e-30f);
             const bool valid = r < rows;
             f_alpha[r] = valid ? al : 1.0f;
-            i_pos[r] = valid ? L - T + r / G : -1;
+            i_pos[r] = valid ? L - T + dev::div_small(r, inv_g) : -1;
           }
         }
         ptx::fence_proxy_async_smem();
@@ -705,56 +714,63 @@ __global__ void __launch_bounds__(kTcWarps * 32, 1)
         if (lane == 0) ptx::mbar_arrive(&bar_empty[stage]);
 
         // S^T of this tile: all NR columns in one TMEM round trip (TMEM reads
-        // queue behind the tensor core's accumulator traffic), then the S
-        // buffer is released for the QK^T after next
-        float y[NR];
-        dev::tmem_ld_cols<NR>(s_col, y);
-        ptx::tc_fence_before();
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(&b_sfree[it & 1]);
-
-        // logits: y = S * k_scale (the row factor alpha is applied in the
-        // exponent), or the softcapped log2-domain logit (alpha = 1); masked
-        // keys -inf
+        // queue behind the tensor core's accumulator traffic).  logits: y =
+        // S * k_scale (the row factor alpha is applied in the exponent), or
+        // the softcapped log2-domain logit (alpha = 1); masked keys -inf.
+        // The S buffer is held until the tile's reference maxima are settled:
+        // the slow path below reads it a second time.
         const bool full = (key0 + KT - 1 <= L - T) && (W == 0 || key0 >= L - W);
-        if (softcap > 0.0f) {
+        float y[NR];
+        auto logits = [&]() {
+          dev::tmem_ld_cols<NR>(s_col, y);
+          if (softcap > 0.0f) {
+#pragma unroll
+            for (int r = 0; r < NR; r += 4) {
+              const float4 a4 = *reinterpret_cast<const float4*>(f_alpha + r);
+              y[r] = softcap * dev::tanh_fast(y[r] * ks * a4.x * inv_cap) * kLog2e;
+              y[r + 1] = softcap * dev::tanh_fast(y[r + 1] * ks * a4.y * inv_cap) * kLog2e;
+              y[r + 2] = softcap * dev::tanh_fast(y[r + 2] * ks * a4.z * inv_cap) * kLog2e;
+              y[r + 3] = softcap * dev::tanh_fast(y[r + 3] * ks * a4.w * inv_cap) * kLog2e;
+            }
+          } else if (k_row) {
+#pragma unroll
+            for (int r = 0; r < NR; ++r) y[r] *= ks;
+          }
+          if (!full) {
+#pragma unroll
+            for (int r = 0; r < NR; r += 4) {
+              const int4 p4 = *reinterpret_cast<const int4*>(i_pos + r);
+              const int ps[4] = {p4.x, p4.y, p4.z, p4.w};
+#pragma unroll
+              for (int i = 0; i < 4; ++i)
+                if (!(key <= ps[i] && (W == 0 || key > ps[i] - W))) y[r + i] = -INFINITY;
+            }
+          }
+        };
+        // y -> the exponent z = alpha * y - mu, in place (f_mu holds -mu)
+        auto to_exponent = [&]() {
 #pragma unroll
           for (int r = 0; r < NR; r += 4) {
-            const float4 a4 = *reinterpret_cast<const float4*>(f_alpha + r);
-            y[r] = softcap * dev::tanh_fast(y[r] * ks * a4.x * inv_cap) * kLog2e;
-            y[r + 1] = softcap * dev::tanh_fast(y[r + 1] * ks * a4.y * inv_cap) * kLog2e;
-            y[r + 2] = softcap * dev::tanh_fast(y[r + 2] * ks * a4.z * inv_cap) * kLog2e;
-            y[r + 3] = softcap * dev::tanh_fast(y[r + 3] * ks * a4.w * inv_cap) * kLog2e;
+            const float4 m4 = *reinterpret_cast<const float4*>(f_mu + q * NR + r);
+            const float4 a4 = softcap > 0.0f ? make_float4(1.0f, 1.0f, 1.0f, 1.0f)
+                                             : *reinterpret_cast<const float4*>(f_alpha + r);
+            y[r] = fmaf(y[r], a4.x, m4.x);
+            y[r + 1] = fmaf(y[r + 1], a4.y, m4.y);
+            y[r + 2] = fmaf(y[r + 2], a4.z, m4.z);
+            y[r + 3] = fmaf(y[r + 3], a4.w, m4.w);
           }
-        } else if (k_row) {
-#pragma unroll
-          for (int r = 0; r < NR; ++r) y[r] *= ks;
-        }
-        if (!full) {
-#pragma unroll
-          for (int r = 0; r < NR; r += 4) {
-            const int4 p4 = *reinterpret_cast<const int4*>(i_pos + r);
-            const int ps[4] = {p4.x, p4.y, p4.z, p4.w};
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-              if (!(key <= ps[i] && (W == 0 || key > ps[i] - W))) y[r + i] = -INFINITY;
-          }
-        }
+        };
+        logits();
 
         // ---- does any logit of the tile exceed its row's reference maximum by
         // more than 8 (P > 2^8)?  f_mu holds -mu (1e30 for a row with no key
         // yet, so that any unmasked key trips the check while a masked one
         // still gives exp2(-inf) = 0).  Only then (and on a piece's first
         // tile) are exact tile maxima taken and the references moved.
+        to_exponent();
         float dmax = -INFINITY;
 #pragma unroll
-        for (int r = 0; r < NR; r += 4) {
-          const float4 m4 = *reinterpret_cast<const float4*>(f_mu + q * NR + r);
-          const float4 a4 = softcap > 0.0f ? make_float4(1.0f, 1.0f, 1.0f, 1.0f)
-                                           : *reinterpret_cast<const float4*>(f_alpha + r);
-          dmax = fmaxf(dmax, fmaxf(fmaxf(fmaf(y[r], a4.x, m4.x), fmaf(y[r + 1], a4.y, m4.y)),
-                                   fmaxf(fmaf(y[r + 2], a4.z, m4.z), fmaf(y[r + 3], a4.w, m4.w))));
-        }
+        for (int r = 0; r < NR; ++r) dmax = fmaxf(dmax, y[r]);
         const bool ovf = __any_sync(0xffffffffu, dmax > 8.0f);
         float* f_flag = f_vmax + 8 * (it & 1);  // [4] overflow flags, [4] V-scale maxima; by tile parity
         {
@@ -781,6 +797,7 @@ __global__ void __launch_bounds__(kTcWarps * 32, 1)
         }
         float c0 = 1.0f, c1 = 1.0f;
         if (slow) {
+          logits();  // y again, from the held S buffer
           // tile maxima per row (of y; alpha > 0 keeps the order)
 #pragma unroll
           for (int r = 0; r < NR; r += 4) {
@@ -802,15 +819,20 @@ __global__ void __launch_bounds__(kTcWarps * 32, 1)
           if (lane < rows) update(lane, mu0, c0);
           if (lane + 32 < rows) update(lane + 32, mu1, c1);
           if (lane < NR) {
-            f_mu[q * NR + lane] = mu0 == -INFINITY ? 1e30f : -mu0;
+            // padding rows (zero Q, no output) get offset 0 and never trip
+            f_mu[q * NR + lane] = lane >= rows ? 0.0f : (mu0 == -INFINITY ? 1e30f : -mu0);
             f_corr[q * NR + lane] = c0;
           }
           if (lane + 32 < NR) {
-            f_mu[q * NR + lane + 32] = mu1 == -INFINITY ? 1e30f : -mu1;
+            f_mu[q * NR + lane + 32] = lane + 32 >= rows ? 0.0f : (mu1 == -INFINITY ? 1e30f : -mu1);
             f_corr[q * NR + lane + 32] = c1;
           }
           __syncwarp();
+          to_exponent();
         }
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&b_sfree[it & 1]);  // the QK^T after next may overwrite S
         const bool need = !first && (fs != 1.0f || (slow && __any_sync(0xffffffffu, c0 != 1.0f || c1 != 1.0f)));
         if (need && !slow) {
           // only the V-scale normaliser grew: O alone is rescaled
@@ -819,27 +841,15 @@ __global__ void __launch_bounds__(kTcWarps * 32, 1)
           __syncwarp();
         }
 
-        // ---- P = exp2(alpha * y - mu), f16, 16 rows at a time; every factor
-        // of a chunk is read before its first P store (loads cannot be
-        // reordered across those stores)
+        // ---- P = exp2(z), f16, 16 rows at a time
         if (it >= 2) wait(&b_pv[it & 1], ((it - 2) >> 1) & 1);  // PV of tile it - 2 has read this buffer
         uint8_t* pbuf = p_s + (it & 1) * C::P_BYTES;
 #pragma unroll
         for (int r0 = 0; r0 < NR; r0 += 16) {
-          float mo[16], al[16];
-#pragma unroll
-          for (int i = 0; i < 16; i += 4) {
-            const float4 m4 = *reinterpret_cast<const float4*>(f_mu + q * NR + r0 + i);
-            const float4 a4 = softcap > 0.0f ? make_float4(1.0f, 1.0f, 1.0f, 1.0f)
-                                             : *reinterpret_cast<const float4*>(f_alpha + r0 + i);
-            mo[i] = m4.x; mo[i + 1] = m4.y; mo[i + 2] = m4.z; mo[i + 3] = m4.w;
-            al[i] = a4.x; al[i + 1] = a4.y; al[i + 2] = a4.z; al[i + 3] = a4.w;
-          }
           __half2 hp[8];
 #pragma unroll
           for (int i = 0; i < 16; i += 2)
-            hp[i / 2] = __floats2half2_rn(ptx::fast_exp2(fmaf(y[r0 + i], al[i], mo[i])),
-                                          ptx::fast_exp2(fmaf(y[r0 + i + 1], al[i + 1], mo[i + 1])));
+            hp[i / 2] = __floats2half2_rn(ptx::fast_exp2(y[r0 + i]), ptx::fast_exp2(y[r0 + i + 1]));
           uint8_t* prow = pbuf + r0 * 128;
 #pragma unroll
           for (int i = 0; i < 16; i += 2) {

@@ -202,6 +202,17 @@ __device__ __forceinline__ float redux_max(float x) {
   return y;
 }
 
+// 16-byte read-only global load that the compiler keeps in program order
+// with the other volatile asm (so a batch of them is issued up front rather
+// than sunk to each use).
+__device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
 // Pulls the 128-byte line holding `p` into L2.
 __device__ __forceinline__ void prefetch_l2(const void* p) {
   asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(p));
