@@ -130,6 +130,23 @@ class Workload:
         return self.window if (self.window and call % 2 == 1) else 0
 
 
+def rope_tables(max_pos: int, rotary_dim: int, base: float = 10000.0):
+    """RoPE input tables cos / sin fp32 [max_pos, rotary_dim / 2] for angles
+    pos * base^(-2i / rotary_dim) (the usual frequency ladder; the tables are
+    the caller's input to the prologue, not part of its arithmetic)."""
+    half = rotary_dim // 2
+    inv = base ** (-np.arange(half, dtype=np.float64) * 2.0 / rotary_dim)
+    ang = np.arange(max_pos, dtype=np.float64)[:, None] * inv[None, :]
+    return np.cos(ang).astype(np.float32), np.sin(ang).astype(np.float32)
+
+
+def norm_weight_bf16(D: int, device, *parts) -> torch.Tensor:
+    """A seeded RMSNorm weight vector, bf16 [D], values around 1."""
+    g = generator("cpu", *parts)
+    w = 1.0 + 0.25 * torch.randn(D, generator=g, dtype=torch.float32)
+    return w.to(torch.bfloat16).to(device)
+
+
 def calibrate_static(w: Workload, device, which: str) -> Optional[torch.Tensor]:
     """Static fp32 scale of side `which` ('k' or 'v') calibrated on the drawn rows:
     PER_TENSOR max|x|/qmax ([1]); PER_CHANNEL max_t |x[t,h,d]|/qmax ([Hkv, D])."""

@@ -35,7 +35,13 @@
  *  R13 sm_scale defaults to 1/sqrt(D); R14 softcap c*tanh(s/c) acts on the
  *  scaled logit, the sink logit is neither scaled nor capped; R15 one sink per
  *  query head for every query token; R16 an empty key set gives o = 0 and
- *  lse = -inf.
+ *  lse = -inf.  For the prologue before the cache write: R19 RMSNorm, then
+ *  RoPE; R20 RMSNorm per (token, head) over the D channels with one bf16 weight
+ *  vector per side, fp64 arithmetic and a single bf16 rounding at the end;
+ *  R21 RoPE angles come as caller tables cos/sin [max_pos, rotary_dim/2]
+ *  indexed by the token's position, half-split pairs unless interleaved is
+ *  asked for; R22 on the cache side only K takes the prologue, V is written as
+ *  given.
  *
  * Parity pins live in tests/ (format table of e4m3 against torch's
  * float8_e4m3fn, brute-force nearest-code search, round-trip bounds, the
@@ -252,6 +258,90 @@ int orc_append(const orc_cache* c, const uint16_t* k_new, const uint16_t* v_new,
       orc_quantize_row(vx, D, c->dtype, c->v_mode, vs, c->v_codes + ri * Dp,
                        c->v_mode == ORC_PER_ROW ? c->v_scale + ri : NULL);
     }
+  }
+  return bad;
+}
+
+/* ------------------------------------------------------------------ */
+/* QK-RMSNorm + RoPE before the cache write (onnxruntime PR #29912,     */
+/* Summary of Changes: q_norm_weight / k_norm_weight inputs,            */
+/* qk_norm_epsilon with default 1e-6, rotary_offset; "QkNormRotaryTNH"  */
+/* fuses QK-RMSNorm and RoPE into one pass, in that order).             */
+/* ------------------------------------------------------------------ */
+
+/* The bf16 value nearest to v, ties to even, from the format definition:
+ * 8 significant bits for |v| >= 2^-126, a fixed quantum of 2^-133 below that
+ * (subnormals), and infinity once the rounded magnitude reaches 2^128. */
+uint16_t orc_f64_to_bf16(double v) {
+  if (isnan(v)) return 0x7FC0;
+  if (v == 0.0) return signbit(v) ? 0x8000 : 0x0000;
+  int e;
+  frexp(fabs(v), &e); /* |v| in [2^(e-1), 2^e) */
+  int lead = e - 1 > -126 ? e - 1 : -126;
+  int qe = lead - 7;
+  double r = ldexp(orc_rne(ldexp(v, -qe)), qe); /* both scalings exact */
+  if (r == 0.0) return signbit(v) ? 0x8000 : 0x0000; /* underflow keeps the sign */
+  if (fabs(r) >= ldexp(1.0, 128)) return v > 0 ? 0x7F80 : 0xFF80;
+  float f = (float)r; /* exact: at most 8 significant bits, inside the float range */
+  uint32_t u;
+  memcpy(&u, &f, sizeof u);
+  return (uint16_t)(u >> 16);
+}
+
+/* One row of D values, fp64 throughout:
+ *   RMSNorm (when w != NULL): y_d = (x_d * r) * w_d with
+ *     r = 1 / sqrt(sum_d x_d^2 / D + eps);
+ *   RoPE (when rd > 0) on channels [off, off + rd), angle index i in
+ *     [0, rd/2): the pair (a, b) = (off + i, off + i + rd/2) (half split) or
+ *     (off + 2i, off + 2i + 1) (interleaved) becomes
+ *     (a cos_i - b sin_i, b cos_i + a sin_i), cos_i = cs[i], sin_i = sn[i]
+ *     (the caller's table row of the token's position);
+ * then one round-to-nearest-even to bf16 per value. */
+void orc_norm_rope_row(const uint16_t* x, int D, const uint16_t* w, double eps, int rd, int off,
+                       int interleaved, const float* cs, const float* sn, uint16_t* out) {
+  double y[512];
+  for (int d = 0; d < D; ++d) y[d] = (double)orc_bf16_to_f32(x[d]);
+  if (w) {
+    double ss = 0.0;
+    for (int d = 0; d < D; ++d) ss += y[d] * y[d];
+    double r = 1.0 / sqrt(ss / (double)D + eps);
+    for (int d = 0; d < D; ++d) y[d] = (y[d] * r) * (double)orc_bf16_to_f32(w[d]);
+  }
+  if (rd > 0) {
+    double z[512];
+    memcpy(z, y, sizeof(double) * (size_t)D);
+    for (int i = 0; i < rd / 2; ++i) {
+      int a = interleaved ? off + 2 * i : off + i;
+      int b = interleaved ? a + 1 : a + rd / 2;
+      double c = (double)cs[i], s = (double)sn[i];
+      z[a] = y[a] * c - y[b] * s;
+      z[b] = y[b] * c + y[a] * s;
+    }
+    memcpy(y, z, sizeof(double) * (size_t)D);
+  }
+  for (int d = 0; d < D; ++d) out[d] = orc_f64_to_bf16(y[d]);
+}
+
+/* The prologue over x [n_tokens, H, D] -> out (same shape, bf16 bits).  The
+ * RoPE tables are [max_pos, rd/2]; a token whose position lies outside
+ * [0, max_pos) while rd > 0 is left untouched in out and counted in the
+ * return value. */
+int orc_norm_rope(const uint16_t* x, int n_tokens, int H, int D, const uint16_t* w, double eps, int rd,
+                  int off, int interleaved, const float* cos_tab, const float* sin_tab, int max_pos,
+                  const int64_t* positions, uint16_t* out) {
+  int bad = 0;
+  if (D > 512 || rd < 0 || rd % 2 || off < 0 || off + rd > D) return -1;
+  for (int n = 0; n < n_tokens; ++n) {
+    int64_t pos = rd > 0 ? positions[n] : 0;
+    if (rd > 0 && (pos < 0 || pos >= max_pos)) {
+      ++bad;
+      continue;
+    }
+    const float* cs = rd > 0 ? cos_tab + (size_t)pos * (rd / 2) : NULL;
+    const float* sn = rd > 0 ? sin_tab + (size_t)pos * (rd / 2) : NULL;
+    for (int h = 0; h < H; ++h)
+      orc_norm_rope_row(x + ((size_t)n * H + h) * D, D, w, eps, rd, off, interleaved, cs, sn,
+                        out + ((size_t)n * H + h) * D);
   }
   return bad;
 }

@@ -82,6 +82,11 @@ def lib():
             L.orc_attend.argtypes = [ctypes.POINTER(_Cache), ctypes.POINTER(_Params), vp, vp, vp, vp,
                                      vp, i32, vp, vp, i32]
             L.orc_attend.restype = i32
+            L.orc_norm_rope.argtypes = [vp, i32, i32, i32, vp, ctypes.c_double, i32, i32, i32, vp, vp, i32,
+                                        vp, vp]
+            L.orc_norm_rope.restype = i32
+            L.orc_f64_to_bf16.argtypes = [ctypes.c_double]
+            L.orc_f64_to_bf16.restype = ctypes.c_uint16
             _lib = L
     return _lib
 
@@ -96,6 +101,40 @@ def _ptr(a):
 
 def bf16_bits_to_f64(u16: np.ndarray) -> np.ndarray:
     return (np.asarray(u16, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def f64_to_bf16(v: float) -> int:
+    """Nearest bf16 (bit pattern) to a double, ties to even."""
+    return int(lib().orc_f64_to_bf16(float(v)))
+
+
+def norm_rope(x_bf16: np.ndarray, *, norm_weight=None, eps: float = 1e-6, rotary_dim: int = 0,
+              rotary_offset: int = 0, interleaved: bool = False, cos=None, sin=None, positions=None):
+    """QK-RMSNorm then RoPE on x [N, H, D] (bf16 bits) -> (bf16 bits, rows skipped).
+
+    onnxruntime PR #29912, Summary of Changes (q_norm_weight / k_norm_weight,
+    qk_norm_epsilon default 1e-6, rotary_offset; QkNormRotaryTNH).  Per row:
+    y = x / sqrt(mean(x^2) + eps) * w, then each rotated pair (a, b) ->
+    (a cos - b sin, b cos + a sin) with cos / sin the tables' row for the
+    token's position; fp64, one bf16 rounding.  Tokens whose position is
+    outside the tables are left zero and counted."""
+    x = np.ascontiguousarray(x_bf16, dtype=np.uint16)
+    N, H, D = x.shape
+    out = np.zeros_like(x)
+    w = None if norm_weight is None else np.ascontiguousarray(norm_weight, dtype=np.uint16)
+    if rotary_dim > 0:
+        cs = np.ascontiguousarray(cos, dtype=np.float32)
+        sn = np.ascontiguousarray(sin, dtype=np.float32)
+        pos = np.ascontiguousarray(positions, dtype=np.int64)
+        max_pos = cs.shape[0]
+    else:
+        cs = sn = pos = None
+        max_pos = 0
+    bad = lib().orc_norm_rope(_ptr(x), N, H, D, _ptr(w), float(eps), int(rotary_dim), int(rotary_offset),
+                              1 if interleaved else 0, _ptr(cs), _ptr(sn), int(max_pos), _ptr(pos), _ptr(out))
+    if bad < 0:
+        raise ValueError("norm_rope: bad shape")
+    return out, bad
 
 
 def row_bytes(dtype: int, D: int) -> int:
