@@ -297,29 +297,39 @@ kvq_status encode_codes_map(const kvq_cache* c, void* base, CUtensorMap* tm) {
 
 kvq_status from_cuda(cudaError_t e) { return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA; }
 
-}  // namespace
-}  // namespace kvq
-
-using namespace kvq;
-
-extern "C" {
-
-KVQ_API const char* kvq_status_string(kvq_status s) {
-  switch (s) {
-    case KVQ_OK: return "ok";
-    case KVQ_ERR_INVALID_ARG: return "invalid argument";
-    case KVQ_ERR_UNSUPPORTED: return "unsupported shape or type";
-    case KVQ_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
-    case KVQ_ERR_CUDA: return "CUDA error";
-    case KVQ_ERR_DEVICE_TIMEOUT: return "device wait timed out";
-  }
-  return "unknown status";
+// Host checks of a norm/RoPE prologue for rows of head_dim channels; fills
+// the kernel-side descriptor.
+kvq_status check_norm_rope(const kvq_norm_rope* p, int head_dim, const int64_t* positions, NormRope* out) {
+  if (!p) return KVQ_ERR_INVALID_ARG;
+  if (p->norm_weight && !aligned(p->norm_weight, 16)) return KVQ_ERR_INVALID_ARG;
+  if (!(p->norm_eps == p->norm_eps)) return KVQ_ERR_INVALID_ARG;  // NaN
+  const int rd = p->rotary_dim, off = p->rotary_offset;
+  if (rd < 0 || (rd & 1) || off < 0 || (long long)off + rd > head_dim) return KVQ_ERR_INVALID_ARG;
+  if (rd > 0 && (!p->cos_cache || !p->sin_cache || !positions || p->max_position <= 0 ||
+                 !aligned(p->cos_cache, 4) || !aligned(p->sin_cache, 4) || !aligned(positions, 8)))
+    return KVQ_ERR_INVALID_ARG;
+  NormRope r{};
+  r.w = static_cast<const uint16_t*>(p->norm_weight);
+  r.eps = p->norm_eps > 0.0f ? (double)p->norm_eps : 1e-6;
+  r.cos_tab = p->cos_cache;
+  r.sin_tab = p->sin_cache;
+  r.positions = positions;
+  r.rd = rd;
+  r.off = off;
+  r.interleaved = p->rotary_interleaved ? 1 : 0;
+  r.max_pos = rd > 0 ? p->max_position : 0;
+  *out = r;
+  return KVQ_OK;
 }
 
-KVQ_API kvq_status kvq_append(const kvq_cache* cache, const void* k_new, const void* v_new,
-                              const int64_t* slot_mapping, int32_t n_tokens, kvq_stream_t stream) {
+kvq_status append_common(const kvq_cache* cache, const kvq_norm_rope* k_prologue, const void* k_new,
+                         const void* v_new, const int64_t* slot_mapping, const int64_t* positions,
+                         int32_t n_tokens, kvq_stream_t stream) {
   if (kvq_status s = check_cache(cache)) return s;
   if (n_tokens < 0) return KVQ_ERR_INVALID_ARG;
+  NormRope pro{};
+  if (k_prologue)
+    if (kvq_status s = check_norm_rope(k_prologue, cache->head_dim, positions, &pro)) return s;
   if (n_tokens == 0) return KVQ_OK;
   if (!k_new || !v_new || !slot_mapping) return KVQ_ERR_INVALID_ARG;
   if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(slot_mapping, 8)) return KVQ_ERR_INVALID_ARG;
@@ -344,7 +354,61 @@ KVQ_API kvq_status kvq_append(const kvq_cache* cache, const void* k_new, const v
   a.k_mode = cache->k_mode;
   a.v_mode = cache->v_mode;
   a.err = dev->err;
+  a.k_prologue = k_prologue ? 1 : 0;
+  a.pro = pro;
   return from_cuda(launch_append(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // namespace
+}  // namespace kvq
+
+using namespace kvq;
+
+extern "C" {
+
+KVQ_API const char* kvq_status_string(kvq_status s) {
+  switch (s) {
+    case KVQ_OK: return "ok";
+    case KVQ_ERR_INVALID_ARG: return "invalid argument";
+    case KVQ_ERR_UNSUPPORTED: return "unsupported shape or type";
+    case KVQ_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case KVQ_ERR_CUDA: return "CUDA error";
+    case KVQ_ERR_DEVICE_TIMEOUT: return "device wait timed out";
+  }
+  return "unknown status";
+}
+
+KVQ_API kvq_status kvq_append(const kvq_cache* cache, const void* k_new, const void* v_new,
+                              const int64_t* slot_mapping, int32_t n_tokens, kvq_stream_t stream) {
+  return append_common(cache, nullptr, k_new, v_new, slot_mapping, nullptr, n_tokens, stream);
+}
+
+KVQ_API kvq_status kvq_append_norm_rope(const kvq_cache* cache, const kvq_norm_rope* k_prologue,
+                                        const void* k_new, const void* v_new, const int64_t* slot_mapping,
+                                        const int64_t* positions, int32_t n_tokens, kvq_stream_t stream) {
+  if (!k_prologue) return KVQ_ERR_INVALID_ARG;
+  return append_common(cache, k_prologue, k_new, v_new, slot_mapping, positions, n_tokens, stream);
+}
+
+KVQ_API kvq_status kvq_norm_rope_apply(const kvq_norm_rope* prologue, const void* x, void* y,
+                                       const int64_t* positions, int32_t n_tokens, int32_t num_heads,
+                                       int32_t head_dim, kvq_stream_t stream) {
+  if (head_dim != 64 && head_dim != 128 && head_dim != 256) return KVQ_ERR_UNSUPPORTED;
+  if (n_tokens < 0 || num_heads <= 0) return KVQ_ERR_INVALID_ARG;
+  NormRopeArgs a{};
+  if (kvq_status s = check_norm_rope(prologue, head_dim, positions, &a.pro)) return s;
+  if (n_tokens == 0) return KVQ_OK;
+  if (!x || !y || !aligned(x, 16) || !aligned(y, 16)) return KVQ_ERR_INVALID_ARG;
+  if ((long long)n_tokens * num_heads > (1LL << 31) - 1) return KVQ_ERR_INVALID_ARG;
+  DeviceInfo* dev;
+  if (kvq_status s = current_device(&dev)) return s;
+  a.x = static_cast<const uint16_t*>(x);
+  a.y = static_cast<uint16_t*>(y);
+  a.n_tokens = n_tokens;
+  a.num_heads = num_heads;
+  a.head_dim = head_dim;
+  a.err = dev->err;
+  return from_cuda(launch_norm_rope(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 KVQ_API kvq_status kvq_decode_workspace_size(const kvq_cache* cache, const kvq_decode_params* params,

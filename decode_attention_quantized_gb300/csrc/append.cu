@@ -1,7 +1,8 @@
 // append.cu -- quantize-on-write of new K/V rows into their paged-cache slots
 // (ReshapeAndCache in onnxruntime PR #29912; per-row absmax scales as in the
 // kv-quant-attn page, section "Method"; int4 two-per-byte packing as in
-// onnxruntime PR #32515).
+// onnxruntime PR #32515), optionally behind the fused QK-RMSNorm + RoPE
+// prologue on K (QkNormRotaryTNH, PR #29912), which also runs alone on Q.
 //
 // One warp per (token, kv head, side): each lane holds D/32 consecutive
 // channels, the row's absmax is a warp max-reduction (exact, order free), the
@@ -55,6 +56,81 @@ __device__ __forceinline__ void store_bytes(uint8_t* dst, const uint8_t (&b)[NB]
   }
 }
 
+// Nearest bf16 to v, ties to even, from the format definition: 8 significant
+// bits for |v| >= 2^-126, the fixed quantum 2^-133 below (subnormals), and
+// infinity once the rounded magnitude reaches 2^128.  Returned as the float
+// it denotes (exact).
+__device__ __forceinline__ float bf16_rne_f64(double v) {
+  if (v != v) return __uint_as_float(0x7FC00000u);
+  if (v == 0.0) return (float)v;
+  int e;
+  frexp(fabs(v), &e);  // |v| in [2^(e-1), 2^e)
+  const int qe = max(e - 1, -126) - 7;
+  const double r = ldexp(rint(ldexp(v, -qe)), qe);  // rint: ties to even; both scalings exact
+  if (fabs(r) >= 0x1p128) return v > 0.0 ? __uint_as_float(0x7F800000u) : __uint_as_float(0xFF800000u);
+  return (float)r;  // exact
+}
+
+// QK-RMSNorm then RoPE on one (token, head) row held by a warp, E channels
+// per lane (channel lane * E + e), in fp64 with one bf16 rounding at the end
+// (QkNormRotaryTNH, onnxruntime PR #29912, Summary of Changes; the readings
+// are the ones kvq.h states).  `ys` is this warp's staging row of 32 E
+// doubles, used to fetch each channel's rotation partner.  Returns false,
+// after flagging KVQ_DEVERR_POSITION, when the token's position is outside
+// the tables (the caller then writes nothing for the token).
+template <int E>
+__device__ bool norm_rope_row(const NormRope& p, int n, int lane, float (&x)[E], double* ys,
+                              unsigned int* err) {
+  constexpr int D = 32 * E;
+  long long pos = 0;
+  if (p.rd > 0) {
+    pos = p.positions[n];
+    if (pos < 0 || pos >= p.max_pos) {
+      if (lane == 0) atomicOr(err, KVQ_DEVERR_POSITION);
+      return false;
+    }
+  }
+  double y[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) y[e] = (double)x[e];
+  if (p.w) {
+    double ss = 0.0;
+#pragma unroll
+    for (int e = 0; e < E; ++e) ss = __dadd_rn(ss, __dmul_rn(y[e], y[e]));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss = __dadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, o));
+    const double r = __ddiv_rn(1.0, __dsqrt_rn(__dadd_rn(__ddiv_rn(ss, (double)D), p.eps)));
+    float w[E];
+    load_bf16<E>(p.w + lane * E, w);
+#pragma unroll
+    for (int e = 0; e < E; ++e) y[e] = __dmul_rn(__dmul_rn(y[e], r), (double)w[e]);
+  }
+  if (p.rd > 0) {
+#pragma unroll
+    for (int e = 0; e < E; ++e) ys[lane * E + e] = y[e];
+    __syncwarp();
+    const int half = p.rd >> 1;
+    const float* cs = p.cos_tab + (size_t)pos * half;
+    const float* sn = p.sin_tab + (size_t)pos * half;
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      const int c = lane * E + e, j = c - p.off;
+      if (j >= 0 && j < p.rd) {
+        const bool first = p.interleaved ? (j & 1) == 0 : j < half;
+        const int i = p.interleaved ? j >> 1 : (first ? j : j - half);
+        const int partner = p.interleaved ? (first ? c + 1 : c - 1) : (first ? c + half : c - half);
+        const double co = (double)cs[i], si = (double)sn[i], o = ys[partner];
+        y[e] = first ? __dsub_rn(__dmul_rn(y[e], co), __dmul_rn(o, si))
+                     : __dadd_rn(__dmul_rn(y[e], co), __dmul_rn(o, si));
+      }
+    }
+    __syncwarp();
+  }
+#pragma unroll
+  for (int e = 0; e < E; ++e) x[e] = bf16_rne_f64(y[e]);
+  return true;
+}
+
 template <int D>
 __global__ void __launch_bounds__(256) append_kernel(const AppendArgs a) {
   constexpr int E = D / 32;  // channels per lane
@@ -78,6 +154,17 @@ __global__ void __launch_bounds__(256) append_kernel(const AppendArgs a) {
 
   float x[E];
   load_bf16<E>((side ? a.v_new : a.k_new) + ((size_t)n * a.num_kv_heads + h) * D + lane * E, x);
+  if (a.k_prologue) {
+    // both sides of a token are skipped when its position is bad: the V warp
+    // checks the position too (without flagging it twice)
+    __shared__ double ys[8][D];
+    if (side == 0) {
+      if (!norm_rope_row<E>(a.pro, n, lane, x, ys[(threadIdx.x >> 5) & 7], a.err)) return;
+    } else if (a.pro.rd > 0) {
+      const long long pos = a.pro.positions[n];
+      if (pos < 0 || pos >= a.pro.max_pos) return;
+    }
+  }
 
   const int mode = side ? a.v_mode : a.k_mode;
   float* sc = side ? a.v_scale : a.k_scale;
@@ -133,7 +220,50 @@ __global__ void __launch_bounds__(256) append_kernel(const AppendArgs a) {
   }
 }
 
+// kvq_norm_rope_apply: one warp per (token, head) row of x -> y.
+template <int D>
+__global__ void __launch_bounds__(256) norm_rope_kernel(const NormRopeArgs a) {
+  constexpr int E = D / 32;
+  __shared__ double ys[8][D];
+  ptx::griddep_wait();
+  ptx::griddep_launch_dependents();
+  const int wg = (int)((blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5);
+  const int lane = threadIdx.x & 31;
+  if (wg >= a.n_tokens * a.num_heads) return;
+  const int n = wg / a.num_heads;
+  const size_t off = (size_t)wg * D + lane * E;
+  float x[E];
+  load_bf16<E>(a.x + off, x);
+  if (!norm_rope_row<E>(a.pro, n, lane, x, ys[(threadIdx.x >> 5) & 7], a.err)) return;
+  uint16_t b[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) b[e] = (uint16_t)(__float_as_uint(x[e]) >> 16);  // exact: x is a bf16 value
+  if constexpr (E == 8) {
+    uint4 v;
+    v.x = b[0] | ((uint32_t)b[1] << 16); v.y = b[2] | ((uint32_t)b[3] << 16);
+    v.z = b[4] | ((uint32_t)b[5] << 16); v.w = b[6] | ((uint32_t)b[7] << 16);
+    *reinterpret_cast<uint4*>(a.y + off) = v;
+  } else if constexpr (E == 4) {
+    uint2 v;
+    v.x = b[0] | ((uint32_t)b[1] << 16); v.y = b[2] | ((uint32_t)b[3] << 16);
+    *reinterpret_cast<uint2*>(a.y + off) = v;
+  } else {
+    *reinterpret_cast<uint32_t*>(a.y + off) = b[0] | ((uint32_t)b[1] << 16);
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_norm_rope(const NormRopeArgs& a, cudaStream_t stream) {
+  const long long warps = (long long)a.n_tokens * a.num_heads;
+  const unsigned blocks = (unsigned)((warps + 7) / 8);
+  switch (a.head_dim) {
+    case 64: return launch_pdl(norm_rope_kernel<64>, blocks, 256, 0, stream, a);
+    case 128: return launch_pdl(norm_rope_kernel<128>, blocks, 256, 0, stream, a);
+    case 256: return launch_pdl(norm_rope_kernel<256>, blocks, 256, 0, stream, a);
+    default: return cudaErrorInvalidValue;
+  }
+}
 
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t stream) {
   const long long warps = (long long)a.n_tokens * a.num_kv_heads * 2;

@@ -19,6 +19,16 @@ constexpr int kSub = 16;        // keys per MMA sub-tile
 constexpr int kMaxBatch = 1024; // sequences whose split plan fits in shared memory
 constexpr int kMaxStages = 8;
 
+// The QK-RMSNorm + RoPE prologue (kvq_norm_rope, host-validated).
+struct NormRope {
+  const uint16_t* w;        // bf16 bits [D] or null (no RMSNorm)
+  double eps;
+  const float* cos_tab;     // [max_pos, rd / 2]
+  const float* sin_tab;
+  const int64_t* positions; // [N] (rd > 0)
+  int rd, off, interleaved, max_pos;
+};
+
 struct AppendArgs {
   const uint16_t* k_new;  // bf16 bits [N, Hkv, D]
   const uint16_t* v_new;
@@ -31,6 +41,16 @@ struct AppendArgs {
   int n_tokens, num_kv_heads, head_dim, block_size, log2_bs;
   int dtype, k_mode, v_mode;
   unsigned int* err;
+  int k_prologue;           // apply `pro` to the K rows before quantizing them
+  NormRope pro;
+};
+
+struct NormRopeArgs {
+  const uint16_t* x;        // bf16 bits [N, H, D]
+  uint16_t* y;
+  int n_tokens, num_heads, head_dim;
+  unsigned int* err;
+  NormRope pro;
 };
 
 struct DecodeArgs {
@@ -115,6 +135,7 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 }
 
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t stream);
+cudaError_t launch_norm_rope(const NormRopeArgs& a, cudaStream_t stream);
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t stream);
 cudaError_t launch_decode_int8(int head_dim, int nt, const CUtensorMap& tk, const CUtensorMap& tv,
                                const DecodeArgs& a, int grid, int threads, size_t smem, cudaStream_t stream);

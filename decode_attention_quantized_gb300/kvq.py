@@ -19,7 +19,7 @@ from .build import LIB_PATH
 
 INT8, FP8_E4M3, INT4 = 1, 2, 3
 PER_ROW, PER_TENSOR, PER_CHANNEL = 1, 2, 3
-DEVERR_SLOT, DEVERR_BLOCK_ID, DEVERR_SEQ_LEN, DEVERR_TIMEOUT = 0x1, 0x2, 0x4, 0x8
+DEVERR_SLOT, DEVERR_BLOCK_ID, DEVERR_SEQ_LEN, DEVERR_TIMEOUT, DEVERR_POSITION = 0x1, 0x2, 0x4, 0x8, 0x10
 STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "workspace too small", 4: "CUDA error",
           5: "device timeout"}
 
@@ -44,6 +44,12 @@ class DecodeParams(ctypes.Structure):
                 ("sm_scale", ctypes.c_float), ("softcap", ctypes.c_float), ("window", ctypes.c_int32)]
 
 
+class NormRopeDesc(ctypes.Structure):
+    _fields_ = [("norm_weight", ctypes.c_void_p), ("norm_eps", ctypes.c_float), ("rotary_dim", ctypes.c_int32),
+                ("rotary_offset", ctypes.c_int32), ("rotary_interleaved", ctypes.c_int32),
+                ("cos_cache", ctypes.c_void_p), ("sin_cache", ctypes.c_void_p), ("max_position", ctypes.c_int32)]
+
+
 # every exported entry point of include/kvq.h with its ctypes signature
 _VP, _I32, _SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
 SIGNATURES = {
@@ -55,6 +61,9 @@ SIGNATURES = {
     "kvq_combine": (_I32, [ctypes.POINTER(CacheDesc), ctypes.POINTER(DecodeParams), _VP, _SZ, _VP, _VP, _VP,
                            _VP]),
     "kvq_get_device_error": (_I32, [ctypes.POINTER(ctypes.c_uint32), _I32, _VP]),
+    "kvq_norm_rope_apply": (_I32, [ctypes.POINTER(NormRopeDesc), _VP, _VP, _VP, _I32, _I32, _I32, _VP]),
+    "kvq_append_norm_rope": (_I32, [ctypes.POINTER(CacheDesc), ctypes.POINTER(NormRopeDesc), _VP, _VP, _VP, _VP,
+                                    _I32, _VP]),
     "kvq_attend_noalloc": (_I32, [ctypes.POINTER(CacheDesc), ctypes.POINTER(DecodeParams), _VP, _VP, _VP, _VP, _VP,
                                   _VP, _VP]),
 }
@@ -146,6 +155,43 @@ def kvq_append(cache: QuantizedPagedCache, k_new: torch.Tensor, v_new: torch.Ten
     d = cache.desc()
     _check("kvq_append", load().kvq_append(ctypes.byref(d), _ptr(k_new), _ptr(v_new), _ptr(slot_mapping),
                                            int(slot_mapping.numel()), _stream(stream)))
+
+
+@dataclass
+class NormRope:
+    """The QK-RMSNorm + RoPE prologue (kvq_norm_rope in kvq.h); tensors on the device.
+    norm_weight bf16 [D] or None; cos / sin fp32 [max_position, rotary_dim / 2]."""
+    norm_weight: Optional[torch.Tensor] = None
+    eps: float = 1e-6
+    rotary_dim: int = 0
+    rotary_offset: int = 0
+    interleaved: bool = False
+    cos: Optional[torch.Tensor] = None
+    sin: Optional[torch.Tensor] = None
+
+    def desc(self) -> NormRopeDesc:
+        return NormRopeDesc(None if self.norm_weight is None else self.norm_weight.data_ptr(), float(self.eps),
+                            int(self.rotary_dim), int(self.rotary_offset), 1 if self.interleaved else 0,
+                            None if self.cos is None else self.cos.data_ptr(),
+                            None if self.sin is None else self.sin.data_ptr(),
+                            0 if self.cos is None else int(self.cos.shape[0]))
+
+
+def kvq_norm_rope_apply(pro: NormRope, x: torch.Tensor, y: torch.Tensor, positions: Optional[torch.Tensor],
+                        stream=None):
+    """x, y bf16 [N, H, D] (y may be x); positions int64 [N]."""
+    N, H, D = x.shape
+    d = pro.desc()
+    _check("kvq_norm_rope_apply", load().kvq_norm_rope_apply(ctypes.byref(d), _ptr(x), _ptr(y), _ptr(positions),
+                                                             N, H, D, _stream(stream)))
+
+
+def kvq_append_norm_rope(cache: QuantizedPagedCache, pro: NormRope, k_new: torch.Tensor, v_new: torch.Tensor,
+                         slot_mapping: torch.Tensor, positions: Optional[torch.Tensor], stream=None):
+    d, p = cache.desc(), pro.desc()
+    _check("kvq_append_norm_rope", load().kvq_append_norm_rope(ctypes.byref(d), ctypes.byref(p), _ptr(k_new),
+                                                               _ptr(v_new), _ptr(slot_mapping), _ptr(positions),
+                                                               k_new.shape[0], _stream(stream)))
 
 
 def kvq_decode_workspace_size(cache: QuantizedPagedCache, params: DecodeParams) -> int:

@@ -90,6 +90,7 @@ typedef enum {
 #define KVQ_DEVERR_BLOCK_ID 0x2u  /* decode: block_table entry outside [0, num_blocks) */
 #define KVQ_DEVERR_SEQ_LEN 0x4u   /* decode: seq_len < 0, > capacity, or > max_seq_len */
 #define KVQ_DEVERR_TIMEOUT 0x8u   /* a bounded pipeline wait gave up */
+#define KVQ_DEVERR_POSITION 0x10u /* norm/RoPE prologue: position outside [0, max_position) */
 
 /* The paged cache: one descriptor per layer (kv-quant-attn "Usage": one cache
  * object per layer).  All pointers are device memory owned by the caller.
@@ -143,6 +144,53 @@ KVQ_API const char* kvq_status_string(kvq_status status);
 KVQ_API kvq_status kvq_append(const kvq_cache* cache, const void* k_new, const void* v_new,
                               const int64_t* slot_mapping, int32_t n_tokens,
                               kvq_stream_t stream);
+
+/* The prologue before the cache write: QK-RMSNorm, then RoPE (QkNormRotaryTNH
+ * in onnxruntime PR #29912, Summary of Changes: q_norm_weight / k_norm_weight
+ * inputs, qk_norm_epsilon with default 1e-6, rotary_offset, which rotates
+ * channels [rotary_offset, rotary_offset + rotary_dim)).  For each (token,
+ * head) row x of head_dim bf16 values, in fp64:
+ *   RMSNorm (norm_weight != NULL): y_d = (x_d * r) * w_d,
+ *     r = 1 / sqrt(sum_d x_d^2 / head_dim + eps);
+ *   RoPE (rotary_dim > 0): the pair (a, b) of angle index i in
+ *     [0, rotary_dim/2) becomes (a cos - b sin, b cos + a sin), with
+ *     cos = cos_cache[pos, i], sin = sin_cache[pos, i] for the token's
+ *     position pos; pairs are (off + i, off + i + rotary_dim/2) (half split)
+ *     or (off + 2i, off + 2i + 1) (rotary_interleaved);
+ * then one round-to-nearest-even to bf16 per value.  The pages fix neither the
+ * rotation layout nor the tables: both are the caller's, as here. */
+typedef struct {
+  const void* norm_weight;    /* bf16 [head_dim] (device), or NULL: no RMSNorm */
+  float norm_eps;             /* <= 0 selects 1e-6 */
+  int32_t rotary_dim;         /* 0: no RoPE; else even, rotary_offset + rotary_dim <= head_dim */
+  int32_t rotary_offset;      /* first rotated channel (>= 0) */
+  int32_t rotary_interleaved; /* 0: half-split pairs; 1: adjacent pairs */
+  const float* cos_cache;     /* fp32 [max_position, rotary_dim/2] (device) */
+  const float* sin_cache;     /* fp32 [max_position, rotary_dim/2] (device) */
+  int32_t max_position;       /* rows of the tables (> 0 when rotary_dim > 0) */
+} kvq_norm_rope;
+
+/* kvq_norm_rope_apply -- the prologue on x [n_tokens, num_heads, head_dim]
+ * bf16 (device) into y (same shape; y == x is allowed), e.g. the queries
+ * before kvq_decode.  positions int64 [n_tokens] (device; may be NULL when
+ * rotary_dim == 0): a position outside [0, max_position) sets
+ * KVQ_DEVERR_POSITION and leaves that token's rows of y unwritten.
+ * head_dim in {64, 128, 256}; x, y 16-byte aligned. */
+KVQ_API kvq_status kvq_norm_rope_apply(const kvq_norm_rope* prologue, const void* x, void* y,
+                                       const int64_t* positions, int32_t n_tokens,
+                                       int32_t num_heads, int32_t head_dim, kvq_stream_t stream);
+
+/* kvq_append_norm_rope -- kvq_append with the prologue fused in front of the
+ * K quantizer: each K row is normalized and rotated as kvq_norm_rope_apply
+ * would (same fp64 arithmetic, same bf16 rounding) and the resulting bf16 row
+ * is quantized exactly as kvq_append quantizes its input; V rows are
+ * quantized as given (the prologue acts on Q and K only).  A token with a
+ * negative slot is skipped; one whose position is outside the tables sets
+ * KVQ_DEVERR_POSITION and neither its K nor its V rows are written. */
+KVQ_API kvq_status kvq_append_norm_rope(const kvq_cache* cache, const kvq_norm_rope* k_prologue,
+                                        const void* k_new, const void* v_new,
+                                        const int64_t* slot_mapping, const int64_t* positions,
+                                        int32_t n_tokens, kvq_stream_t stream);
 
 /* Bytes of workspace kvq_decode needs for these shapes on the current device
  * (split partials and the device-side split plan).  Host-only arithmetic plus

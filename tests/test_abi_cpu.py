@@ -129,3 +129,45 @@ def test_binding_refuses_to_run_without_the_library(tmp_path):
             kvq.load(str(tmp_path / "missing.so"))
     finally:
         kvq._lib = saved
+
+
+def good_norm_rope(kvq, **kw):
+    d = dict(norm_weight=FAKE, norm_eps=1e-6, rotary_dim=64, rotary_offset=0, rotary_interleaved=0,
+             cos_cache=FAKE + 4096, sin_cache=FAKE + 8192, max_position=128)
+    d.update(kw)
+    return kvq.NormRopeDesc(**d)
+
+
+@pytest.mark.parametrize("bad", [
+    dict(rotary_dim=-2), dict(rotary_dim=63), dict(rotary_offset=-1), dict(rotary_offset=96),
+    dict(rotary_dim=130), dict(cos_cache=None), dict(sin_cache=None), dict(max_position=0),
+    dict(norm_weight=FAKE + 2), dict(cos_cache=FAKE + 2), dict(norm_eps=float("nan")),
+])
+def test_norm_rope_rejects_bad_prologue(kvq, bad):
+    """Invalid prologues are refused on the host, for the Q-side call and the
+    fused append alike (head_dim 128: offset + rotary_dim must fit)."""
+    lib = kvq.load()
+    p = good_norm_rope(kvq, **bad)
+    assert lib.kvq_norm_rope_apply(ctypes.byref(p), FAKE, FAKE, FAKE, 4, 8, 128, None) == 1
+    c = good_cache(kvq)
+    assert lib.kvq_append_norm_rope(ctypes.byref(c), ctypes.byref(p), FAKE, FAKE, FAKE, FAKE, 4, None) == 1
+
+
+def test_norm_rope_rejects_bad_shapes_and_pointers(kvq):
+    lib = kvq.load()
+    p = good_norm_rope(kvq)
+    assert lib.kvq_norm_rope_apply(ctypes.byref(p), FAKE, FAKE, FAKE, 4, 8, 96, None) == 2  # head_dim
+    assert lib.kvq_norm_rope_apply(ctypes.byref(p), FAKE, FAKE, FAKE, -1, 8, 128, None) == 1
+    assert lib.kvq_norm_rope_apply(ctypes.byref(p), FAKE, FAKE, FAKE, 4, 0, 128, None) == 1
+    assert lib.kvq_norm_rope_apply(ctypes.byref(p), FAKE, FAKE, None, 4, 8, 128, None) == 1  # positions
+    assert lib.kvq_norm_rope_apply(ctypes.byref(p), FAKE + 8, FAKE, FAKE, 4, 8, 128, None) == 1  # x alignment
+    assert lib.kvq_norm_rope_apply(None, FAKE, FAKE, FAKE, 4, 8, 128, None) == 1
+    # nothing to do: no device call is made
+    assert lib.kvq_norm_rope_apply(ctypes.byref(p), FAKE, FAKE, FAKE, 0, 8, 128, None) == 0
+    # RMSNorm alone needs neither tables nor positions
+    q = good_norm_rope(kvq, rotary_dim=0, cos_cache=None, sin_cache=None, max_position=0)
+    assert lib.kvq_norm_rope_apply(ctypes.byref(q), FAKE, FAKE, None, 0, 8, 128, None) == 0
+    c = good_cache(kvq)
+    assert lib.kvq_append_norm_rope(ctypes.byref(c), None, FAKE, FAKE, FAKE, FAKE, 4, None) == 1
+    assert lib.kvq_append_norm_rope(ctypes.byref(c), ctypes.byref(p), FAKE, FAKE, FAKE, None, 4, None) == 1
+    assert lib.kvq_append_norm_rope(ctypes.byref(c), ctypes.byref(p), FAKE, FAKE, FAKE, FAKE, 0, None) == 0
