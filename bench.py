@@ -45,6 +45,7 @@ def parse():
     p.add_argument("--no-sweep", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-prologue", action="store_true", help="skip the QK-RMSNorm + RoPE prologue timing")
     return p.parse_args()
 
 
@@ -318,6 +319,90 @@ def measure_e2e(w, gws, plist, windows, steps, warmup, k_new, v_new, slots, qs):
     return dict(wall_s=wall, h2d=h2d, d2h=d2h)
 
 
+def measure_prologue(w, steps, warmup, peak):
+    """The fused QK-RMSNorm + RoPE prologue (kvq_append_norm_rope on the new
+    K/V rows, kvq_norm_rope_apply on the queries) at the step's sizes, next to
+    the plain kvq_append, each as a graph of `steps` launches; and a bulk
+    kvq_append_norm_rope over enough tokens that its bf16 inputs exceed L2,
+    reported against the HBM peak (algorithmic bytes: bf16 K/V read, codes and
+    per-row scales written, slots, positions and the tables' rows read)."""
+    import torch
+    from decode_attention_quantized_gb300 import kvq, synth
+
+    dev = torch.cuda.current_device()
+    D, Hkv, Hq = w.head_dim, w.num_kv_heads, w.num_q_heads
+    max_pos = 8192  # table rows; positions are taken modulo this
+    cos, sin = synth.rope_tables(max_pos, D)
+    pro = kvq.NormRope(norm_weight=synth.norm_weight_bf16(D, f"cuda:{dev}", "bench", "norm"), eps=1e-6,
+                       rotary_dim=D, cos=torch.from_numpy(cos).cuda(), sin=torch.from_numpy(sin).cuda())
+    qmax = {kvq.INT8: 127.0, kvq.INT4: 7.0, kvq.FP8_E4M3: 448.0}[w.dtype]
+
+    def cache_for(n_tokens):
+        bs = 256
+        nb = (n_tokens + bs - 1) // bs
+        def static(mode):
+            if mode == kvq.PER_TENSOR:
+                return torch.full((1,), 4.0 / qmax)
+            if mode == kvq.PER_CHANNEL:
+                return torch.full((Hkv, D), 4.0 / qmax)
+            return None
+        return kvq.QuantizedPagedCache(w.dtype, w.k_mode, w.v_mode, nb, bs, Hkv, D, device=f"cuda:{dev}",
+                                       k_static=static(w.k_mode), v_static=static(w.v_mode))
+
+    def timed_graph(fn, n):
+        for _ in range(max(3, warmup)):
+            fn()
+        torch.cuda.synchronize()
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr):
+            for _ in range(n):
+                fn()
+        gr.replay()
+        torch.cuda.synchronize()
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record()
+        gr.replay()
+        t1.record()
+        torch.cuda.synchronize()
+        return t0.elapsed_time(t1) / n
+
+    N = w.batch * w.q_tokens
+    cache = cache_for(N)
+    k = synth.randn_bf16((N, Hkv, D), f"cuda:{dev}", "bench", "pro-k")
+    v = synth.randn_bf16((N, Hkv, D), f"cuda:{dev}", "bench", "pro-v")
+    q = synth.randn_bf16((N, Hq, D), f"cuda:{dev}", "bench", "pro-q")
+    qo = torch.empty_like(q)
+    slots = torch.arange(N, dtype=torch.int64, device=f"cuda:{dev}")
+    pos = (torch.arange(N, dtype=torch.int64, device=f"cuda:{dev}") * 7) % max_pos
+    us_app = 1e3 * timed_graph(lambda: kvq.kvq_append(cache, k, v, slots), steps)
+    us_fused = 1e3 * timed_graph(lambda: kvq.kvq_append_norm_rope(cache, pro, k, v, slots, pos), steps)
+    us_q = 1e3 * timed_graph(lambda: kvq.kvq_norm_rope_apply(pro, q, qo, pos), steps)
+    del cache, k, v, q, qo
+
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    nb_tok = max(1024, int(2 * l2 // (2 * Hkv * D * 2)))  # bf16 K + V twice the L2 size
+    cache = cache_for(nb_tok)
+    k = synth.randn_bf16((nb_tok, Hkv, D), f"cuda:{dev}", "bench", "pro-bulk-k")
+    v = synth.randn_bf16((nb_tok, Hkv, D), f"cuda:{dev}", "bench", "pro-bulk-v")
+    slots = torch.arange(nb_tok, dtype=torch.int64, device=f"cuda:{dev}")
+    pos = slots % max_pos
+    ms = timed_graph(lambda: kvq.kvq_append_norm_rope(cache, pro, k, v, slots, pos), 5)
+    assert kvq.kvq_get_device_error() == 0, "device error flags set in the prologue timing"
+    dp = D // 2 if w.dtype == kvq.INT4 else D
+    rows = nb_tok * Hkv
+    nbytes = (2 * rows * D * 2 + 2 * rows * dp + 4 * rows * ((w.k_mode == kvq.PER_ROW) + (w.v_mode == kvq.PER_ROW))
+              + nb_tok * (8 + 8 + 2 * 4 * (D // 2)))
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    del cache, k, v
+    torch.cuda.empty_cache()
+    return {"step_tokens": N, "append_us": round(us_app, 2), "append_norm_rope_us": round(us_fused, 2),
+            "norm_rope_q_us": round(us_q, 2),
+            "bulk": {"tokens": nb_tok, "append_norm_rope_us": round(1e3 * ms, 1), "gbs": round(gbs, 1),
+                     "frac_of_hbm": round(gbs / peak, 3), "bytes": int(nbytes)},
+            "prologue": f"RMSNorm (bf16 weight, eps 1e-6) + RoPE on all {D} channels (half split), fixed-order fp32"}
+
+
 def traffic_from_profiles(kernel_tag: str):
     """DRAM bytes per launch of the decode kernel from the committed ncu
     summary, if it was taken on the current kernel source."""
@@ -435,6 +520,8 @@ def run_ours(args):
         line["e2e"] = {"value": round(step_bytes / e2e_wall / 1e9, 1), "unit": "GB/s",
                        "us_per_step": round(1e6 * e2e_wall / K, 2),
                        "h2d_bytes_per_step": e["h2d"], "d2h_bytes_per_step": e["d2h"]}
+    if rank == 0 and world == 1 and not args.no_prologue:
+        line["prologue"] = measure_prologue(w, args.steps, args.warmup, peak)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, windows[0], budget_s=12.0)
     if rank == 0:

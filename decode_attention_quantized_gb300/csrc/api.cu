@@ -310,7 +310,7 @@ kvq_status check_norm_rope(const kvq_norm_rope* p, int head_dim, const int64_t* 
     return KVQ_ERR_INVALID_ARG;
   NormRope r{};
   r.w = static_cast<const uint16_t*>(p->norm_weight);
-  r.eps = p->norm_eps > 0.0f ? (double)p->norm_eps : 1e-6;
+  r.eps = p->norm_eps > 0.0f ? p->norm_eps : 1e-6f;
   r.cos_tab = p->cos_cache;
   r.sin_tab = p->sin_cache;
   r.positions = positions;

@@ -56,31 +56,30 @@ __device__ __forceinline__ void store_bytes(uint8_t* dst, const uint8_t (&b)[NB]
   }
 }
 
-// Nearest bf16 to v, ties to even, from the format definition: 8 significant
-// bits for |v| >= 2^-126, the fixed quantum 2^-133 below (subnormals), and
-// infinity once the rounded magnitude reaches 2^128.  Returned as the float
-// it denotes (exact).
-__device__ __forceinline__ float bf16_rne_f64(double v) {
-  if (v != v) return __uint_as_float(0x7FC00000u);
-  if (v == 0.0) return (float)v;
-  int e;
-  frexp(fabs(v), &e);  // |v| in [2^(e-1), 2^e)
-  const int qe = max(e - 1, -126) - 7;
-  const double r = ldexp(rint(ldexp(v, -qe)), qe);  // rint: ties to even; both scalings exact
-  if (fabs(r) >= 0x1p128) return v > 0.0 ? __uint_as_float(0x7F800000u) : __uint_as_float(0xFF800000u);
-  return (float)r;  // exact
+// Nearest bf16 to the float f, ties to even, as the float it denotes: add
+// half a bf16 unit less one to the bit pattern, plus the kept lowest bit, and
+// truncate (a carry into the exponent rounds up to the next binade or to
+// infinity); NaN stays a quiet NaN.
+__device__ __forceinline__ float bf16_rne(float f) {
+  uint32_t u = __float_as_uint(f);
+  if ((u & 0x7FFFFFFFu) > 0x7F800000u) return __uint_as_float(0x7FC00000u);
+  u += 0x7FFFu + ((u >> 16) & 1u);
+  return __uint_as_float(u & 0xFFFF0000u);
 }
 
 // QK-RMSNorm then RoPE on one (token, head) row held by a warp, E channels
-// per lane (channel lane * E + e), in fp64 with one bf16 rounding at the end
-// (QkNormRotaryTNH, onnxruntime PR #29912, Summary of Changes; the readings
-// are the ones kvq.h states).  `ys` is this warp's staging row of 32 E
-// doubles, used to fetch each channel's rotation partner.  Returns false,
-// after flagging KVQ_DEVERR_POSITION, when the token's position is outside
-// the tables (the caller then writes nothing for the token).
+// per lane (channel lane * E + e), one bf16 rounding at the end
+// (QkNormRotaryTNH, onnxruntime PR #29912, Summary of Changes).  The bf16
+// result decides the quantized codes, so every step is one IEEE fp32
+// operation in a fixed order: per-lane sums of squares in channel order, then
+// a butterfly over lanes 16, 8, 4, 2, 1 (every lane ends with the same bits),
+// r = 1 / sqrt(s / D + eps), y = (x * r) * w, and each rotated value as
+// (y * cos) -+ (partner * sin) with both products rounded.  `ys` is this
+// warp's staging row of 32 E floats, used to fetch each channel's rotation
+// partner.  Returns false, after flagging KVQ_DEVERR_POSITION, when the
+// token's position is outside the tables (the caller then writes nothing).
 template <int E>
-__device__ bool norm_rope_row(const NormRope& p, int n, int lane, float (&x)[E], double* ys,
-                              unsigned int* err) {
+__device__ bool norm_rope_row(const NormRope& p, int n, int lane, float (&x)[E], float* ys, unsigned int* err) {
   constexpr int D = 32 * E;
   long long pos = 0;
   if (p.rd > 0) {
@@ -90,24 +89,21 @@ __device__ bool norm_rope_row(const NormRope& p, int n, int lane, float (&x)[E],
       return false;
     }
   }
-  double y[E];
-#pragma unroll
-  for (int e = 0; e < E; ++e) y[e] = (double)x[e];
   if (p.w) {
-    double ss = 0.0;
+    float ss = 0.0f;
 #pragma unroll
-    for (int e = 0; e < E; ++e) ss = __dadd_rn(ss, __dmul_rn(y[e], y[e]));
+    for (int e = 0; e < E; ++e) ss = __fadd_rn(ss, __fmul_rn(x[e], x[e]));
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) ss = __dadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, o));
-    const double r = __ddiv_rn(1.0, __dsqrt_rn(__dadd_rn(__ddiv_rn(ss, (double)D), p.eps)));
+    for (int o = 16; o > 0; o >>= 1) ss = __fadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, o));
+    const float r = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ss, (float)D), p.eps)));
     float w[E];
     load_bf16<E>(p.w + lane * E, w);
 #pragma unroll
-    for (int e = 0; e < E; ++e) y[e] = __dmul_rn(__dmul_rn(y[e], r), (double)w[e]);
+    for (int e = 0; e < E; ++e) x[e] = __fmul_rn(__fmul_rn(x[e], r), w[e]);
   }
   if (p.rd > 0) {
 #pragma unroll
-    for (int e = 0; e < E; ++e) ys[lane * E + e] = y[e];
+    for (int e = 0; e < E; ++e) ys[lane * E + e] = x[e];
     __syncwarp();
     const int half = p.rd >> 1;
     const float* cs = p.cos_tab + (size_t)pos * half;
@@ -119,15 +115,15 @@ __device__ bool norm_rope_row(const NormRope& p, int n, int lane, float (&x)[E],
         const bool first = p.interleaved ? (j & 1) == 0 : j < half;
         const int i = p.interleaved ? j >> 1 : (first ? j : j - half);
         const int partner = p.interleaved ? (first ? c + 1 : c - 1) : (first ? c + half : c - half);
-        const double co = (double)cs[i], si = (double)sn[i], o = ys[partner];
-        y[e] = first ? __dsub_rn(__dmul_rn(y[e], co), __dmul_rn(o, si))
-                     : __dadd_rn(__dmul_rn(y[e], co), __dmul_rn(o, si));
+        const float co = cs[i], si = sn[i], o = ys[partner];
+        x[e] = first ? __fsub_rn(__fmul_rn(x[e], co), __fmul_rn(o, si))
+                     : __fadd_rn(__fmul_rn(x[e], co), __fmul_rn(o, si));
       }
     }
     __syncwarp();
   }
 #pragma unroll
-  for (int e = 0; e < E; ++e) x[e] = bf16_rne_f64(y[e]);
+  for (int e = 0; e < E; ++e) x[e] = bf16_rne(x[e]);
   return true;
 }
 
@@ -157,7 +153,7 @@ __global__ void __launch_bounds__(256) append_kernel(const AppendArgs a) {
   if (a.k_prologue) {
     // both sides of a token are skipped when its position is bad: the V warp
     // checks the position too (without flagging it twice)
-    __shared__ double ys[8][D];
+    __shared__ float ys[8][D];
     if (side == 0) {
       if (!norm_rope_row<E>(a.pro, n, lane, x, ys[(threadIdx.x >> 5) & 7], a.err)) return;
     } else if (a.pro.rd > 0) {
@@ -224,7 +220,7 @@ __global__ void __launch_bounds__(256) append_kernel(const AppendArgs a) {
 template <int D>
 __global__ void __launch_bounds__(256) norm_rope_kernel(const NormRopeArgs a) {
   constexpr int E = D / 32;
-  __shared__ double ys[8][D];
+  __shared__ float ys[8][D];
   ptx::griddep_wait();
   ptx::griddep_launch_dependents();
   const int wg = (int)((blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5);

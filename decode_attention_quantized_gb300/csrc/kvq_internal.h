@@ -22,7 +22,7 @@ constexpr int kMaxStages = 8;
 // The QK-RMSNorm + RoPE prologue (kvq_norm_rope, host-validated).
 struct NormRope {
   const uint16_t* w;        // bf16 bits [D] or null (no RMSNorm)
-  double eps;
+  float eps;
   const float* cos_tab;     // [max_pos, rd / 2]
   const float* sin_tab;
   const int64_t* positions; // [N] (rd > 0)

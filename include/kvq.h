@@ -149,7 +149,7 @@ KVQ_API kvq_status kvq_append(const kvq_cache* cache, const void* k_new, const v
  * in onnxruntime PR #29912, Summary of Changes: q_norm_weight / k_norm_weight
  * inputs, qk_norm_epsilon with default 1e-6, rotary_offset, which rotates
  * channels [rotary_offset, rotary_offset + rotary_dim)).  For each (token,
- * head) row x of head_dim bf16 values, in fp64:
+ * head) row x of head_dim bf16 values:
  *   RMSNorm (norm_weight != NULL): y_d = (x_d * r) * w_d,
  *     r = 1 / sqrt(sum_d x_d^2 / head_dim + eps);
  *   RoPE (rotary_dim > 0): the pair (a, b) of angle index i in
@@ -157,8 +157,14 @@ KVQ_API kvq_status kvq_append(const kvq_cache* cache, const void* k_new, const v
  *     cos = cos_cache[pos, i], sin = sin_cache[pos, i] for the token's
  *     position pos; pairs are (off + i, off + i + rotary_dim/2) (half split)
  *     or (off + 2i, off + 2i + 1) (rotary_interleaved);
- * then one round-to-nearest-even to bf16 per value.  The pages fix neither the
- * rotation layout nor the tables: both are the caller's, as here. */
+ * then one round-to-nearest-even to bf16 per value.  Arithmetic is IEEE fp32,
+ * one rounding per operation in a fixed order, so results are reproducible
+ * bit for bit: with E = head_dim / 32, the squares of channels
+ * l*E .. l*E + E - 1 are summed in order into partial l (l = 0..31), then for
+ * o = 16, 8, 4, 2, 1 each partial l becomes partial l + partial (l xor o);
+ * each rotated value is (y * cos) -+ (partner * sin) with both products
+ * rounded.  The pages fix neither the rotation layout nor the tables: both
+ * are the caller's, as here. */
 typedef struct {
   const void* norm_weight;    /* bf16 [head_dim] (device), or NULL: no RMSNorm */
   float norm_eps;             /* <= 0 selects 1e-6 */
@@ -182,7 +188,7 @@ KVQ_API kvq_status kvq_norm_rope_apply(const kvq_norm_rope* prologue, const void
 
 /* kvq_append_norm_rope -- kvq_append with the prologue fused in front of the
  * K quantizer: each K row is normalized and rotated as kvq_norm_rope_apply
- * would (same fp64 arithmetic, same bf16 rounding) and the resulting bf16 row
+ * would (same fp32 arithmetic, same bf16 rounding) and the resulting bf16 row
  * is quantized exactly as kvq_append quantizes its input; V rows are
  * quantized as given (the prologue acts on Q and K only).  A token with a
  * negative slot is skipped; one whose position is outside the tables sets

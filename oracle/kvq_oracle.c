@@ -37,7 +37,8 @@
  *  query head for every query token; R16 an empty key set gives o = 0 and
  *  lse = -inf.  For the prologue before the cache write: R19 RMSNorm, then
  *  RoPE; R20 RMSNorm per (token, head) over the D channels with one bf16 weight
- *  vector per side, fp64 arithmetic and a single bf16 rounding at the end;
+ *  vector per side, in fp32 with a fixed operation order (its bf16 result
+ *  decides the codes) and a single bf16 rounding at the end;
  *  R21 RoPE angles come as caller tables cos/sin [max_pos, rotary_dim/2]
  *  indexed by the token's position, half-split pairs unless interleaved is
  *  asked for; R22 on the cache side only K takes the prologue, V is written as
@@ -288,49 +289,69 @@ uint16_t orc_f64_to_bf16(double v) {
   return (uint16_t)(u >> 16);
 }
 
-/* One row of D values, fp64 throughout:
- *   RMSNorm (when w != NULL): y_d = (x_d * r) * w_d with
- *     r = 1 / sqrt(sum_d x_d^2 / D + eps);
- *   RoPE (when rd > 0) on channels [off, off + rd), angle index i in
- *     [0, rd/2): the pair (a, b) = (off + i, off + i + rd/2) (half split) or
+/* One row of D values.  The bf16 result decides the quantized codes, so it is
+ * taken in the kernel's precision, fp32, with every operation in a fixed order
+ * (reading R20; each step is one IEEE binary32 operation, no contraction):
+ *   RMSNorm (w != NULL): lane l = 0..31 owns channels l*E .. l*E + E - 1
+ *     (E = D/32) and sums their squares in channel order (s = s + x*x); then,
+ *     for o = 16, 8, 4, 2, 1, every lane's partial becomes its own plus lane
+ *     (l xor o)'s; r = 1 / sqrt(s / D + eps); y_d = (x_d * r) * w_d;
+ *   RoPE (rd > 0) on channels [off, off + rd), angle index i in [0, rd/2):
+ *     the pair (a, b) = (off + i, off + i + rd/2) (half split) or
  *     (off + 2i, off + 2i + 1) (interleaved) becomes
- *     (a cos_i - b sin_i, b cos_i + a sin_i), cos_i = cs[i], sin_i = sn[i]
+ *     (a*cos_i - b*sin_i, b*cos_i + a*sin_i), cos_i = cs[i], sin_i = sn[i]
  *     (the caller's table row of the token's position);
- * then one round-to-nearest-even to bf16 per value. */
-void orc_norm_rope_row(const uint16_t* x, int D, const uint16_t* w, double eps, int rd, int off,
+ * then round to nearest even to bf16. */
+void orc_norm_rope_row(const uint16_t* x, int D, const uint16_t* w, float eps, int rd, int off,
                        int interleaved, const float* cs, const float* sn, uint16_t* out) {
-  double y[512];
-  for (int d = 0; d < D; ++d) y[d] = (double)orc_bf16_to_f32(x[d]);
+  float y[512];
+  for (int d = 0; d < D; ++d) y[d] = orc_bf16_to_f32(x[d]);
   if (w) {
-    double ss = 0.0;
-    for (int d = 0; d < D; ++d) ss += y[d] * y[d];
-    double r = 1.0 / sqrt(ss / (double)D + eps);
-    for (int d = 0; d < D; ++d) y[d] = (y[d] * r) * (double)orc_bf16_to_f32(w[d]);
+    int E = D / 32;
+    float part[32], nxt[32];
+    for (int l = 0; l < 32; ++l) {
+      float acc = 0.0f;
+      for (int e = 0; e < E; ++e) {
+        float sq = y[l * E + e] * y[l * E + e];
+        acc = acc + sq;
+      }
+      part[l] = acc;
+    }
+    for (int o = 16; o > 0; o >>= 1) {
+      for (int l = 0; l < 32; ++l) nxt[l] = part[l] + part[l ^ o];
+      memcpy(part, nxt, sizeof part);
+    }
+    float ms = part[0] / (float)D;
+    float r = 1.0f / sqrtf(ms + eps);
+    for (int d = 0; d < D; ++d) {
+      float t = y[d] * r;
+      y[d] = t * orc_bf16_to_f32(w[d]);
+    }
   }
   if (rd > 0) {
-    double z[512];
-    memcpy(z, y, sizeof(double) * (size_t)D);
+    float z[512];
+    memcpy(z, y, sizeof(float) * (size_t)D);
     for (int i = 0; i < rd / 2; ++i) {
       int a = interleaved ? off + 2 * i : off + i;
       int b = interleaved ? a + 1 : a + rd / 2;
-      double c = (double)cs[i], s = (double)sn[i];
-      z[a] = y[a] * c - y[b] * s;
-      z[b] = y[b] * c + y[a] * s;
+      float ac = y[a] * cs[i], bs = y[b] * sn[i], bc = y[b] * cs[i], as = y[a] * sn[i];
+      z[a] = ac - bs;
+      z[b] = bc + as;
     }
-    memcpy(y, z, sizeof(double) * (size_t)D);
+    memcpy(y, z, sizeof(float) * (size_t)D);
   }
-  for (int d = 0; d < D; ++d) out[d] = orc_f64_to_bf16(y[d]);
+  for (int d = 0; d < D; ++d) out[d] = orc_f64_to_bf16((double)y[d]);
 }
 
 /* The prologue over x [n_tokens, H, D] -> out (same shape, bf16 bits).  The
  * RoPE tables are [max_pos, rd/2]; a token whose position lies outside
  * [0, max_pos) while rd > 0 is left untouched in out and counted in the
  * return value. */
-int orc_norm_rope(const uint16_t* x, int n_tokens, int H, int D, const uint16_t* w, double eps, int rd,
+int orc_norm_rope(const uint16_t* x, int n_tokens, int H, int D, const uint16_t* w, float eps, int rd,
                   int off, int interleaved, const float* cos_tab, const float* sin_tab, int max_pos,
                   const int64_t* positions, uint16_t* out) {
   int bad = 0;
-  if (D > 512 || rd < 0 || rd % 2 || off < 0 || off + rd > D) return -1;
+  if (D > 512 || D % 32 || rd < 0 || rd % 2 || off < 0 || off + rd > D) return -1;
   for (int n = 0; n < n_tokens; ++n) {
     int64_t pos = rd > 0 ? positions[n] : 0;
     if (rd > 0 && (pos < 0 || pos >= max_pos)) {

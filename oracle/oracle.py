@@ -82,7 +82,7 @@ def lib():
             L.orc_attend.argtypes = [ctypes.POINTER(_Cache), ctypes.POINTER(_Params), vp, vp, vp, vp,
                                      vp, i32, vp, vp, i32]
             L.orc_attend.restype = i32
-            L.orc_norm_rope.argtypes = [vp, i32, i32, i32, vp, ctypes.c_double, i32, i32, i32, vp, vp, i32,
+            L.orc_norm_rope.argtypes = [vp, i32, i32, i32, vp, ctypes.c_float, i32, i32, i32, vp, vp, i32,
                                         vp, vp]
             L.orc_norm_rope.restype = i32
             L.orc_f64_to_bf16.argtypes = [ctypes.c_double]
@@ -116,7 +116,8 @@ def norm_rope(x_bf16: np.ndarray, *, norm_weight=None, eps: float = 1e-6, rotary
     qk_norm_epsilon default 1e-6, rotary_offset; QkNormRotaryTNH).  Per row:
     y = x / sqrt(mean(x^2) + eps) * w, then each rotated pair (a, b) ->
     (a cos - b sin, b cos + a sin) with cos / sin the tables' row for the
-    token's position; fp64, one bf16 rounding.  Tokens whose position is
+    token's position; fp32 in the fixed order kvq_oracle.c states (the bf16
+    result decides the codes), one bf16 rounding.  Tokens whose position is
     outside the tables are left zero and counted."""
     x = np.ascontiguousarray(x_bf16, dtype=np.uint16)
     N, H, D = x.shape

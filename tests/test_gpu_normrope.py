@@ -2,8 +2,9 @@
 (QkNormRotaryTNH, onnxruntime PR #29912, Summary of Changes).
 
 kvq_norm_rope_apply's bf16 rows and kvq_append_norm_rope's codes and scales
-are compared element by element with the oracle; both sides compute in fp64
-and round once to bf16, so the rows agree bit for bit.  Then a decode over
+are compared element by element with the oracle; both sides compute in fp32
+in the same fixed order and round once to bf16, so the rows agree bit for
+bit.  Then a decode over
 prologue-rotated queries and keys is compared with oracle attention."""
 import numpy as np
 import pytest

@@ -26,9 +26,11 @@ def bits_to_f64(u):
 
 
 def half_ulp_bf16(v):
-    """Half the bf16 spacing at |v| (normal range)."""
+    """Half the bf16 spacing at |v| (normal range), plus the few fp32 roundings
+    of the prologue's arithmetic (relative 2^-20), which can move a value that
+    sits next to a bf16 tie across it."""
     e = np.floor(np.log2(np.maximum(np.abs(v), 2.0 ** -126)))
-    return np.ldexp(1.0, (e - 8).astype(int))
+    return np.ldexp(1.0, (e - 8).astype(int)) + np.abs(v) * 2.0 ** -20
 
 
 def rows(shape, *parts):
@@ -63,6 +65,36 @@ def test_f64_to_bf16_rounds_once_from_double(orc):
 
 # ------------------------------------------------------------------ RMSNorm
 
+def test_rms_norm_sum_order_is_the_stated_butterfly(orc):
+    """The sum of squares follows the stated order (per-lane sums, then the
+    lane butterfly), retyped here in float32 NumPy on rows whose order
+    matters (mixed magnitudes): the oracle's row equals the one built from
+    that sum, and differs from a plain sequential sum on some row."""
+    D, E = 256, 8
+    g = np.random.default_rng(11)
+    x = (g.standard_normal((40, D)) * np.exp2(g.integers(-12, 12, (40, D)))).astype(np.float32)
+    xb = bf16_bits(x)
+    xf = bits_to_f64(xb).astype(np.float32)
+    w = np.full(D, 0x3F80, np.uint16)
+    out, _ = orc.norm_rope(xb[:, None, :], norm_weight=w, eps=1e-6)
+    seq_differs = False
+    for n in range(40):
+        part = np.zeros(32, np.float32)
+        for l in range(32):
+            for e in range(E):
+                part[l] = np.float32(part[l] + np.float32(xf[n, l * E + e] * xf[n, l * E + e]))
+        for o in (16, 8, 4, 2, 1):
+            part = (part + part[np.arange(32) ^ o]).astype(np.float32)
+        r = np.float32(1.0) / np.sqrt(np.float32(part[0] / np.float32(D)) + np.float32(1e-6))
+        want = bf16_bits((xf[n] * r).astype(np.float32))
+        assert np.array_equal(out[n, 0], want)
+        s = np.float32(0)
+        for d in range(D):
+            s = np.float32(s + np.float32(xf[n, d] * xf[n, d]))
+        seq_differs |= s != part[0]
+    assert seq_differs
+
+
 def test_rms_norm_of_a_constant_row_is_closed_form(orc):
     D, eps = 128, 1e-6
     for c in (0.5, -3.0, 1e-3):
@@ -72,7 +104,7 @@ def test_rms_norm_of_a_constant_row_is_closed_form(orc):
         cf = float(bits_to_f64(x[0, 0, 0]))
         ref = cf / math.sqrt(cf * cf + eps) * bits_to_f64(w)
         assert bad == 0
-        assert np.array_equal(out[0, 0], np.array([orc.f64_to_bf16(v) for v in ref], np.uint16))
+        assert (np.abs(bits_to_f64(out[0, 0]) - ref) <= half_ulp_bf16(ref)).all()
 
 
 def test_rms_norm_matches_torch_fp64(orc):
@@ -84,7 +116,7 @@ def test_rms_norm_matches_torch_fp64(orc):
         ref = torch.nn.functional.rms_norm(torch.from_numpy(bits_to_f64(x)), (D,),
                                            torch.from_numpy(bits_to_f64(w)), eps).numpy()
         got = bits_to_f64(out)
-        assert (np.abs(got - ref) <= half_ulp_bf16(ref) * (1 + 1e-9)).all()
+        assert (np.abs(got - ref) <= half_ulp_bf16(ref)).all()
 
 
 def test_rms_norm_is_scale_invariant_and_has_unit_rms(orc):
@@ -190,4 +222,4 @@ def test_norm_then_rope_order_and_bad_positions(orc):
     z = y.copy()
     z[:32] = y[:32] * c - y[32:] * s
     z[32:] = y[32:] * c + y[:32] * s
-    assert (np.abs(bits_to_f64(out[0, 0]) - z) <= half_ulp_bf16(z) * (1 + 1e-9)).all()
+    assert (np.abs(bits_to_f64(out[0, 0]) - z) <= half_ulp_bf16(z)).all()
