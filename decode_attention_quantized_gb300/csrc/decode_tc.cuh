@@ -294,7 +294,8 @@ __global__ void __launch_bounds__(kTcWarps * 32, 1)
   } else if (warp >= kDqK && warp < kDqK + 4) {
     // ========================================================== K dequant
     // thread = key 32 q + lane of the tile = TMEM lane of the K operand; the
-    // two channel halves are written (and freed by QK^T) one after the other
+    // two channel halves are written (and freed by QK^T) one after the other,
+    // each converted before the wait for the QK^T that frees it
     const int q = warp - kDqK, kk = 32 * q + lane;
     const uint32_t t_k = tmem + ((uint32_t)(32 * q) << 16) + C::K_COL;
     constexpr int HCH = Gm::NCH / 2;  // 16-byte chunks of a channel half
@@ -308,13 +309,9 @@ __global__ void __launch_bounds__(kTcWarps * 32, 1)
         const uint8_t* st = ring + (size_t)stage * Gm::STAGE_STRIDE;
 #pragma unroll 1
         for (int half = 0; half < 2; ++half) {
-          if (it > 0) {
-            if (half == 0) wait(b_kh0, (it - 1) & 1);                        // QK^T(t-1) read channel half 0
-            else wait(&b_qk[(it - 1) & 1], ((it - 1) >> 1) & 1);             // QK^T(t-1) complete
-          }
-          ptx::tc_fence_after();
-          // all of the half's chunks are read before the first TMEM store
-          // (loads cannot move across the stores' memory clobber)
+          // the half's codes are read and converted before the wait for the
+          // previous QK^T, so only the TMEM stores follow its completion
+          constexpr int CW = DT == KVQ_INT4 ? 16 : 8;  // K columns per 16-byte chunk
           uint4 w[HCH];
 #pragma unroll
           for (int jj = 0; jj < HCH; ++jj) {
@@ -322,19 +319,19 @@ __global__ void __launch_bounds__(kTcWarps * 32, 1)
             w[jj] = *reinterpret_cast<const uint4*>(
                 st + (byte / Gm::SPAN) * (KT * Gm::SPAN) + dev::swz<Gm::SPAN>(kk * Gm::SPAN + byte % Gm::SPAN));
           }
+          uint32_t v[HCH * CW];
 #pragma unroll
-          for (int jj = 0; jj < HCH; ++jj) {
-            const int j = half * HCH + jj;
-            if constexpr (DT == KVQ_INT4) {
-              uint32_t v[16];
-              dev::k_cols<DT>(w[jj], v);
-              ptx::tmem_st16(t_k + 16 * j, v);
-            } else {
-              uint32_t v[8];
-              dev::k_cols<DT>(w[jj], v);
-              ptx::tmem_st8(t_k + 8 * j, v);
-            }
+          for (int jj = 0; jj < HCH; ++jj) dev::k_cols<DT>(w[jj], v + CW * jj);
+          if (it > 0) {
+            if (half == 0) wait(b_kh0, (it - 1) & 1);                        // QK^T(t-1) read channel half 0
+            else wait(&b_qk[(it - 1) & 1], ((it - 1) >> 1) & 1);             // QK^T(t-1) complete
           }
+          ptx::tc_fence_after();
+          // the half's HCH * CW columns (32 or 64) in one store
+          if constexpr (HCH * CW == 64)
+            ptx::tmem_st64(t_k + HCH * CW * half, v);
+          else
+            ptx::tmem_st32(t_k + HCH * CW * half, v);
           ptx::tmem_wait_st();
           ptx::tc_fence_before();
           __syncwarp();
