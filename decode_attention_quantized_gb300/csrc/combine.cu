@@ -39,15 +39,16 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const Combi
   const int h = hq / a.group;
   const int r = t * a.group + (hq % a.group);  // row inside a work unit
 
-  // pieces of segment s = b * Hkv + h are the CTAs whose tile slices meet it;
-  // the piece of CTA x sits in slot s + x
-  const int W = a.plan[0];
+  // pieces of segment s = b * Hkv + h are the CTAs whose cost ranges [x W,
+  // (x + 1) W) meet the segment's tiles, which sit at cost positions
+  // first tile + c s onward; the piece of CTA x sits in slot s + x
+  const int W = a.plan[0], c = a.plan[2];
   const int* pre = a.plan + 4;
   const int nb = pre[b + 1] - pre[b];
   const int seg = b * a.num_kv_heads + h;
-  const int s_first = pre[b] * a.num_kv_heads + h * nb;
-  const int i0 = nb > 0 ? seg + s_first / W : 0;
-  const int i1 = nb > 0 ? seg + (s_first + nb - 1) / W + 1 : 0;
+  const long long s_cost = (long long)pre[b] * a.num_kv_heads + (long long)h * nb + (long long)c * seg;
+  const int i0 = nb > 0 ? seg + (int)(s_cost / W) : 0;
+  const int i1 = nb > 0 ? seg + (int)((s_cost + nb - 1) / W) + 1 : 0;
   auto lse_of = [&](int slot) { return a.part_lse[(size_t)slot * a.rows + r]; };
 
   float m = -INFINITY;

@@ -66,7 +66,8 @@ struct DecodeArgs {
   int window;
   int row_groups, key_warps, stages;
   int units_max;    // partial slots (grid + batch * Hkv)
-  int* plan;        // workspace: [0] tiles per CTA, [1] total tiles, [2] batch, [3] slots, then tile prefix[B+1]
+  int piece_cost;   // tiles' worth of time a CTA spends on each piece change (split planning)
+  int* plan;        // workspace: [0] cost per CTA, [1] total tiles, [2] piece cost, [3] slots, then tile prefix[B+1]
   float* part_lse;  // [units_max, rows]   base-2 log-sum-exp of each piece
   float* part_o;    // [units_max, rows, D] normalized piece output
   unsigned int* err;

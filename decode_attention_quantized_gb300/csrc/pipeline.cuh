@@ -46,12 +46,15 @@ __device__ __forceinline__ uint32_t swz(uint32_t o) {
 
 // The split plan.  Segment s = b * Hkv + h is sequence b's key range
 // [lo_b, L_b) for kv head h: n_b = ceil((L_b - lo_b) / KT) tiles.  The
-// segments laid end to end in s order make `total` tiles, and CTA x takes the
-// contiguous slice [x W, (x + 1) W) with W = ceil(total / gridDim.x), so
-// every CTA streams the same number of tiles whatever the length mix.  The
-// piece of segment s in CTA x's slice writes its partial to slot s + x:
-// distinct for every piece and contiguous over the pieces of one segment
-// (the combine walks them in that order).
+// segments laid end to end in s order make `total` tiles.  Each CTA also
+// pays a fixed time per piece it starts (the query prologue, the merge and
+// the partial write), worth `c` tiles (DecodeArgs::piece_cost): so on a cost
+// line each segment occupies its n_b tiles followed by c units of gap, and
+// CTA x takes the cost range [x W, (x + 1) W), W = ceil(total cost / grid).
+// A CTA whose range straddles a segment change takes c fewer tiles; c = 0 is
+// the plain equal-tiles split.  The piece of segment s in CTA x writes its
+// partial to slot s + x: distinct for every piece and contiguous over the
+// pieces of one segment (the combine walks them in that order).
 template <int KT>
 struct Slice {
   const int* pre;  // shared [B + 1]: tile prefix over sequences
@@ -112,6 +115,7 @@ __device__ Slice<KT> build_slice(const DecodeArgs& a, int* pl_pre, int* pl_misc)
     pl_pre[b] = (max(0, L - lo) + KT - 1) / KT;  // tiles, for now
   }
   __syncthreads();
+  const int c = a.piece_cost;
   if (warp == 0) {
     const int seg = (B + 31) / 32;
     const int s0 = min(B, lane * seg), s1 = min(B, s0 + seg);
@@ -131,17 +135,33 @@ __device__ Slice<KT> build_slice(const DecodeArgs& a, int* pl_pre, int* pl_misc)
     }
     if (lane == 31) {
       const int total = incl * Hkv;
+      const long long cost = total > 0 ? (long long)total + (long long)c * (B * Hkv - 1) : 0;
       pl_pre[B] = incl;
-      pl_misc[0] = max(1, (total + (int)gridDim.x - 1) / (int)gridDim.x);
+      pl_misc[0] = (int)max(1LL, (cost + gridDim.x - 1) / gridDim.x);
       pl_misc[1] = total;
+      pl_misc[2] = (int)cost;
     }
   }
   __syncthreads();
   // the combine may be scheduled now; it waits for this grid to complete
   ptx::griddep_launch_dependents();
-  const int W = pl_misc[0];
-  sp.t_begin = min((int)blockIdx.x * W, pl_misc[1]);
-  sp.t_end = min(sp.t_begin + W, pl_misc[1]);
+  const int W = pl_misc[0], total = pl_misc[1], cost = pl_misc[2];
+  // first tile at or after cost position p
+  auto tile_at = [&](long long p) -> int {
+    if (p >= cost) return total;
+    int lo = 0, hi = B - 1;  // last b whose first segment starts at or before p
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if ((long long)pl_pre[mid] * Hkv + (long long)c * mid * Hkv <= p) lo = mid; else hi = mid - 1;
+    }
+    const int nb = pl_pre[lo + 1] - pl_pre[lo];
+    const long long base = (long long)pl_pre[lo] * Hkv + (long long)c * lo * Hkv;
+    const int h = (int)min((long long)(Hkv - 1), (p - base) / (nb + c));
+    const long long off = p - base - (long long)h * (nb + c);
+    return pl_pre[lo] * Hkv + h * nb + (int)min(off, (long long)nb);
+  };
+  sp.t_begin = tile_at((long long)blockIdx.x * W);
+  sp.t_end = max(sp.t_begin, tile_at((long long)(blockIdx.x + 1) * W));
   return sp;
 }
 
@@ -154,7 +174,7 @@ __device__ __forceinline__ void publish_slice(const DecodeArgs& a, const int* pl
   if (lane == 0) {
     a.plan[0] = pl_misc[0];
     a.plan[1] = pl_misc[1];
-    a.plan[2] = a.batch;
+    a.plan[2] = a.piece_cost;
     a.plan[3] = a.units_max;
   }
 }
