@@ -180,8 +180,8 @@ __device__ __forceinline__ void publish_slice(const DecodeArgs& a, const int* pl
 }
 
 // The producer warp.  The whole warp fetches a piece's block ids 32 pages at
-// a time (one coalesced load per 32 pages) and hands them to lane 0 by
-// shuffles.  The first piece's ids are read before the wait on the preceding
+// a time (one coalesced load per 32 pages, the next batch loaded while the
+// current one is used) and hands them to lane 0 by shuffles.  The first piece's ids are read before the wait on the preceding
 // grid (no kvq kernel writes the block table); the cache is read, and the
 // plan published, only after it.  Lane 0 waits for a free stage and issues,
 // per page segment of the stage, one TMA tensor copy per (slab, side) with
@@ -223,6 +223,9 @@ __device__ void produce(const DecodeArgs& a, const Slice<Gm::KEYS>& sp, const CU
     const int p_last = (k1 - 1) >> a.log2_bs;
     int base = k0 >> a.log2_bs;
     int my_id = base + lane <= p_last ? bt[base + lane] : -1;
+    // the next 32 ids are in flight while these are used, so a batch change
+    // does not stall the copies on a block-table read
+    int nx_id = base + 32 + lane <= p_last ? bt[base + 32 + lane] : -1;
     gate();
     if (gt != sp.t_begin) {
       // the consumers read this piece's query rows once the previous piece
@@ -257,7 +260,8 @@ __device__ void produce(const DecodeArgs& a, const Slice<Gm::KEYS>& sp, const CU
           const int page = skey >> a.log2_bs;
           if (page - base >= 32) {
             base += 32;
-            my_id = base + lane <= p_last ? bt[base + lane] : -1;
+            my_id = nx_id;
+            nx_id = base + 32 + lane <= p_last ? bt[base + 32 + lane] : -1;
           }
           const int id = __shfl_sync(0xffffffffu, my_id, page - base);
           if (id < 0 || id >= a.num_blocks) {
@@ -294,7 +298,8 @@ __device__ void produce(const DecodeArgs& a, const Slice<Gm::KEYS>& sp, const CU
           const int page = skey >> a.log2_bs;
           if (page - base >= 32) {
             base += 32;
-            my_id = base + lane <= p_last ? bt[base + lane] : -1;
+            my_id = nx_id;
+            nx_id = base + 32 + lane <= p_last ? bt[base + 32 + lane] : -1;
           }
           const int id = __shfl_sync(0xffffffffu, my_id, page - base);
           if (lane == 0) {
