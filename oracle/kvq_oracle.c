@@ -42,7 +42,9 @@
  *  R21 RoPE angles come as caller tables cos/sin [max_pos, rotary_dim/2]
  *  indexed by the token's position, half-split pairs unless interleaved is
  *  asked for; R22 on the cache side only K takes the prologue, V is written as
- *  given.
+ *  given; R23 the optional Walsh-Hadamard rotation (onnxruntime PR #32515,
+ *  note on the stacked change that adds it) comes after RoPE, on Q and K
+ *  alike (so dot products are unchanged), in Sylvester order.
  *
  * Parity pins live in tests/ (format table of e4m3 against torch's
  * float8_e4m3fn, brute-force nearest-code search, round-trip bounds, the
@@ -301,9 +303,10 @@ uint16_t orc_f64_to_bf16(double v) {
  *     (off + 2i, off + 2i + 1) (interleaved) becomes
  *     (a*cos_i - b*sin_i, b*cos_i + a*sin_i), cos_i = cs[i], sin_i = sn[i]
  *     (the caller's table row of the token's position);
- * then round to nearest even to bf16. */
+ * then (optionally) the Walsh-Hadamard rotation below, then round to nearest
+ * even to bf16. */
 void orc_norm_rope_row(const uint16_t* x, int D, const uint16_t* w, float eps, int rd, int off,
-                       int interleaved, const float* cs, const float* sn, uint16_t* out) {
+                       int interleaved, const float* cs, const float* sn, int hadamard, uint16_t* out) {
   float y[512];
   for (int d = 0; d < D; ++d) y[d] = orc_bf16_to_f32(x[d]);
   if (w) {
@@ -340,6 +343,21 @@ void orc_norm_rope_row(const uint16_t* x, int D, const uint16_t* w, float eps, i
     }
     memcpy(y, z, sizeof(float) * (size_t)D);
   }
+  if (hadamard) {
+    /* orthonormal Walsh-Hadamard rotation (Sylvester order, entry (i, j) =
+     * (-1)^popcount(i & j) / sqrt(D)): butterflies of span 1, 2, 4, ...,
+     * D/2, each pair (i, i + span) with i & span == 0 becoming
+     * (a + b, a - b) in fp32, then every value times fl32(1 / fl32(sqrt(D))) */
+    for (int span = 1; span < D; span <<= 1)
+      for (int i = 0; i < D; ++i)
+        if (!(i & span)) {
+          float a = y[i], b = y[i + span];
+          y[i] = a + b;
+          y[i + span] = a - b;
+        }
+    float sc = 1.0f / sqrtf((float)D);
+    for (int d = 0; d < D; ++d) y[d] = y[d] * sc;
+  }
   for (int d = 0; d < D; ++d) out[d] = orc_f64_to_bf16((double)y[d]);
 }
 
@@ -349,9 +367,10 @@ void orc_norm_rope_row(const uint16_t* x, int D, const uint16_t* w, float eps, i
  * return value. */
 int orc_norm_rope(const uint16_t* x, int n_tokens, int H, int D, const uint16_t* w, float eps, int rd,
                   int off, int interleaved, const float* cos_tab, const float* sin_tab, int max_pos,
-                  const int64_t* positions, uint16_t* out) {
+                  const int64_t* positions, int hadamard, uint16_t* out) {
   int bad = 0;
-  if (D > 512 || D % 32 || rd < 0 || rd % 2 || off < 0 || off + rd > D) return -1;
+  if (D > 512 || D % 32 || rd < 0 || rd % 2 || off < 0 || off + rd > D || (hadamard && (D & (D - 1))))
+    return -1;
   for (int n = 0; n < n_tokens; ++n) {
     int64_t pos = rd > 0 ? positions[n] : 0;
     if (rd > 0 && (pos < 0 || pos >= max_pos)) {
@@ -361,7 +380,7 @@ int orc_norm_rope(const uint16_t* x, int n_tokens, int H, int D, const uint16_t*
     const float* cs = rd > 0 ? cos_tab + (size_t)pos * (rd / 2) : NULL;
     const float* sn = rd > 0 ? sin_tab + (size_t)pos * (rd / 2) : NULL;
     for (int h = 0; h < H; ++h)
-      orc_norm_rope_row(x + ((size_t)n * H + h) * D, D, w, eps, rd, off, interleaved, cs, sn,
+      orc_norm_rope_row(x + ((size_t)n * H + h) * D, D, w, eps, rd, off, interleaved, cs, sn, hadamard,
                         out + ((size_t)n * H + h) * D);
   }
   return bad;

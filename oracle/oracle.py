@@ -83,7 +83,7 @@ def lib():
                                      vp, i32, vp, vp, i32]
             L.orc_attend.restype = i32
             L.orc_norm_rope.argtypes = [vp, i32, i32, i32, vp, ctypes.c_float, i32, i32, i32, vp, vp, i32,
-                                        vp, vp]
+                                        vp, i32, vp]
             L.orc_norm_rope.restype = i32
             L.orc_f64_to_bf16.argtypes = [ctypes.c_double]
             L.orc_f64_to_bf16.restype = ctypes.c_uint16
@@ -109,16 +109,20 @@ def f64_to_bf16(v: float) -> int:
 
 
 def norm_rope(x_bf16: np.ndarray, *, norm_weight=None, eps: float = 1e-6, rotary_dim: int = 0,
-              rotary_offset: int = 0, interleaved: bool = False, cos=None, sin=None, positions=None):
+              rotary_offset: int = 0, interleaved: bool = False, cos=None, sin=None, positions=None,
+              hadamard: bool = False):
     """QK-RMSNorm then RoPE on x [N, H, D] (bf16 bits) -> (bf16 bits, rows skipped).
 
     onnxruntime PR #29912, Summary of Changes (q_norm_weight / k_norm_weight,
     qk_norm_epsilon default 1e-6, rotary_offset; QkNormRotaryTNH).  Per row:
     y = x / sqrt(mean(x^2) + eps) * w, then each rotated pair (a, b) ->
     (a cos - b sin, b cos + a sin) with cos / sin the tables' row for the
-    token's position; fp32 in the fixed order kvq_oracle.c states (the bf16
-    result decides the codes), one bf16 rounding.  Tokens whose position is
-    outside the tables are left zero and counted."""
+    token's position, then (hadamard) the orthonormal Walsh-Hadamard
+    rotation (named as the follow-up to the int4 cache in onnxruntime PR
+    #32515's stacked-change note); fp32 in the fixed order kvq_oracle.c
+    states (the bf16 result
+    decides the codes), one bf16 rounding.  Tokens whose position is outside
+    the tables are left zero and counted."""
     x = np.ascontiguousarray(x_bf16, dtype=np.uint16)
     N, H, D = x.shape
     out = np.zeros_like(x)
@@ -132,7 +136,8 @@ def norm_rope(x_bf16: np.ndarray, *, norm_weight=None, eps: float = 1e-6, rotary
         cs = sn = pos = None
         max_pos = 0
     bad = lib().orc_norm_rope(_ptr(x), N, H, D, _ptr(w), float(eps), int(rotary_dim), int(rotary_offset),
-                              1 if interleaved else 0, _ptr(cs), _ptr(sn), int(max_pos), _ptr(pos), _ptr(out))
+                              1 if interleaved else 0, _ptr(cs), _ptr(sn), int(max_pos), _ptr(pos),
+                              1 if hadamard else 0, _ptr(out))
     if bad < 0:
         raise ValueError("norm_rope: bad shape")
     return out, bad

@@ -223,3 +223,65 @@ def test_norm_then_rope_order_and_bad_positions(orc):
     z[:32] = y[:32] * c - y[32:] * s
     z[32:] = y[32:] * c + y[:32] * s
     assert (np.abs(bits_to_f64(out[0, 0]) - z) <= half_ulp_bf16(z)).all()
+
+
+# ---------------------------------------------------------- Hadamard rotation
+
+def test_hadamard_matches_scipys_matrix(orc):
+    """The rotation is scipy's Sylvester Hadamard matrix over sqrt(D), within
+    the fp32 roundings of the butterflies and one bf16 rounding."""
+    from scipy.linalg import hadamard
+    for D in (64, 128, 256):
+        x = rows((3, 2, D), "normrope", "had", D)
+        out, _ = orc.norm_rope(x, hadamard=True)
+        ref = bits_to_f64(x) @ (hadamard(D).astype(np.float64) / math.sqrt(D)).T
+        tol = half_ulp_bf16(ref) + np.log2(D) * 2.0 ** -23 * np.abs(bits_to_f64(x)).sum(-1, keepdims=True) / math.sqrt(D)
+        assert (np.abs(bits_to_f64(out) - ref) <= tol).all()
+
+
+def test_hadamard_of_a_basis_vector_is_a_signed_row(orc):
+    # H e_j = column j: entries (-1)^popcount(i & j) / sqrt(D), exact for D = 64, 256
+    for D in (64, 256):
+        for j in (0, 1, 5, D - 1):
+            x = np.zeros((1, 1, D), np.uint16)
+            x[0, 0, j] = 0x3F80
+            out, _ = orc.norm_rope(x, hadamard=True)
+            sign = np.array([(-1) ** bin(i & j).count("1") for i in range(D)], np.float64)
+            assert np.array_equal(bits_to_f64(out[0, 0]), sign / math.sqrt(D))
+
+
+def test_hadamard_keeps_dot_products_and_is_its_own_inverse(orc):
+    D = 128
+    x = rows((4, 1, D), "normrope", "had-dot")
+    y = rows((4, 1, D), "normrope", "had-dot2")
+    hx, _ = orc.norm_rope(x, hadamard=True)
+    hy, _ = orc.norm_rope(y, hadamard=True)
+    d0 = (bits_to_f64(x) * bits_to_f64(y)).sum(-1)
+    d1 = (bits_to_f64(hx) * bits_to_f64(hy)).sum(-1)
+    scale = np.linalg.norm(bits_to_f64(x), axis=-1) * np.linalg.norm(bits_to_f64(y), axis=-1)
+    assert (np.abs(d1 - d0) <= 2 ** -7 * scale).all()
+    hhx, _ = orc.norm_rope(hx, hadamard=True)
+    assert np.allclose(bits_to_f64(hhx), bits_to_f64(x), rtol=2 ** -6, atol=2 ** -6 * np.abs(bits_to_f64(x)).max())
+
+
+def test_hadamard_spreads_an_outlier_channel_and_narrows_int4_error(orc):
+    """The reason for the rotation: a row with one large channel quantizes
+    badly per-row at int4 (every other channel rounds to zero); rotated, the
+    energy spreads over all channels and the dequantized row is closer."""
+    D = 128
+    x = rows((32, 1, D), "normrope", "had-outlier").astype(np.uint16)
+    xf = bits_to_f64(x)
+    xf[:, 0, 7] = 40.0
+    x = bf16_bits(xf.astype(np.float32))
+    hx, _ = orc.norm_rope(x, hadamard=True)
+
+    def err(rows_bits):
+        e = 0.0
+        for r in rows_bits[:, 0]:
+            codes, sc = orc.quantize_row(r, orc.INT4, orc.PER_ROW)
+            deq = orc.code_values(codes, orc.INT4, D) * sc
+            e += float(((deq - bits_to_f64(r)) ** 2).sum())
+        return e
+
+    # both in the rotated frame's norm (the rotation is orthonormal)
+    assert err(hx) < 0.5 * err(x)
