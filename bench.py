@@ -378,6 +378,9 @@ def measure_prologue(w, steps, warmup, peak):
     us_app = 1e3 * timed_graph(lambda: kvq.kvq_append(cache, k, v, slots), steps)
     us_fused = 1e3 * timed_graph(lambda: kvq.kvq_append_norm_rope(cache, pro, k, v, slots, pos), steps)
     us_q = 1e3 * timed_graph(lambda: kvq.kvq_norm_rope_apply(pro, q, qo, pos), steps)
+    pro_h = kvq.NormRope(norm_weight=pro.norm_weight, eps=pro.eps, rotary_dim=D, cos=pro.cos, sin=pro.sin,
+                         hadamard=True)
+    us_fused_h = 1e3 * timed_graph(lambda: kvq.kvq_append_norm_rope(cache, pro_h, k, v, slots, pos), steps)
     del cache, k, v, q, qo
 
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
@@ -397,7 +400,7 @@ def measure_prologue(w, steps, warmup, peak):
     del cache, k, v
     torch.cuda.empty_cache()
     return {"step_tokens": N, "append_us": round(us_app, 2), "append_norm_rope_us": round(us_fused, 2),
-            "norm_rope_q_us": round(us_q, 2),
+            "norm_rope_q_us": round(us_q, 2), "append_norm_rope_hadamard_us": round(us_fused_h, 2),
             "bulk": {"tokens": nb_tok, "append_norm_rope_us": round(1e3 * ms, 1), "gbs": round(gbs, 1),
                      "frac_of_hbm": round(gbs / peak, 3), "bytes": int(nbytes)},
             "prologue": f"RMSNorm (bf16 weight, eps 1e-6) + RoPE on all {D} channels (half split), fixed-order fp32"}

@@ -325,6 +325,9 @@ kvq_status check_norm_rope(const kvq_norm_rope* p, int head_dim, const int64_t* 
   r.off = off;
   r.interleaved = p->rotary_interleaved ? 1 : 0;
   r.max_pos = rd > 0 ? p->max_position : 0;
+  if (p->hadamard != 0 && p->hadamard != 1) return KVQ_ERR_INVALID_ARG;
+  r.hadamard = p->hadamard;
+  r.had_scale = 1.0f / std::sqrt((float)head_dim);
   *out = r;
   return KVQ_OK;
 }

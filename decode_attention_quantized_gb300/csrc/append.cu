@@ -67,8 +67,9 @@ __device__ __forceinline__ float bf16_rne(float f) {
   return __uint_as_float(u & 0xFFFF0000u);
 }
 
-// QK-RMSNorm then RoPE on one (token, head) row held by a warp, E channels
-// per lane (channel lane * E + e), one bf16 rounding at the end
+// QK-RMSNorm, RoPE, then optionally the Walsh-Hadamard rotation, on one
+// (token, head) row held by a warp, E channels per lane (channel lane * E +
+// e), one bf16 rounding at the end
 // (QkNormRotaryTNH, onnxruntime PR #29912, Summary of Changes).  The bf16
 // result decides the quantized codes, so every step is one IEEE fp32
 // operation in a fixed order: per-lane sums of squares in channel order, then
@@ -121,6 +122,32 @@ __device__ bool norm_rope_row(const NormRope& p, int n, int lane, float (&x)[E],
       }
     }
     __syncwarp();
+  }
+  if (p.hadamard) {
+    // Sylvester-order butterflies: span s pairs channels c and c + s (c & s
+    // == 0) into (a + b, a - b); spans below E stay inside the lane, the rest
+    // pair lane l with lane l ^ (s / E)
+#pragma unroll
+    for (int s = 1; s < E; s <<= 1) {
+#pragma unroll
+      for (int e = 0; e < E; ++e)
+        if (!(e & s)) {
+          const float a0 = x[e], b0 = x[e + s];
+          x[e] = __fadd_rn(a0, b0);
+          x[e + s] = __fsub_rn(a0, b0);
+        }
+    }
+#pragma unroll
+    for (int m = 1; m < 32; m <<= 1) {
+      const bool upper = (lane & m) != 0;
+#pragma unroll
+      for (int e = 0; e < E; ++e) {
+        const float o = __shfl_xor_sync(0xffffffffu, x[e], m);
+        x[e] = upper ? __fsub_rn(o, x[e]) : __fadd_rn(x[e], o);
+      }
+    }
+#pragma unroll
+    for (int e = 0; e < E; ++e) x[e] = __fmul_rn(x[e], p.had_scale);
   }
 #pragma unroll
   for (int e = 0; e < E; ++e) x[e] = bf16_rne(x[e]);

@@ -27,6 +27,8 @@ struct NormRope {
   const float* sin_tab;
   const int64_t* positions; // [N] (rd > 0)
   int rd, off, interleaved, max_pos;
+  int hadamard;             // Walsh-Hadamard rotation after RoPE
+  float had_scale;          // fl32(1 / fl32(sqrt(D)))
 };
 
 struct AppendArgs {

@@ -47,7 +47,8 @@ class DecodeParams(ctypes.Structure):
 class NormRopeDesc(ctypes.Structure):
     _fields_ = [("norm_weight", ctypes.c_void_p), ("norm_eps", ctypes.c_float), ("rotary_dim", ctypes.c_int32),
                 ("rotary_offset", ctypes.c_int32), ("rotary_interleaved", ctypes.c_int32),
-                ("cos_cache", ctypes.c_void_p), ("sin_cache", ctypes.c_void_p), ("max_position", ctypes.c_int32)]
+                ("cos_cache", ctypes.c_void_p), ("sin_cache", ctypes.c_void_p), ("max_position", ctypes.c_int32),
+                ("hadamard", ctypes.c_int32)]
 
 
 # every exported entry point of include/kvq.h with its ctypes signature
@@ -168,13 +169,14 @@ class NormRope:
     interleaved: bool = False
     cos: Optional[torch.Tensor] = None
     sin: Optional[torch.Tensor] = None
+    hadamard: bool = False
 
     def desc(self) -> NormRopeDesc:
         return NormRopeDesc(None if self.norm_weight is None else self.norm_weight.data_ptr(), float(self.eps),
                             int(self.rotary_dim), int(self.rotary_offset), 1 if self.interleaved else 0,
                             None if self.cos is None else self.cos.data_ptr(),
                             None if self.sin is None else self.sin.data_ptr(),
-                            0 if self.cos is None else int(self.cos.shape[0]))
+                            0 if self.cos is None else int(self.cos.shape[0]), 1 if self.hadamard else 0)
 
 
 def kvq_norm_rope_apply(pro: NormRope, x: torch.Tensor, y: torch.Tensor, positions: Optional[torch.Tensor],

@@ -174,6 +174,14 @@ typedef struct {
   const float* cos_cache;     /* fp32 [max_position, rotary_dim/2] (device) */
   const float* sin_cache;     /* fp32 [max_position, rotary_dim/2] (device) */
   int32_t max_position;       /* rows of the tables (> 0 when rotary_dim > 0) */
+  int32_t hadamard;           /* 1: then rotate the row by the orthonormal Walsh-Hadamard
+                                 matrix (Sylvester order, entry (i, j) =
+                                 (-1)^popcount(i & j) / sqrt(head_dim)): butterflies of
+                                 span 1, 2, 4, ... in fp32, then times
+                                 fl32(1 / fl32(sqrt(head_dim))).  Apply it to Q and K alike:
+                                 dot products are unchanged while an outlier channel is
+                                 spread over the row before quantization (the rotation
+                                 PR #32515 names as the follow-up for the int4 cache) */
 } kvq_norm_rope;
 
 /* kvq_norm_rope_apply -- the prologue on x [n_tokens, num_heads, head_dim]

@@ -133,7 +133,7 @@ def test_binding_refuses_to_run_without_the_library(tmp_path):
 
 def good_norm_rope(kvq, **kw):
     d = dict(norm_weight=FAKE, norm_eps=1e-6, rotary_dim=64, rotary_offset=0, rotary_interleaved=0,
-             cos_cache=FAKE + 4096, sin_cache=FAKE + 8192, max_position=128)
+             cos_cache=FAKE + 4096, sin_cache=FAKE + 8192, max_position=128, hadamard=0)
     d.update(kw)
     return kvq.NormRopeDesc(**d)
 
@@ -141,7 +141,7 @@ def good_norm_rope(kvq, **kw):
 @pytest.mark.parametrize("bad", [
     dict(rotary_dim=-2), dict(rotary_dim=63), dict(rotary_offset=-1), dict(rotary_offset=96),
     dict(rotary_dim=130), dict(cos_cache=None), dict(sin_cache=None), dict(max_position=0),
-    dict(norm_weight=FAKE + 2), dict(cos_cache=FAKE + 2), dict(norm_eps=float("nan")),
+    dict(norm_weight=FAKE + 2), dict(cos_cache=FAKE + 2), dict(norm_eps=float("nan")), dict(hadamard=2),
 ])
 def test_norm_rope_rejects_bad_prologue(kvq, bad):
     """Invalid prologues are refused on the host, for the Q-side call and the

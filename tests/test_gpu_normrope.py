@@ -28,31 +28,32 @@ def bits(t):
     return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
 
 
-def prologue(D, *, norm, rd, off, inter, max_pos=4096, seed=0):
+def prologue(D, *, norm, rd, off, inter, max_pos=4096, seed=0, had=False):
     w = synth.norm_weight_bf16(D, "cpu", "gpu-normrope", seed) if norm else None
     cos, sin = synth.rope_tables(max_pos, rd) if rd else (None, None)
     dev = kvq.NormRope(norm_weight=None if w is None else w.cuda(), eps=1e-6, rotary_dim=rd, rotary_offset=off,
                        interleaved=inter,
                        cos=None if cos is None else torch.from_numpy(cos).cuda(),
-                       sin=None if sin is None else torch.from_numpy(sin).cuda())
+                       sin=None if sin is None else torch.from_numpy(sin).cuda(), hadamard=had)
     host = dict(norm_weight=None if w is None else bits(w), eps=1e-6, rotary_dim=rd, rotary_offset=off,
-                interleaved=inter, cos=cos, sin=sin)
+                interleaved=inter, cos=cos, sin=sin, hadamard=had)
     return dev, host
 
 
-CASES = [  # (D, norm, rotary_dim, rotary_offset, interleaved)
-    (64, True, 64, 0, False), (128, True, 128, 0, True), (256, True, 64, 192, False),
-    (128, False, 32, 40, False), (256, True, 0, 0, False), (64, False, 16, 48, True),
+CASES = [  # (D, norm, rotary_dim, rotary_offset, interleaved, hadamard)
+    (64, True, 64, 0, False, False), (128, True, 128, 0, True, False), (256, True, 64, 192, False, False),
+    (128, False, 32, 40, False, False), (256, True, 0, 0, False, False), (64, False, 16, 48, True, False),
+    (64, True, 64, 0, False, True), (128, True, 128, 0, False, True), (256, False, 0, 0, False, True),
 ]
 
 
-@pytest.mark.parametrize("D,norm,rd,off,inter", CASES)
-def test_norm_rope_apply_bit_exact(lib, orc, D, norm, rd, off, inter):
+@pytest.mark.parametrize("D,norm,rd,off,inter,had", CASES)
+def test_norm_rope_apply_bit_exact(lib, orc, D, norm, rd, off, inter, had):
     N, H = 37, 6  # a ragged token count
     x = synth.randn_bf16((N, H, D), "cpu", "gpu-normrope", "x", D) * 3
     pos = torch.randint(0, 4096, (N,), generator=synth.generator("cpu", "gpu-normrope", "pos", D))
     pos[0], pos[1] = 0, 4095
-    dev, host = prologue(D, norm=norm, rd=rd, off=off, inter=inter)
+    dev, host = prologue(D, norm=norm, rd=rd, off=off, inter=inter, had=had)
     y = torch.zeros_like(x).cuda()
     kvq.kvq_norm_rope_apply(dev, x.cuda(), y, pos.cuda() if rd else None)
     assert kvq.kvq_get_device_error() == 0
@@ -84,9 +85,10 @@ def test_norm_rope_apply_flags_positions_outside_the_tables(lib, orc):
 
 @pytest.mark.parametrize("dt", list(DT))
 @pytest.mark.parametrize("km,vm", [("row", "row"), ("channel", "tensor")])
-@pytest.mark.parametrize("D,norm,rd,off,inter", [(128, True, 128, 0, False), (256, True, 64, 0, True),
-                                                 (64, False, 32, 16, False)])
-def test_append_norm_rope_codes_bit_exact(lib, orc, dt, km, vm, D, norm, rd, off, inter):
+@pytest.mark.parametrize("D,norm,rd,off,inter,had", [(128, True, 128, 0, False, False), (256, True, 64, 0, True, False),
+                                                     (64, False, 32, 16, False, False), (128, True, 128, 0, False, True),
+                                                     (256, True, 256, 0, False, True)])
+def test_append_norm_rope_codes_bit_exact(lib, orc, dt, km, vm, D, norm, rd, off, inter, had):
     """The fused prologue + quantizer writes exactly the codes (and per-row
     scales) the oracle gets by normalizing and rotating K, rounding it to
     bf16 and quantizing that; V is quantized as given."""
@@ -99,7 +101,7 @@ def test_append_norm_rope_codes_bit_exact(lib, orc, dt, km, vm, D, norm, rd, off
     slots = torch.randperm(NB * bs, generator=g)[:N].to(torch.int64)
     slots[4] = -1
     pos = torch.randint(0, 4096, (N,), generator=g)
-    dev, host = prologue(D, norm=norm, rd=rd, off=off, inter=inter, seed=1)
+    dev, host = prologue(D, norm=norm, rd=rd, off=off, inter=inter, seed=1, had=had)
     kr, bad = orc.norm_rope(bits(k), positions=pos.numpy(), **host)  # the oracle's own K rows
     assert bad == 0
     qmax = orc.QMAX[dtype]
@@ -141,18 +143,19 @@ def test_append_norm_rope_skips_tokens_with_bad_positions(lib, orc):
     assert not (kc[0, :, 3] == 0x5A).all()
 
 
-def test_decode_over_prologue_rows_matches_oracle_attention(lib, orc):
-    """q through kvq_norm_rope_apply, K through kvq_append_norm_rope, then
-    decode + combine: within 2e-3 relative L2 of oracle attention over the
-    oracle's own normalized rows."""
+@pytest.mark.parametrize("dt,had", [("int8", False), ("int4", True), ("int4", False)])
+def test_decode_over_prologue_rows_matches_oracle_attention(lib, orc, dt, had):
+    """q through kvq_norm_rope_apply, K through kvq_append_norm_rope (with and
+    without the Hadamard rotation), then decode + combine: within 2e-3
+    relative L2 of oracle attention over the oracle's own prologue rows."""
     B, Hq, Hkv, D, T, bs = 3, 8, 2, 128, 2, 16
     L = np.array([40, 97, 2], np.int32)
     mb = 8
     NB = B * mb
     table = (np.arange(B)[:, None] * mb + np.arange(mb)[None, :]).astype(np.int32)
-    dev, host = prologue(D, norm=True, rd=128, off=0, inter=False, max_pos=256, seed=2)
-    cache = kvq.QuantizedPagedCache(kvq.INT8, kvq.PER_ROW, kvq.PER_ROW, NB, bs, Hkv, D)
-    oc = orc.OracleCache(kvq.INT8, kvq.PER_ROW, kvq.PER_ROW, NB, bs, Hkv, D)
+    dev, host = prologue(D, norm=True, rd=128, off=0, inter=False, max_pos=256, seed=2, had=had)
+    cache = kvq.QuantizedPagedCache(DT[dt], kvq.PER_ROW, kvq.PER_ROW, NB, bs, Hkv, D)
+    oc = orc.OracleCache(DT[dt], kvq.PER_ROW, kvq.PER_ROW, NB, bs, Hkv, D)
     for b in range(B):
         n = int(L[b])
         k = synth.randn_bf16((n, Hkv, D), "cpu", "gpu-normrope-dec", "k", b)
