@@ -369,6 +369,99 @@ kvq_status append_common(const kvq_cache* cache, const kvq_norm_rope* k_prologue
   return from_cuda(launch_append(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+// kvq_decode with the block-table row of sequence b at b / bt_div and, when
+// early_reads is 0, seq_lens read only after the wait on the preceding grid
+// (kvq_prefill's virtual sequences, whose lengths that grid writes).
+kvq_status decode_impl(const kvq_cache* cache, const kvq_decode_params* params, const void* q,
+                       const int32_t* block_table, const int32_t* seq_lens, int bt_div, int early_reads,
+                       void* workspace, size_t workspace_bytes, kvq_stream_t stream) {
+  if (kvq_status s = check_cache(cache)) return s;
+  if (kvq_status s = check_params(cache, params)) return s;
+  if (params->batch == 0) return KVQ_OK;
+  if (!q || !block_table || !seq_lens || !workspace) return KVQ_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(block_table, 4) || !aligned(seq_lens, 4) || !aligned(workspace, 256))
+    return KVQ_ERR_INVALID_ARG;
+  DeviceInfo* dev;
+  if (kvq_status s = current_device(&dev)) return s;
+  Plan P;
+  if (kvq_status s = make_plan(cache, params, *dev, &P)) return s;
+  if (workspace_bytes < P.ws_total) return KVQ_ERR_WORKSPACE_TOO_SMALL;
+
+  alignas(64) CUtensorMap tk, tv;
+  if (kvq_status s = encode_codes_map(cache, cache->k_codes, &tk)) return s;
+  if (kvq_status s = encode_codes_map(cache, cache->v_codes, &tv)) return s;
+
+  DecodeArgs a{};
+  a.q = static_cast<const uint16_t*>(q);
+  a.block_table = block_table;
+  a.seq_lens = seq_lens;
+  a.k_scale = cache->k_scale;
+  a.v_scale = cache->v_scale;
+  a.k_mode = cache->k_mode;
+  a.v_mode = cache->v_mode;
+  a.num_blocks = cache->num_blocks;
+  a.block_size = cache->block_size;
+  a.log2_bs = ilog2(cache->block_size);
+  a.num_kv_heads = cache->num_kv_heads;
+  a.batch = params->batch;
+  a.num_q_heads = params->num_q_heads;
+  a.q_tokens = params->q_tokens;
+  a.group = params->num_q_heads / cache->num_kv_heads;
+  a.rows = P.rows;
+  a.max_blocks_per_seq = params->max_blocks_per_seq;
+  a.max_seq_len = params->max_seq_len;
+  a.sm_scale = params->sm_scale > 0.0f ? params->sm_scale : 1.0f / std::sqrt((float)cache->head_dim);
+  a.softcap = params->softcap;
+  a.window = params->window;
+  a.row_groups = P.row_groups;
+  a.key_warps = P.key_warps;
+  a.stages = P.stages;
+  a.units_max = P.units_max;
+  // a piece change (query prologue, merge and partial write, refill of the
+  // role pipeline) is charged as a few tiles when the split is planned
+  a.piece_cost = P.tc_nr ? kTcPieceCost : kPieceCost;
+  a.bt_div = bt_div;
+  a.early_reads = early_reads;
+  char* ws = static_cast<char*>(workspace);
+  a.plan = reinterpret_cast<int*>(ws);
+  a.part_lse = reinterpret_cast<float*>(ws + P.ws_plan);
+  a.part_o = reinterpret_cast<float*>(ws + P.ws_plan + P.ws_lse);
+  a.err = dev->err;
+
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (P.tc_nr) {
+    switch (cache->dtype) {
+      case KVQ_INT8: e = launch_decode_tc_int8(cache->head_dim, P.tc_nr, tk, tv, a, P.grid, P.smem, st); break;
+      case KVQ_FP8_E4M3: e = launch_decode_tc_fp8(cache->head_dim, P.tc_nr, tk, tv, a, P.grid, P.smem, st); break;
+      default: e = launch_decode_tc_int4(cache->head_dim, P.tc_nr, tk, tv, a, P.grid, P.smem, st); break;
+    }
+  } else {
+    switch (cache->dtype) {
+      case KVQ_INT8: e = launch_decode_int8(cache->head_dim, P.nt, tk, tv, a, P.grid, P.threads, P.smem, st); break;
+      case KVQ_FP8_E4M3: e = launch_decode_fp8(cache->head_dim, P.nt, tk, tv, a, P.grid, P.threads, P.smem, st); break;
+      default: e = launch_decode_int4(cache->head_dim, P.nt, tk, tv, a, P.grid, P.threads, P.smem, st); break;
+    }
+  }
+  return from_cuda(e);
+}
+
+// A prefill chunk of C tokens per sequence as virtual decode sequences of T
+// tokens (T the largest of 8, 4, 2, 1 dividing C), n = C / T per sequence.
+kvq_status prefill_shape(const kvq_decode_params* p, kvq_decode_params* v, int* n) {
+  if (!p || p->q_tokens < 1 || p->batch < 0) return KVQ_ERR_INVALID_ARG;
+  const int C = p->q_tokens;
+  int T = 8;
+  while (C % T) T >>= 1;
+  const long long vb = (long long)p->batch * (C / T);
+  if (vb > kMaxBatch) return KVQ_ERR_UNSUPPORTED;
+  *v = *p;
+  v->batch = (int32_t)vb;
+  v->q_tokens = T;
+  *n = C / T;
+  return KVQ_OK;
+}
+
 }  // namespace
 }  // namespace kvq
 
@@ -437,73 +530,7 @@ KVQ_API kvq_status kvq_decode_workspace_size(const kvq_cache* cache, const kvq_d
 KVQ_API kvq_status kvq_decode(const kvq_cache* cache, const kvq_decode_params* params, const void* q,
                               const int32_t* block_table, const int32_t* seq_lens, void* workspace,
                               size_t workspace_bytes, kvq_stream_t stream) {
-  if (kvq_status s = check_cache(cache)) return s;
-  if (kvq_status s = check_params(cache, params)) return s;
-  if (params->batch == 0) return KVQ_OK;
-  if (!q || !block_table || !seq_lens || !workspace) return KVQ_ERR_INVALID_ARG;
-  if (!aligned(q, 16) || !aligned(block_table, 4) || !aligned(seq_lens, 4) || !aligned(workspace, 256))
-    return KVQ_ERR_INVALID_ARG;
-  DeviceInfo* dev;
-  if (kvq_status s = current_device(&dev)) return s;
-  Plan P;
-  if (kvq_status s = make_plan(cache, params, *dev, &P)) return s;
-  if (workspace_bytes < P.ws_total) return KVQ_ERR_WORKSPACE_TOO_SMALL;
-
-  alignas(64) CUtensorMap tk, tv;
-  if (kvq_status s = encode_codes_map(cache, cache->k_codes, &tk)) return s;
-  if (kvq_status s = encode_codes_map(cache, cache->v_codes, &tv)) return s;
-
-  DecodeArgs a{};
-  a.q = static_cast<const uint16_t*>(q);
-  a.block_table = block_table;
-  a.seq_lens = seq_lens;
-  a.k_scale = cache->k_scale;
-  a.v_scale = cache->v_scale;
-  a.k_mode = cache->k_mode;
-  a.v_mode = cache->v_mode;
-  a.num_blocks = cache->num_blocks;
-  a.block_size = cache->block_size;
-  a.log2_bs = ilog2(cache->block_size);
-  a.num_kv_heads = cache->num_kv_heads;
-  a.batch = params->batch;
-  a.num_q_heads = params->num_q_heads;
-  a.q_tokens = params->q_tokens;
-  a.group = params->num_q_heads / cache->num_kv_heads;
-  a.rows = P.rows;
-  a.max_blocks_per_seq = params->max_blocks_per_seq;
-  a.max_seq_len = params->max_seq_len;
-  a.sm_scale = params->sm_scale > 0.0f ? params->sm_scale : 1.0f / std::sqrt((float)cache->head_dim);
-  a.softcap = params->softcap;
-  a.window = params->window;
-  a.row_groups = P.row_groups;
-  a.key_warps = P.key_warps;
-  a.stages = P.stages;
-  a.units_max = P.units_max;
-  // a piece change (query prologue, merge and partial write, refill of the
-  // role pipeline) is charged as a few tiles when the split is planned
-  a.piece_cost = P.tc_nr ? kTcPieceCost : kPieceCost;
-  char* ws = static_cast<char*>(workspace);
-  a.plan = reinterpret_cast<int*>(ws);
-  a.part_lse = reinterpret_cast<float*>(ws + P.ws_plan);
-  a.part_o = reinterpret_cast<float*>(ws + P.ws_plan + P.ws_lse);
-  a.err = dev->err;
-
-  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e;
-  if (P.tc_nr) {
-    switch (cache->dtype) {
-      case KVQ_INT8: e = launch_decode_tc_int8(cache->head_dim, P.tc_nr, tk, tv, a, P.grid, P.smem, st); break;
-      case KVQ_FP8_E4M3: e = launch_decode_tc_fp8(cache->head_dim, P.tc_nr, tk, tv, a, P.grid, P.smem, st); break;
-      default: e = launch_decode_tc_int4(cache->head_dim, P.tc_nr, tk, tv, a, P.grid, P.smem, st); break;
-    }
-  } else {
-    switch (cache->dtype) {
-      case KVQ_INT8: e = launch_decode_int8(cache->head_dim, P.nt, tk, tv, a, P.grid, P.threads, P.smem, st); break;
-      case KVQ_FP8_E4M3: e = launch_decode_fp8(cache->head_dim, P.nt, tk, tv, a, P.grid, P.threads, P.smem, st); break;
-      default: e = launch_decode_int4(cache->head_dim, P.nt, tk, tv, a, P.grid, P.threads, P.smem, st); break;
-    }
-  }
-  return from_cuda(e);
+  return decode_impl(cache, params, q, block_table, seq_lens, 1, 1, workspace, workspace_bytes, stream);
 }
 
 KVQ_API kvq_status kvq_combine(const kvq_cache* cache, const kvq_decode_params* params, const void* workspace,
@@ -539,6 +566,48 @@ KVQ_API kvq_status kvq_combine(const kvq_cache* cache, const kvq_decode_params* 
   a.rows = P.rows;
   a.head_dim = cache->head_dim;
   return from_cuda(launch_combine(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+KVQ_API kvq_status kvq_prefill_workspace_size(const kvq_cache* cache, const kvq_decode_params* params,
+                                              size_t* workspace_bytes) {
+  if (!workspace_bytes) return KVQ_ERR_INVALID_ARG;
+  kvq_decode_params v;
+  int n = 0;
+  if (kvq_status s = prefill_shape(params, &v, &n)) return s;
+  size_t ws = 0;
+  if (kvq_status s = kvq_decode_workspace_size(cache, &v, &ws)) return s;
+  *workspace_bytes = align256((size_t)v.batch * 4) + ws;
+  return KVQ_OK;
+}
+
+KVQ_API kvq_status kvq_prefill(const kvq_cache* cache, const kvq_decode_params* params, const void* q,
+                               const int32_t* block_table, const int32_t* seq_lens, const float* head_sink,
+                               void* out, float* lse_out, void* workspace, size_t workspace_bytes,
+                               kvq_stream_t stream) {
+  if (kvq_status s = check_cache(cache)) return s;
+  kvq_decode_params v;
+  int n = 0;
+  if (kvq_status s = prefill_shape(params, &v, &n)) return s;
+  if (kvq_status s = check_params(cache, &v)) return s;
+  if (params->batch == 0) return KVQ_OK;
+  if (!q || !block_table || !seq_lens || !workspace || !out) return KVQ_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(block_table, 4) || !aligned(seq_lens, 4) || !aligned(workspace, 256) ||
+      !aligned(out, 16) || (lse_out && !aligned(lse_out, 4)) || (head_sink && !aligned(head_sink, 4)))
+    return KVQ_ERR_INVALID_ARG;
+  size_t need = 0;
+  if (kvq_status s = kvq_prefill_workspace_size(cache, params, &need)) return s;
+  if (workspace_bytes < need) return KVQ_ERR_WORKSPACE_TOO_SMALL;
+  // the virtual sequences' lengths head the workspace; the decode reads them
+  // only after it has waited for the kernel that writes them
+  const size_t head = align256((size_t)v.batch * 4);
+  int32_t* lens = static_cast<int32_t*>(workspace);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaError_t e = launch_prefill_lens(seq_lens, lens, params->batch, n, params->q_tokens, v.q_tokens, st))
+    return from_cuda(e);
+  char* ws = static_cast<char*>(workspace) + head;
+  if (kvq_status s = decode_impl(cache, &v, q, block_table, lens, n, 0, ws, workspace_bytes - head, stream))
+    return s;
+  return kvq_combine(cache, &v, ws, workspace_bytes - head, head_sink, out, lse_out, stream);
 }
 
 KVQ_API kvq_status kvq_get_device_error(uint32_t* flags, int32_t clear, kvq_stream_t stream) {

@@ -144,7 +144,25 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const Combi
   if (a.lse_out && lane == 0) a.lse_out[row_id] = lse_nat;
 }
 
+// Sequence lengths of a prefill chunk's virtual sequences (one thread each).
+__global__ void __launch_bounds__(256) prefill_lens_kernel(const int32_t* seq_lens, int32_t* out, int total, int n,
+                                                           int C, int T) {
+  ptx::griddep_wait();
+  ptx::griddep_launch_dependents();
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= total) return;
+  const int b = i / n, j = i - b * n;
+  out[i] = max(0, seq_lens[b] - C + T * (j + 1));
+}
+
 }  // namespace
+
+cudaError_t launch_prefill_lens(const int32_t* seq_lens, int32_t* out, int batch, int n, int C, int T,
+                                cudaStream_t stream) {
+  const int total = batch * n;
+  return launch_pdl(prefill_lens_kernel, (unsigned)((total + 255) / 256), 256, 0, stream, seq_lens, out, total,
+                    n, C, T);
+}
 
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t stream) {
   const unsigned blocks = (unsigned)((long long)a.batch * a.q_tokens * a.num_q_heads);

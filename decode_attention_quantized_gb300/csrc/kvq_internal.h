@@ -69,6 +69,8 @@ struct DecodeArgs {
   int row_groups, key_warps, stages;
   int units_max;    // partial slots (grid + batch * Hkv)
   int piece_cost;   // tiles' worth of time a CTA spends on each piece change (split planning)
+  int bt_div;       // block-table row of sequence b is b / bt_div (prefill: virtual sequences)
+  int early_reads;  // 1: read seq_lens, block table and q before the wait on the preceding grid
   int* plan;        // workspace: [0] cost per CTA, [1] total tiles, [2] piece cost, [3] slots, then tile prefix[B+1]
   float* part_lse;  // [units_max, rows]   base-2 log-sum-exp of each piece
   float* part_o;    // [units_max, rows, D] normalized piece output
@@ -140,6 +142,10 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t stream);
 cudaError_t launch_norm_rope(const NormRopeArgs& a, cudaStream_t stream);
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t stream);
+// out[b * n + j] = max(0, seq_lens[b] - C + T (j + 1)) for the n = C / T groups
+// of a prefill chunk (virtual sequences of T tokens).
+cudaError_t launch_prefill_lens(const int32_t* seq_lens, int32_t* out, int batch, int n, int C, int T,
+                                cudaStream_t stream);
 cudaError_t launch_decode_int8(int head_dim, int nt, const CUtensorMap& tk, const CUtensorMap& tv,
                                const DecodeArgs& a, int grid, int threads, size_t smem, cudaStream_t stream);
 cudaError_t launch_decode_fp8(int head_dim, int nt, const CUtensorMap& tk, const CUtensorMap& tv,

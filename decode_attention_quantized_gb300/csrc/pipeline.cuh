@@ -104,6 +104,7 @@ __device__ Slice<KT> build_slice(const DecodeArgs& a, int* pl_pre, int* pl_misc)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int B = a.batch, Hkv = a.num_kv_heads;
   const int cap = a.max_blocks_per_seq * a.block_size;
+  if (!a.early_reads) ptx::griddep_wait();  // seq_lens may come from the preceding grid
   Slice<KT> sp;
   sp.pre = pl_pre;
   sp.lim = (a.max_seq_len > 0 && a.max_seq_len < cap) ? a.max_seq_len : cap;
@@ -219,7 +220,7 @@ __device__ void produce(const DecodeArgs& a, const Slice<Gm::KEYS>& sp, const CU
   for (int gt = sp.t_begin, next; gt < sp.t_end; gt = next) {
     int b, h, k0, k1, L, slot;
     sp.piece(a, gt, b, h, k0, k1, L, slot, next);
-    const int32_t* bt = a.block_table + (size_t)b * a.max_blocks_per_seq;
+    const int32_t* bt = a.block_table + (size_t)(b / a.bt_div) * a.max_blocks_per_seq;
     const int p_last = (k1 - 1) >> a.log2_bs;
     int base = k0 >> a.log2_bs;
     int my_id = base + lane <= p_last ? bt[base + lane] : -1;

@@ -63,6 +63,10 @@ SIGNATURES = {
                            _VP]),
     "kvq_get_device_error": (_I32, [ctypes.POINTER(ctypes.c_uint32), _I32, _VP]),
     "kvq_norm_rope_apply": (_I32, [ctypes.POINTER(NormRopeDesc), _VP, _VP, _VP, _I32, _I32, _I32, _VP]),
+    "kvq_prefill_workspace_size": (_I32, [ctypes.POINTER(CacheDesc), ctypes.POINTER(DecodeParams),
+                                          ctypes.POINTER(_SZ)]),
+    "kvq_prefill": (_I32, [ctypes.POINTER(CacheDesc), ctypes.POINTER(DecodeParams), _VP, _VP, _VP, _VP, _VP, _VP,
+                           _VP, _SZ, _VP]),
     "kvq_append_norm_rope": (_I32, [ctypes.POINTER(CacheDesc), ctypes.POINTER(NormRopeDesc), _VP, _VP, _VP, _VP,
                                     _I32, _VP]),
     "kvq_attend_noalloc": (_I32, [ctypes.POINTER(CacheDesc), ctypes.POINTER(DecodeParams), _VP, _VP, _VP, _VP, _VP,
@@ -194,6 +198,25 @@ def kvq_append_norm_rope(cache: QuantizedPagedCache, pro: NormRope, k_new: torch
     _check("kvq_append_norm_rope", load().kvq_append_norm_rope(ctypes.byref(d), ctypes.byref(p), _ptr(k_new),
                                                                _ptr(v_new), _ptr(slot_mapping), _ptr(positions),
                                                                k_new.shape[0], _stream(stream)))
+
+
+def kvq_prefill_workspace_size(cache: QuantizedPagedCache, params: DecodeParams) -> int:
+    d = cache.desc()
+    n = ctypes.c_size_t(0)
+    _check("kvq_prefill_workspace_size", load().kvq_prefill_workspace_size(ctypes.byref(d), ctypes.byref(params),
+                                                                           ctypes.byref(n)))
+    return n.value
+
+
+def kvq_prefill(cache: QuantizedPagedCache, params: DecodeParams, q: torch.Tensor, block_table: torch.Tensor,
+                seq_lens: torch.Tensor, head_sink: Optional[torch.Tensor], out: torch.Tensor,
+                lse_out: Optional[torch.Tensor], workspace: torch.Tensor, stream=None):
+    """q, out bf16 [B, C, Hq, D] with C = params.q_tokens; lse_out fp32 [B, C, Hq] or None."""
+    d = cache.desc()
+    _check("kvq_prefill", load().kvq_prefill(ctypes.byref(d), ctypes.byref(params), _ptr(q), _ptr(block_table),
+                                             _ptr(seq_lens), _ptr(head_sink), _ptr(out), _ptr(lse_out),
+                                             _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                             _stream(stream)))
 
 
 def kvq_decode_workspace_size(cache: QuantizedPagedCache, params: DecodeParams) -> int:

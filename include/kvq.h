@@ -249,6 +249,27 @@ KVQ_API kvq_status kvq_combine(const kvq_cache* cache, const kvq_decode_params* 
                                const float* head_sink, void* out, float* lse_out,
                                kvq_stream_t stream);
 
+/* kvq_prefill -- attention of a chunk of C = params->q_tokens new query tokens
+ * per sequence over the quantized cache (chunked prefill / prompt attention:
+ * PR #29912 and PR #32515 testing name prefill and chunked prefill; the head
+ * sink applies as in decode).  The chunk's K/V rows are appended first
+ * (kvq_append); token c of sequence b sits at position seq_lens[b] - C + c
+ * and sees keys 0..that position (and the window, when set).  q, out bf16
+ * [B, C, Hq, D]; lse_out fp32 [B, C, Hq] or NULL; head_sink as in
+ * kvq_combine.  It runs as one decode pass and one combine over B * C / T
+ * virtual sequences of T tokens each (T the largest of 8, 4, 2, 1 that
+ * divides C; B * C / T <= 1024), sequence b's j-th group seeing the prefix
+ * seq_lens[b] - C + T (j + 1): each group re-reads its prefix, so a chunk
+ * costs about C / T decode steps of cache reads, shared through L2 where they
+ * coincide.  C >= 1 (no upper bound besides the virtual batch).  workspace:
+ * at least kvq_prefill_workspace_size bytes, 256-byte aligned. */
+KVQ_API kvq_status kvq_prefill_workspace_size(const kvq_cache* cache, const kvq_decode_params* params,
+                                              size_t* workspace_bytes);
+KVQ_API kvq_status kvq_prefill(const kvq_cache* cache, const kvq_decode_params* params, const void* q,
+                               const int32_t* block_table, const int32_t* seq_lens, const float* head_sink,
+                               void* out, float* lse_out, void* workspace, size_t workspace_bytes,
+                               kvq_stream_t stream);
+
 /* kvq_attend_noalloc -- kvq_decode then kvq_combine, with the split-partial
  * scratch in a library-owned 16 MiB device array instead of a caller
  * workspace.  The pages have no counterpart: this exists for callers that

@@ -171,3 +171,28 @@ def test_norm_rope_rejects_bad_shapes_and_pointers(kvq):
     assert lib.kvq_append_norm_rope(ctypes.byref(c), None, FAKE, FAKE, FAKE, FAKE, 4, None) == 1
     assert lib.kvq_append_norm_rope(ctypes.byref(c), ctypes.byref(p), FAKE, FAKE, FAKE, None, 4, None) == 1
     assert lib.kvq_append_norm_rope(ctypes.byref(c), ctypes.byref(p), FAKE, FAKE, FAKE, FAKE, 0, None) == 0
+
+
+def test_prefill_rejects_bad_arguments_on_the_host(kvq):
+    lib = kvq.load()
+    c = good_cache(kvq)
+    n = ctypes.c_size_t(0)
+    # a chunk of 0 tokens
+    p = good_params(kvq, q_tokens=0)
+    assert lib.kvq_prefill_workspace_size(ctypes.byref(c), ctypes.byref(p), ctypes.byref(n)) == 1
+    assert lib.kvq_prefill(ctypes.byref(c), ctypes.byref(p), FAKE, FAKE, FAKE, None, FAKE, None, FAKE, 1 << 30,
+                           None) == 1
+    # 200 sequences x 64 tokens = 1600 virtual sequences of 8: beyond the plan's 1024
+    p = good_params(kvq, batch=200, q_tokens=64)
+    assert lib.kvq_prefill_workspace_size(ctypes.byref(c), ctypes.byref(p), ctypes.byref(n)) == 2
+    # missing or misaligned pointers
+    p = good_params(kvq, q_tokens=12)
+    for args in [(None, FAKE, FAKE, None, FAKE), (FAKE, FAKE, None, None, FAKE), (FAKE, FAKE, FAKE, None, None),
+                 (FAKE + 8, FAKE, FAKE, None, FAKE), (FAKE, FAKE, FAKE, FAKE + 2, FAKE)]:
+        q, bt, sl, hs, out = args
+        assert lib.kvq_prefill(ctypes.byref(c), ctypes.byref(p), q, bt, sl, hs, out, None, FAKE, 1 << 30,
+                               None) == 1
+    # an empty batch is a no-op
+    p = good_params(kvq, batch=0, q_tokens=12)
+    assert lib.kvq_prefill(ctypes.byref(c), ctypes.byref(p), None, None, None, None, None, None, None, 0,
+                           None) == 0
