@@ -46,6 +46,7 @@ def parse():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-prologue", action="store_true", help="skip the QK-RMSNorm + RoPE prologue timing")
+    p.add_argument("--no-prefill", action="store_true", help="skip the chunked-prefill timing")
     return p.parse_args()
 
 
@@ -406,6 +407,60 @@ def measure_prologue(w, steps, warmup, peak):
             "prologue": f"RMSNorm (bf16 weight, eps 1e-6) + RoPE on all {D} channels (half split), fixed-order fp32"}
 
 
+def measure_prefill(w, steps, warmup, peak, chunk=64):
+    """kvq_prefill of a chunk of `chunk` query tokens per sequence at the end of
+    the workload's sequences (the chunk's rows already in the cache), as a
+    graph of `steps` calls.  Reported against the bytes a single pass over
+    the cache would read: kvq_prefill re-reads each prefix once per group of
+    up to 8 chunk tokens, so the fraction shows that cost."""
+    import torch
+    from decode_attention_quantized_gb300 import kvq, synth
+    from decode_attention_quantized_gb300.workload import GpuWorkload
+
+    dev = torch.cuda.current_device()
+    gw = GpuWorkload(w, device=f"cuda:{dev}", gen_device="cuda")
+    gw.fill_history()
+    k_new, v_new, slots = gw.new_tokens()
+    kvq.kvq_append(gw.cache, k_new, v_new, slots)
+    C = chunk
+    params = kvq.make_params(w.batch, w.num_q_heads, C, w.max_blocks, max_seq_len=gw.max_seq_len,
+                             softcap=w.softcap)
+    q = synth.randn_bf16((w.batch, C, w.num_q_heads, w.head_dim), f"cuda:{dev}", "bench", "prefill-q")
+    out = torch.empty_like(q)
+    lse = torch.empty((w.batch, C, w.num_q_heads), dtype=torch.float32, device=f"cuda:{dev}")
+    ws = torch.empty(kvq.kvq_prefill_workspace_size(gw.cache, params) // 4 + 64, dtype=torch.int32,
+                     device=f"cuda:{dev}")
+
+    def call():
+        kvq.kvq_prefill(gw.cache, params, q, gw.block_table, gw.seq_lens, gw.head_sink, out, lse, ws)
+
+    for _ in range(max(3, warmup)):
+        call()
+    torch.cuda.synchronize()
+    gr = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gr):
+        for _ in range(steps):
+            call()
+    gr.replay()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record()
+    gr.replay()
+    t1.record()
+    torch.cuda.synchronize()
+    assert kvq.kvq_get_device_error() == 0, "device error flags set in the prefill timing"
+    ms = t0.elapsed_time(t1) / steps
+    one_pass = synth.decode_bytes(w)
+    del gw, q, out, lse, ws
+    torch.cuda.empty_cache()
+    return {"chunk_tokens": C, "us_per_chunk": round(1e3 * ms, 2),
+            "tokens_per_s": round(w.batch * C / (ms * 1e-3), 1),
+            "single_pass_gbs": round(one_pass / (ms * 1e-3) / 1e9, 1),
+            "single_pass_frac_of_hbm": round(one_pass / (ms * 1e-3) / 1e9 / peak, 3),
+            "groups_per_sequence": C // max(t for t in (8, 4, 2, 1) if C % t == 0)}
+
+
 def traffic_from_profiles(kernel_tag: str):
     """DRAM bytes per launch of the decode kernel from the committed ncu
     summary, if it was taken on the current kernel source."""
@@ -525,6 +580,8 @@ def run_ours(args):
                        "h2d_bytes_per_step": e["h2d"], "d2h_bytes_per_step": e["d2h"]}
     if rank == 0 and world == 1 and not args.no_prologue:
         line["prologue"] = measure_prologue(w, args.steps, args.warmup, peak)
+    if rank == 0 and world == 1 and not args.no_prefill:
+        line["prefill"] = measure_prefill(w, max(3, args.steps // 3), args.warmup, peak)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, windows[0], budget_s=12.0)
     if rank == 0:
