@@ -197,14 +197,21 @@ class OracleCache:
     """Host copy of a quantized paged cache with the oracle's append/attend."""
 
     def __init__(self, dtype, k_mode, v_mode, num_blocks, block_size, num_kv_heads, head_dim,
-                 k_static=None, v_static=None):
+                 k_static=None, v_static=None, latent=False, v_head_size=0):
+        """latent: the absorbed-MLA layout of onnxruntime PR #29912 (kv_cache_layout
+        LATENT, v_head_size): one cache, V read as the leading v_head_size
+        channels of the same row that supplies K, with K's scales."""
+        self.latent = bool(latent)
+        self.v_head_size = (v_head_size or head_dim) if latent else head_dim
+        if latent:
+            v_mode, v_static = k_mode, k_static
         self.dtype, self.k_mode, self.v_mode = dtype, k_mode, v_mode
         self.num_blocks, self.block_size = num_blocks, block_size
         self.num_kv_heads, self.head_dim = num_kv_heads, head_dim
         Dp = row_bytes(dtype, head_dim)
         shape = (num_blocks, num_kv_heads, block_size, Dp)
         self.k_codes = np.zeros(shape, dtype=np.uint8)
-        self.v_codes = np.zeros(shape, dtype=np.uint8)
+        self.v_codes = self.k_codes if latent else np.zeros(shape, dtype=np.uint8)
 
         def scale_arr(mode, static):
             if mode == PER_ROW:
@@ -214,7 +221,7 @@ class OracleCache:
             return np.ascontiguousarray(np.asarray(static, dtype=np.float32).reshape(num_kv_heads, head_dim))
 
         self.k_scale = scale_arr(k_mode, k_static)
-        self.v_scale = scale_arr(v_mode, v_static)
+        self.v_scale = self.k_scale if latent else scale_arr(v_mode, v_static)
 
     def _struct(self):
         return _Cache(self.dtype, self.k_mode, self.v_mode, self.num_blocks, self.block_size,
@@ -224,7 +231,8 @@ class OracleCache:
     def append(self, k_new_bf16: np.ndarray, v_new_bf16: np.ndarray, slot_mapping: np.ndarray) -> int:
         """k_new/v_new uint16 [N, Hkv, D] (bf16 bits); slot_mapping int64 [N]. Returns #bad slots."""
         k = np.ascontiguousarray(k_new_bf16, dtype=np.uint16)
-        v = np.ascontiguousarray(v_new_bf16, dtype=np.uint16)
+        # latent: the V side shares the K arrays and rows (writing K twice, identically)
+        v = k if self.latent else np.ascontiguousarray(v_new_bf16, dtype=np.uint16)
         sm = np.ascontiguousarray(slot_mapping, dtype=np.int64)
         st = self._struct()
         return lib().orc_append(ctypes.byref(st), _ptr(k), _ptr(v), _ptr(sm), int(sm.size))
@@ -266,6 +274,8 @@ class OracleCache:
                               _ptr(r), nr, _ptr(out), _ptr(lse), int(nth))
         if rc != 0:
             raise ValueError(f"oracle attend rejected its inputs (code {rc})")
+        if self.latent:  # V is the leading v_head_size channels of each row
+            out = np.ascontiguousarray(out[..., :self.v_head_size])
         return out, lse
 
 

@@ -387,3 +387,25 @@ def test_quantization_error_statistics(orc):
     assert 2.5e-3 < errs[1] < 4e-2, errs
     assert 4.5e-2 < errs[3] < 0.7, errs
     assert errs[3] > 5 * errs[1]
+
+
+def test_latent_layout_equals_brute_force_with_v_from_k(orc):
+    """Absorbed-MLA layout (onnxruntime PR #29912, kv_cache_layout LATENT,
+    v_head_size): one cache, V = the leading v_head_size channels of the
+    dequantized K rows.  Against the NumPy brute force fed K as V (attention
+    is linear in V, so its leading channels are the latent output)."""
+    D, Dv, Hkv, G, T, bs = 64, 48, 2, 2, 2, 16
+    L = 37
+    rng = np.random.default_rng(3)
+    k = rng.standard_normal((L, Hkv, D)).astype(np.float32)
+    kb = (k.view(np.uint32) >> 16).astype(np.uint16)
+    oc = orc.OracleCache(orc.INT8, orc.PER_ROW, orc.PER_ROW, 4, bs, Hkv, D, latent=True, v_head_size=Dv)
+    assert oc.append(kb, None, np.arange(L, dtype=np.int64)) == 0
+    q = (rng.standard_normal((1, T, Hkv * G, D)).astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    table = np.arange(4, dtype=np.int32)[None, :]
+    out, lse = oc.attend(q, table, np.array([L], np.int32), q_tokens=T)
+    assert out.shape == (1, T, Hkv * G, Dv)
+    kd = np.stack([oc.dequant_seq(table[0], h, L)[0] for h in range(Hkv)], axis=1)  # [L, Hkv, D]
+    ref, ref_lse = orc.brute_attention(orc.bf16_bits_to_f64(q[0]), kd, kd, L)
+    assert np.allclose(out[0], ref[..., :Dv], rtol=1e-12, atol=1e-12)
+    assert np.allclose(lse[0], ref_lse, rtol=1e-12, atol=1e-12)
