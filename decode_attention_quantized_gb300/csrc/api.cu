@@ -81,6 +81,28 @@ kvq_status check_cache(const kvq_cache* c) {
   return KVQ_OK;
 }
 
+// The effective descriptor: a LATENT cache reads V from the K codes and
+// scales (the leading v_head_size channels are kept by the combine);
+// v_head_size is filled in for both layouts.  Then the usual checks.
+kvq_status resolve_cache(const kvq_cache* c, kvq_cache* eff) {
+  if (!c) return KVQ_ERR_INVALID_ARG;
+  *eff = *c;
+  if (c->layout == KVQ_LAYOUT_LATENT) {
+    eff->v_codes = c->k_codes;
+    eff->v_scale = c->k_scale;
+    eff->v_mode = c->k_mode;
+    const int dv = c->v_head_size == 0 ? c->head_dim : c->v_head_size;
+    if (dv < 8 || dv > c->head_dim || dv % 8) return KVQ_ERR_INVALID_ARG;
+    eff->v_head_size = dv;
+  } else if (c->layout == KVQ_LAYOUT_SEPARATE) {
+    if (c->v_head_size != 0 && c->v_head_size != c->head_dim) return KVQ_ERR_INVALID_ARG;
+    eff->v_head_size = c->head_dim;
+  } else {
+    return KVQ_ERR_INVALID_ARG;
+  }
+  return check_cache(eff);
+}
+
 kvq_status check_params(const kvq_cache* c, const kvq_decode_params* p) {
   if (!p) return KVQ_ERR_INVALID_ARG;
   if (p->batch < 0 || p->num_q_heads <= 0 || p->q_tokens <= 0 || p->max_blocks_per_seq <= 0 ||
@@ -335,14 +357,18 @@ kvq_status check_norm_rope(const kvq_norm_rope* p, int head_dim, const int64_t* 
 kvq_status append_common(const kvq_cache* cache, const kvq_norm_rope* k_prologue, const void* k_new,
                          const void* v_new, const int64_t* slot_mapping, const int64_t* positions,
                          int32_t n_tokens, kvq_stream_t stream) {
-  if (kvq_status s = check_cache(cache)) return s;
+  kvq_cache eff_;
+  if (kvq_status s = resolve_cache(cache, &eff_)) return s;
+  cache = &eff_;
   if (n_tokens < 0) return KVQ_ERR_INVALID_ARG;
   NormRope pro{};
   if (k_prologue)
     if (kvq_status s = check_norm_rope(k_prologue, cache->head_dim, positions, &pro)) return s;
   if (n_tokens == 0) return KVQ_OK;
-  if (!k_new || !v_new || !slot_mapping) return KVQ_ERR_INVALID_ARG;
-  if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(slot_mapping, 8)) return KVQ_ERR_INVALID_ARG;
+  const bool latent = cache->layout == KVQ_LAYOUT_LATENT;  // V is the K row: v_new unused
+  if (!k_new || (!v_new && !latent) || !slot_mapping) return KVQ_ERR_INVALID_ARG;
+  if (!aligned(k_new, 16) || (v_new && !aligned(v_new, 16)) || !aligned(slot_mapping, 8))
+    return KVQ_ERR_INVALID_ARG;
   if ((long long)n_tokens * cache->num_kv_heads * 2 > (1LL << 31) - 1) return KVQ_ERR_INVALID_ARG;
   DeviceInfo* dev;
   if (kvq_status s = current_device(&dev)) return s;
@@ -365,6 +391,7 @@ kvq_status append_common(const kvq_cache* cache, const kvq_norm_rope* k_prologue
   a.v_mode = cache->v_mode;
   a.err = dev->err;
   a.k_prologue = k_prologue ? 1 : 0;
+  a.latent = latent ? 1 : 0;
   a.pro = pro;
   return from_cuda(launch_append(a, reinterpret_cast<cudaStream_t>(stream)));
 }
@@ -375,7 +402,9 @@ kvq_status append_common(const kvq_cache* cache, const kvq_norm_rope* k_prologue
 kvq_status decode_impl(const kvq_cache* cache, const kvq_decode_params* params, const void* q,
                        const int32_t* block_table, const int32_t* seq_lens, int bt_div, int early_reads,
                        void* workspace, size_t workspace_bytes, kvq_stream_t stream) {
-  if (kvq_status s = check_cache(cache)) return s;
+  kvq_cache eff_;
+  if (kvq_status s = resolve_cache(cache, &eff_)) return s;
+  cache = &eff_;
   if (kvq_status s = check_params(cache, params)) return s;
   if (params->batch == 0) return KVQ_OK;
   if (!q || !block_table || !seq_lens || !workspace) return KVQ_ERR_INVALID_ARG;
@@ -516,7 +545,9 @@ KVQ_API kvq_status kvq_norm_rope_apply(const kvq_norm_rope* prologue, const void
 
 KVQ_API kvq_status kvq_decode_workspace_size(const kvq_cache* cache, const kvq_decode_params* params,
                                              size_t* workspace_bytes) {
-  if (kvq_status s = check_cache(cache)) return s;
+  kvq_cache eff_;
+  if (kvq_status s = resolve_cache(cache, &eff_)) return s;
+  cache = &eff_;
   if (kvq_status s = check_params(cache, params)) return s;
   if (!workspace_bytes) return KVQ_ERR_INVALID_ARG;
   DeviceInfo* dev;
@@ -536,7 +567,9 @@ KVQ_API kvq_status kvq_decode(const kvq_cache* cache, const kvq_decode_params* p
 KVQ_API kvq_status kvq_combine(const kvq_cache* cache, const kvq_decode_params* params, const void* workspace,
                                size_t workspace_bytes, const float* head_sink, void* out, float* lse_out,
                                kvq_stream_t stream) {
-  if (kvq_status s = check_cache(cache)) return s;
+  kvq_cache eff_;
+  if (kvq_status s = resolve_cache(cache, &eff_)) return s;
+  cache = &eff_;
   if (kvq_status s = check_params(cache, params)) return s;
   if (params->batch == 0) return KVQ_OK;
   if (!workspace || !out) return KVQ_ERR_INVALID_ARG;
@@ -565,6 +598,7 @@ KVQ_API kvq_status kvq_combine(const kvq_cache* cache, const kvq_decode_params* 
   a.group = params->num_q_heads / cache->num_kv_heads;
   a.rows = P.rows;
   a.head_dim = cache->head_dim;
+  a.out_dim = cache->v_head_size;
   return from_cuda(launch_combine(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -584,7 +618,9 @@ KVQ_API kvq_status kvq_prefill(const kvq_cache* cache, const kvq_decode_params* 
                                const int32_t* block_table, const int32_t* seq_lens, const float* head_sink,
                                void* out, float* lse_out, void* workspace, size_t workspace_bytes,
                                kvq_stream_t stream) {
-  if (kvq_status s = check_cache(cache)) return s;
+  kvq_cache eff_;
+  if (kvq_status s = resolve_cache(cache, &eff_)) return s;
+  cache = &eff_;
   kvq_decode_params v;
   int n = 0;
   if (kvq_status s = prefill_shape(params, &v, &n)) return s;

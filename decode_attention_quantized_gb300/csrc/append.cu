@@ -163,6 +163,7 @@ __global__ void __launch_bounds__(256) append_kernel(const AppendArgs a) {
   const int lane = threadIdx.x & 31;
   if (wg >= a.n_tokens * a.num_kv_heads * 2) return;
   const int side = wg & 1;  // 0: K, 1: V
+  if (side == 1 && a.latent) return;  // LATENT: the K row is also V
   const int n = (wg >> 1) / a.num_kv_heads;
   const int h = (wg >> 1) % a.num_kv_heads;
   const long long slot = a.slots[n];

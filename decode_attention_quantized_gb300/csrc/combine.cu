@@ -133,7 +133,9 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const Combi
     const __nv_bfloat162 v = __floats2bfloat162_rn(acc[e], acc[e + 1]);
     packed[e / 2] = *reinterpret_cast<const uint32_t*>(&v);
   }
-  uint16_t* dst = a.out + (size_t)row_id * D + lane * E;
+  if (a.lse_out && lane == 0) a.lse_out[row_id] = lse_nat;
+  if (lane * E >= a.out_dim) return;  // LATENT: only the leading v_head_size channels
+  uint16_t* dst = a.out + (size_t)row_id * a.out_dim + lane * E;
   if constexpr (E == 8) {
     *reinterpret_cast<uint4*>(dst) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
   } else if constexpr (E == 4) {
@@ -141,7 +143,6 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const Combi
   } else {
     *reinterpret_cast<uint32_t*>(dst) = packed[0];
   }
-  if (a.lse_out && lane == 0) a.lse_out[row_id] = lse_nat;
 }
 
 // Sequence lengths of a prefill chunk's virtual sequences (one thread each).

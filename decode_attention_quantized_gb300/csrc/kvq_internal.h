@@ -44,6 +44,7 @@ struct AppendArgs {
   int dtype, k_mode, v_mode;
   unsigned int* err;
   int k_prologue;           // apply `pro` to the K rows before quantizing them
+  int latent;               // LATENT layout: only the K rows are written
   NormRope pro;
 };
 
@@ -84,9 +85,10 @@ struct CombineArgs {
   const float* head_sink;  // [Hq] or null
   const float* v_scale;    // static V scale (PER_TENSOR [1] / PER_CHANNEL [Hkv, D]) or null
   int v_mode;
-  uint16_t* out;           // bf16 bits [B, T, Hq, D]
+  uint16_t* out;           // bf16 bits [B, T, Hq, out_dim]
   float* lse_out;          // [B, T, Hq] or null
   int batch, q_tokens, num_q_heads, num_kv_heads, group, rows, head_dim;
+  int out_dim;             // channels written per row: head_dim, or v_head_size (LATENT)
 };
 
 // The tensor-memory decode kernel (many query rows per kv head): 128 keys per

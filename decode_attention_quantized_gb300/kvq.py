@@ -18,6 +18,7 @@ import torch
 from .build import LIB_PATH
 
 INT8, FP8_E4M3, INT4 = 1, 2, 3
+LAYOUT_SEPARATE, LAYOUT_LATENT = 0, 1
 PER_ROW, PER_TENSOR, PER_CHANNEL = 1, 2, 3
 DEVERR_SLOT, DEVERR_BLOCK_ID, DEVERR_SEQ_LEN, DEVERR_TIMEOUT, DEVERR_POSITION = 0x1, 0x2, 0x4, 0x8, 0x10
 STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "workspace too small", 4: "CUDA error",
@@ -35,7 +36,8 @@ class CacheDesc(ctypes.Structure):
                 ("num_blocks", ctypes.c_int32), ("block_size", ctypes.c_int32),
                 ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
                 ("k_codes", ctypes.c_void_p), ("v_codes", ctypes.c_void_p),
-                ("k_scale", ctypes.c_void_p), ("v_scale", ctypes.c_void_p)]
+                ("k_scale", ctypes.c_void_p), ("v_scale", ctypes.c_void_p),
+                ("layout", ctypes.c_int32), ("v_head_size", ctypes.c_int32)]
 
 
 class DecodeParams(ctypes.Structure):
@@ -118,14 +120,20 @@ class QuantizedPagedCache:
 
     def __init__(self, dtype: int, k_mode: int, v_mode: int, num_blocks: int, block_size: int,
                  num_kv_heads: int, head_dim: int, *, device="cuda", k_static: Optional[torch.Tensor] = None,
-                 v_static: Optional[torch.Tensor] = None):
+                 v_static: Optional[torch.Tensor] = None, latent: bool = False, v_head_size: int = 0):
+        """latent: one cache (absorbed MLA); V is the leading v_head_size channels
+        of each K row, with K's scales, and no V arrays are allocated."""
+        self.layout = LAYOUT_LATENT if latent else LAYOUT_SEPARATE
+        self.v_head_size = v_head_size
+        if latent:
+            v_mode = k_mode
         self.dtype, self.k_mode, self.v_mode = dtype, k_mode, v_mode
         self.num_blocks, self.block_size = num_blocks, block_size
         self.num_kv_heads, self.head_dim = num_kv_heads, head_dim
         dp = head_dim // 2 if dtype == INT4 else head_dim
         shape = (num_blocks, num_kv_heads, block_size, dp)
         self.k_codes = torch.zeros(shape, dtype=torch.uint8, device=device)
-        self.v_codes = torch.zeros(shape, dtype=torch.uint8, device=device)
+        self.v_codes = self.k_codes if latent else torch.zeros(shape, dtype=torch.uint8, device=device)
 
         def scales(mode, static):
             if mode == PER_ROW:
@@ -136,12 +144,17 @@ class QuantizedPagedCache:
             return static.to(device=device, dtype=torch.float32).reshape(want).contiguous()
 
         self.k_scale = scales(k_mode, k_static)
-        self.v_scale = scales(v_mode, v_static)
+        self.v_scale = self.k_scale if latent else scales(v_mode, v_static)
 
     def desc(self) -> CacheDesc:
         return CacheDesc(self.dtype, self.k_mode, self.v_mode, self.num_blocks, self.block_size,
                          self.num_kv_heads, self.head_dim, self.k_codes.data_ptr(), self.v_codes.data_ptr(),
-                         self.k_scale.data_ptr(), self.v_scale.data_ptr())
+                         self.k_scale.data_ptr(), self.v_scale.data_ptr(), self.layout, self.v_head_size)
+
+    @property
+    def out_dim(self) -> int:
+        """Channels of an output row: head_dim, or v_head_size for a LATENT cache."""
+        return (self.v_head_size or self.head_dim) if self.layout == LAYOUT_LATENT else self.head_dim
 
 
 def make_params(batch, num_q_heads, q_tokens, max_blocks_per_seq, *, max_seq_len=0, sm_scale=0.0, softcap=0.0,
@@ -275,7 +288,7 @@ def alloc_decode_buffers(cache: QuantizedPagedCache, params: DecodeParams) -> De
     """Caller-side allocation of the workspace (256-byte aligned) and outputs."""
     nbytes = kvq_decode_workspace_size(cache, params)
     ws = torch.empty(max(nbytes, 256) // 4 + 64, dtype=torch.int32, device=cache.k_codes.device)
-    shape = (params.batch, params.q_tokens, params.num_q_heads, cache.head_dim)
+    shape = (params.batch, params.q_tokens, params.num_q_heads, cache.out_dim)
     out = torch.empty(shape, dtype=torch.bfloat16, device=cache.k_codes.device)
     lse = torch.empty(shape[:3], dtype=torch.float32, device=cache.k_codes.device)
     return DecodeBuffers(ws, out, lse)

@@ -92,6 +92,11 @@ typedef enum {
 #define KVQ_DEVERR_TIMEOUT 0x8u   /* a bounded pipeline wait gave up */
 #define KVQ_DEVERR_POSITION 0x10u /* norm/RoPE prologue: position outside [0, max_position) */
 
+/* Cache layouts (PR #29912, kv_cache_layout and v_head_size): SEPARATE K and V
+ * caches, or LATENT (absorbed MLA): one cache whose rows serve as K, and whose
+ * leading v_head_size channels serve as V. */
+typedef enum { KVQ_LAYOUT_SEPARATE = 0, KVQ_LAYOUT_LATENT = 1 } kvq_layout;
+
 /* The paged cache: one descriptor per layer (kv-quant-attn "Usage": one cache
  * object per layer).  All pointers are device memory owned by the caller.
  * k_scale / v_scale: PER_ROW arrays written by kvq_append, or the static
@@ -108,6 +113,12 @@ typedef struct {
   void* v_codes;
   float* k_scale;
   float* v_scale;
+  int32_t layout;       /* kvq_layout; LATENT: v_codes, v_scale, v_mode are ignored (V is the K
+                           row, with K's scales) and may be NULL / 0; kvq_append writes K only
+                           and ignores v_new; kvq_combine writes out [B, T, Hq, v_head_size] */
+  int32_t v_head_size;  /* LATENT: channels of V, a multiple of 8 in [8, head_dim]; 0 = head_dim.
+                           The pages' DeepSeek-V3 example (576/512) is above this library's
+                           head_dim limit of 256. */
 } kvq_cache;
 
 /* One decode call (PagedAttention's inputs, PR #29912 Summary of Changes). */

@@ -196,3 +196,19 @@ def test_prefill_rejects_bad_arguments_on_the_host(kvq):
     p = good_params(kvq, batch=0, q_tokens=12)
     assert lib.kvq_prefill(ctypes.byref(c), ctypes.byref(p), None, None, None, None, None, None, None, 0,
                            None) == 0
+
+
+@pytest.mark.parametrize("bad", [dict(layout=2), dict(layout=-1), dict(layout=1, v_head_size=12),
+                                 dict(layout=1, v_head_size=136), dict(layout=0, v_head_size=64),
+                                 dict(layout=1, k_codes=None)])
+def test_latent_layout_validation(kvq, bad):
+    lib = kvq.load()
+    c = good_cache(kvq, **bad)
+    assert lib.kvq_append(ctypes.byref(c), FAKE, FAKE, FAKE, 4, None) == 1
+
+
+def test_latent_cache_needs_no_v_arrays(kvq):
+    lib = kvq.load()
+    c = good_cache(kvq, layout=1, v_head_size=64, v_codes=None, v_scale=None, v_mode=0)
+    # valid: nothing to append, and V arguments may be NULL
+    assert lib.kvq_append(ctypes.byref(c), FAKE, None, FAKE, 0, None) == 0
