@@ -81,10 +81,23 @@ __device__ __forceinline__ uint32_t i4pair(uint32_t x, int shift) {
 }
 // e4m3: byte b = s.eeee.mmm moved to bits 15..8 of a half, then sign kept
 // and eeee.mmm shifted right by one: exactly the f16 value b * 2^-8
-// (subnormals included; the 2^8 is applied to the logit / output scale).
+// (subnormals included; the tensor-memory kernel's V path, which applies the
+// 2^8 at its output).
 __device__ __forceinline__ uint32_t f8pair(uint32_t w, uint32_t sel) {
   const uint32_t y = ptx::prmt(w, 0u, sel);
   return (y & 0x80008000u) | ((y >> 1) & 0x3F803F80u);
+}
+
+// e4m3 pair (bytes selected by sel into a 16-bit word) -> exact f16x2 by the
+// hardware conversion, then max with -448 so a NaN code (a stale byte under a
+// masked key) becomes finite.
+__device__ __forceinline__ uint32_t f8cvt(uint32_t w, uint32_t sel) {
+  const uint32_t x = ptx::prmt(w, 0u, sel);
+  uint32_t d;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(d) : "h"((uint16_t)(x & 0xFFFFu)));
+  uint32_t r;
+  asm("max.f16x2 %0, %1, %2;" : "=r"(r) : "r"(d), "r"(0xDF00DF00u));
+  return r;
 }
 
 // tanh(x) = 1 - 2 / (e^{2x} + 1), from the definition; absolute error a few
@@ -599,10 +612,10 @@ __global__ void __launch_bounds__(288, MINB)
                   A[2] = dev::i8pair(xh, 0x4240u);
                   A[3] = dev::i8pair(xh, 0x4341u);
                 } else {
-                  A[0] = dev::f8pair(wl, 0x2404u);
-                  A[1] = dev::f8pair(wl, 0x3414u);
-                  A[2] = dev::f8pair(wh, 0x2404u);
-                  A[3] = dev::f8pair(wh, 0x3414u);
+                  A[0] = dev::f8cvt(wl, 0x0020u);
+                  A[1] = dev::f8cvt(wl, 0x0031u);
+                  A[2] = dev::f8cvt(wh, 0x0020u);
+                  A[3] = dev::f8cvt(wh, 0x0031u);
                 }
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) ptx::mma_16816(acc[jl][nt], A, pb[nt][0], pb[nt][1]);
@@ -627,7 +640,6 @@ __global__ void __launch_bounds__(288, MINB)
         }
       ptx::named_bar_sync(1, 8 * 32);
       float to_true = v_row ? dev::pow2i(F) : 1.0f;
-      if constexpr (DT == KVQ_FP8_E4M3) to_true *= 256.0f;
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
         const int r0 = rh * RW + nt * 8 + 2 * c, r1 = r0 + 1;
@@ -847,10 +859,10 @@ __global__ void __launch_bounds__(288, MINB)
                 A[2] = dev::i8pair(xh, 0x4240u);
                 A[3] = dev::i8pair(xh, 0x4341u);
               } else {
-                A[0] = dev::f8pair(wl, 0x2404u);
-                A[1] = dev::f8pair(wl, 0x3414u);
-                A[2] = dev::f8pair(wh, 0x2404u);
-                A[3] = dev::f8pair(wh, 0x3414u);
+                A[0] = dev::f8cvt(wl, 0x0020u);
+                A[1] = dev::f8cvt(wl, 0x0031u);
+                A[2] = dev::f8cvt(wh, 0x0020u);
+                A[3] = dev::f8cvt(wh, 0x0031u);
               }
               ptx::mma_16816(acc[j], A, pb0, pb1);
             }
@@ -870,7 +882,6 @@ __global__ void __launch_bounds__(288, MINB)
       l1 += __shfl_xor_sync(0xffffffffu, l1, o);
     }
     float to_true = v_row ? dev::pow2i(F) : 1.0f;  // acc * to_true = sum_j p_j dequant(v_j)
-    if constexpr (DT == KVQ_FP8_E4M3) to_true *= 256.0f;
     float* slot = scr + rg * kScrPerRg;
     for (int k = 1; k < a.key_warps; ++k) {
       if (kw == k - 1) {
