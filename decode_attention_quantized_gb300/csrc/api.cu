@@ -128,14 +128,19 @@ constexpr int kPieceCost = 3;
 // Launch shape of the decode kernel and the workspace it implies.
 struct Plan {
   int rows, row_groups, key_warps, nt, tc_nr, threads, stages, grid, units_max;
-  size_t smem, ws_plan, ws_lse, ws_o, ws_total;
+  size_t stride, smem, ws_plan, ws_lse, ws_o, ws_total;
 };
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
+// K and V code rows of one stage, then room for the K and V per-row scales
+// only when a side has them (a 16-row fp8 stage of head_dim 128 is then
+// 16 KB, so four CTAs with three stages each fit on an SM); 1 KB multiples
+// keep every stage on the 128-byte swizzle's alignment.
 size_t stage_stride(const kvq_cache* c) {
   const size_t code = (size_t)kTile * row_bytes(c);
-  return (2 * code + 2 * kTile * 4 + 1023) / 1024 * 1024;
+  const bool row = c->k_mode == KVQ_SCALE_PER_ROW || c->v_mode == KVQ_SCALE_PER_ROW;
+  return (2 * code + (row ? 2 * kTile * 4 : 0) + 1023) / 1024 * 1024;
 }
 
 size_t fixed_smem(const kvq_cache* c, int row_groups, int key_warps, int nt, int batch, int stages) {
@@ -178,6 +183,7 @@ kvq_status make_plan_tc(const kvq_cache* c, const kvq_decode_params* p, const De
     if ((size_t)tc_smem_layout(c->head_dim, dp, P->tc_nr, s, B).total + 1024 <= kMaxSmem) stages = s;
   if (stages == 0) return KVQ_ERR_UNSUPPORTED;
   P->stages = stages;
+  P->stride = (size_t)tc_stage_stride(dp);
   P->smem = (size_t)tc_smem_layout(c->head_dim, dp, P->tc_nr, stages, B).total + 1024;
   P->threads = kTcWarps * 32;
   P->row_groups = 0;
@@ -222,6 +228,7 @@ kvq_status make_plan_uncached(const kvq_cache* c, const kvq_decode_params* p, co
   P.threads = 32 * (n_cw + 1);
   const int B = p->batch > 0 ? p->batch : 1;
   const size_t stride = stage_stride(c);
+  P.stride = stride;
   // the most CTAs per SM whose ring still holds >= 3 stages (more warps per
   // SM hide more latency); one CTA with >= 2 stages as the last resort
   int occ = 0;
@@ -445,6 +452,7 @@ kvq_status decode_impl(const kvq_cache* cache, const kvq_decode_params* params, 
   a.row_groups = P.row_groups;
   a.key_warps = P.key_warps;
   a.stages = P.stages;
+  a.stage_stride = (int)P.stride;
   a.units_max = P.units_max;
   // a piece change (query prologue, merge and partial write, refill of the
   // role pipeline) is charged as a few tiles when the split is planned

@@ -89,16 +89,23 @@ __device__ __forceinline__ uint32_t f8pair(uint32_t w, uint32_t sel) {
 }
 
 // e4m3 pair (bytes selected by sel into a 16-bit word) -> exact f16x2 by the
-// hardware conversion, then max with -448 so a NaN code (a stale byte under a
-// masked key) becomes finite.
+// hardware conversion.  kClamp: then max with -448 so that a NaN code (a
+// stale byte past the sequence end, under a masked key) becomes finite.
+template <bool kClamp = true>
 __device__ __forceinline__ uint32_t f8cvt(uint32_t w, uint32_t sel) {
   const uint32_t x = ptx::prmt(w, 0u, sel);
   uint32_t d;
   asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(d) : "h"((uint16_t)(x & 0xFFFFu)));
+  if constexpr (!kClamp) return d;
   uint32_t r;
   asm("max.f16x2 %0, %1, %2;" : "=r"(r) : "r"(d), "r"(0xDF00DF00u));
   return r;
 }
+
+template <bool B>
+struct Flag {
+  static constexpr bool value = B;
+};
 
 // tanh(x) = 1 - 2 / (e^{2x} + 1), from the definition; absolute error a few
 // 1e-7 (ex2.approx and an approximate divide), saturating to +-1.
@@ -259,7 +266,7 @@ __global__ void __launch_bounds__(288, MINB)
 
   const int n_cw = a.row_groups * a.key_warps;
   constexpr int kScrPerRg = (Gm::NMT * 4 + 4) * 32;  // floats: accumulators + (m, l) of one warp, [elem][lane]
-  float* scr = reinterpret_cast<float*>(ring + (size_t)a.stages * Gm::STAGE_STRIDE);
+  float* scr = reinterpret_cast<float*>(ring + (size_t)a.stages * a.stage_stride);
   const int scr_floats =
       NT > 0 ? wide_scratch_floats<NT, D>() : (a.key_warps > 1 ? a.row_groups * kScrPerRg : 0);
   int* pl_pre = reinterpret_cast<int*>(scr + scr_floats);  // [B + 1]
@@ -379,7 +386,7 @@ __global__ void __launch_bounds__(288, MINB)
           ok = ptx::mbar_wait_bounded_inl(&bar_full[stage], (it / a.stages) & 1);
           if (!ok) atomicOr(a.err, KVQ_DEVERR_TIMEOUT);
         }
-        const uint8_t* st = ring + (size_t)stage * Gm::STAGE_STRIDE;
+        const uint8_t* st = ring + (size_t)stage * a.stage_stride;
         const uint32_t sk_base = ptx::smem_u32(st);
         const uint32_t sv_base = sk_base + Gm::CODE_BYTES;
         const float* ks_row = reinterpret_cast<const float*>(st + 2 * Gm::CODE_BYTES);
@@ -713,7 +720,7 @@ __global__ void __launch_bounds__(288, MINB)
         ok = ptx::mbar_wait_bounded_inl(&bar_full[stage], (it / a.stages) & 1);
         if (!ok) atomicOr(a.err, KVQ_DEVERR_TIMEOUT);
       }
-      const uint8_t* st = ring + (size_t)stage * Gm::STAGE_STRIDE;
+      const uint8_t* st = ring + (size_t)stage * a.stage_stride;
       const uint32_t sk_base = ptx::smem_u32(st);
       const uint32_t sv_base = sk_base + Gm::CODE_BYTES;
       const float* ks_row = reinterpret_cast<const float*>(st + 2 * Gm::CODE_BYTES);
@@ -830,43 +837,54 @@ __global__ void __launch_bounds__(288, MINB)
         const uint32_t pb0 = ptx::movmatrix_trans(dev::pack_h2(p0 * vsa, p1 * vsa));
         const uint32_t pb1 = ptx::movmatrix_trans(dev::pack_h2(p2 * vsb, p3 * vsb));
 
-        // ---- O += V^T P^T for all channels (channels are MMA-M)
+        // ---- O += V^T P^T for all channels (channels are MMA-M).  Every key
+        // below the sequence end holds a code the quantizer wrote (never NaN);
+        // only a sub-tile reaching past it can meet stale e4m3 NaN bytes, and
+        // only there are the V codes clamped.
+        auto pv = [&](auto clamp) {
 #pragma unroll
-        for (int jj = 0; jj < Gm::NCH / 2; ++jj) {
-          const uint32_t byte = (uint32_t)(2 * jj + ld_chunk) * 16;
-          const uint32_t addr =
-              sv_base + (byte / Gm::SPAN) * (kTile * Gm::SPAN) + dev::swz<Gm::SPAN>(row_off + byte % Gm::SPAN);
-          uint32_t R[4];
-          ptx::ldmatrix_x4_trans(R, addr);
+          for (int jj = 0; jj < Gm::NCH / 2; ++jj) {
+            const uint32_t byte = (uint32_t)(2 * jj + ld_chunk) * 16;
+            const uint32_t addr =
+                sv_base + (byte / Gm::SPAN) * (kTile * Gm::SPAN) + dev::swz<Gm::SPAN>(row_off + byte % Gm::SPAN);
+            uint32_t R[4];
+            ptx::ldmatrix_x4_trans(R, addr);
 #pragma unroll
-          for (int h2 = 0; h2 < 2; ++h2) {
-            const int j = 2 * jj + h2;
-            const uint32_t wl = R[2 * h2], wh = R[2 * h2 + 1];
-            if constexpr (DT == KVQ_INT4) {
-              const uint32_t xl = wl ^ 0x88888888u, xh = wh ^ 0x88888888u;
+            for (int h2 = 0; h2 < 2; ++h2) {
+              const int j = 2 * jj + h2;
+              const uint32_t wl = R[2 * h2], wh = R[2 * h2 + 1];
+              if constexpr (DT == KVQ_INT4) {
+                const uint32_t xl = wl ^ 0x88888888u, xh = wh ^ 0x88888888u;
 #pragma unroll
-              for (int t = 0; t < 2; ++t) {
-                const uint32_t A[4] = {dev::i4pair(xl, 8 * t), dev::i4pair(xl, 8 * t + 4), dev::i4pair(xh, 8 * t),
-                                       dev::i4pair(xh, 8 * t + 4)};
-                ptx::mma_16816(acc[2 * j + t], A, pb0, pb1);
-              }
-            } else {
-              uint32_t A[4];
-              if constexpr (DT == KVQ_INT8) {
-                const uint32_t xl = wl ^ 0x80808080u, xh = wh ^ 0x80808080u;
-                A[0] = dev::i8pair(xl, 0x4240u);
-                A[1] = dev::i8pair(xl, 0x4341u);
-                A[2] = dev::i8pair(xh, 0x4240u);
-                A[3] = dev::i8pair(xh, 0x4341u);
+                for (int t = 0; t < 2; ++t) {
+                  const uint32_t A[4] = {dev::i4pair(xl, 8 * t), dev::i4pair(xl, 8 * t + 4), dev::i4pair(xh, 8 * t),
+                                         dev::i4pair(xh, 8 * t + 4)};
+                  ptx::mma_16816(acc[2 * j + t], A, pb0, pb1);
+                }
               } else {
-                A[0] = dev::f8cvt(wl, 0x0020u);
-                A[1] = dev::f8cvt(wl, 0x0031u);
-                A[2] = dev::f8cvt(wh, 0x0020u);
-                A[3] = dev::f8cvt(wh, 0x0031u);
+                uint32_t A[4];
+                if constexpr (DT == KVQ_INT8) {
+                  const uint32_t xl = wl ^ 0x80808080u, xh = wh ^ 0x80808080u;
+                  A[0] = dev::i8pair(xl, 0x4240u);
+                  A[1] = dev::i8pair(xl, 0x4341u);
+                  A[2] = dev::i8pair(xh, 0x4240u);
+                  A[3] = dev::i8pair(xh, 0x4341u);
+                } else {
+                  constexpr bool kC = decltype(clamp)::value;
+                  A[0] = dev::f8cvt<kC>(wl, 0x0020u);
+                  A[1] = dev::f8cvt<kC>(wl, 0x0031u);
+                  A[2] = dev::f8cvt<kC>(wh, 0x0020u);
+                  A[3] = dev::f8cvt<kC>(wh, 0x0031u);
+                }
+                ptx::mma_16816(acc[j], A, pb0, pb1);
               }
-              ptx::mma_16816(acc[j], A, pb0, pb1);
             }
           }
+        };
+        if constexpr (DT == KVQ_FP8_E4M3) {
+          if (kb + kSub <= L) pv(dev::Flag<false>{}); else pv(dev::Flag<true>{});
+        } else {
+          pv(dev::Flag<false>{});
         }
       }
       __syncwarp();

@@ -68,6 +68,7 @@ struct DecodeArgs {
   float sm_scale, softcap;
   int window;
   int row_groups, key_warps, stages;
+  int stage_stride;  // bytes between ring stages (a multiple of 1024)
   int units_max;    // partial slots (grid + batch * Hkv)
   int piece_cost;   // tiles' worth of time a CTA spends on each piece change (split planning)
   int bt_div;       // block-table row of sequence b is b / bt_div (prefill: virtual sequences)

@@ -19,7 +19,10 @@ constexpr int round_up_c(int x, int m) { return (x + m - 1) / m * m; }
 
 // One stage holds KT keys: the K code rows, then the V code rows, each as
 // SLABS column slabs of [KT rows][SPAN bytes] in the TMA swizzle, then KT K
-// scales and KT V scales (fp32, per-row mode only).
+// scales and KT V scales (fp32, per-row mode only).  STAGE_STRIDE always
+// leaves room for the scales (the tensor-memory kernel's ring); the mma.sync
+// kernel and the producer step by DecodeArgs::stage_stride, which the host
+// sizes without the scale area when neither side has per-row scales.
 template <int DT, int D_, int KT = kTile>
 struct Geo {
   static constexpr int D = D_;
@@ -246,7 +249,7 @@ __device__ void produce(const DecodeArgs& a, const Slice<Gm::KEYS>& sp, const CU
         if (!ok) atomicOr(a.err, KVQ_DEVERR_TIMEOUT);
       }
       ok = __shfl_sync(0xffffffffu, ok, 0);
-      uint8_t* st = ring + (size_t)stage * Gm::STAGE_STRIDE;
+      uint8_t* st = ring + (size_t)stage * a.stage_stride;
       const int kend = ok ? min(key0 + KT, k1) : key0;  // nothing is loaded after a timeout
       if constexpr (kBurst) {
         // the stage's block ids first (whole warp), then one burst of copies

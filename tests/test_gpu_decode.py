@@ -236,3 +236,35 @@ def test_tensor_memory_layout(lib, orc, case):
     assert torch.equal(bufs.out, ref)
     if W:
         run_case(orc, w, window=W, check_cache=False, q_scale=qs)
+
+
+@pytest.mark.parametrize("G,T", [(4, 1), (8, 4)], ids=["mma-sync", "tensor-memory"])
+def test_fp8_nan_bytes_past_the_sequence_end(lib, orc, G, T):
+    """Every slot no append wrote holds the e4m3 NaN byte 0x7F, so the keys
+    past each sequence's end inside its last page are NaN codes.  Their
+    weights are zero; the result must still equal the oracle's (which never
+    reads them) and be finite.  Both decode layouts: 4 rows per kv head (the
+    mma.sync kernel) and 32 (the tensor-memory kernel)."""
+    Hkv, D, bs = 2, 128, 16
+    L = np.array([37, 300, 129, 8], np.int32)
+    mb = math.ceil(int(L.max()) / bs)
+    table = np.random.default_rng(7).permutation(len(L) * mb).astype(np.int32).reshape(len(L), mb)
+    w = synth.Workload("nan", kvq.FP8_E4M3, kvq.PER_TENSOR, kvq.PER_TENSOR, len(L), G * Hkv, Hkv, D, T, bs, L,
+                       table, len(L) * mb, seed=11)
+    gw = GpuWorkload(w, gen_device="cpu")
+    gw.cache.k_codes.fill_(0x7F)
+    gw.cache.v_codes.fill_(0x7F)
+    gw.fill_history()
+    k_new, v_new, slots = gw.new_tokens()
+    params = gw.params()
+    bufs = gw.buffers(params)
+    q = w.q("cpu").to("cuda")
+    out, lse = gw.step(q, k_new, v_new, slots, params, bufs)
+    torch.cuda.synchronize()
+    assert kvq.kvq_get_device_error(clear=True) == 0
+    got = out.float().cpu().numpy().astype(np.float64)
+    assert np.isfinite(got).all()
+    side = OracleSide(orc, w, range(w.batch), "cpu", gw.k_static, gw.v_static)
+    ref, ref_lse = side.attend(q, window=0, sink=gw.head_sink)
+    check_rows(got, ref)
+    check_lse(lse.cpu().numpy().astype(np.float64), ref_lse)
