@@ -44,7 +44,13 @@
  *  asked for; R22 on the cache side only K takes the prologue, V is written as
  *  given; R23 the optional Walsh-Hadamard rotation (onnxruntime PR #32515,
  *  note on the stacked change that adds it) comes after RoPE, on Q and K
- *  alike (so dot products are unchanged), in Sylvester order.
+ *  alike (so dot products are unchanged), in Sylvester order.  For the
+ *  group-wise scales the kv-quant-attn page lists as not done (section
+ *  "Requirements and limits"): R25 a group is a run of group_size consecutive channels of
+ *  one (token, kv head) row (group_size divides D), quantized exactly like a
+ *  PER_ROW row of group_size values (absmax / qmax, R1-R4), one fp32 scale
+ *  per group stored [num_blocks, Hkv, block_size, D / group_size]; PER_ROW is
+ *  the case group_size = D.
  *
  * Parity pins live in tests/ (format table of e4m3 against torch's
  * float8_e4m3fn, brute-force nearest-code search, round-trip bounds, the
@@ -64,6 +70,7 @@
 #define ORC_PER_ROW 1
 #define ORC_PER_TENSOR 2
 #define ORC_PER_CHANNEL 3
+#define ORC_PER_GROUP 4
 
 /* ------------------------------------------------------------------ */
 /* scalar helpers                                                      */
@@ -156,28 +163,33 @@ int orc_row_bytes(int dtype, int D) { return dtype == ORC_INT4 ? (D + 1) / 2 : D
 /* ------------------------------------------------------------------ */
 
 /* Quantize one (token, kv head) row of D bf16 values.
- *   PER_ROW:     scale = absmax / qmax (fp32 division), stored to *scale_out
+ *   PER_ROW:     scale = absmax / qmax (fp32 division), stored to scale_out[0]
+ *   PER_GROUP:   the same for each run of group_size channels (R25): group
+ *                g's scale = absmax of channels [g G, (g+1) G) / qmax, stored to
+ *                scale_out[g]
  *   PER_TENSOR:  scale = static_scale[0]
  *   PER_CHANNEL: scale_d = static_scale[d]  (this head's D values)
  * int8 / int4: code = clamp(rne(x / scale), -qmax, qmax); e4m3: encode(x/scale).
  * int4 codes are packed two per byte, even channel in the low nibble. */
-void orc_quantize_row(const uint16_t* x_bf16, int D, int dtype, int mode,
-                      const float* static_scale, uint8_t* codes, float* scale_out) {
+void orc_quantize_row_g(const uint16_t* x_bf16, int D, int dtype, int mode, const float* static_scale,
+                        int group_size, uint8_t* codes, float* scale_out) {
   float qmaxf = (float)orc_qmax(dtype);
-  float row_scale = 0.0f;
-  if (mode == ORC_PER_ROW) {
-    float amax = 0.0f;
-    for (int d = 0; d < D; ++d) {
-      float a = fabsf(orc_bf16_to_f32(x_bf16[d]));
-      if (a > amax) amax = a;
-    }
-    row_scale = orc_fdiv(amax, qmaxf);
-    if (scale_out) *scale_out = row_scale;
-  }
+  int absmax_mode = mode == ORC_PER_ROW || mode == ORC_PER_GROUP;
+  int G = mode == ORC_PER_GROUP ? group_size : D;
+  float grp_scale = 0.0f;
   int nbytes = orc_row_bytes(dtype, D);
   if (dtype == ORC_INT4) memset(codes, 0, (size_t)nbytes);
   for (int d = 0; d < D; ++d) {
-    float s = mode == ORC_PER_ROW ? row_scale
+    if (absmax_mode && d % G == 0) {
+      float amax = 0.0f;
+      for (int k = d; k < d + G && k < D; ++k) {
+        float a = fabsf(orc_bf16_to_f32(x_bf16[k]));
+        if (a > amax) amax = a;
+      }
+      grp_scale = orc_fdiv(amax, qmaxf);
+      if (scale_out) scale_out[d / G] = grp_scale;
+    }
+    float s = absmax_mode ? grp_scale
               : mode == ORC_PER_TENSOR ? static_scale[0]
                                         : static_scale[d];
     float x = orc_bf16_to_f32(x_bf16[d]);
@@ -206,6 +218,11 @@ void orc_quantize_row(const uint16_t* x_bf16, int D, int dtype, int mode,
   }
 }
 
+void orc_quantize_row(const uint16_t* x_bf16, int D, int dtype, int mode, const float* static_scale,
+                      uint8_t* codes, float* scale_out) {
+  orc_quantize_row_g(x_bf16, D, dtype, mode, static_scale, D, codes, scale_out);
+}
+
 /* Code value of channel d in a row (int8 / int4 sign-extended / e4m3). */
 static double orc_code_value(const uint8_t* codes, int d, int dtype) {
   if (dtype == ORC_INT8) return (double)(int8_t)codes[d];
@@ -224,8 +241,15 @@ typedef struct {
   int dtype, k_mode, v_mode;
   int num_blocks, block_size, num_kv_heads, head_dim;
   uint8_t *k_codes, *v_codes; /* [NB, Hkv, bs, Dp] */
-  float *k_scale, *v_scale;   /* PER_ROW [NB, Hkv, bs]; PER_TENSOR [1]; PER_CHANNEL [Hkv, D] */
+  float *k_scale, *v_scale;   /* PER_ROW [NB, Hkv, bs]; PER_TENSOR [1]; PER_CHANNEL [Hkv, D];
+                                 PER_GROUP [NB, Hkv, bs, D / group_size] */
+  int group_size;             /* PER_GROUP: channels per scale group (divides D) */
 } orc_cache;
+
+/* fp32 scales per cached row of a side in this mode (0: static scales). */
+static int orc_scales_per_row(const orc_cache* c, int mode) {
+  return mode == ORC_PER_ROW ? 1 : mode == ORC_PER_GROUP ? c->head_dim / c->group_size : 0;
+}
 
 static size_t orc_row_index(const orc_cache* c, int blk, int h, int row) {
   return ((size_t)blk * c->num_kv_heads + h) * c->block_size + row;
@@ -256,10 +280,11 @@ int orc_append(const orc_cache* c, const uint16_t* k_new, const uint16_t* v_new,
       const float* vs = c->v_mode == ORC_PER_TENSOR ? c->v_scale
                         : c->v_mode == ORC_PER_CHANNEL ? c->v_scale + (size_t)h * D
                                                        : NULL;
-      orc_quantize_row(kx, D, c->dtype, c->k_mode, ks, c->k_codes + ri * Dp,
-                       c->k_mode == ORC_PER_ROW ? c->k_scale + ri : NULL);
-      orc_quantize_row(vx, D, c->dtype, c->v_mode, vs, c->v_codes + ri * Dp,
-                       c->v_mode == ORC_PER_ROW ? c->v_scale + ri : NULL);
+      int nk = orc_scales_per_row(c, c->k_mode), nv = orc_scales_per_row(c, c->v_mode);
+      orc_quantize_row_g(kx, D, c->dtype, c->k_mode, ks, c->group_size, c->k_codes + ri * Dp,
+                         nk ? c->k_scale + ri * nk : NULL);
+      orc_quantize_row_g(vx, D, c->dtype, c->v_mode, vs, c->group_size, c->v_codes + ri * Dp,
+                         nv ? c->v_scale + ri * nv : NULL);
     }
   }
   return bad;
@@ -387,7 +412,8 @@ int orc_norm_rope(const uint16_t* x, int n_tokens, int H, int D, const uint16_t*
 }
 
 /* Dequantize one cached row (token position t of sequence with block-table
- * row bt) in fp64: code * row scale, * tensor scale, or * channel scale. */
+ * row bt) in fp64: code * row scale, * group scale, * tensor scale, or *
+ * channel scale. */
 static void orc_dequant_row(const orc_cache* c, const uint8_t* codes_base, const float* scale,
                             int mode, const int32_t* bt, int h, int t, double* out) {
   int D = c->head_dim, Dp = orc_row_bytes(c->dtype, D);
@@ -396,6 +422,7 @@ static void orc_dequant_row(const orc_cache* c, const uint8_t* codes_base, const
   const uint8_t* codes = codes_base + ri * Dp;
   for (int d = 0; d < D; ++d) {
     double s = mode == ORC_PER_ROW ? (double)scale[ri]
+               : mode == ORC_PER_GROUP ? (double)scale[ri * (size_t)(D / c->group_size) + d / c->group_size]
                : mode == ORC_PER_TENSOR ? (double)scale[0]
                                          : (double)scale[(size_t)h * D + d];
     out[d] = orc_code_value(codes, d, c->dtype) * s;

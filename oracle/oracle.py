@@ -10,7 +10,10 @@ What it computes (the pages' statement of the method):
   * append -- per-row absmax quantisation ("kv-quant-attn", section "Method";
     onnxruntime PR #32515, Description: step max/127 for int8, max/7 for int4)
     or static PER_TENSOR / PER_CHANNEL scales (onnxruntime PR #29912, Summary
-    of Changes, k_scale / v_scale), written to the slot that slot_mapping names.
+    of Changes, k_scale / v_scale), written to the slot that slot_mapping names;
+    or PER_GROUP: the per-row rule applied to each run of group_size channels
+    (the group-wise scaling the kv-quant-attn page lists under "Requirements
+    and limits" as not done there).
   * attend -- dequantise every cached row, then fp64 softmax attention with the
     head sink rescale 1/(1+exp(s_h - lse)) (PR #29912, ApplyHeadSink), softcap,
     sliding window and causal drafts (PR #32515, speculative decode).
@@ -18,7 +21,8 @@ What it computes (the pages' statement of the method):
 Cache layout (the library's data format, restated independently here):
 codes uint8 [num_blocks, Hkv, block_size, Dp] with Dp = D (int8, e4m3) or
 (D+1)//2 (int4, even channel in the low nibble); PER_ROW scales fp32
-[num_blocks, Hkv, block_size]; PER_TENSOR one fp32; PER_CHANNEL fp32 [Hkv, D].
+[num_blocks, Hkv, block_size]; PER_TENSOR one fp32; PER_CHANNEL fp32 [Hkv, D];
+PER_GROUP fp32 [num_blocks, Hkv, block_size, D // group_size].
 """
 from __future__ import annotations
 
@@ -30,7 +34,7 @@ import threading
 import numpy as np
 
 INT8, FP8_E4M3, INT4 = 1, 2, 3
-PER_ROW, PER_TENSOR, PER_CHANNEL = 1, 2, 3
+PER_ROW, PER_TENSOR, PER_CHANNEL, PER_GROUP = 1, 2, 3, 4
 QMAX = {INT8: 127.0, INT4: 7.0, FP8_E4M3: 448.0}
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -58,7 +62,8 @@ class _Cache(ctypes.Structure):
                 ("num_blocks", ctypes.c_int), ("block_size", ctypes.c_int),
                 ("num_kv_heads", ctypes.c_int), ("head_dim", ctypes.c_int),
                 ("k_codes", ctypes.c_void_p), ("v_codes", ctypes.c_void_p),
-                ("k_scale", ctypes.c_void_p), ("v_scale", ctypes.c_void_p)]
+                ("k_scale", ctypes.c_void_p), ("v_scale", ctypes.c_void_p),
+                ("group_size", ctypes.c_int)]
 
 
 class _Params(ctypes.Structure):
@@ -76,6 +81,7 @@ def lib():
             L.orc_e4m3_encode_n.argtypes = [vp, vp, i64]
             L.orc_e4m3_decode_n.argtypes = [vp, vp, i64]
             L.orc_quantize_row.argtypes = [vp, i32, i32, i32, vp, vp, vp]
+            L.orc_quantize_row_g.argtypes = [vp, i32, i32, i32, vp, i32, vp, vp]
             L.orc_append.argtypes = [ctypes.POINTER(_Cache), vp, vp, vp, i32]
             L.orc_append.restype = i32
             L.orc_dequant_seq.argtypes = [ctypes.POINTER(_Cache), vp, i32, i32, vp, vp]
@@ -165,14 +171,20 @@ def e4m3_decode(c: np.ndarray) -> np.ndarray:
     return out
 
 
-def quantize_row(x_bf16: np.ndarray, dtype: int, mode: int, static_scale=None):
-    """One row of D bf16 values -> (codes uint8 [Dp], row scale or None)."""
+def quantize_row(x_bf16: np.ndarray, dtype: int, mode: int, static_scale=None, group_size: int = 0):
+    """One row of D bf16 values -> (codes uint8 [Dp], scale): the row scale
+    (PER_ROW), the D // group_size group scales as float32 (PER_GROUP), or
+    None (static modes)."""
     x = np.ascontiguousarray(x_bf16, dtype=np.uint16)
     D = x.size
+    G = group_size if mode == PER_GROUP else D
+    assert G > 0 and D % G == 0
     codes = np.zeros(row_bytes(dtype, D), dtype=np.uint8)
-    sc = np.zeros(1, dtype=np.float32)
+    sc = np.zeros(D // G, dtype=np.float32)
     ss = None if static_scale is None else np.ascontiguousarray(static_scale, dtype=np.float32)
-    lib().orc_quantize_row(_ptr(x), D, dtype, mode, _ptr(ss), _ptr(codes), _ptr(sc))
+    lib().orc_quantize_row_g(_ptr(x), D, dtype, mode, _ptr(ss), G, _ptr(codes), _ptr(sc))
+    if mode == PER_GROUP:
+        return codes, sc
     return codes, (float(sc[0]) if mode == PER_ROW else None)
 
 
@@ -197,10 +209,14 @@ class OracleCache:
     """Host copy of a quantized paged cache with the oracle's append/attend."""
 
     def __init__(self, dtype, k_mode, v_mode, num_blocks, block_size, num_kv_heads, head_dim,
-                 k_static=None, v_static=None, latent=False, v_head_size=0):
+                 k_static=None, v_static=None, latent=False, v_head_size=0, group_size=0):
         """latent: the absorbed-MLA layout of onnxruntime PR #29912 (kv_cache_layout
         LATENT, v_head_size): one cache, V read as the leading v_head_size
-        channels of the same row that supplies K, with K's scales."""
+        channels of the same row that supplies K, with K's scales.
+        group_size: channels per scale group of a PER_GROUP side (divides D)."""
+        if PER_GROUP in (k_mode, v_mode):
+            assert group_size > 0 and head_dim % group_size == 0
+        self.group_size = int(group_size)
         self.latent = bool(latent)
         self.v_head_size = (v_head_size or head_dim) if latent else head_dim
         if latent:
@@ -216,6 +232,8 @@ class OracleCache:
         def scale_arr(mode, static):
             if mode == PER_ROW:
                 return np.zeros((num_blocks, num_kv_heads, block_size), dtype=np.float32)
+            if mode == PER_GROUP:
+                return np.zeros((num_blocks, num_kv_heads, block_size, head_dim // group_size), dtype=np.float32)
             if mode == PER_TENSOR:
                 return np.ascontiguousarray(np.asarray(static, dtype=np.float32).reshape(1))
             return np.ascontiguousarray(np.asarray(static, dtype=np.float32).reshape(num_kv_heads, head_dim))
@@ -226,7 +244,7 @@ class OracleCache:
     def _struct(self):
         return _Cache(self.dtype, self.k_mode, self.v_mode, self.num_blocks, self.block_size,
                       self.num_kv_heads, self.head_dim, self.k_codes.ctypes.data, self.v_codes.ctypes.data,
-                      self.k_scale.ctypes.data, self.v_scale.ctypes.data)
+                      self.k_scale.ctypes.data, self.v_scale.ctypes.data, self.group_size)
 
     def append(self, k_new_bf16: np.ndarray, v_new_bf16: np.ndarray, slot_mapping: np.ndarray) -> int:
         """k_new/v_new uint16 [N, Hkv, D] (bf16 bits); slot_mapping int64 [N]. Returns #bad slots."""
