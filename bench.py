@@ -47,6 +47,7 @@ def parse():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-prologue", action="store_true", help="skip the QK-RMSNorm + RoPE prologue timing")
     p.add_argument("--no-prefill", action="store_true", help="skip the chunked-prefill timing")
+    p.add_argument("--no-group", action="store_true", help="skip the group-wise-scale decode timing")
     return p.parse_args()
 
 
@@ -461,6 +462,27 @@ def measure_prefill(w, steps, warmup, peak, chunk=64):
             "groups_per_sequence": C // max(t for t in (8, 4, 2, 1) if C % t == 0)}
 
 
+def measure_group(w, steps, warmup, peak, group_size=64):
+    """The same workload with group-wise scales on both sides (PER_GROUP, one
+    fp32 scale per group_size channels of each K and V row): decode timed as
+    a graph of K launches, like the main line's roofline figure.  Its
+    algorithmic bytes include the group scales."""
+    import dataclasses
+    import torch
+    from decode_attention_quantized_gb300 import synth
+
+    wg = dataclasses.replace(w, k_mode=synth.PER_GROUP, v_mode=synth.PER_GROUP, group_size=group_size)
+    r = measure(wg, steps, warmup)
+    dec_ms = statistics.mean(r["decode_ms"])
+    dec_bytes = statistics.mean(r["decode_bytes"])
+    gbs = dec_bytes / (dec_ms * 1e-3) / 1e9
+    del r
+    torch.cuda.empty_cache()
+    return {"group_size": group_size, "modes": "K and V per-group", "decode_us": round(1e3 * dec_ms, 2),
+            "decode_gbs": round(gbs, 1), "frac_of_hbm": round(gbs / peak, 3),
+            "algorithmic_bytes_per_launch": int(dec_bytes)}
+
+
 def traffic_from_profiles(kernel_tag: str):
     """DRAM bytes per launch of the decode kernel from the committed ncu
     summary, if it was taken on the current kernel source."""
@@ -582,6 +604,8 @@ def run_ours(args):
         line["prologue"] = measure_prologue(w, args.steps, args.warmup, peak)
     if rank == 0 and world == 1 and not args.no_prefill:
         line["prefill"] = measure_prefill(w, max(3, args.steps // 3), args.warmup, peak)
+    if rank == 0 and world == 1 and not args.no_group:
+        line["group_scales"] = measure_group(w, args.steps, args.warmup, peak)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, windows[0], budget_s=12.0)
     if rank == 0:

@@ -64,20 +64,31 @@ int ilog2(int x) {
   return l;
 }
 int row_bytes(const kvq_cache* c) { return c->dtype == KVQ_INT4 ? c->head_dim / 2 : c->head_dim; }
+// fp32 scales per cached row of a side in mode m (0: static scales)
+int scales_per_row(const kvq_cache* c, int m) {
+  return m == KVQ_SCALE_PER_ROW ? 1 : (m == KVQ_SCALE_PER_GROUP && c->group_size > 0 ? c->head_dim / c->group_size : 0);
+}
+bool any_group(const kvq_cache* c) {
+  return c->k_mode == KVQ_SCALE_PER_GROUP || c->v_mode == KVQ_SCALE_PER_GROUP;
+}
 
 kvq_status check_cache(const kvq_cache* c) {
   if (!c) return KVQ_ERR_INVALID_ARG;
   if (c->dtype < KVQ_INT8 || c->dtype > KVQ_INT4) return KVQ_ERR_INVALID_ARG;
   for (int m : {c->k_mode, c->v_mode})
-    if (m < KVQ_SCALE_PER_ROW || m > KVQ_SCALE_PER_CHANNEL) return KVQ_ERR_INVALID_ARG;
+    if (m < KVQ_SCALE_PER_ROW || m > KVQ_SCALE_PER_GROUP) return KVQ_ERR_INVALID_ARG;
   if (c->num_blocks <= 0 || c->num_kv_heads <= 0 || c->head_dim <= 0) return KVQ_ERR_INVALID_ARG;
   if (!pow2(c->block_size) || c->block_size < 16 || c->block_size > (1 << 20)) return KVQ_ERR_INVALID_ARG;
   if ((long long)c->num_blocks * c->block_size > (1LL << 31) - 1) return KVQ_ERR_INVALID_ARG;
   if (c->head_dim != 64 && c->head_dim != 128 && c->head_dim != 256) return KVQ_ERR_UNSUPPORTED;
   if (!c->k_codes || !c->v_codes || !c->k_scale || !c->v_scale) return KVQ_ERR_INVALID_ARG;
   if (!aligned(c->k_codes, 16) || !aligned(c->v_codes, 16)) return KVQ_ERR_INVALID_ARG;
-  if (!aligned(c->k_scale, c->k_mode == KVQ_SCALE_PER_ROW ? 16 : 4)) return KVQ_ERR_INVALID_ARG;
-  if (!aligned(c->v_scale, c->v_mode == KVQ_SCALE_PER_ROW ? 16 : 4)) return KVQ_ERR_INVALID_ARG;
+  if (!aligned(c->k_scale, scales_per_row(c, c->k_mode) ? 16 : 4)) return KVQ_ERR_INVALID_ARG;
+  if (!aligned(c->v_scale, scales_per_row(c, c->v_mode) ? 16 : 4)) return KVQ_ERR_INVALID_ARG;
+  if (c->k_mode == KVQ_SCALE_PER_GROUP || c->v_mode == KVQ_SCALE_PER_GROUP) {
+    const int g = c->group_size;
+    if ((g != 32 && g != 64 && g != 128) || g > c->head_dim) return KVQ_ERR_INVALID_ARG;
+  }
   return KVQ_OK;
 }
 
@@ -133,14 +144,17 @@ struct Plan {
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
-// K and V code rows of one stage, then room for the K and V per-row scales
-// only when a side has them (a 16-row fp8 stage of head_dim 128 is then
-// 16 KB, so four CTAs with three stages each fit on an SM); 1 KB multiples
-// keep every stage on the 128-byte swizzle's alignment.
+// K and V code rows of one stage, then room for the K and V per-row or
+// per-group scales only when a side has them (a 16-row fp8 stage of head_dim
+// 128 is then 16 KB, so four CTAs with three stages each fit on an SM): K's
+// [kTile][sk_n] floats, then V's [kTile][sv_n] at kTile * max(1, sk_n)
+// floats.  1 KB multiples keep every stage on the 128-byte swizzle's
+// alignment.
 size_t stage_stride(const kvq_cache* c) {
   const size_t code = (size_t)kTile * row_bytes(c);
-  const bool row = c->k_mode == KVQ_SCALE_PER_ROW || c->v_mode == KVQ_SCALE_PER_ROW;
-  return (2 * code + (row ? 2 * kTile * 4 : 0) + 1023) / 1024 * 1024;
+  const int nk = scales_per_row(c, c->k_mode), nv = scales_per_row(c, c->v_mode);
+  const size_t sc = (nk || nv) ? (size_t)kTile * 4 * ((nk > 1 ? nk : 1) + (nv > 1 ? nv : 1)) : 0;
+  return (2 * code + sc + 1023) / 1024 * 1024;
 }
 
 size_t fixed_smem(const kvq_cache* c, int row_groups, int key_warps, int nt, int batch, int stages) {
@@ -153,6 +167,10 @@ size_t fixed_smem(const kvq_cache* c, int row_groups, int key_warps, int nt, int
   s += (size_t)stages * 2 * 8;                                                       // mbarriers
   return s;
 }
+
+// The mma.sync kernel instance: the plan's consumer layout nt (0 grouped, 2 / 3
+// wide), or -group_size for the grouped layout with per-group scales.
+int kernel_nt(const kvq_cache* c, const Plan& P) { return any_group(c) ? -c->group_size : P.nt; }
 
 cudaError_t occupancy(const kvq_cache* c, int nt, int threads, size_t smem, int* n) {
   switch (c->dtype) {
@@ -202,7 +220,10 @@ kvq_status make_plan_uncached(const kvq_cache* c, const kvq_decode_params* p, co
   Plan P{};
   const int G = p->num_q_heads / c->num_kv_heads;
   P.rows = G * p->q_tokens;
-  P.tc_nr = tc_rows(c, P.rows);
+  // a PER_GROUP side scales each channel group of a key separately, which the
+  // tensor-memory kernel's single QK^T per tile cannot: the grouped layout
+  // takes every row count
+  P.tc_nr = any_group(c) ? 0 : tc_rows(c, P.rows);
   if (P.tc_nr) {
     if (kvq_status s = make_plan_tc(c, p, dev, &P)) return s;
     const int B = p->batch > 0 ? p->batch : 1;
@@ -219,7 +240,7 @@ kvq_status make_plan_uncached(const kvq_cache* c, const kvq_decode_params* p, co
   // 17..48 rows (e.g. drafts x GQA group): the wide layout, 4 key quarters x 2
   // row halves of nt n-tiles, when a channel quarter spans >= 2 code chunks
   const bool wide_fits = c->dtype == KVQ_INT4 ? c->head_dim == 256 : c->head_dim >= 128;
-  P.nt = (wide_fits && P.row_groups >= 3 && P.row_groups <= 6) ? (P.row_groups + 1) / 2 : 0;
+  P.nt = (wide_fits && !any_group(c) && P.row_groups >= 3 && P.row_groups <= 6) ? (P.row_groups + 1) / 2 : 0;
   if (P.nt > 0) {
     P.row_groups = 2;
     P.key_warps = 4;
@@ -242,7 +263,7 @@ kvq_status make_plan_uncached(const kvq_cache* c, const kvq_decode_params* p, co
     stages = stages > kMaxStages ? kMaxStages : stages;
     const size_t smem = fixed_smem(c, P.row_groups, P.key_warps, P.nt, B, stages) + (size_t)stages * stride;
     int n = 0;
-    if (occupancy(c, P.nt, P.threads, smem, &n) != cudaSuccess) return KVQ_ERR_CUDA;
+    if (occupancy(c, kernel_nt(c, P), P.threads, smem, &n) != cudaSuccess) return KVQ_ERR_CUDA;
     if (n >= target) {
       occ = target;
       P.stages = stages;
@@ -269,8 +290,8 @@ kvq_status make_plan_uncached(const kvq_cache* c, const kvq_decode_params* p, co
 // The launch plan depends only on shapes and the device; calls with the same
 // shapes reuse it (no occupancy query on the hot path).
 struct PlanKey {
-  int dev, dtype, k_mode, v_mode, head_dim, num_kv_heads, block_size, batch, num_q_heads, q_tokens,
-      max_blocks_per_seq, max_seq_len;
+  int dev, dtype, k_mode, v_mode, group_size, head_dim, num_kv_heads, block_size, batch, num_q_heads,
+      q_tokens, max_blocks_per_seq, max_seq_len;
   bool operator==(const PlanKey& o) const { return std::memcmp(this, &o, sizeof(PlanKey)) == 0; }
 };
 constexpr int kPlanCache = 64;
@@ -285,6 +306,7 @@ kvq_status make_plan(const kvq_cache* c, const kvq_decode_params* p, const Devic
   k.dtype = c->dtype;
   k.k_mode = c->k_mode;
   k.v_mode = c->v_mode;
+  k.group_size = any_group(c) ? c->group_size : 0;
   k.head_dim = c->head_dim;
   k.num_kv_heads = c->num_kv_heads;
   k.block_size = c->block_size;
@@ -396,6 +418,7 @@ kvq_status append_common(const kvq_cache* cache, const kvq_norm_rope* k_prologue
   a.dtype = cache->dtype;
   a.k_mode = cache->k_mode;
   a.v_mode = cache->v_mode;
+  a.log2_group = any_group(cache) ? ilog2(cache->group_size) : 0;
   a.err = dev->err;
   a.k_prologue = k_prologue ? 1 : 0;
   a.latent = latent ? 1 : 0;
@@ -435,6 +458,8 @@ kvq_status decode_impl(const kvq_cache* cache, const kvq_decode_params* params, 
   a.v_scale = cache->v_scale;
   a.k_mode = cache->k_mode;
   a.v_mode = cache->v_mode;
+  a.sk_n = scales_per_row(cache, cache->k_mode);
+  a.sv_n = scales_per_row(cache, cache->v_mode);
   a.num_blocks = cache->num_blocks;
   a.block_size = cache->block_size;
   a.log2_bs = ilog2(cache->block_size);
@@ -475,9 +500,9 @@ kvq_status decode_impl(const kvq_cache* cache, const kvq_decode_params* params, 
     }
   } else {
     switch (cache->dtype) {
-      case KVQ_INT8: e = launch_decode_int8(cache->head_dim, P.nt, tk, tv, a, P.grid, P.threads, P.smem, st); break;
-      case KVQ_FP8_E4M3: e = launch_decode_fp8(cache->head_dim, P.nt, tk, tv, a, P.grid, P.threads, P.smem, st); break;
-      default: e = launch_decode_int4(cache->head_dim, P.nt, tk, tv, a, P.grid, P.threads, P.smem, st); break;
+      case KVQ_INT8: e = launch_decode_int8(cache->head_dim, kernel_nt(cache, P), tk, tv, a, P.grid, P.threads, P.smem, st); break;
+      case KVQ_FP8_E4M3: e = launch_decode_fp8(cache->head_dim, kernel_nt(cache, P), tk, tv, a, P.grid, P.threads, P.smem, st); break;
+      default: e = launch_decode_int4(cache->head_dim, kernel_nt(cache, P), tk, tv, a, P.grid, P.threads, P.smem, st); break;
     }
   }
   return from_cuda(e);
@@ -596,7 +621,9 @@ KVQ_API kvq_status kvq_combine(const kvq_cache* cache, const kvq_decode_params* 
   a.part_o = reinterpret_cast<const float*>(ws + P.ws_plan + P.ws_lse);
   a.head_sink = head_sink;
   a.v_mode = cache->v_mode;
-  a.v_scale = cache->v_mode == KVQ_SCALE_PER_ROW ? nullptr : cache->v_scale;
+  // per-row and per-group V scales are applied inside the decode kernel
+  a.v_scale = (cache->v_mode == KVQ_SCALE_PER_ROW || cache->v_mode == KVQ_SCALE_PER_GROUP) ? nullptr
+                                                                                          : cache->v_scale;
   a.out = static_cast<uint16_t*>(out);
   a.lse_out = lse_out;
   a.batch = params->batch;

@@ -4,8 +4,13 @@
 // onnxruntime PR #32515), optionally behind the fused QK-RMSNorm + RoPE
 // prologue on K (QkNormRotaryTNH, PR #29912), which also runs alone on Q.
 //
+// Per-group scales (the group-wise scaling the kv-quant-attn page lists under
+// "Requirements and limits" as not done there) apply the per-row rule to each
+// run of group_size channels.
+//
 // One warp per (token, kv head, side): each lane holds D/32 consecutive
-// channels, the row's absmax is a warp max-reduction (exact, order free), the
+// channels, the row's absmax is a warp max-reduction (exact, order free; a
+// group's over the lanes that hold it), the
 // scale and every code use IEEE fp32 division (never a reciprocal multiply,
 // which overflows for subnormal scales), codes round half to even.
 #include <cuda_bf16.h>
@@ -204,6 +209,17 @@ __global__ void __launch_bounds__(256) append_kernel(const AppendArgs a) {
 #pragma unroll
     for (int e = 0; e < E; ++e) s[e] = rs;
     if (lane == 0) sc[ridx] = rs;
+  } else if (mode == KVQ_SCALE_PER_GROUP) {
+    // the same per run of G channels: G / E consecutive lanes hold a group
+    const int gl = (1 << a.log2_group) / E;
+    float amax = 0.0f;
+#pragma unroll
+    for (int e = 0; e < E; ++e) amax = fmaxf(amax, fabsf(x[e]));
+    for (int o = gl >> 1; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    const float rs = __fdiv_rn(amax, qmax);
+#pragma unroll
+    for (int e = 0; e < E; ++e) s[e] = rs;
+    if ((lane & (gl - 1)) == 0) sc[ridx * (size_t)(D >> a.log2_group) + lane / gl] = rs;
   } else if (mode == KVQ_SCALE_PER_TENSOR) {
     const float t = sc[0];
 #pragma unroll

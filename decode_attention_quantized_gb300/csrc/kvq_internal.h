@@ -42,6 +42,7 @@ struct AppendArgs {
   long long capacity;     // num_blocks * block_size
   int n_tokens, num_kv_heads, head_dim, block_size, log2_bs;
   int dtype, k_mode, v_mode;
+  int log2_group;           // PER_GROUP sides: log2 of the channels per scale group
   unsigned int* err;
   int k_prologue;           // apply `pro` to the K rows before quantizing them
   int latent;               // LATENT layout: only the K rows are written
@@ -60,9 +61,11 @@ struct DecodeArgs {
   const uint16_t* q;            // bf16 bits [B, T, Hq, D]
   const int32_t* block_table;   // [B, max_blocks_per_seq]
   const int32_t* seq_lens;      // [B]
-  const float* k_scale;         // PER_ROW array or static scales
+  const float* k_scale;         // PER_ROW / PER_GROUP array or static scales
   const float* v_scale;
   int k_mode, v_mode;
+  int sk_n, sv_n;     // fp32 scales per cached row of K / V: 1 PER_ROW, groups PER_GROUP, 0 static
+                      // (the group size itself is the kernel instance's)
   int num_blocks, block_size, log2_bs, num_kv_heads;
   int batch, num_q_heads, q_tokens, group, rows, max_blocks_per_seq, max_seq_len;
   float sm_scale, softcap;

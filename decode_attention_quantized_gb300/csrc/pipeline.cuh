@@ -213,10 +213,13 @@ __device__ void produce(const DecodeArgs& a, const Slice<Gm::KEYS>& sp, const CU
     publish_slice(a, pl_pre, pl_misc);
     waited = true;
   };
-  const bool k_row = a.k_mode == KVQ_SCALE_PER_ROW, v_row = a.v_mode == KVQ_SCALE_PER_ROW;
+  // per-row / per-group scales: nk (nv) floats per K (V) row, K's [KT][nk]
+  // after the codes, V's [KT][nv] at KT * max(1, nk) floats after that
+  const int nk = a.sk_n, nv = a.sv_n;
+  const uint32_t v_sc = 2 * Gm::CODE_BYTES + KT * 4 * (nk > 1 ? nk : 1);
   const int Hkv = a.num_kv_heads;
   const int seg_rows = min(a.block_size, kTile);  // rows of one TMA box
-  const uint32_t seg_bytes = (uint32_t)seg_rows * (2 * Gm::DP + (k_row ? 4 : 0) + (v_row ? 4 : 0));
+  const uint32_t seg_bytes = (uint32_t)seg_rows * (2 * Gm::DP + 4 * nk + 4 * nv);
   const uint32_t S = (uint32_t)a.stages;
   uint32_t it = 0;
   int ok = 1;
@@ -288,11 +291,11 @@ __device__ void produce(const DecodeArgs& a, const Slice<Gm::KEYS>& sp, const CU
               ptx::tma_load_4d(dk + Gm::CODE_BYTES, tmv, sl * Gm::SPAN, row0, h, blk[s], &bar_full[stage]);
             }
             const size_t srow = ((size_t)blk[s] * Hkv + h) * a.block_size + row0;
-            if (k_row)
-              ptx::bulk_load(st + 2 * Gm::CODE_BYTES + s * seg_rows * 4, a.k_scale + srow, seg_rows * 4,
-                             &bar_full[stage]);
-            if (v_row)
-              ptx::bulk_load(st + 2 * Gm::CODE_BYTES + KT * 4 + s * seg_rows * 4, a.v_scale + srow, seg_rows * 4,
+            if (nk)
+              ptx::bulk_load(st + 2 * Gm::CODE_BYTES + s * seg_rows * 4 * nk, a.k_scale + srow * nk,
+                             seg_rows * 4 * nk, &bar_full[stage]);
+            if (nv)
+              ptx::bulk_load(st + v_sc + s * seg_rows * 4 * nv, a.v_scale + srow * nv, seg_rows * 4 * nv,
                              &bar_full[stage]);
           }
         }
@@ -320,12 +323,12 @@ __device__ void produce(const DecodeArgs& a, const Slice<Gm::KEYS>& sp, const CU
                 ptx::tma_load_4d(dk + Gm::CODE_BYTES, tmv, sl * Gm::SPAN, row0, h, id, &bar_full[stage]);
               }
               const size_t srow = ((size_t)id * Hkv + h) * a.block_size + row0;
-              if (k_row)
-                ptx::bulk_load(st + 2 * Gm::CODE_BYTES + s * seg_rows * 4, a.k_scale + srow, seg_rows * 4,
+              if (nk)
+                ptx::bulk_load(st + 2 * Gm::CODE_BYTES + s * seg_rows * 4 * nk, a.k_scale + srow * nk,
+                               seg_rows * 4 * nk, &bar_full[stage]);
+              if (nv)
+                ptx::bulk_load(st + v_sc + s * seg_rows * 4 * nv, a.v_scale + srow * nv, seg_rows * 4 * nv,
                                &bar_full[stage]);
-              if (v_row)
-                ptx::bulk_load(st + 2 * Gm::CODE_BYTES + KT * 4 + s * seg_rows * 4, a.v_scale + srow,
-                               seg_rows * 4, &bar_full[stage]);
             }
           }
         }

@@ -19,7 +19,7 @@ from .build import LIB_PATH
 
 INT8, FP8_E4M3, INT4 = 1, 2, 3
 LAYOUT_SEPARATE, LAYOUT_LATENT = 0, 1
-PER_ROW, PER_TENSOR, PER_CHANNEL = 1, 2, 3
+PER_ROW, PER_TENSOR, PER_CHANNEL, PER_GROUP = 1, 2, 3, 4
 DEVERR_SLOT, DEVERR_BLOCK_ID, DEVERR_SEQ_LEN, DEVERR_TIMEOUT, DEVERR_POSITION = 0x1, 0x2, 0x4, 0x8, 0x10
 STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "workspace too small", 4: "CUDA error",
           5: "device timeout"}
@@ -37,7 +37,7 @@ class CacheDesc(ctypes.Structure):
                 ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
                 ("k_codes", ctypes.c_void_p), ("v_codes", ctypes.c_void_p),
                 ("k_scale", ctypes.c_void_p), ("v_scale", ctypes.c_void_p),
-                ("layout", ctypes.c_int32), ("v_head_size", ctypes.c_int32)]
+                ("layout", ctypes.c_int32), ("v_head_size", ctypes.c_int32), ("group_size", ctypes.c_int32)]
 
 
 class DecodeParams(ctypes.Structure):
@@ -116,15 +116,19 @@ class QuantizedPagedCache:
     """A quantized paged KV cache in device memory (torch allocates it).
 
     codes uint8 [num_blocks, Hkv, block_size, Dp]; PER_ROW scales fp32
-    [num_blocks, Hkv, block_size]; static scales as given ([1] or [Hkv, D])."""
+    [num_blocks, Hkv, block_size]; PER_GROUP scales fp32 [num_blocks, Hkv,
+    block_size, D // group_size]; static scales as given ([1] or [Hkv, D])."""
 
     def __init__(self, dtype: int, k_mode: int, v_mode: int, num_blocks: int, block_size: int,
                  num_kv_heads: int, head_dim: int, *, device="cuda", k_static: Optional[torch.Tensor] = None,
-                 v_static: Optional[torch.Tensor] = None, latent: bool = False, v_head_size: int = 0):
+                 v_static: Optional[torch.Tensor] = None, latent: bool = False, v_head_size: int = 0,
+                 group_size: int = 0):
         """latent: one cache (absorbed MLA); V is the leading v_head_size channels
-        of each K row, with K's scales, and no V arrays are allocated."""
+        of each K row, with K's scales, and no V arrays are allocated.
+        group_size: channels per scale group of a PER_GROUP side (32, 64, 128)."""
         self.layout = LAYOUT_LATENT if latent else LAYOUT_SEPARATE
         self.v_head_size = v_head_size
+        self.group_size = int(group_size)
         if latent:
             v_mode = k_mode
         self.dtype, self.k_mode, self.v_mode = dtype, k_mode, v_mode
@@ -138,6 +142,11 @@ class QuantizedPagedCache:
         def scales(mode, static):
             if mode == PER_ROW:
                 return torch.zeros((num_blocks, num_kv_heads, block_size), dtype=torch.float32, device=device)
+            if mode == PER_GROUP:
+                if group_size <= 0 or head_dim % group_size:
+                    raise ValueError("PER_GROUP needs a group_size dividing head_dim")
+                return torch.zeros((num_blocks, num_kv_heads, block_size, head_dim // group_size),
+                                   dtype=torch.float32, device=device)
             if static is None:
                 raise ValueError("static scale mode needs a scale tensor")
             want = (1,) if mode == PER_TENSOR else (num_kv_heads, head_dim)
@@ -149,7 +158,8 @@ class QuantizedPagedCache:
     def desc(self) -> CacheDesc:
         return CacheDesc(self.dtype, self.k_mode, self.v_mode, self.num_blocks, self.block_size,
                          self.num_kv_heads, self.head_dim, self.k_codes.data_ptr(), self.v_codes.data_ptr(),
-                         self.k_scale.data_ptr(), self.v_scale.data_ptr(), self.layout, self.v_head_size)
+                         self.k_scale.data_ptr(), self.v_scale.data_ptr(), self.layout, self.v_head_size,
+                         self.group_size)
 
     @property
     def out_dim(self) -> int:

@@ -35,7 +35,7 @@ import numpy as np
 import torch
 
 INT8, FP8_E4M3, INT4 = 1, 2, 3
-PER_ROW, PER_TENSOR, PER_CHANNEL = 1, 2, 3
+PER_ROW, PER_TENSOR, PER_CHANNEL, PER_GROUP = 1, 2, 3, 4
 QMAX = {INT8: 127.0, INT4: 7.0, FP8_E4M3: 448.0}
 
 
@@ -75,6 +75,7 @@ class Workload:
     use_sink: bool = False
     k_channel_lognormal: float = 0.0   # sigma of per-(h, d) K factors (0: none)
     seed: int = 0
+    group_size: int = 0                # channels per scale group of a PER_GROUP side
 
     @property
     def group(self) -> int:
@@ -151,7 +152,7 @@ def calibrate_static(w: Workload, device, which: str) -> Optional[torch.Tensor]:
     """Static fp32 scale of side `which` ('k' or 'v') calibrated on the drawn rows:
     PER_TENSOR max|x|/qmax ([1]); PER_CHANNEL max_t |x[t,h,d]|/qmax ([Hkv, D])."""
     mode = w.k_mode if which == "k" else w.v_mode
-    if mode == PER_ROW:
+    if mode in (PER_ROW, PER_GROUP):
         return None
     amax = torch.zeros((w.num_kv_heads, w.head_dim), dtype=torch.float32, device=device)
     for b in range(w.batch):
@@ -248,7 +249,9 @@ def step_bytes(w: Workload, window: int = 0) -> dict:
         keys += max(0, L - lo)
         if L > lo:
             pages += (L - 1) // w.block_size - lo // w.block_size + 1
-    scales = (4 if w.k_mode == PER_ROW else 0) + (4 if w.v_mode == PER_ROW else 0)
+    def scale_bytes(mode):
+        return 4 if mode == PER_ROW else (4 * (w.head_dim // w.group_size) if mode == PER_GROUP else 0)
+    scales = scale_bytes(w.k_mode) + scale_bytes(w.v_mode)
     per_key = 2 * w.row_bytes() + scales
     qo = w.batch * w.q_tokens * w.num_q_heads * w.head_dim * 2
     new = w.batch * w.q_tokens

@@ -28,7 +28,7 @@ class GpuWorkload:
         self.k_static, self.v_static = k_static, v_static
         self.cache = kvq.QuantizedPagedCache(w.dtype, w.k_mode, w.v_mode, w.num_blocks, w.block_size,
                                              w.num_kv_heads, w.head_dim, device=device, k_static=k_static,
-                                             v_static=v_static)
+                                             v_static=v_static, group_size=w.group_size)
         self.block_table = torch.from_numpy(np.ascontiguousarray(w.block_table)).to(device)
         self.seq_lens = torch.from_numpy(np.ascontiguousarray(w.seq_lens)).to(device)
         sink = w.head_sink(gen_device)

@@ -76,11 +76,16 @@ typedef enum { KVQ_INT8 = 1, KVQ_FP8_E4M3 = 2, KVQ_INT4 = 3 } kvq_dtype;
 
 /* Scale granularity: PER_ROW is one absmax scale per (token, kv head) row,
  * computed on append (kv-quant-attn "Method"; issue #29783 per-token);
- * PER_TENSOR and PER_CHANNEL are static caller-given scales (PR #29912). */
+ * PER_TENSOR and PER_CHANNEL are static caller-given scales (PR #29912);
+ * PER_GROUP applies the PER_ROW rule to each run of kvq_cache.group_size
+ * consecutive channels of a row, one scale per group (the group-wise scaling
+ * the kv-quant-attn page lists under "Requirements and limits" as not done
+ * there, which would narrow the int4 error around outlier channels). */
 typedef enum {
   KVQ_SCALE_PER_ROW = 1,
   KVQ_SCALE_PER_TENSOR = 2,
-  KVQ_SCALE_PER_CHANNEL = 3
+  KVQ_SCALE_PER_CHANNEL = 3,
+  KVQ_SCALE_PER_GROUP = 4
 } kvq_scale_mode;
 
 /* Device-side data violations, OR-ed into a per-device flag word.  The
@@ -99,8 +104,11 @@ typedef enum { KVQ_LAYOUT_SEPARATE = 0, KVQ_LAYOUT_LATENT = 1 } kvq_layout;
 
 /* The paged cache: one descriptor per layer (kv-quant-attn "Usage": one cache
  * object per layer).  All pointers are device memory owned by the caller.
- * k_scale / v_scale: PER_ROW arrays written by kvq_append, or the static
- * scales (finite and > 0: the precondition the PR #447 scale loader checks). */
+ * k_scale / v_scale: PER_ROW fp32 [num_blocks, Hkv, block_size] or PER_GROUP
+ * fp32 [num_blocks, Hkv, block_size, head_dim / group_size] arrays written by
+ * kvq_append (16-byte aligned), or the static scales (PER_TENSOR [1],
+ * PER_CHANNEL [Hkv, head_dim]; finite and > 0: the precondition the PR #447
+ * scale loader checks). */
 typedef struct {
   int32_t dtype;        /* kvq_dtype */
   int32_t k_mode;       /* kvq_scale_mode of K */
@@ -119,6 +127,10 @@ typedef struct {
   int32_t v_head_size;  /* LATENT: channels of V, a multiple of 8 in [8, head_dim]; 0 = head_dim.
                            The pages' DeepSeek-V3 example (576/512) is above this library's
                            head_dim limit of 256. */
+  int32_t group_size;   /* PER_GROUP on either side: channels per scale group, 32, 64 or 128
+                           and at most head_dim (one group size for both sides); otherwise
+                           ignored.  Decode with a PER_GROUP side runs on the mma.sync
+                           kernel's grouped layout for every query-row count. */
 } kvq_cache;
 
 /* One decode call (PagedAttention's inputs, PR #29912 Summary of Changes). */
@@ -146,7 +158,8 @@ KVQ_API const char* kvq_status_string(kvq_status status);
  * int4 nibble packing, PR #32515).
  * For each token n and kv head h, the D bf16 values of k_new[n, h, :] (and of
  * v_new) are quantized: PER_ROW scale = absmax / qmax (IEEE fp32 division,
- * qmax 127 / 7 / 448, an all-zero row stores scale 0 and zero codes), then
+ * qmax 127 / 7 / 448, an all-zero row stores scale 0 and zero codes; PER_GROUP
+ * the same over each group of group_size channels), then
  * code = clamp(round_half_even(x / scale), -qmax, qmax) for int8 / int4, or
  * the nearest e4m3 value (ties to even, finite overflow saturated to 448).
  * slot_mapping int64 [n_tokens] (device): slot < 0 skips the token (padding);

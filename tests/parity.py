@@ -39,7 +39,7 @@ class OracleSide:
         ks = None if k_static is None else k_static.detach().cpu().numpy()
         vs = None if v_static is None else v_static.detach().cpu().numpy()
         self.cache = orc.OracleCache(w.dtype, w.k_mode, w.v_mode, len(self.gpu_blocks), bs, w.num_kv_heads,
-                                     w.head_dim, ks, vs)
+                                     w.head_dim, ks, vs, group_size=w.group_size)
         for r, b in enumerate(self.seqs):
             L = int(w.seq_lens[b])
             if L == 0:
@@ -51,14 +51,14 @@ class OracleSide:
         self.lens = np.array([int(w.seq_lens[b]) for b in self.seqs], np.int32)
 
     def compare_cache(self, gw: GpuWorkload):
-        """Codes and per-row scales of the sampled sequences, byte for byte."""
+        """Codes and per-row / per-group scales of the sampled sequences, byte for byte."""
         ids = torch.tensor(self.gpu_blocks, dtype=torch.long, device=gw.cache.k_codes.device)
         for name in ("k_codes", "v_codes"):
             g = getattr(gw.cache, name).index_select(0, ids).cpu().numpy()
             o = getattr(self.cache, name)
             assert np.array_equal(g, o), f"{name} differ in {np.count_nonzero(g != o)} bytes"
         for side, mode in (("k_scale", self.w.k_mode), ("v_scale", self.w.v_mode)):
-            if mode == synth.PER_ROW:
+            if mode in (synth.PER_ROW, synth.PER_GROUP):
                 g = getattr(gw.cache, side).index_select(0, ids).cpu().numpy()
                 o = getattr(self.cache, side)
                 assert np.array_equal(g.view(np.uint32), o.view(np.uint32)), f"{side} differ"

@@ -212,3 +212,24 @@ def test_latent_cache_needs_no_v_arrays(kvq):
     c = good_cache(kvq, layout=1, v_head_size=64, v_codes=None, v_scale=None, v_mode=0)
     # valid: nothing to append, and V arguments may be NULL
     assert lib.kvq_append(ctypes.byref(c), FAKE, None, FAKE, 0, None) == 0
+
+
+@pytest.mark.parametrize("bad", [dict(k_mode=4, group_size=0), dict(v_mode=4, group_size=16),
+                                 dict(k_mode=4, group_size=48), dict(k_mode=4, v_mode=4, group_size=256),
+                                 dict(head_dim=64, k_mode=4, group_size=128), dict(k_mode=5, group_size=32),
+                                 dict(k_mode=4, group_size=32, k_scale=FAKE + 8)])
+def test_group_scale_validation(kvq, bad):
+    """PER_GROUP: group_size 32, 64 or 128, at most head_dim; per-group scale
+    arrays 16-byte aligned (the pipeline moves them with bulk copies)."""
+    lib = kvq.load()
+    c = good_cache(kvq, **bad)
+    assert lib.kvq_append(ctypes.byref(c), FAKE, FAKE, FAKE, 4, None) == 1
+
+
+def test_group_size_is_ignored_without_a_group_side(kvq):
+    lib = kvq.load()
+    c = good_cache(kvq, group_size=48)  # PER_ROW on both sides: no group size is read
+    assert lib.kvq_append(ctypes.byref(c), FAKE, FAKE, FAKE, 0, None) == 0
+    for g in (32, 64, 128):
+        c = good_cache(kvq, k_mode=4, v_mode=4, group_size=g)
+        assert lib.kvq_append(ctypes.byref(c), FAKE, FAKE, FAKE, 0, None) == 0

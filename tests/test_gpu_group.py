@@ -1,0 +1,154 @@
+"""Group-wise scales (KVQ_SCALE_PER_GROUP) on the GPU against the fp64 oracle:
+kvq_append's codes and group scales byte for byte, kvq_decode + kvq_combine
+within the decode tolerance, over element types, head dims, group sizes,
+scale-mode pairs and query-row counts (every row count runs on the mma.sync
+kernel's grouped layout when a side is PER_GROUP)."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from decode_attention_quantized_gb300 import kvq, synth
+from decode_attention_quantized_gb300.workload import GpuWorkload
+
+from parity import OracleSide, check_lse, check_rows
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from decode_attention_quantized_gb300 import build
+    build.build()
+    return kvq.load()
+
+
+def workload(dt, km, vm, D, gsize, *, G=4, T=1, L=(150, 77, 9, 300), bs=16, seed=0, **kw):
+    # no one-key sequence by default: such a row is one dequantized V row, whose
+    # bf16 rounding errors share the scale's mantissa and alone can exceed the
+    # 2e-3 bar (2.27e-3 for the fp64 oracle's own output on one int4 input);
+    # one-token sequences are in the row-count test
+    L = np.array(L, np.int32)
+    mb = max(1, math.ceil(int(L.max()) / bs))
+    table = np.random.default_rng(seed).permutation(len(L) * mb).astype(np.int32).reshape(len(L), mb)
+    return synth.Workload("group", dt, km, vm, len(L), G * 2, 2, D, T, bs, L, table, len(L) * mb,
+                          k_channel_lognormal=0.5, seed=seed, group_size=gsize, **kw)
+
+
+def run(orc, w, *, window=0):
+    gw = GpuWorkload(w, gen_device="cpu")
+    gw.fill_history()
+    k_new, v_new, slots = gw.new_tokens()
+    params = gw.params(window=window)
+    bufs = gw.buffers(params)
+    q = w.q("cpu").to("cuda")
+    out, lse = gw.step(q, k_new, v_new, slots, params, bufs)
+    torch.cuda.synchronize()
+    assert kvq.kvq_get_device_error(clear=True) == 0
+    side = OracleSide(orc, w, range(w.batch), "cpu", gw.k_static, gw.v_static)
+    side.compare_cache(gw)
+    ref, ref_lse = side.attend(q, window=window, sink=gw.head_sink)
+    got = out.float().cpu().numpy().astype(np.float64)
+    err = check_rows(got, ref)
+    check_lse(lse.cpu().numpy().astype(np.float64), ref_lse)
+    return gw, params, bufs, q, err
+
+
+GRID = [(64, 32), (64, 64), (128, 32), (128, 64), (128, 128), (256, 32), (256, 128)]
+
+
+@pytest.mark.parametrize("dt", [kvq.INT8, kvq.FP8_E4M3, kvq.INT4])
+@pytest.mark.parametrize("D,gsize", GRID)
+def test_group_both_sides(lib, orc, dt, D, gsize):
+    run(orc, workload(dt, kvq.PER_GROUP, kvq.PER_GROUP, D, gsize, seed=D + gsize + dt))
+
+
+@pytest.mark.parametrize("dt", [kvq.INT8, kvq.FP8_E4M3, kvq.INT4])
+@pytest.mark.parametrize("km,vm", [(4, 1), (1, 4), (4, 2), (3, 4), (4, 3), (2, 4)])
+def test_group_with_the_other_modes(lib, orc, dt, km, vm):
+    run(orc, workload(dt, km, vm, 128, 32, seed=10 * km + vm + dt))
+
+
+@pytest.mark.parametrize("G,T", [(1, 1), (8, 1), (6, 8), (8, 8), (3, 5)])
+def test_group_row_counts(lib, orc, G, T):
+    """1 to 64 query rows per kv head, all on the grouped layout (row groups of
+    8, one key warp each above 32 rows)."""
+    run(orc, workload(kvq.INT4, kvq.PER_GROUP, kvq.PER_GROUP, 256, 64, G=G, T=T, L=(200, T, 66), seed=G + T))
+
+
+def test_group_with_sink_softcap_window_and_nan_bytes(lib, orc):
+    """Sink, softcap and a window together; every unwritten slot holds the e4m3
+    NaN byte and every unwritten scale slot a NaN, so the keys past each
+    sequence's end carry NaN codes and NaN group scales."""
+    w = workload(kvq.FP8_E4M3, kvq.PER_GROUP, kvq.PER_GROUP, 128, 32, G=4, T=2, L=(37, 300, 129, 8),
+                 use_sink=True, softcap=20.0, seed=3)
+    gw = GpuWorkload(w, gen_device="cpu")
+    gw.cache.k_codes.fill_(0x7F)
+    gw.cache.v_codes.fill_(0x7F)
+    gw.cache.k_scale.fill_(float("nan"))
+    gw.cache.v_scale.fill_(float("nan"))
+    gw.fill_history()
+    k_new, v_new, slots = gw.new_tokens()
+    for window in (0, 50):
+        params = gw.params(window=window)
+        bufs = gw.buffers(params)
+        q = w.q("cpu").to("cuda")
+        if window == 0:
+            out, lse = gw.step(q, k_new, v_new, slots, params, bufs)
+        else:
+            out, lse = kvq.decode_step(gw.cache, params, q, gw.block_table, gw.seq_lens, bufs, gw.head_sink)
+        torch.cuda.synchronize()
+        assert kvq.kvq_get_device_error(clear=True) == 0
+        got = out.float().cpu().numpy().astype(np.float64)
+        assert np.isfinite(got).all()
+        side = OracleSide(orc, w, range(w.batch), "cpu", gw.k_static, gw.v_static)
+        ref, ref_lse = side.attend(q, window=window, sink=gw.head_sink)
+        check_rows(got, ref)
+        check_lse(lse.cpu().numpy().astype(np.float64), ref_lse)
+
+
+def test_group_decode_is_deterministic(lib, orc):
+    gw, params, bufs, q, _ = run(orc, workload(kvq.INT8, kvq.PER_GROUP, kvq.PER_GROUP, 256, 32,
+                                               L=(3000, 17, 900), seed=9))
+    ref = bufs.out.clone()
+    for _ in range(5):
+        kvq.decode_step(gw.cache, params, q, gw.block_table, gw.seq_lens, bufs)
+        assert torch.equal(bufs.out, ref)
+
+
+def test_group_scales_narrow_the_int4_error_on_outlier_channels(lib):
+    """The page's reason for group-wise scales: with a few outlier channels
+    per kv head, int4 per-group decode is closer to unquantized attention
+    than int4 per-row decode (both measured on the GPU outputs)."""
+    B, Hkv, G, D, L, bs = 2, 2, 4, 128, 512, 16
+    gen = torch.Generator().manual_seed(1)
+    k = torch.randn(B, L, Hkv, D, generator=gen)
+    v = torch.randn(B, L, Hkv, D, generator=gen)
+    k[..., 5] *= 30.0
+    v[..., 77] *= 30.0
+    k, v = k.to(torch.bfloat16), v.to(torch.bfloat16)
+    q = torch.randn(B, 1, Hkv * G, D, generator=gen).to(torch.bfloat16)
+    mb = L // bs
+    table = torch.arange(B * mb, dtype=torch.int32).reshape(B, mb)
+    lens = torch.full((B,), L, dtype=torch.int32)
+    # unquantized reference in fp64
+    kd, vd = k.double(), v.double()
+    ref = torch.empty(B, Hkv * G, D, dtype=torch.float64)
+    for b in range(B):
+        for i in range(Hkv * G):
+            s = kd[b, :, i // G] @ q[b, 0, i].double() / math.sqrt(D)
+            ref[b, i] = torch.softmax(s, 0) @ vd[b, :, i // G]
+    errs = {}
+    for mode in (kvq.PER_ROW, kvq.PER_GROUP):
+        cache = kvq.QuantizedPagedCache(kvq.INT4, mode, mode, B * mb, bs, Hkv, D, group_size=32)
+        slots = (table.long()[:, :, None] * bs + torch.arange(bs)).reshape(B, L)
+        for b in range(B):
+            kvq.kvq_append(cache, k[b].cuda(), v[b].cuda(), slots[b].cuda())
+        params = kvq.make_params(B, Hkv * G, 1, mb)
+        bufs = kvq.alloc_decode_buffers(cache, params)
+        out, _ = kvq.decode_step(cache, params, q.cuda(), table.cuda(), lens.cuda(), bufs)
+        torch.cuda.synchronize()
+        got = out.float().cpu().double()[:, 0]
+        errs[mode] = float((got - ref).norm() / ref.norm())
+    assert errs[kvq.PER_GROUP] < 0.5 * errs[kvq.PER_ROW], errs
