@@ -765,9 +765,10 @@ __global__ void __launch_bounds__(kTcWarps * 32, 1)
         // still gives exp2(-inf) = 0).  Only then (and on a piece's first
         // tile) are exact tile maxima taken and the references moved.
         to_exponent();
-        float dmax = -INFINITY;
+        float dm[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};  // four short chains, not one long one
 #pragma unroll
-        for (int r = 0; r < NR; ++r) dmax = fmaxf(dmax, y[r]);
+        for (int r = 0; r < NR; ++r) dm[r & 3] = fmaxf(dm[r & 3], y[r]);
+        const float dmax = fmaxf(fmaxf(dm[0], dm[1]), fmaxf(dm[2], dm[3]));
         const bool ovf = __any_sync(0xffffffffu, dmax > 8.0f);
         float* f_flag = f_vmax + 8 * (it & 1);  // [4] overflow flags, [4] V-scale maxima; by tile parity
         {
