@@ -682,328 +682,325 @@ __global__ void __launch_bounds__(288, MINB)
   }
 
   // ============================================ consumers, grouped layout
-  auto grouped = [&]() {
-    const int cw = warp;
-    const int rg = cw % a.row_groups, kw = cw / a.row_groups;
-    const int g = lane >> 2, c = lane & 3;
-    const int G = a.group, Hq = a.num_q_heads;
-    const float softcap = a.softcap;
-    const float inv_cap = softcap > 0.0f ? 1.0f / softcap : 0.0f;
-    // ldmatrix row address of this lane: matrix (lane >> 3) covers keys
-    // 0-7 / 8-15 of the sub-tile and the even / odd 16-byte chunk of a pair
-    const int ld_key = ((lane >> 3) & 1) * 8 + (lane & 7);
-    const int ld_chunk = lane >> 4;
-    // group-wise scales: a group is GS channels, i.e. GS / CH code chunks of
-    // CH channels (16-byte chunks: 16 int8 / e4m3 codes or 32 int4 codes)
-    constexpr bool GRP = GS > 0;
-    const bool k_grp = GRP && a.k_mode == KVQ_SCALE_PER_GROUP, v_grp = GRP && a.v_mode == KVQ_SCALE_PER_GROUP;
-    const bool v_sc = v_row || v_grp;  // V scales enter P under the normaliser 2^F
-    constexpr int gmask = GRP ? GS - 1 : 0, NG = GRP ? D / GS : 1;
-    const int ngk = a.sk_n;
-    constexpr int CH = DT == KVQ_INT4 ? 32 : 16;
-    uint32_t it = 0;
-    bool ok = true;
+  const int cw = warp;
+  const int rg = cw % a.row_groups, kw = cw / a.row_groups;
+  const int g = lane >> 2, c = lane & 3;
+  const int G = a.group, Hq = a.num_q_heads;
+  const float softcap = a.softcap;
+  const float inv_cap = softcap > 0.0f ? 1.0f / softcap : 0.0f;
+  // ldmatrix row address of this lane: matrix (lane >> 3) covers keys
+  // 0-7 / 8-15 of the sub-tile and the even / odd 16-byte chunk of a pair
+  const int ld_key = ((lane >> 3) & 1) * 8 + (lane & 7);
+  const int ld_chunk = lane >> 4;
+  // group-wise scales: a group is GS channels, i.e. GS / CH code chunks of
+  // CH channels (16-byte chunks: 16 int8 / e4m3 codes or 32 int4 codes)
+  constexpr bool GRP = GS > 0;
+  const bool k_grp = GRP && a.k_mode == KVQ_SCALE_PER_GROUP, v_grp = GRP && a.v_mode == KVQ_SCALE_PER_GROUP;
+  const bool v_sc = v_row || v_grp;  // V scales enter P under the normaliser 2^F
+  constexpr int gmask = GRP ? GS - 1 : 0, NG = GRP ? D / GS : 1;
+  const int ngk = a.sk_n;
+  constexpr int CH = DT == KVQ_INT4 ? 32 : 16;
+  uint32_t it = 0;
+  bool ok = true;
 
-    for (int gt = t_begin, next; gt < t_end; gt = next) {
-      int b, h, k0, k1, L, u;
-      piece(gt, b, h, k0, k1, L, u, next);
+  for (int gt = t_begin, next; gt < t_end; gt = next) {
+    int b, h, k0, k1, L, u;
+    piece(gt, b, h, k0, k1, L, u, next);
 
-      // ---- Q prologue: this lane's channels of query row g of the row group
-      uint32_t qf[Gm::NMT][2];
-      const float alpha_g = dev::q_prologue<DT, D>(a, rg * 8 + g, b, h, c, qf);
-      ptx::griddep_wait();  // before the first workspace write (no-op after the first)
-      const int r0 = rg * 8 + 2 * c, r1 = r0 + 1;
-      const float al0 = __shfl_sync(0xffffffffu, alpha_g, (2 * c) * 4);
-      const float al1 = __shfl_sync(0xffffffffu, alpha_g, (2 * c + 1) * 4);
-      const float inv_g = __frcp_rn((float)G);
-      const int pos0 = r0 < a.rows ? L - T + dev::div_small(r0, inv_g) : -1;
-      const int pos1 = r1 < a.rows ? L - T + dev::div_small(r1, inv_g) : -1;
-      const int W = a.window;
+    // ---- Q prologue: this lane's channels of query row g of the row group
+    uint32_t qf[Gm::NMT][2];
+    const float alpha_g = dev::q_prologue<DT, D>(a, rg * 8 + g, b, h, c, qf);
+    ptx::griddep_wait();  // before the first workspace write (no-op after the first)
+    const int r0 = rg * 8 + 2 * c, r1 = r0 + 1;
+    const float al0 = __shfl_sync(0xffffffffu, alpha_g, (2 * c) * 4);
+    const float al1 = __shfl_sync(0xffffffffu, alpha_g, (2 * c + 1) * 4);
+    const float inv_g = __frcp_rn((float)G);
+    const int pos0 = r0 < a.rows ? L - T + dev::div_small(r0, inv_g) : -1;
+    const int pos1 = r1 < a.rows ? L - T + dev::div_small(r1, inv_g) : -1;
+    const int W = a.window;
 
-      float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.0f, l1 = 0.0f;
-      int F = v_sc ? -126 : 0;  // V-scale normaliser exponent (warp uniform)
-      float acc[Gm::NMT][4];
-  #pragma unroll
-      for (int mt = 0; mt < Gm::NMT; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.0f;
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.0f, l1 = 0.0f;
+    int F = v_sc ? -126 : 0;  // V-scale normaliser exponent (warp uniform)
+    float acc[Gm::NMT][4];
+#pragma unroll
+    for (int mt = 0; mt < Gm::NMT; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.0f;
 
-      for (int key0 = k0; key0 < k1; key0 += kTile, ++it) {
-        const int stage = (int)(it % (uint32_t)a.stages);
-        if (ok) {
-          ok = ptx::mbar_wait_bounded_inl(&bar_full[stage], (it / a.stages) & 1);
-          if (!ok) atomicOr(a.err, KVQ_DEVERR_TIMEOUT);
+    for (int key0 = k0; key0 < k1; key0 += kTile, ++it) {
+      const int stage = (int)(it % (uint32_t)a.stages);
+      if (ok) {
+        ok = ptx::mbar_wait_bounded_inl(&bar_full[stage], (it / a.stages) & 1);
+        if (!ok) atomicOr(a.err, KVQ_DEVERR_TIMEOUT);
+      }
+      const uint8_t* st = ring + (size_t)stage * a.stage_stride;
+      const uint32_t sk_base = ptx::smem_u32(st);
+      const uint32_t sv_base = sk_base + Gm::CODE_BYTES;
+      const float* ks_row = reinterpret_cast<const float*>(st + 2 * Gm::CODE_BYTES);
+      const float* vs_row = ks_row + kTile * (GRP && ngk > 1 ? ngk : 1);
+      for (int sub = kw; ok && sub < kTile / kSub; sub += a.key_warps) {
+        const int kb = key0 + sub * kSub;
+        if (kb >= k1) break;
+        const uint32_t row_off = (uint32_t)(sub * kSub + ld_key) * Gm::SPAN;
+
+        // ---- S = K Q^T for 16 keys x 8 rows (keys are MMA-M).  Per-group K:
+        // each group's partial dot product is scaled by its keys' group scales
+        // into gx as soon as the group's last chunk is in.
+        float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+        float gx[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int kk = 0; kk < Gm::NCH / 2; ++kk) {
+          const uint32_t byte = (uint32_t)(2 * kk + ld_chunk) * 16;
+          const uint32_t addr =
+              sk_base + (byte / Gm::SPAN) * (kTile * Gm::SPAN) + dev::swz<Gm::SPAN>(row_off + byte % Gm::SPAN);
+          uint32_t R[4];
+          ptx::ldmatrix_x4(R, addr);
+#pragma unroll
+          for (int h2 = 0; h2 < 2; ++h2) {
+            const int j = 2 * kk + h2;
+            const uint32_t wl = R[2 * h2], wh = R[2 * h2 + 1];
+            if constexpr (DT == KVQ_INT4) {
+#pragma unroll
+              for (int t = 0; t < 2; ++t) {
+                uint32_t A[4];
+                dev::k_frag<DT>(wl, wh, t, A);
+                if (t == 0)
+                  ptx::mma_16816(sa, A, qf[2 * j + t][0], qf[2 * j + t][1]);
+                else
+                  ptx::mma_16816(sb, A, qf[2 * j + t][0], qf[2 * j + t][1]);
+              }
+            } else {
+              uint32_t A[4];
+              dev::k_frag<DT>(wl, wh, 0, A);
+              if (h2 == 0)
+                ptx::mma_16816(sa, A, qf[j][0], qf[j][1]);
+              else
+                ptx::mma_16816(sb, A, qf[j][0], qf[j][1]);
+            }
+            if (k_grp && (((j + 1) * CH) & gmask) == 0) {
+              const int grp = (j + 1) * CH / (GRP ? GS : 1) - 1;
+              const float ga = ks_row[(sub * kSub + g) * NG + grp];
+              const float gb = ks_row[(sub * kSub + g + 8) * NG + grp];
+              gx[0] = fmaf(sa[0] + sb[0], ga, gx[0]);
+              gx[1] = fmaf(sa[1] + sb[1], ga, gx[1]);
+              gx[2] = fmaf(sa[2] + sb[2], gb, gx[2]);
+              gx[3] = fmaf(sa[3] + sb[3], gb, gx[3]);
+#pragma unroll
+              for (int e = 0; e < 4; ++e) sa[e] = sb[e] = 0.0f;
+            }
+          }
         }
-        const uint8_t* st = ring + (size_t)stage * a.stage_stride;
-        const uint32_t sk_base = ptx::smem_u32(st);
-        const uint32_t sv_base = sk_base + Gm::CODE_BYTES;
-        const float* ks_row = reinterpret_cast<const float*>(st + 2 * Gm::CODE_BYTES);
-        const float* vs_row = ks_row + kTile * (ngk > 1 ? ngk : 1);
-        for (int sub = kw; ok && sub < kTile / kSub; sub += a.key_warps) {
-          const int kb = key0 + sub * kSub;
-          if (kb >= k1) break;
-          const uint32_t row_off = (uint32_t)(sub * kSub + ld_key) * Gm::SPAN;
+        if (k_grp) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) sa[e] = gx[e];
+        }
 
-          // ---- S = K Q^T for 16 keys x 8 rows (keys are MMA-M).  Per-group K:
-          // each group's partial dot product is scaled by its keys' group scales
-          // into gx as soon as the group's last chunk is in.
-          float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
-          float gx[4] = {0.f, 0.f, 0.f, 0.f};
-  #pragma unroll
-          for (int kk = 0; kk < Gm::NCH / 2; ++kk) {
-            const uint32_t byte = (uint32_t)(2 * kk + ld_chunk) * 16;
+        // ---- logits: element e -> key kb + g (+8 for e >= 2), row 2c (+1 for odd e)
+        const int key_a = kb + g, key_b = key_a + 8;
+        float ksa = 1.0f, ksb = 1.0f;
+        if (k_row) {
+          ksa = ks_row[sub * kSub + g];
+          ksb = ks_row[sub * kSub + g + 8];
+        }
+        float x[4] = {(sa[0] + sb[0]) * al0 * ksa, (sa[1] + sb[1]) * al1 * ksa, (sa[2] + sb[2]) * al0 * ksb,
+                      (sa[3] + sb[3]) * al1 * ksb};
+        if (softcap > 0.0f) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) x[e] = softcap * dev::tanh_fast(x[e] * inv_cap) * kLog2e;
+        }
+        const bool va0 = key_a <= pos0 && (W == 0 || key_a > pos0 - W);
+        const bool va1 = key_a <= pos1 && (W == 0 || key_a > pos1 - W);
+        const bool vb0 = key_b <= pos0 && (W == 0 || key_b > pos0 - W);
+        const bool vb1 = key_b <= pos1 && (W == 0 || key_b > pos1 - W);
+        x[0] = va0 ? x[0] : -INFINITY;
+        x[1] = va1 ? x[1] : -INFINITY;
+        x[2] = vb0 ? x[2] : -INFINITY;
+        x[3] = vb1 ? x[3] : -INFINITY;
+
+        // ---- online softmax (rows 2c, 2c+1; reduce over the 8 key lanes)
+        float t0 = fmaxf(x[0], x[2]), t1 = fmaxf(x[1], x[3]);
+#pragma unroll
+        for (int o = 4; o < 32; o <<= 1) {
+          t0 = fmaxf(t0, __shfl_xor_sync(0xffffffffu, t0, o));
+          t1 = fmaxf(t1, __shfl_xor_sync(0xffffffffu, t1, o));
+        }
+        const float mn0 = fmaxf(m0, t0), mn1 = fmaxf(m1, t1);
+        const float mu0 = mn0 == -INFINITY ? 0.0f : mn0;
+        const float mu1 = mn1 == -INFINITY ? 0.0f : mn1;
+        const float c0 = ptx::fast_exp2(m0 - mu0), c1 = ptx::fast_exp2(m1 - mu1);
+        m0 = mn0;
+        m1 = mn1;
+        const float p0 = ptx::fast_exp2(x[0] - mu0), p1 = ptx::fast_exp2(x[1] - mu1);
+        const float p2 = ptx::fast_exp2(x[2] - mu0), p3 = ptx::fast_exp2(x[3] - mu1);
+        l0 = l0 * c0 + p0 + p2;
+        l1 = l1 * c1 + p1 + p3;
+
+        // ---- per-row (per-group) V scales enter P (each channel group's P),
+        // normalised by 2^F >= their maximum; keys past the sequence end get
+        // scale 0 (their scale slots may hold anything)
+        float vsa = 1.0f, vsb = 1.0f, fs = 1.0f, vinv = 1.0f;
+        if (v_sc) {
+          float ua = 0.0f, ub = 0.0f;
+          if (GRP && v_grp) {
+#pragma unroll
+            for (int gi = 0; gi < NG; ++gi) {
+              if (key_a < L) ua = fmaxf(ua, vs_row[(sub * kSub + g) * NG + gi]);
+              if (key_b < L) ub = fmaxf(ub, vs_row[(sub * kSub + g + 8) * NG + gi]);
+            }
+          } else {
+            ua = key_a < L ? vs_row[sub * kSub + g] : 0.0f;
+            ub = key_b < L ? vs_row[sub * kSub + g + 8] : 0.0f;
+          }
+          float vm = fmaxf(ua, ub);
+#pragma unroll
+          for (int o = 4; o < 32; o <<= 1) vm = fmaxf(vm, __shfl_xor_sync(0xffffffffu, vm, o));
+          if (vm > 0.0f) {
+            const int fn = min(126, max(-126, dev::ceil_log2(vm)));
+            if (fn > F) {
+              fs = (F - fn < -126) ? 0.0f : dev::pow2i(F - fn);
+              F = fn;
+            }
+          }
+          vinv = dev::pow2i(-F);
+          vsa = ua * vinv;
+          vsb = ub * vinv;
+        }
+        const float rs0 = c0 * fs, rs1 = c1 * fs;
+        if (!__all_sync(0xffffffffu, rs0 == 1.0f && rs1 == 1.0f)) {
+#pragma unroll
+          for (int mt = 0; mt < Gm::NMT; ++mt) {
+            acc[mt][0] *= rs0;
+            acc[mt][1] *= rs1;
+            acc[mt][2] *= rs0;
+            acc[mt][3] *= rs1;
+          }
+        }
+        // P (keys x rows) -> PV operand (rows x keys) by an 8x8 transpose
+        const uint32_t pb0 = ptx::movmatrix_trans(dev::pack_h2(p0 * vsa, p1 * vsa));
+        const uint32_t pb1 = ptx::movmatrix_trans(dev::pack_h2(p2 * vsb, p3 * vsb));
+
+        // ---- O += V^T P^T for all channels (channels are MMA-M).  Every key
+        // below the sequence end holds a code the quantizer wrote (never NaN);
+        // only a sub-tile reaching past it can meet stale e4m3 NaN bytes, and
+        // only there are the V codes clamped.
+        auto pv = [&](auto clamp) {
+          uint32_t qb0 = pb0, qb1 = pb1;  // this channel group's P (per-group V scales)
+#pragma unroll
+          for (int jj = 0; jj < Gm::NCH / 2; ++jj) {
+            const uint32_t byte = (uint32_t)(2 * jj + ld_chunk) * 16;
             const uint32_t addr =
-                sk_base + (byte / Gm::SPAN) * (kTile * Gm::SPAN) + dev::swz<Gm::SPAN>(row_off + byte % Gm::SPAN);
+                sv_base + (byte / Gm::SPAN) * (kTile * Gm::SPAN) + dev::swz<Gm::SPAN>(row_off + byte % Gm::SPAN);
             uint32_t R[4];
-            ptx::ldmatrix_x4(R, addr);
-  #pragma unroll
+            ptx::ldmatrix_x4_trans(R, addr);
+#pragma unroll
             for (int h2 = 0; h2 < 2; ++h2) {
-              const int j = 2 * kk + h2;
+              const int j = 2 * jj + h2;
               const uint32_t wl = R[2 * h2], wh = R[2 * h2 + 1];
+              if (v_grp && ((j * CH) & gmask) == 0) {
+                const int grp = j * CH / (GRP ? GS : 1);
+                const float ga = key_a < L ? vs_row[(sub * kSub + g) * NG + grp] * vinv : 0.0f;
+                const float gb = key_b < L ? vs_row[(sub * kSub + g + 8) * NG + grp] * vinv : 0.0f;
+                qb0 = ptx::movmatrix_trans(dev::pack_h2(p0 * ga, p1 * ga));
+                qb1 = ptx::movmatrix_trans(dev::pack_h2(p2 * gb, p3 * gb));
+              }
               if constexpr (DT == KVQ_INT4) {
-  #pragma unroll
+                const uint32_t xl = wl ^ 0x88888888u, xh = wh ^ 0x88888888u;
+#pragma unroll
                 for (int t = 0; t < 2; ++t) {
-                  uint32_t A[4];
-                  dev::k_frag<DT>(wl, wh, t, A);
-                  if (t == 0)
-                    ptx::mma_16816(sa, A, qf[2 * j + t][0], qf[2 * j + t][1]);
-                  else
-                    ptx::mma_16816(sb, A, qf[2 * j + t][0], qf[2 * j + t][1]);
+                  const uint32_t A[4] = {dev::i4pair(xl, 8 * t), dev::i4pair(xl, 8 * t + 4), dev::i4pair(xh, 8 * t),
+                                         dev::i4pair(xh, 8 * t + 4)};
+                  ptx::mma_16816(acc[2 * j + t], A, qb0, qb1);
                 }
               } else {
                 uint32_t A[4];
-                dev::k_frag<DT>(wl, wh, 0, A);
-                if (h2 == 0)
-                  ptx::mma_16816(sa, A, qf[j][0], qf[j][1]);
-                else
-                  ptx::mma_16816(sb, A, qf[j][0], qf[j][1]);
-              }
-              if (k_grp && (((j + 1) * CH) & gmask) == 0) {
-                const int grp = (j + 1) * CH / (GRP ? GS : 1) - 1;
-                const float ga = ks_row[(sub * kSub + g) * NG + grp];
-                const float gb = ks_row[(sub * kSub + g + 8) * NG + grp];
-                gx[0] = fmaf(sa[0] + sb[0], ga, gx[0]);
-                gx[1] = fmaf(sa[1] + sb[1], ga, gx[1]);
-                gx[2] = fmaf(sa[2] + sb[2], gb, gx[2]);
-                gx[3] = fmaf(sa[3] + sb[3], gb, gx[3]);
-  #pragma unroll
-                for (int e = 0; e < 4; ++e) sa[e] = sb[e] = 0.0f;
-              }
-            }
-          }
-          if (k_grp) {
-  #pragma unroll
-            for (int e = 0; e < 4; ++e) sa[e] = gx[e];
-          }
-
-          // ---- logits: element e -> key kb + g (+8 for e >= 2), row 2c (+1 for odd e)
-          const int key_a = kb + g, key_b = key_a + 8;
-          float ksa = 1.0f, ksb = 1.0f;
-          if (k_row) {
-            ksa = ks_row[sub * kSub + g];
-            ksb = ks_row[sub * kSub + g + 8];
-          }
-          float x[4] = {(sa[0] + sb[0]) * al0 * ksa, (sa[1] + sb[1]) * al1 * ksa, (sa[2] + sb[2]) * al0 * ksb,
-                        (sa[3] + sb[3]) * al1 * ksb};
-          if (softcap > 0.0f) {
-  #pragma unroll
-            for (int e = 0; e < 4; ++e) x[e] = softcap * dev::tanh_fast(x[e] * inv_cap) * kLog2e;
-          }
-          const bool va0 = key_a <= pos0 && (W == 0 || key_a > pos0 - W);
-          const bool va1 = key_a <= pos1 && (W == 0 || key_a > pos1 - W);
-          const bool vb0 = key_b <= pos0 && (W == 0 || key_b > pos0 - W);
-          const bool vb1 = key_b <= pos1 && (W == 0 || key_b > pos1 - W);
-          x[0] = va0 ? x[0] : -INFINITY;
-          x[1] = va1 ? x[1] : -INFINITY;
-          x[2] = vb0 ? x[2] : -INFINITY;
-          x[3] = vb1 ? x[3] : -INFINITY;
-
-          // ---- online softmax (rows 2c, 2c+1; reduce over the 8 key lanes)
-          float t0 = fmaxf(x[0], x[2]), t1 = fmaxf(x[1], x[3]);
-  #pragma unroll
-          for (int o = 4; o < 32; o <<= 1) {
-            t0 = fmaxf(t0, __shfl_xor_sync(0xffffffffu, t0, o));
-            t1 = fmaxf(t1, __shfl_xor_sync(0xffffffffu, t1, o));
-          }
-          const float mn0 = fmaxf(m0, t0), mn1 = fmaxf(m1, t1);
-          const float mu0 = mn0 == -INFINITY ? 0.0f : mn0;
-          const float mu1 = mn1 == -INFINITY ? 0.0f : mn1;
-          const float c0 = ptx::fast_exp2(m0 - mu0), c1 = ptx::fast_exp2(m1 - mu1);
-          m0 = mn0;
-          m1 = mn1;
-          const float p0 = ptx::fast_exp2(x[0] - mu0), p1 = ptx::fast_exp2(x[1] - mu1);
-          const float p2 = ptx::fast_exp2(x[2] - mu0), p3 = ptx::fast_exp2(x[3] - mu1);
-          l0 = l0 * c0 + p0 + p2;
-          l1 = l1 * c1 + p1 + p3;
-
-          // ---- per-row (per-group) V scales enter P (each channel group's P),
-          // normalised by 2^F >= their maximum; keys past the sequence end get
-          // scale 0 (their scale slots may hold anything)
-          float vsa = 1.0f, vsb = 1.0f, fs = 1.0f, vinv = 1.0f;
-          if (v_sc) {
-            float ua = 0.0f, ub = 0.0f;
-            if (GRP && v_grp) {
-#pragma unroll
-              for (int gi = 0; gi < NG; ++gi) {
-                if (key_a < L) ua = fmaxf(ua, vs_row[(sub * kSub + g) * NG + gi]);
-                if (key_b < L) ub = fmaxf(ub, vs_row[(sub * kSub + g + 8) * NG + gi]);
-              }
-            } else {
-              ua = key_a < L ? vs_row[sub * kSub + g] : 0.0f;
-              ub = key_b < L ? vs_row[sub * kSub + g + 8] : 0.0f;
-            }
-            float vm = fmaxf(ua, ub);
-  #pragma unroll
-            for (int o = 4; o < 32; o <<= 1) vm = fmaxf(vm, __shfl_xor_sync(0xffffffffu, vm, o));
-            if (vm > 0.0f) {
-              const int fn = min(126, max(-126, dev::ceil_log2(vm)));
-              if (fn > F) {
-                fs = (F - fn < -126) ? 0.0f : dev::pow2i(F - fn);
-                F = fn;
-              }
-            }
-            vinv = dev::pow2i(-F);
-            vsa = ua * vinv;
-            vsb = ub * vinv;
-          }
-          const float rs0 = c0 * fs, rs1 = c1 * fs;
-          if (!__all_sync(0xffffffffu, rs0 == 1.0f && rs1 == 1.0f)) {
-  #pragma unroll
-            for (int mt = 0; mt < Gm::NMT; ++mt) {
-              acc[mt][0] *= rs0;
-              acc[mt][1] *= rs1;
-              acc[mt][2] *= rs0;
-              acc[mt][3] *= rs1;
-            }
-          }
-          // P (keys x rows) -> PV operand (rows x keys) by an 8x8 transpose
-          const uint32_t pb0 = ptx::movmatrix_trans(dev::pack_h2(p0 * vsa, p1 * vsa));
-          const uint32_t pb1 = ptx::movmatrix_trans(dev::pack_h2(p2 * vsb, p3 * vsb));
-
-          // ---- O += V^T P^T for all channels (channels are MMA-M).  Every key
-          // below the sequence end holds a code the quantizer wrote (never NaN);
-          // only a sub-tile reaching past it can meet stale e4m3 NaN bytes, and
-          // only there are the V codes clamped.
-          auto pv = [&](auto clamp) {
-            uint32_t qb0 = pb0, qb1 = pb1;  // this channel group's P (per-group V scales)
-  #pragma unroll
-            for (int jj = 0; jj < Gm::NCH / 2; ++jj) {
-              const uint32_t byte = (uint32_t)(2 * jj + ld_chunk) * 16;
-              const uint32_t addr =
-                  sv_base + (byte / Gm::SPAN) * (kTile * Gm::SPAN) + dev::swz<Gm::SPAN>(row_off + byte % Gm::SPAN);
-              uint32_t R[4];
-              ptx::ldmatrix_x4_trans(R, addr);
-  #pragma unroll
-              for (int h2 = 0; h2 < 2; ++h2) {
-                const int j = 2 * jj + h2;
-                const uint32_t wl = R[2 * h2], wh = R[2 * h2 + 1];
-                if (v_grp && ((j * CH) & gmask) == 0) {
-                  const int grp = j * CH / (GRP ? GS : 1);
-                  const float ga = key_a < L ? vs_row[(sub * kSub + g) * NG + grp] * vinv : 0.0f;
-                  const float gb = key_b < L ? vs_row[(sub * kSub + g + 8) * NG + grp] * vinv : 0.0f;
-                  qb0 = ptx::movmatrix_trans(dev::pack_h2(p0 * ga, p1 * ga));
-                  qb1 = ptx::movmatrix_trans(dev::pack_h2(p2 * gb, p3 * gb));
-                }
-                if constexpr (DT == KVQ_INT4) {
-                  const uint32_t xl = wl ^ 0x88888888u, xh = wh ^ 0x88888888u;
-  #pragma unroll
-                  for (int t = 0; t < 2; ++t) {
-                    const uint32_t A[4] = {dev::i4pair(xl, 8 * t), dev::i4pair(xl, 8 * t + 4), dev::i4pair(xh, 8 * t),
-                                           dev::i4pair(xh, 8 * t + 4)};
-                    ptx::mma_16816(acc[2 * j + t], A, qb0, qb1);
-                  }
+                if constexpr (DT == KVQ_INT8) {
+                  const uint32_t xl = wl ^ 0x80808080u, xh = wh ^ 0x80808080u;
+                  A[0] = dev::i8pair(xl, 0x4240u);
+                  A[1] = dev::i8pair(xl, 0x4341u);
+                  A[2] = dev::i8pair(xh, 0x4240u);
+                  A[3] = dev::i8pair(xh, 0x4341u);
                 } else {
-                  uint32_t A[4];
-                  if constexpr (DT == KVQ_INT8) {
-                    const uint32_t xl = wl ^ 0x80808080u, xh = wh ^ 0x80808080u;
-                    A[0] = dev::i8pair(xl, 0x4240u);
-                    A[1] = dev::i8pair(xl, 0x4341u);
-                    A[2] = dev::i8pair(xh, 0x4240u);
-                    A[3] = dev::i8pair(xh, 0x4341u);
-                  } else {
-                    constexpr bool kC = decltype(clamp)::value;
-                    A[0] = dev::f8cvt<kC>(wl, 0x0020u);
-                    A[1] = dev::f8cvt<kC>(wl, 0x0031u);
-                    A[2] = dev::f8cvt<kC>(wh, 0x0020u);
-                    A[3] = dev::f8cvt<kC>(wh, 0x0031u);
-                  }
-                  ptx::mma_16816(acc[j], A, qb0, qb1);
+                  constexpr bool kC = decltype(clamp)::value;
+                  A[0] = dev::f8cvt<kC>(wl, 0x0020u);
+                  A[1] = dev::f8cvt<kC>(wl, 0x0031u);
+                  A[2] = dev::f8cvt<kC>(wh, 0x0020u);
+                  A[3] = dev::f8cvt<kC>(wh, 0x0031u);
                 }
+                ptx::mma_16816(acc[j], A, qb0, qb1);
               }
             }
-          };
-          if constexpr (DT == KVQ_FP8_E4M3) {
-            if (kb + kSub <= L) pv(dev::Flag<false>{}); else pv(dev::Flag<true>{});
-          } else {
-            pv(dev::Flag<false>{});
           }
+        };
+        if constexpr (DT == KVQ_FP8_E4M3) {
+          if (kb + kSub <= L) pv(dev::Flag<false>{}); else pv(dev::Flag<true>{});
+        } else {
+          pv(dev::Flag<false>{});
         }
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(&bar_empty[stage]);
       }
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&bar_empty[stage]);
+    }
 
-      // ---- unit end: the key warps of a row group merge their states in a
-      // fixed chain (warp 0 into 1, the result into 2, ...) through one shared
-      // slot per row group; the last warp of the chain writes the partial
-  #pragma unroll
-      for (int o = 4; o < 32; o <<= 1) {
-        l0 += __shfl_xor_sync(0xffffffffu, l0, o);
-        l1 += __shfl_xor_sync(0xffffffffu, l1, o);
+    // ---- unit end: the key warps of a row group merge their states in a
+    // fixed chain (warp 0 into 1, the result into 2, ...) through one shared
+    // slot per row group; the last warp of the chain writes the partial
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) {
+      l0 += __shfl_xor_sync(0xffffffffu, l0, o);
+      l1 += __shfl_xor_sync(0xffffffffu, l1, o);
+    }
+    float to_true = v_sc ? dev::pow2i(F) : 1.0f;  // acc * to_true = sum_j p_j dequant(v_j)
+    float* slot = scr + rg * kScrPerRg;
+    for (int k = 1; k < a.key_warps; ++k) {
+      if (kw == k - 1) {
+#pragma unroll
+        for (int mt = 0; mt < Gm::NMT; ++mt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) slot[(mt * 4 + e) * 32 + lane] = acc[mt][e] * to_true;
+        slot[(Gm::NMT * 4 + 0) * 32 + lane] = m0;
+        slot[(Gm::NMT * 4 + 1) * 32 + lane] = m1;
+        slot[(Gm::NMT * 4 + 2) * 32 + lane] = l0;
+        slot[(Gm::NMT * 4 + 3) * 32 + lane] = l1;
       }
-      float to_true = v_sc ? dev::pow2i(F) : 1.0f;  // acc * to_true = sum_j p_j dequant(v_j)
-      float* slot = scr + rg * kScrPerRg;
-      for (int k = 1; k < a.key_warps; ++k) {
-        if (kw == k - 1) {
-  #pragma unroll
-          for (int mt = 0; mt < Gm::NMT; ++mt)
-  #pragma unroll
-            for (int e = 0; e < 4; ++e) slot[(mt * 4 + e) * 32 + lane] = acc[mt][e] * to_true;
-          slot[(Gm::NMT * 4 + 0) * 32 + lane] = m0;
-          slot[(Gm::NMT * 4 + 1) * 32 + lane] = m1;
-          slot[(Gm::NMT * 4 + 2) * 32 + lane] = l0;
-          slot[(Gm::NMT * 4 + 3) * 32 + lane] = l1;
-        }
-        ptx::named_bar_sync(1, (uint32_t)n_cw * 32);
-        if (kw == k) {
-          const float pm0 = slot[(Gm::NMT * 4 + 0) * 32 + lane], pm1 = slot[(Gm::NMT * 4 + 1) * 32 + lane];
-          const float pl0 = slot[(Gm::NMT * 4 + 2) * 32 + lane], pl1 = slot[(Gm::NMT * 4 + 3) * 32 + lane];
-          const float M0 = fmaxf(m0, pm0), M1 = fmaxf(m1, pm1);
-          const float a0 = M0 == -INFINITY ? 0.0f : ptx::fast_exp2(m0 - M0);
-          const float b0 = M0 == -INFINITY ? 0.0f : ptx::fast_exp2(pm0 - M0);
-          const float a1 = M1 == -INFINITY ? 0.0f : ptx::fast_exp2(m1 - M1);
-          const float b1 = M1 == -INFINITY ? 0.0f : ptx::fast_exp2(pm1 - M1);
-  #pragma unroll
-          for (int mt = 0; mt < Gm::NMT; ++mt) {
-            acc[mt][0] = acc[mt][0] * to_true * a0 + slot[(mt * 4 + 0) * 32 + lane] * b0;
-            acc[mt][1] = acc[mt][1] * to_true * a1 + slot[(mt * 4 + 1) * 32 + lane] * b1;
-            acc[mt][2] = acc[mt][2] * to_true * a0 + slot[(mt * 4 + 2) * 32 + lane] * b0;
-            acc[mt][3] = acc[mt][3] * to_true * a1 + slot[(mt * 4 + 3) * 32 + lane] * b1;
-          }
-          l0 = l0 * a0 + pl0 * b0;
-          l1 = l1 * a1 + pl1 * b1;
-          m0 = M0;
-          m1 = M1;
-          to_true = 1.0f;
-        }
-        ptx::named_bar_sync(1, (uint32_t)n_cw * 32);
-      }
-      if (kw == a.key_warps - 1) {
-        const float f0 = l0 > 0.0f ? to_true / l0 : 0.0f, f1 = l1 > 0.0f ? to_true / l1 : 0.0f;
-        const int rr0 = rg * 8 + 2 * c, rr1 = rr0 + 1;
-        float* o0 = a.part_o + ((size_t)u * a.rows + rr0) * D;
-        float* o1 = o0 + D;
-  #pragma unroll
+      ptx::named_bar_sync(1, (uint32_t)n_cw * 32);
+      if (kw == k) {
+        const float pm0 = slot[(Gm::NMT * 4 + 0) * 32 + lane], pm1 = slot[(Gm::NMT * 4 + 1) * 32 + lane];
+        const float pl0 = slot[(Gm::NMT * 4 + 2) * 32 + lane], pl1 = slot[(Gm::NMT * 4 + 3) * 32 + lane];
+        const float M0 = fmaxf(m0, pm0), M1 = fmaxf(m1, pm1);
+        const float a0 = M0 == -INFINITY ? 0.0f : ptx::fast_exp2(m0 - M0);
+        const float b0 = M0 == -INFINITY ? 0.0f : ptx::fast_exp2(pm0 - M0);
+        const float a1 = M1 == -INFINITY ? 0.0f : ptx::fast_exp2(m1 - M1);
+        const float b1 = M1 == -INFINITY ? 0.0f : ptx::fast_exp2(pm1 - M1);
+#pragma unroll
         for (int mt = 0; mt < Gm::NMT; ++mt) {
-          const int ch = dev::out_channel<DT>(mt, 0, g);
-          if (rr0 < a.rows) *reinterpret_cast<float2*>(o0 + ch) = make_float2(acc[mt][0] * f0, acc[mt][2] * f0);
-          if (rr1 < a.rows) *reinterpret_cast<float2*>(o1 + ch) = make_float2(acc[mt][1] * f1, acc[mt][3] * f1);
+          acc[mt][0] = acc[mt][0] * to_true * a0 + slot[(mt * 4 + 0) * 32 + lane] * b0;
+          acc[mt][1] = acc[mt][1] * to_true * a1 + slot[(mt * 4 + 1) * 32 + lane] * b1;
+          acc[mt][2] = acc[mt][2] * to_true * a0 + slot[(mt * 4 + 2) * 32 + lane] * b0;
+          acc[mt][3] = acc[mt][3] * to_true * a1 + slot[(mt * 4 + 3) * 32 + lane] * b1;
         }
-        if (g == 0) {
-          if (rr0 < a.rows) a.part_lse[(size_t)u * a.rows + rr0] = l0 > 0.0f ? m0 + ptx::fast_log2(l0) : -INFINITY;
-          if (rr1 < a.rows) a.part_lse[(size_t)u * a.rows + rr1] = l1 > 0.0f ? m1 + ptx::fast_log2(l1) : -INFINITY;
-        }
+        l0 = l0 * a0 + pl0 * b0;
+        l1 = l1 * a1 + pl1 * b1;
+        m0 = M0;
+        m1 = M1;
+        to_true = 1.0f;
+      }
+      ptx::named_bar_sync(1, (uint32_t)n_cw * 32);
+    }
+    if (kw == a.key_warps - 1) {
+      const float f0 = l0 > 0.0f ? to_true / l0 : 0.0f, f1 = l1 > 0.0f ? to_true / l1 : 0.0f;
+      const int rr0 = rg * 8 + 2 * c, rr1 = rr0 + 1;
+      float* o0 = a.part_o + ((size_t)u * a.rows + rr0) * D;
+      float* o1 = o0 + D;
+#pragma unroll
+      for (int mt = 0; mt < Gm::NMT; ++mt) {
+        const int ch = dev::out_channel<DT>(mt, 0, g);
+        if (rr0 < a.rows) *reinterpret_cast<float2*>(o0 + ch) = make_float2(acc[mt][0] * f0, acc[mt][2] * f0);
+        if (rr1 < a.rows) *reinterpret_cast<float2*>(o1 + ch) = make_float2(acc[mt][1] * f1, acc[mt][3] * f1);
+      }
+      if (g == 0) {
+        if (rr0 < a.rows) a.part_lse[(size_t)u * a.rows + rr0] = l0 > 0.0f ? m0 + ptx::fast_log2(l0) : -INFINITY;
+        if (rr1 < a.rows) a.part_lse[(size_t)u * a.rows + rr1] = l1 > 0.0f ? m1 + ptx::fast_log2(l1) : -INFINITY;
       }
     }
-  };
-  grouped();
+  }
 }
 
 // Raises (never lowers) the kernel's dynamic shared-memory limit on the

@@ -152,3 +152,28 @@ def test_group_scales_narrow_the_int4_error_on_outlier_channels(lib):
         got = out.float().cpu().double()[:, 0]
         errs[mode] = float((got - ref).norm() / ref.norm())
     assert errs[kvq.PER_GROUP] < 0.5 * errs[kvq.PER_ROW], errs
+
+
+def test_group_prefill_matches_oracle(lib, orc):
+    """kvq_prefill over a per-group cache: a 24-token chunk per sequence (three
+    virtual sequences of 8), causal inside the chunk, against oracle attention."""
+    w = workload(kvq.INT8, kvq.PER_GROUP, kvq.PER_GROUP, 128, 32, G=4, T=1, L=(300, 64, 700), seed=21)
+    gw = GpuWorkload(w, gen_device="cpu")
+    gw.fill_history()
+    k_new, v_new, slots = gw.new_tokens()
+    kvq.kvq_append(gw.cache, k_new, v_new, slots)
+    B, C, Hq, D = w.batch, 24, w.num_q_heads, w.head_dim
+    q = synth.randn_bf16((B, C, Hq, D), "cpu", "group-prefill", 0, "q")
+    params = kvq.make_params(B, Hq, C, w.max_blocks)
+    ws = torch.empty(kvq.kvq_prefill_workspace_size(gw.cache, params) // 4 + 64, dtype=torch.int32, device="cuda")
+    out = torch.empty((B, C, Hq, D), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((B, C, Hq), dtype=torch.float32, device="cuda")
+    kvq.kvq_prefill(gw.cache, params, q.cuda(), gw.block_table, gw.seq_lens, None, out, lse, ws)
+    torch.cuda.synchronize()
+    assert kvq.kvq_get_device_error(clear=True) == 0
+    side = OracleSide(orc, w, range(B), "cpu", gw.k_static, gw.v_static)
+    bits = q.contiguous().view(torch.int16).numpy().view(np.uint16)
+    ref, ref_lse = side.cache.attend(bits, side.table, side.lens, q_tokens=C)
+    got = out.float().cpu().numpy().astype(np.float64)
+    check_rows(got, ref)
+    check_lse(lse.cpu().numpy().astype(np.float64), ref_lse)

@@ -24,7 +24,7 @@ def bits(t):
     return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
 
 
-def build_case(orc, *, dt, kmode, D, Dv, Hq, Hkv, lens, bs=16, seed=0):
+def build_case(orc, *, dt, kmode, D, Dv, Hq, Hkv, lens, bs=16, seed=0, group_size=0):
     B = len(lens)
     mb = max((L + bs - 1) // bs for L in lens)
     NB = B * mb + 3
@@ -36,9 +36,10 @@ def build_case(orc, *, dt, kmode, D, Dv, Hq, Hkv, lens, bs=16, seed=0):
     rows = [synth.randn_bf16((L, Hkv, D), "cpu", "latent", seed, "k", b) for b, L in enumerate(lens)]
     if kmode == kvq.PER_CHANNEL:
         ks = torch.stack([r.float().abs().amax(0) for r in rows]).amax(0) / qmax * 1.05
-    cache = kvq.QuantizedPagedCache(DT[dt], kmode, kmode, NB, bs, Hkv, D, k_static=ks, latent=True, v_head_size=Dv)
+    cache = kvq.QuantizedPagedCache(DT[dt], kmode, kmode, NB, bs, Hkv, D, k_static=ks, latent=True, v_head_size=Dv,
+                                    group_size=group_size)
     oc = orc.OracleCache(DT[dt], kmode, kmode, NB, bs, Hkv, D, None if ks is None else ks.numpy(), latent=True,
-                         v_head_size=Dv)
+                         v_head_size=Dv, group_size=group_size)
     for b, (L, k) in enumerate(zip(lens, rows)):
         t = np.arange(L)
         slots = torch.from_numpy(table[b, t // bs].astype(np.int64) * bs + t % bs)
@@ -46,7 +47,7 @@ def build_case(orc, *, dt, kmode, D, Dv, Hq, Hkv, lens, bs=16, seed=0):
         assert oc.append(bits(k), None, slots.numpy()) == 0
     assert kvq.kvq_get_device_error() == 0
     assert np.array_equal(cache.k_codes.cpu().numpy(), oc.k_codes)
-    if kmode == kvq.PER_ROW:
+    if kmode in (kvq.PER_ROW, kvq.PER_GROUP):
         assert np.array_equal(cache.k_scale.cpu().numpy().view(np.uint32), oc.k_scale.view(np.uint32))
     return cache, oc, table, np.array(lens, np.int32)
 
@@ -87,3 +88,24 @@ def test_latent_prefill_matches_oracle(lib, orc):
     ref, _ = oc.attend(bits(q), table, lens, q_tokens=C)
     rel = np.linalg.norm(out.float().cpu().numpy().astype(np.float64) - ref) / np.linalg.norm(ref)
     assert rel <= 2e-3, rel
+
+
+@pytest.mark.parametrize("dt", list(DT))
+@pytest.mark.parametrize("D,Dv,gsize,Hq,Hkv,T", [(128, 64, 32, 16, 2, 1), (256, 192, 64, 8, 4, 2)])
+def test_latent_with_group_scales(lib, orc, dt, D, Dv, gsize, Hq, Hkv, T):
+    """A LATENT cache with per-group scales: V, the leading Dv channels of the
+    K row, takes K's group scales channel group by channel group."""
+    cache, oc, table, lens = build_case(orc, dt=dt, kmode=kvq.PER_GROUP, D=D, Dv=Dv, Hq=Hq, Hkv=Hkv,
+                                        lens=[300, 41, 1000], group_size=gsize)
+    B = len(lens)
+    q = synth.randn_bf16((B, T, Hq, D), "cpu", "latent", "q-group", T)
+    params = kvq.make_params(B, Hq, T, table.shape[1])
+    bufs = kvq.alloc_decode_buffers(cache, params)
+    out, lse = kvq.decode_step(cache, params, q.cuda(), torch.from_numpy(table).cuda(), torch.from_numpy(lens).cuda(),
+                               bufs)
+    assert kvq.kvq_get_device_error() == 0
+    ref, ref_lse = oc.attend(bits(q), table, lens, q_tokens=T)
+    got = out.float().cpu().numpy().astype(np.float64)
+    rel = np.linalg.norm(got - ref) / np.linalg.norm(ref)
+    assert rel <= 2e-3, rel
+    assert np.allclose(lse.cpu().numpy(), ref_lse, atol=1e-3)
