@@ -806,14 +806,19 @@ __global__ void __launch_bounds__(288, MINB)
 #pragma unroll
           for (int e = 0; e < 4; ++e) x[e] = softcap * dev::tanh_fast(x[e] * inv_cap) * kLog2e;
         }
-        const bool va0 = key_a <= pos0 && (W == 0 || key_a > pos0 - W);
-        const bool va1 = key_a <= pos1 && (W == 0 || key_a > pos1 - W);
-        const bool vb0 = key_b <= pos0 && (W == 0 || key_b > pos0 - W);
-        const bool vb1 = key_b <= pos1 && (W == 0 || key_b > pos1 - W);
-        x[0] = va0 ? x[0] : -INFINITY;
-        x[1] = va1 ? x[1] : -INFINITY;
-        x[2] = vb0 ? x[2] : -INFINITY;
-        x[3] = vb1 ? x[3] : -INFINITY;
+        // a sub-tile whose keys every query position sees (below the first
+        // draft, inside every row's window) needs no mask; padding rows then
+        // keep finite scores, which only feed their own unwritten outputs
+        if (!(kb + kSub - 1 <= L - T && (W == 0 || kb > L - 1 - W))) {
+          const bool va0 = key_a <= pos0 && (W == 0 || key_a > pos0 - W);
+          const bool va1 = key_a <= pos1 && (W == 0 || key_a > pos1 - W);
+          const bool vb0 = key_b <= pos0 && (W == 0 || key_b > pos0 - W);
+          const bool vb1 = key_b <= pos1 && (W == 0 || key_b > pos1 - W);
+          x[0] = va0 ? x[0] : -INFINITY;
+          x[1] = va1 ? x[1] : -INFINITY;
+          x[2] = vb0 ? x[2] : -INFINITY;
+          x[3] = vb1 ? x[3] : -INFINITY;
+        }
 
         // ---- online softmax (rows 2c, 2c+1; reduce over the 8 key lanes)
         float t0 = fmaxf(x[0], x[2]), t1 = fmaxf(x[1], x[3]);
