@@ -800,8 +800,13 @@ __global__ void __launch_bounds__(288, MINB)
           ksa = ks_row[sub * kSub + g];
           ksb = ks_row[sub * kSub + g + 8];
         }
-        float x[4] = {(sa[0] + sb[0]) * al0 * ksa, (sa[1] + sb[1]) * al1 * ksa, (sa[2] + sb[2]) * al0 * ksb,
-                      (sa[3] + sb[3]) * al1 * ksb};
+        float x[4] = {(sa[0] + sb[0]) * al0, (sa[1] + sb[1]) * al1, (sa[2] + sb[2]) * al0, (sa[3] + sb[3]) * al1};
+        if (k_row) {
+          x[0] *= ksa;
+          x[1] *= ksa;
+          x[2] *= ksb;
+          x[3] *= ksb;
+        }
         if (softcap > 0.0f) {
 #pragma unroll
           for (int e = 0; e < 4; ++e) x[e] = softcap * dev::tanh_fast(x[e] * inv_cap) * kLog2e;
@@ -820,19 +825,26 @@ __global__ void __launch_bounds__(288, MINB)
           x[3] = vb1 ? x[3] : -INFINITY;
         }
 
-        // ---- online softmax (rows 2c, 2c+1; reduce over the 8 key lanes)
+        // ---- online softmax (rows 2c, 2c+1; reduce over the 8 key lanes) with
+        // lazy reference maxima: m moves (to the exact running maximum) only
+        // when a score of the sub-tile exceeds it by more than 8, so P <= 2^8
+        // in f16 and most sub-tiles skip the reduction and the rescale
         float t0 = fmaxf(x[0], x[2]), t1 = fmaxf(x[1], x[3]);
+        float c0 = 1.0f, c1 = 1.0f;
+        if (__any_sync(0xffffffffu, t0 > m0 + 8.0f || t1 > m1 + 8.0f)) {
 #pragma unroll
-        for (int o = 4; o < 32; o <<= 1) {
-          t0 = fmaxf(t0, __shfl_xor_sync(0xffffffffu, t0, o));
-          t1 = fmaxf(t1, __shfl_xor_sync(0xffffffffu, t1, o));
+          for (int o = 4; o < 32; o <<= 1) {
+            t0 = fmaxf(t0, __shfl_xor_sync(0xffffffffu, t0, o));
+            t1 = fmaxf(t1, __shfl_xor_sync(0xffffffffu, t1, o));
+          }
+          const float mn0 = fmaxf(m0, t0), mn1 = fmaxf(m1, t1);
+          c0 = ptx::fast_exp2(m0 - (mn0 == -INFINITY ? 0.0f : mn0));
+          c1 = ptx::fast_exp2(m1 - (mn1 == -INFINITY ? 0.0f : mn1));
+          m0 = mn0;
+          m1 = mn1;
         }
-        const float mn0 = fmaxf(m0, t0), mn1 = fmaxf(m1, t1);
-        const float mu0 = mn0 == -INFINITY ? 0.0f : mn0;
-        const float mu1 = mn1 == -INFINITY ? 0.0f : mn1;
-        const float c0 = ptx::fast_exp2(m0 - mu0), c1 = ptx::fast_exp2(m1 - mu1);
-        m0 = mn0;
-        m1 = mn1;
+        const float mu0 = m0 == -INFINITY ? 0.0f : m0;
+        const float mu1 = m1 == -INFINITY ? 0.0f : m1;
         const float p0 = ptx::fast_exp2(x[0] - mu0), p1 = ptx::fast_exp2(x[1] - mu1);
         const float p2 = ptx::fast_exp2(x[2] - mu0), p3 = ptx::fast_exp2(x[3] - mu1);
         l0 = l0 * c0 + p0 + p2;
@@ -879,8 +891,8 @@ __global__ void __launch_bounds__(288, MINB)
           }
         }
         // P (keys x rows) -> PV operand (rows x keys) by an 8x8 transpose
-        const uint32_t pb0 = ptx::movmatrix_trans(dev::pack_h2(p0 * vsa, p1 * vsa));
-        const uint32_t pb1 = ptx::movmatrix_trans(dev::pack_h2(p2 * vsb, p3 * vsb));
+        const uint32_t pb0 = ptx::movmatrix_trans(v_sc ? dev::pack_h2(p0 * vsa, p1 * vsa) : dev::pack_h2(p0, p1));
+        const uint32_t pb1 = ptx::movmatrix_trans(v_sc ? dev::pack_h2(p2 * vsb, p3 * vsb) : dev::pack_h2(p2, p3));
 
         // ---- O += V^T P^T for all channels (channels are MMA-M).  Every key
         // below the sequence end holds a code the quantizer wrote (never NaN);
