@@ -712,8 +712,13 @@ __global__ void __launch_bounds__(288, MINB)
     const float alpha_g = dev::q_prologue<DT, D>(a, rg * 8 + g, b, h, c, qf);
     ptx::griddep_wait();  // before the first workspace write (no-op after the first)
     const int r0 = rg * 8 + 2 * c, r1 = r0 + 1;
-    const float al0 = __shfl_sync(0xffffffffu, alpha_g, (2 * c) * 4);
-    const float al1 = __shfl_sync(0xffffffffu, alpha_g, (2 * c + 1) * 4);
+    // with a softcap the row factors also carry 1/softcap (clamped to FLT_MAX
+    // like the factors themselves, so zero codes keep zero scores), and the
+    // capped log2-domain logit is cap_l2 * tanh(x)
+    const float cf = softcap > 0.0f ? inv_cap : 1.0f;
+    const float al0 = fminf(__shfl_sync(0xffffffffu, alpha_g, (2 * c) * 4) * cf, 3.4028234e38f);
+    const float al1 = fminf(__shfl_sync(0xffffffffu, alpha_g, (2 * c + 1) * 4) * cf, 3.4028234e38f);
+    const float cap_l2 = softcap * kLog2e;
     const float inv_g = __frcp_rn((float)G);
     const int pos0 = r0 < a.rows ? L - T + dev::div_small(r0, inv_g) : -1;
     const int pos1 = r1 < a.rows ? L - T + dev::div_small(r1, inv_g) : -1;
@@ -809,7 +814,7 @@ __global__ void __launch_bounds__(288, MINB)
         }
         if (softcap > 0.0f) {
 #pragma unroll
-          for (int e = 0; e < 4; ++e) x[e] = softcap * dev::tanh_fast(x[e] * inv_cap) * kLog2e;
+          for (int e = 0; e < 4; ++e) x[e] = cap_l2 * dev::tanh_fast(x[e]);
         }
         // a sub-tile whose keys every query position sees (below the first
         // draft, inside every row's window) needs no mask; padding rows then
