@@ -66,3 +66,13 @@ def test_spec_int4_per_channel_eight_queries(lib, orc):
 def test_mixed_sink_and_alternating_window(lib, orc):
     w = synth.make("mixed")
     run_full(orc, w, windows=(w.window_for_call(0), w.window_for_call(1)))
+
+
+@pytest.mark.parametrize("name", ["gqa", "paged"])
+def test_group_scales_at_full_size(lib, orc, name):
+    """The workloads with group-wise scales on both sides (64-channel groups),
+    as bench.py's group_scales measurement runs them."""
+    import dataclasses
+    base = synth.make("gqa", ctx=262144) if name == "gqa" else synth.make(name)
+    w = dataclasses.replace(base, k_mode=kvq.PER_GROUP, v_mode=kvq.PER_GROUP, group_size=64)
+    run_full(orc, w, seqs=[0] if name == "gqa" else None)
