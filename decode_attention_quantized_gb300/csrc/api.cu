@@ -681,6 +681,13 @@ KVQ_API kvq_status kvq_prefill(const kvq_cache* cache, const kvq_decode_params* 
   return kvq_combine(cache, &v, ws, workspace_bytes - head, head_sink, out, lse_out, stream);
 }
 
+KVQ_API kvq_status kvq_check_wait_timeout(uint32_t limit_us, kvq_stream_t stream) {
+  if (limit_us == 0 || limit_us > 2000000u) return KVQ_ERR_INVALID_ARG;
+  DeviceInfo* dev;
+  if (kvq_status s = current_device(&dev)) return s;
+  return from_cuda(launch_wait_probe(dev->err, 1000ull * limit_us, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 KVQ_API kvq_status kvq_get_device_error(uint32_t* flags, int32_t clear, kvq_stream_t stream) {
   if (!flags) return KVQ_ERR_INVALID_ARG;
   DeviceInfo* dev;

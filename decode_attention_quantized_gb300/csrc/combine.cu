@@ -156,7 +156,23 @@ __global__ void __launch_bounds__(256) prefill_lens_kernel(const int32_t* seq_le
   out[i] = max(0, seq_lens[b] - C + T * (j + 1));
 }
 
+// One thread waits on an mbarrier that nothing arrives on, with the bounded
+// wait every pipeline wait uses, here given `limit_ns`: it must give up and
+// flag KVQ_DEVERR_TIMEOUT, leaving the context usable.
+__global__ void __launch_bounds__(32) wait_probe_kernel(unsigned int* err, unsigned long long limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x != 0) return;
+  ptx::mbar_init(&bar, 1);
+  ptx::fence_mbar_init();
+  if (!ptx::mbar_wait_slow(&bar, 0, limit_ns)) atomicOr(err, KVQ_DEVERR_TIMEOUT);
+}
+
 }  // namespace
+
+cudaError_t launch_wait_probe(unsigned int* err, unsigned long long limit_ns, cudaStream_t stream) {
+  wait_probe_kernel<<<1, 32, 0, stream>>>(err, limit_ns);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_prefill_lens(const int32_t* seq_lens, int32_t* out, int batch, int n, int C, int T,
                                 cudaStream_t stream) {

@@ -147,6 +147,8 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t stream);
 cudaError_t launch_norm_rope(const NormRopeArgs& a, cudaStream_t stream);
+// The bounded-wait check: one wait that runs out after limit_ns.
+cudaError_t launch_wait_probe(unsigned int* err, unsigned long long limit_ns, cudaStream_t stream);
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t stream);
 // out[b * n + j] = max(0, seq_lens[b] - C + T (j + 1)) for the n = C / T groups
 // of a prefill chunk (virtual sequences of T tokens).

@@ -62,11 +62,14 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 // false; callers record KVQ_DEVERR_TIMEOUT and keep every barrier balanced.
 // The polling loop is out of line: only the first poll is inlined at each of
 // the many wait sites, which keeps the kernels' instruction footprint small.
-static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity) {
+constexpr uint64_t kWaitLimitNs = 1500000000ull;  // the pipeline waits' bound
+
+static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity,
+                                                   uint64_t limit_ns = kWaitLimitNs) {
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t i = 0; i < (1u << 24); ++i) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 255u) == 255u && globaltimer_ns() - t0 > 1500000000ull) return false;
+    if ((i & 255u) == 255u && globaltimer_ns() - t0 > limit_ns) return false;
   }
   return false;
 }
@@ -84,7 +87,7 @@ __device__ __forceinline__ bool mbar_wait_bounded_inl(uint64_t* bar, uint32_t pa
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t i = 0; i < (1u << 24); ++i) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 255u) == 255u && globaltimer_ns() - t0 > 1500000000ull) return false;
+    if ((i & 255u) == 255u && globaltimer_ns() - t0 > kWaitLimitNs) return false;
   }
   return false;
 }

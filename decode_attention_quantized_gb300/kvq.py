@@ -63,6 +63,7 @@ SIGNATURES = {
     "kvq_decode": (_I32, [ctypes.POINTER(CacheDesc), ctypes.POINTER(DecodeParams), _VP, _VP, _VP, _VP, _SZ, _VP]),
     "kvq_combine": (_I32, [ctypes.POINTER(CacheDesc), ctypes.POINTER(DecodeParams), _VP, _SZ, _VP, _VP, _VP,
                            _VP]),
+    "kvq_check_wait_timeout": (_I32, [ctypes.c_uint32, _VP]),
     "kvq_get_device_error": (_I32, [ctypes.POINTER(ctypes.c_uint32), _I32, _VP]),
     "kvq_norm_rope_apply": (_I32, [ctypes.POINTER(NormRopeDesc), _VP, _VP, _VP, _I32, _I32, _I32, _VP]),
     "kvq_prefill_workspace_size": (_I32, [ctypes.POINTER(CacheDesc), ctypes.POINTER(DecodeParams),
@@ -265,6 +266,13 @@ def kvq_combine(cache: QuantizedPagedCache, params: DecodeParams, workspace: tor
     _check("kvq_combine", load().kvq_combine(ctypes.byref(d), ctypes.byref(params), _ptr(workspace),
                                              workspace.numel() * workspace.element_size(), _ptr(head_sink),
                                              _ptr(out), _ptr(lse_out), _stream(stream)))
+
+
+def kvq_check_wait_timeout(limit_us: int, stream=None):
+    """Launch the bounded-wait check: one wait on a barrier nothing arrives on
+    gives up after limit_us and sets DEVERR_TIMEOUT (read it with
+    kvq_get_device_error)."""
+    _check("kvq_check_wait_timeout", load().kvq_check_wait_timeout(int(limit_us), _stream(stream)))
 
 
 def kvq_get_device_error(clear: bool = True, stream=None) -> int:

@@ -312,6 +312,15 @@ KVQ_API kvq_status kvq_attend_noalloc(const kvq_cache* cache, const kvq_decode_p
                                       const int32_t* seq_lens, const float* head_sink, void* out,
                                       float* lse_out, kvq_stream_t stream);
 
+/* kvq_check_wait_timeout -- failure-detection check of the bounded waits.
+ * Launches one thread that waits on an mbarrier nothing ever arrives on, with
+ * the same bounded wait the decode pipelines use (there bounded at 1.5 s),
+ * here given limit_us microseconds (1 .. 2,000,000).  The wait gives up,
+ * KVQ_DEVERR_TIMEOUT is set in the device flag word, and the context stays
+ * usable: kvq_get_device_error then returns KVQ_ERR_DEVICE_TIMEOUT.  Nothing
+ * is faulted or trapped.  Asynchronous on `stream`. */
+KVQ_API kvq_status kvq_check_wait_timeout(uint32_t limit_us, kvq_stream_t stream);
+
 /* Reads the current device's KVQ_DEVERR_* flag word into *flags (host).  This
  * call synchronizes `stream` before reading.  clear != 0 resets the word. */
 KVQ_API kvq_status kvq_get_device_error(uint32_t* flags, int32_t clear, kvq_stream_t stream);

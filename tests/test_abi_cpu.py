@@ -233,3 +233,9 @@ def test_group_size_is_ignored_without_a_group_side(kvq):
     for g in (32, 64, 128):
         c = good_cache(kvq, k_mode=4, v_mode=4, group_size=g)
         assert lib.kvq_append(ctypes.byref(c), FAKE, FAKE, FAKE, 0, None) == 0
+
+
+def test_wait_check_rejects_bad_limits_on_the_host(kvq):
+    lib = kvq.load()
+    assert lib.kvq_check_wait_timeout(0, None) == 1
+    assert lib.kvq_check_wait_timeout(2000001, None) == 1

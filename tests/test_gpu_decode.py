@@ -268,3 +268,20 @@ def test_fp8_nan_bytes_past_the_sequence_end(lib, orc, G, T):
     ref, ref_lse = side.attend(q, window=0, sink=gw.head_sink)
     check_rows(got, ref)
     check_lse(lse.cpu().numpy().astype(np.float64), ref_lse)
+
+
+def test_bounded_wait_runs_out_and_leaves_the_context_usable(lib, orc):
+    """Failure detection without a fault: a wait on a barrier nothing arrives
+    on (the pipelines' bounded wait, here limited to 20 ms) gives up, the
+    host reads KVQ_DEVERR_TIMEOUT, and a decode afterwards is correct."""
+    import time
+    kvq.kvq_get_device_error(clear=True)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    kvq.kvq_check_wait_timeout(20000)
+    flags = kvq.kvq_get_device_error(clear=True)
+    elapsed = time.perf_counter() - t0
+    assert flags & kvq.DEVERR_TIMEOUT
+    assert 0.02 <= elapsed < 1.0, elapsed
+    assert kvq.kvq_get_device_error(clear=True) == 0
+    run_case(orc, synth.make("tiny"))
