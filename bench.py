@@ -276,36 +276,57 @@ def measure(w, steps, warmup, *, windows=(0,), e2e=False, reps=0):
 def measure_e2e(w, gws, plist, windows, steps, warmup, k_new, v_new, slots, qs):
     """Same steps through the public API with host buffers: every step copies
     its inputs (q, new K/V rows, slot_mapping, seq_lens) from pinned host memory,
-    runs append + decode + combine, and reads the output (and LSE) back."""
+    runs append + decode + combine, and reads the output and LSE back.  The
+    inputs of a step sit in one pinned staging buffer (each at a 256-byte
+    aligned offset) and travel in one copy; the output and LSE are written
+    into one device buffer and come back in one copy."""
     import torch
     from decode_attention_quantized_gb300 import kvq
 
     dev = torch.cuda.current_device()
     stream = torch.cuda.current_stream()
-    h_q = [q.cpu().pin_memory() for q in qs]
-    h_k, h_v, h_s = k_new.cpu().pin_memory(), v_new.cpu().pin_memory(), slots.cpu().pin_memory()
-    h_l = gws[0].seq_lens.cpu().pin_memory()
-    d_q = torch.empty_like(qs[0])
-    d_k, d_v, d_s = torch.empty_like(k_new), torch.empty_like(v_new), torch.empty_like(slots)
-    d_l = torch.empty_like(gws[0].seq_lens)
+    seq_lens = gws[0].seq_lens
+
+    def layout(tensors):
+        offs, off = [], 0
+        for t in tensors:
+            offs.append(off)
+            off += (t.numel() * t.element_size() + 255) // 256 * 256
+        return offs, off
+
+    ins = [qs[0], k_new, v_new, slots, seq_lens]
+    in_offs, in_bytes = layout(ins)
+    # one pinned host buffer per query draw; K/V rows, slots and lengths are the same in each
+    h_in = []
+    for q in qs:
+        h = torch.empty(in_bytes, dtype=torch.uint8).pin_memory()
+        for t, o in zip([q, k_new, v_new, slots, seq_lens], in_offs):
+            n = t.numel() * t.element_size()
+            h[o:o + n].copy_(t.contiguous().view(-1).view(torch.uint8).cpu())
+        h_in.append(h)
+    d_in = torch.empty(in_bytes, dtype=torch.uint8, device=f"cuda:{dev}")
+
+    def view(buf, off, like):
+        n = like.numel() * like.element_size()
+        return buf[off:off + n].view(like.dtype).view(like.shape)
+
+    d_q, d_k, d_v, d_s, d_l = (view(d_in, o, t) for t, o in zip(ins, in_offs))
     bufs = [gws[0].buffers(p) for p in plist]
-    h_out = torch.empty(bufs[0].out.shape, dtype=bufs[0].out.dtype).pin_memory()
-    h_lse = torch.empty(bufs[0].lse.shape, dtype=torch.float32).pin_memory()
+    outs = [bufs[0].out, bufs[0].lse]
+    out_offs, out_bytes = layout(outs)
+    d_outbuf = torch.empty(out_bytes, dtype=torch.uint8, device=f"cuda:{dev}")
+    d_out, d_lse = (view(d_outbuf, o, t) for t, o in zip(outs, out_offs))
+    h_outbuf = torch.empty(out_bytes, dtype=torch.uint8).pin_memory()
     reps = len(gws)
 
     def one(i):
         g = gws[i % reps]
         j = i % len(windows)
-        d_q.copy_(h_q[i % len(h_q)], non_blocking=True)
-        d_k.copy_(h_k, non_blocking=True)
-        d_v.copy_(h_v, non_blocking=True)
-        d_s.copy_(h_s, non_blocking=True)
-        d_l.copy_(h_l, non_blocking=True)
+        d_in.copy_(h_in[i % len(h_in)], non_blocking=True)
         kvq.kvq_append(g.cache, d_k, d_v, d_s, stream)
         kvq.kvq_decode(g.cache, plist[j], d_q, g.block_table, d_l, bufs[j].workspace, stream)
-        kvq.kvq_combine(g.cache, plist[j], bufs[j].workspace, g.head_sink, bufs[j].out, bufs[j].lse, stream)
-        h_out.copy_(bufs[j].out, non_blocking=True)
-        h_lse.copy_(bufs[j].lse, non_blocking=True)
+        kvq.kvq_combine(g.cache, plist[j], bufs[j].workspace, g.head_sink, d_out, d_lse, stream)
+        h_outbuf.copy_(d_outbuf, non_blocking=True)
         stream.synchronize()
 
     for i in range(warmup):
@@ -316,8 +337,8 @@ def measure_e2e(w, gws, plist, windows, steps, warmup, k_new, v_new, slots, qs):
         one(warmup + i)
     torch.cuda.synchronize()
     wall = time.perf_counter() - t
-    h2d = (qs[0].numel() * 2 + k_new.numel() * 2 + v_new.numel() * 2 + slots.numel() * 8 + h_l.numel() * 4)
-    d2h = h_out.numel() * 2 + h_lse.numel() * 4
+    h2d = (qs[0].numel() * 2 + k_new.numel() * 2 + v_new.numel() * 2 + slots.numel() * 8 + seq_lens.numel() * 4)
+    d2h = d_out.numel() * 2 + d_lse.numel() * 4
     return dict(wall_s=wall, h2d=h2d, d2h=d2h)
 
 
