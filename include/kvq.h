@@ -25,7 +25,9 @@
  *  - "kv-quant-attn" page, sections "Method" and "Correctness": per-row absmax
  *    scales, one block per (batch, kv head) resolving the whole GQA group from
  *    one read, warp-private softmax state, fixed-order merge (bitwise
- *    reproducible), GQA ratio at most 8, head dimension at most 256.
+ *    reproducible), GQA ratio at most 8, head dimension at most 256; section
+ *    "Requirements and limits": the group-wise scaling it leaves undone, here
+ *    as PER_GROUP.
  *
  * Data layout (all tensors dense, row-major, innermost last):
  *   codes       uint8  [num_blocks, num_kv_heads, block_size, Dp]
@@ -35,6 +37,7 @@
  *   PER_ROW     scales fp32 [num_blocks, num_kv_heads, block_size]
  *   PER_TENSOR  scale  fp32 [1]
  *   PER_CHANNEL scales fp32 [num_kv_heads, head_dim]
+ *   PER_GROUP   scales fp32 [num_blocks, num_kv_heads, block_size, head_dim / group_size]
  *   cache slot  s = block * block_size + row
  *   q, out      bf16   [batch, q_tokens, num_q_heads, head_dim]
  *   k_new/v_new bf16   [n_tokens, num_kv_heads, head_dim]
