@@ -187,8 +187,10 @@ WIDE = [
 
 @pytest.mark.parametrize("case", WIDE, ids=lambda c: f"dt{c[0]}-D{c[1]}-rows{c[2] * c[3]}")
 def test_many_query_rows_layout(lib, orc, case):
-    """17..48 query rows per kv head (drafts x GQA group) take the layout in
-    which four key quarters share each tile's row maxima and P."""
+    """17..48 query rows per kv head (drafts x GQA group): the tensor-memory
+    kernel by default (test_gpu_wide_layout.py runs the same cases on the
+    mma.sync kernel's wide layout, in which four key quarters share each
+    tile's row maxima and P)."""
     dt, D, G, T, km, vm, cap, W, sink = case
     Hkv, bs = 2, 32
     L = np.array([300, T - 2, 129, 64, 1], np.int32)
