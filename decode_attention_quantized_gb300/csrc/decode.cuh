@@ -344,6 +344,7 @@ __global__ void __launch_bounds__(288, MINB)
       return (uint32_t)(row * 2 * D + ((((k >> 3) & ~7) | (((k >> 3) ^ row) & 7)) << 4) + (k & 7) * 2);
     };
     uint32_t it = 0;
+    RingPos rp;
     bool ok = true;
     for (int gt = t_begin, next; gt < t_end; gt = next) {
       int b, h, k0, k1, L, u;
@@ -383,10 +384,10 @@ __global__ void __launch_bounds__(288, MINB)
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) acc[mt][nt][0] = acc[mt][nt][1] = acc[mt][nt][2] = acc[mt][nt][3] = 0.0f;
 
-      for (int key0 = k0; key0 < k1; key0 += kTile, ++it) {
-        const int stage = (int)(it % (uint32_t)a.stages);
+      for (int key0 = k0; key0 < k1; key0 += kTile, ++it, rp.next(a.stages)) {
+        const int stage = (int)rp.stage;
         if (ok) {
-          ok = ptx::mbar_wait_bounded_inl(&bar_full[stage], (it / a.stages) & 1);
+          ok = ptx::mbar_wait_bounded_inl(&bar_full[stage], rp.phase);
           if (!ok) atomicOr(a.err, KVQ_DEVERR_TIMEOUT);
         }
         const uint8_t* st = ring + (size_t)stage * a.stage_stride;
@@ -701,6 +702,7 @@ __global__ void __launch_bounds__(288, MINB)
   const int ngk = a.sk_n;
   constexpr int CH = DT == KVQ_INT4 ? 32 : 16;
   uint32_t it = 0;
+  RingPos rp;
   bool ok = true;
 
   for (int gt = t_begin, next; gt < t_end; gt = next) {
@@ -730,10 +732,10 @@ __global__ void __launch_bounds__(288, MINB)
 #pragma unroll
     for (int mt = 0; mt < Gm::NMT; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.0f;
 
-    for (int key0 = k0; key0 < k1; key0 += kTile, ++it) {
-      const int stage = (int)(it % (uint32_t)a.stages);
+    for (int key0 = k0; key0 < k1; key0 += kTile, ++it, rp.next(a.stages)) {
+      const int stage = (int)rp.stage;
       if (ok) {
-        ok = ptx::mbar_wait_bounded_inl(&bar_full[stage], (it / a.stages) & 1);
+        ok = ptx::mbar_wait_bounded_inl(&bar_full[stage], rp.phase);
         if (!ok) atomicOr(a.err, KVQ_DEVERR_TIMEOUT);
       }
       const uint8_t* st = ring + (size_t)stage * a.stage_stride;

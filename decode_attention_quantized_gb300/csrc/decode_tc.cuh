@@ -300,12 +300,13 @@ __global__ void __launch_bounds__(kTcWarps * 32, 1)
     const uint32_t t_k = tmem + ((uint32_t)(32 * q) << 16) + C::K_COL;
     constexpr int HCH = Gm::NCH / 2;  // 16-byte chunks of a channel half
     uint32_t it = 0;
+    RingPos rp;
     for (int gt = sp.t_begin, next; gt < sp.t_end; gt = next) {
       int b, h, k0, k1, L, u;
       sp.piece(a, gt, b, h, k0, k1, L, u, next);
-      for (int key0 = k0; key0 < k1; key0 += KT, ++it) {
-        const uint32_t stage = it % (uint32_t)a.stages;
-        wait(&bar_full[stage], (it / a.stages) & 1);
+      for (int key0 = k0; key0 < k1; key0 += KT, ++it, rp.next(a.stages)) {
+        const uint32_t stage = rp.stage;
+        wait(&bar_full[stage], rp.phase);
         const uint8_t* st = ring + (size_t)stage * Gm::STAGE_STRIDE;
 #pragma unroll 1
         for (int half = 0; half < 2; ++half) {
@@ -350,13 +351,14 @@ __global__ void __launch_bounds__(kTcWarps * 32, 1)
     const int ld_key = ((lane >> 3) & 1) * 8 + (lane & 7), ld_chunk = lane >> 4;
     const int c = lane & 3;
     uint32_t it = 0;
+    RingPos rp;
     for (int gt = sp.t_begin, next; gt < sp.t_end; gt = next) {
       int b, h, k0, k1, L, u;
       sp.piece(a, gt, b, h, k0, k1, L, u, next);
       int F = -126;
-      for (int key0 = k0; key0 < k1; key0 += KT, ++it) {
-        const uint32_t stage = it % (uint32_t)a.stages;
-        wait(&bar_full[stage], (it / a.stages) & 1);
+      for (int key0 = k0; key0 < k1; key0 += KT, ++it, rp.next(a.stages)) {
+        const uint32_t stage = rp.stage;
+        wait(&bar_full[stage], rp.phase);
         const uint8_t* st = ring + (size_t)stage * Gm::STAGE_STRIDE;
         const uint32_t sv = ptx::smem_u32(st) + Gm::CODE_BYTES;
         uint32_t s_lo[8], s_hi[8];
@@ -586,6 +588,7 @@ __global__ void __launch_bounds__(kTcWarps * 32, 1)
     };
 
     uint32_t it = 0;
+    RingPos rp;
     int pc = 0;
     int e_u = 0, e_F = 0;  // the previous piece, for its epilogue
     uint32_t e_last = 0;
@@ -692,9 +695,9 @@ __global__ void __launch_bounds__(kTcWarps * 32, 1)
 
       float mu0 = -INFINITY, mu1 = -INFINITY;  // reference maxima of rows lane, lane + 32
       int F = v_row ? -126 : 0;                // V-scale normaliser exponent
-      for (int key0 = k0; key0 < k1; key0 += KT, ++it) {
+      for (int key0 = k0; key0 < k1; key0 += KT, ++it, rp.next(a.stages)) {
         const bool first = key0 == k0;
-        const uint32_t stage = it % (uint32_t)a.stages;
+        const uint32_t stage = rp.stage;
         const uint32_t s_col = t_lane + C::S_COL + (it & 1) * NR;
         wait(&b_qk[it & 1], (it >> 1) & 1);
         ptx::tc_fence_after();
@@ -702,7 +705,7 @@ __global__ void __launch_bounds__(kTcWarps * 32, 1)
         const int key = key0 + kk;
         float ks = 1.0f, vs = 0.0f;  // vs only sets the normaliser F here; V^T carries the scale
         if (k_row || v_row) {
-          wait(&bar_full[stage], (it / a.stages) & 1);
+          wait(&bar_full[stage], rp.phase);
           const float* sc = reinterpret_cast<const float*>(ring + (size_t)stage * Gm::STAGE_STRIDE + 2 * Gm::CODE_BYTES);
           if (k_row) ks = sc[kk];
           if (v_row && key < L) vs = sc[KT + kk];

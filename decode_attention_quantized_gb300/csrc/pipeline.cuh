@@ -47,6 +47,19 @@ __device__ __forceinline__ uint32_t swz(uint32_t o) {
 
 }  // namespace dev
 
+// Ring position of a running tile counter it: stage = it mod S and the phase
+// bit (it / S) & 1, kept by one add and one compare per tile instead of a
+// division by the run-time stage count.
+struct RingPos {
+  uint32_t stage = 0, phase = 0;
+  __device__ __forceinline__ void next(uint32_t S) {
+    if (++stage == S) {
+      stage = 0;
+      phase ^= 1u;
+    }
+  }
+};
+
 // The split plan.  Segment s = b * Hkv + h is sequence b's key range
 // [lo_b, L_b) for kv head h: n_b = ceil((L_b - lo_b) / KT) tiles.  The
 // segments laid end to end in s order make `total` tiles.  Each CTA also
@@ -222,6 +235,7 @@ __device__ void produce(const DecodeArgs& a, const Slice<Gm::KEYS>& sp, const CU
   const uint32_t seg_bytes = (uint32_t)seg_rows * (2 * Gm::DP + 4 * nk + 4 * nv);
   const uint32_t S = (uint32_t)a.stages;
   uint32_t it = 0;
+  RingPos rp;
   int ok = 1;
   for (int gt = sp.t_begin, next; gt < sp.t_end; gt = next) {
     int b, h, k0, k1, L, slot;
@@ -244,11 +258,11 @@ __device__ void produce(const DecodeArgs& a, const Slice<Gm::KEYS>& sp, const CU
         ptx::prefetch_l2(a.q + (((size_t)b * a.q_tokens + t) * a.num_q_heads + (size_t)h * a.group) * Gm::D + c * 64);
       }
     }
-    for (int key0 = k0; key0 < k1; key0 += KT, ++it) {
-      const int stage = (int)(it % S);
+    for (int key0 = k0; key0 < k1; key0 += KT, ++it, rp.next(S)) {
+      const int stage = (int)rp.stage;
       if (lane == 0 && it >= S && ok) {
-        ok = (kBurst ? ptx::mbar_wait_bounded_inl(&bar_empty[stage], ((it / S) - 1) & 1)
-                     : ptx::mbar_wait_bounded(&bar_empty[stage], ((it / S) - 1) & 1)) ? 1 : 0;
+        ok = (kBurst ? ptx::mbar_wait_bounded_inl(&bar_empty[stage], rp.phase ^ 1u)
+                     : ptx::mbar_wait_bounded(&bar_empty[stage], rp.phase ^ 1u)) ? 1 : 0;
         if (!ok) atomicOr(a.err, KVQ_DEVERR_TIMEOUT);
       }
       ok = __shfl_sync(0xffffffffu, ok, 0);
