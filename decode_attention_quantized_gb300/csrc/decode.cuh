@@ -733,9 +733,12 @@ __global__ void __launch_bounds__(288, MINB)
     for (int mt = 0; mt < Gm::NMT; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.0f;
 
     for (int key0 = k0; key0 < k1; key0 += kTile, ++it, rp.next(a.stages)) {
-      const int stage = (int)rp.stage;
+      // (the head_dim 128 group-scale instances keep the division: with the
+      // counter their code ran at half speed)
+      constexpr bool kDiv = GRP && D < 256;
+      const int stage = kDiv ? (int)(it % (uint32_t)a.stages) : (int)rp.stage;
       if (ok) {
-        ok = ptx::mbar_wait_bounded_inl(&bar_full[stage], rp.phase);
+        ok = ptx::mbar_wait_bounded_inl(&bar_full[stage], kDiv ? (it / a.stages) & 1 : rp.phase);
         if (!ok) atomicOr(a.err, KVQ_DEVERR_TIMEOUT);
       }
       const uint8_t* st = ring + (size_t)stage * a.stage_stride;
