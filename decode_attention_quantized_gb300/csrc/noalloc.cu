@@ -23,7 +23,7 @@ namespace {
 
 constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;
 
-__device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
 constexpr int kMaxDev = 64;
 std::mutex g_noalloc_mu;

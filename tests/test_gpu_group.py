@@ -14,6 +14,8 @@ from decode_attention_quantized_gb300.workload import GpuWorkload
 
 from parity import OracleSide, check_lse, check_rows
 
+from guard import guarded
+
 pytestmark = pytest.mark.gpu
 
 
@@ -165,9 +167,9 @@ def test_group_prefill_matches_oracle(lib, orc):
     B, C, Hq, D = w.batch, 24, w.num_q_heads, w.head_dim
     q = synth.randn_bf16((B, C, Hq, D), "cpu", "group-prefill", 0, "q")
     params = kvq.make_params(B, Hq, C, w.max_blocks)
-    ws = torch.empty(kvq.kvq_prefill_workspace_size(gw.cache, params) // 4 + 64, dtype=torch.int32, device="cuda")
-    out = torch.empty((B, C, Hq, D), dtype=torch.bfloat16, device="cuda")
-    lse = torch.empty((B, C, Hq), dtype=torch.float32, device="cuda")
+    ws = guarded(torch.empty((kvq.kvq_prefill_workspace_size(gw.cache, params) + 3) // 4, dtype=torch.int32, device="cuda"))
+    out = guarded(torch.empty((B, C, Hq, D), dtype=torch.bfloat16, device="cuda"))
+    lse = guarded(torch.empty((B, C, Hq), dtype=torch.float32, device="cuda"))
     kvq.kvq_prefill(gw.cache, params, q.cuda(), gw.block_table, gw.seq_lens, None, out, lse, ws)
     torch.cuda.synchronize()
     assert kvq.kvq_get_device_error(clear=True) == 0

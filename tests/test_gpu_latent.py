@@ -8,6 +8,8 @@ import torch
 
 from decode_attention_quantized_gb300 import kvq, synth
 
+from guard import guarded
+
 pytestmark = pytest.mark.gpu
 
 DT = {"int8": kvq.INT8, "fp8": kvq.FP8_E4M3, "int4": kvq.INT4}
@@ -80,8 +82,8 @@ def test_latent_prefill_matches_oracle(lib, orc):
     B, C, Hq = len(lens), 24, 16
     q = synth.randn_bf16((B, C, Hq, 256), "cpu", "latent", "prefill-q")
     params = kvq.make_params(B, Hq, C, table.shape[1])
-    ws = torch.empty(kvq.kvq_prefill_workspace_size(cache, params) // 4 + 64, dtype=torch.int32, device="cuda")
-    out = torch.empty((B, C, Hq, 192), dtype=torch.bfloat16, device="cuda")
+    ws = guarded(torch.empty((kvq.kvq_prefill_workspace_size(cache, params) + 3) // 4, dtype=torch.int32, device="cuda"))
+    out = guarded(torch.empty((B, C, Hq, 192), dtype=torch.bfloat16, device="cuda"))
     kvq.kvq_prefill(cache, params, q.cuda(), torch.from_numpy(table).cuda(), torch.from_numpy(lens).cuda(), None,
                     out, None, ws)
     assert kvq.kvq_get_device_error() == 0

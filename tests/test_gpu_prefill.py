@@ -9,6 +9,8 @@ import torch
 
 from decode_attention_quantized_gb300 import kvq, synth
 
+from guard import guarded
+
 pytestmark = pytest.mark.gpu
 
 DT = {"int8": kvq.INT8, "fp8": kvq.FP8_E4M3, "int4": kvq.INT4}
@@ -45,9 +47,9 @@ def run_prefill(orc, *, dt, D, Hq, Hkv, C, lens, bs=16, window=0, sink=False, so
     q = synth.randn_bf16((B, C, Hq, D), "cpu", "prefill", seed, "q")
     hs = torch.randn(Hq, generator=synth.generator("cpu", "prefill", seed, "sink")) if sink else None
     params = kvq.make_params(B, Hq, C, mb, window=window, softcap=softcap)
-    ws = torch.empty(kvq.kvq_prefill_workspace_size(cache, params) // 4 + 64, dtype=torch.int32, device="cuda")
-    out = torch.empty((B, C, Hq, D), dtype=torch.bfloat16, device="cuda")
-    lse = torch.empty((B, C, Hq), dtype=torch.float32, device="cuda")
+    ws = guarded(torch.empty((kvq.kvq_prefill_workspace_size(cache, params) + 3) // 4, dtype=torch.int32, device="cuda"))
+    out = guarded(torch.empty((B, C, Hq, D), dtype=torch.bfloat16, device="cuda"))
+    lse = guarded(torch.empty((B, C, Hq), dtype=torch.float32, device="cuda"))
     args = (cache, params, q.cuda(), torch.from_numpy(table).cuda(), torch.from_numpy(np.array(lens, np.int32)).cuda(),
             None if hs is None else hs.cuda(), out, lse, ws)
     kvq.kvq_prefill(*args)
