@@ -205,7 +205,9 @@ def measure(w, steps, warmup, *, windows=(0,), e2e=False, reps=0):
     k_new, v_new, slots = gws[0].new_tokens()
     nq = 8
     qs = [w.q("cuda", i).to(f"cuda:{dev}") for i in range(nq)]
-    plist = [gws[0].params(window=wd) for wd in windows]
+    # q, the block table and seq_lens are never written by the kernel before
+    # kvq_decode (kvq_append): the decode may read them while append finishes
+    plist = [gws[0].params(window=wd, flags=kvq.DECODE_EARLY_INPUTS) for wd in windows]
     bufs = [gws[0].buffers(p) for p in plist]
     stream = torch.cuda.current_stream()
 
@@ -586,7 +588,7 @@ def run_ours(args):
             "workload": describe(w),
             "cache_dtype": {1: "int8", 2: "fp8-e4m3", 3: "int4"}[w.dtype],
             "compute": "f16 x f16 -> f32 tensor-core mma, fp32 softmax",
-            "step": "kvq_append (new tokens) + kvq_decode + kvq_combine",
+            "step": "kvq_append (new tokens) + kvq_decode (flags KVQ_DECODE_EARLY_INPUTS) + kvq_combine",
             "timing": "K steps captured once in a CUDA graph and replayed between CUDA events; per-kernel "
                       "times from graphs of K launches of that kernel alone",
             "windows_per_call": list(windows),

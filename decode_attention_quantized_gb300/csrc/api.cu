@@ -2,7 +2,6 @@
 // TMA descriptor encoding and kernel launches.  No allocation, no host sync
 // (except kvq_get_device_error, which says so), no device data read back.
 #include <cmath>
-#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
@@ -121,6 +120,7 @@ kvq_status check_params(const kvq_cache* c, const kvq_decode_params* p) {
     return KVQ_ERR_INVALID_ARG;
   if (p->num_q_heads % c->num_kv_heads != 0) return KVQ_ERR_INVALID_ARG;
   if (!std::isfinite(p->sm_scale) || !std::isfinite(p->softcap) || p->softcap < 0.0f) return KVQ_ERR_INVALID_ARG;
+  if (p->flags & ~(KVQ_DECODE_EARLY_INPUTS | KVQ_DECODE_NO_TCGEN05)) return KVQ_ERR_INVALID_ARG;
   if ((long long)p->max_blocks_per_seq * c->block_size > (1LL << 30)) return KVQ_ERR_INVALID_ARG;
   if (p->num_q_heads / c->num_kv_heads > 8 || p->q_tokens > 8 || p->batch > kMaxBatch) return KVQ_ERR_UNSUPPORTED;
   // the tile space of all (sequence, kv head) ranges must index with int
@@ -182,10 +182,9 @@ cudaError_t occupancy(const kvq_cache* c, int nt, int threads, size_t smem, int*
 
 // The tensor-memory kernel takes 17..48 query rows per kv head at head_dim
 // 256 and 17..64 at head_dim 128 (its TMEM columns bound rows x head_dim);
-// KVQ_NO_TC=1 in the environment keeps such shapes on the mma.sync layouts.
-int tc_rows(const kvq_cache* c, int rows) {
-  const char* off = std::getenv("KVQ_NO_TC");
-  if (off && off[0] == '1') return 0;
+// KVQ_DECODE_NO_TCGEN05 keeps such shapes on the mma.sync layouts.
+int tc_rows(const kvq_cache* c, const kvq_decode_params* p, int rows) {
+  if (p->flags & KVQ_DECODE_NO_TCGEN05) return 0;
   if (rows < 17) return 0;
   if (c->head_dim == 256 && rows <= 48) return rows <= 32 ? 32 : 48;
   if (c->head_dim == 128 && rows <= 64) return rows <= 32 ? 32 : (rows <= 48 ? 48 : 64);
@@ -223,7 +222,7 @@ kvq_status make_plan_uncached(const kvq_cache* c, const kvq_decode_params* p, co
   // a PER_GROUP side scales each channel group of a key separately, which the
   // tensor-memory kernel's single QK^T per tile cannot: the grouped layout
   // takes every row count
-  P.tc_nr = any_group(c) ? 0 : tc_rows(c, P.rows);
+  P.tc_nr = any_group(c) ? 0 : tc_rows(c, p, P.rows);
   if (P.tc_nr) {
     if (kvq_status s = make_plan_tc(c, p, dev, &P)) return s;
     const int B = p->batch > 0 ? p->batch : 1;
@@ -291,7 +290,7 @@ kvq_status make_plan_uncached(const kvq_cache* c, const kvq_decode_params* p, co
 // shapes reuse it (no occupancy query on the hot path).
 struct PlanKey {
   int dev, dtype, k_mode, v_mode, group_size, head_dim, num_kv_heads, block_size, batch, num_q_heads,
-      q_tokens, max_blocks_per_seq, max_seq_len;
+      q_tokens, max_blocks_per_seq, max_seq_len, no_tc;
   bool operator==(const PlanKey& o) const { return std::memcmp(this, &o, sizeof(PlanKey)) == 0; }
 };
 constexpr int kPlanCache = 64;
@@ -315,6 +314,7 @@ kvq_status make_plan(const kvq_cache* c, const kvq_decode_params* p, const Devic
   k.q_tokens = p->q_tokens;
   k.max_blocks_per_seq = p->max_blocks_per_seq;
   k.max_seq_len = p->max_seq_len;
+  k.no_tc = (p->flags & KVQ_DECODE_NO_TCGEN05) ? 1 : 0;
   {
     std::lock_guard<std::mutex> lk(g_mu);
     for (int i = 0; i < g_plan_count; ++i)
@@ -426,9 +426,11 @@ kvq_status append_common(const kvq_cache* cache, const kvq_norm_rope* k_prologue
   return from_cuda(launch_append(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
-// kvq_decode with the block-table row of sequence b at b / bt_div and, when
-// early_reads is 0, seq_lens read only after the wait on the preceding grid
-// (kvq_prefill's virtual sequences, whose lengths that grid writes).
+// kvq_decode with the block-table row of sequence b at b / bt_div.  With
+// early_reads 1, q, the block table, seq_lens and the static scales are read
+// before the wait on the preceding grid (KVQ_DECODE_EARLY_INPUTS); with 0,
+// every input is read after it (the default, and kvq_prefill's virtual
+// sequences, whose lengths that grid writes).
 kvq_status decode_impl(const kvq_cache* cache, const kvq_decode_params* params, const void* q,
                        const int32_t* block_table, const int32_t* seq_lens, int bt_div, int early_reads,
                        void* workspace, size_t workspace_bytes, kvq_stream_t stream) {
@@ -594,7 +596,8 @@ KVQ_API kvq_status kvq_decode_workspace_size(const kvq_cache* cache, const kvq_d
 KVQ_API kvq_status kvq_decode(const kvq_cache* cache, const kvq_decode_params* params, const void* q,
                               const int32_t* block_table, const int32_t* seq_lens, void* workspace,
                               size_t workspace_bytes, kvq_stream_t stream) {
-  return decode_impl(cache, params, q, block_table, seq_lens, 1, 1, workspace, workspace_bytes, stream);
+  const int early = (params && (params->flags & KVQ_DECODE_EARLY_INPUTS)) ? 1 : 0;
+  return decode_impl(cache, params, q, block_table, seq_lens, 1, early, workspace, workspace_bytes, stream);
 }
 
 KVQ_API kvq_status kvq_combine(const kvq_cache* cache, const kvq_decode_params* params, const void* workspace,

@@ -69,11 +69,11 @@ class GpuWorkload:
         return (torch.cat(ks).to(self.device).contiguous(), torch.cat(vs).to(self.device).contiguous(),
                 torch.from_numpy(np.concatenate(sl)).to(self.device))
 
-    def params(self, window: int = 0, max_seq_len: Optional[int] = None):
+    def params(self, window: int = 0, max_seq_len: Optional[int] = None, flags: int = 0):
         w = self.w
         return kvq.make_params(w.batch, w.num_q_heads, w.q_tokens, w.max_blocks,
                                max_seq_len=self.max_seq_len if max_seq_len is None else max_seq_len,
-                               softcap=w.softcap, window=window)
+                               softcap=w.softcap, window=window, flags=flags)
 
     def buffers(self, params):
         return kvq.alloc_decode_buffers(self.cache, params)

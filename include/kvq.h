@@ -151,7 +151,29 @@ typedef struct {
   float softcap;              /* > 0: logit s -> softcap * tanh(s / softcap); 0 = off */
   int32_t window;             /* > 0: keep the `window` most recent keys up to and
                                  including the query position; 0 = off */
+  uint32_t flags;             /* KVQ_DECODE_* bits below; 0 = the defaults */
 } kvq_decode_params;
+
+/* kvq_decode_params.flags.
+ *
+ * KVQ_DECODE_EARLY_INPUTS: every kvq kernel may start while the kernel enqueued
+ * just before it on the stream finishes (programmatic dependent launch).  By
+ * default kvq_decode reads nothing until that preceding kernel has completed.
+ * With this bit it reads q, block_table, seq_lens and the static scales
+ * (PER_TENSOR / PER_CHANNEL) while the preceding kernel is still running, and
+ * waits only before it reads the cache and writes the workspace: the split plan
+ * and the query prologue then overlap that kernel's tail.  Set it only when
+ * none of those inputs is written by the operation enqueued just before
+ * kvq_decode on the stream: e.g. they were copied from the host, or that
+ * operation is kvq_append (which writes only the cache).  It must not be set
+ * when that operation is kvq_norm_rope_apply producing q, or any kernel that
+ * writes q, block_table or seq_lens.
+ *
+ * KVQ_DECODE_NO_TCGEN05: keep shapes of 17..64 query rows per kv head on the
+ * mma.sync kernel's layouts instead of the tensor-memory (tcgen05) kernel
+ * (for comparing the two; results agree within the parity tolerance). */
+#define KVQ_DECODE_EARLY_INPUTS 0x1u
+#define KVQ_DECODE_NO_TCGEN05 0x2u
 
 /* Human-readable name of a status code (static storage). */
 KVQ_API const char* kvq_status_string(kvq_status status);
@@ -250,13 +272,9 @@ KVQ_API kvq_status kvq_decode_workspace_size(const kvq_cache* cache,
  * same stream.  Per query row, logits are sm_scale * <q, k_j>, capped by
  * softcap, masked to keys j <= pos (and j > pos - window when set).
  * The kvq kernels let the next kernel on the stream start early
- * (programmatic dependent launch).  kvq_decode reads q, block_table,
- * seq_lens and the static (PER_TENSOR / PER_CHANNEL) scales before it waits
- * for the kernel launched just before it on the stream to finish, and reads
- * the cache and writes the workspace only after that wait: q, block_table,
- * seq_lens and those scales must therefore not be outputs of that preceding
- * kvq kernel (kvq_combine's out or lse_out).  Outputs of any other kernel
- * are safe: such a kernel completes before kvq_decode starts. */
+ * (programmatic dependent launch); kvq_decode itself waits for the preceding
+ * kernel to complete before it reads any input, unless params->flags has
+ * KVQ_DECODE_EARLY_INPUTS (see there for when that is allowed). */
 KVQ_API kvq_status kvq_decode(const kvq_cache* cache, const kvq_decode_params* params,
                               const void* q, const int32_t* block_table,
                               const int32_t* seq_lens, void* workspace,

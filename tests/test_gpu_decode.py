@@ -23,11 +23,11 @@ def lib():
     return kvq.load()
 
 
-def run_case(orc, w, *, window=0, gen="cpu", step=0, check_cache=True, max_seq_len=None, q_scale=1.0):
+def run_case(orc, w, *, window=0, gen="cpu", step=0, check_cache=True, max_seq_len=None, q_scale=1.0, flags=0):
     gw = GpuWorkload(w, gen_device=gen)
     gw.fill_history()
     k_new, v_new, slots = gw.new_tokens()
-    params = gw.params(window=window, max_seq_len=max_seq_len)
+    params = gw.params(window=window, max_seq_len=max_seq_len, flags=flags)
     bufs = gw.buffers(params)
     q = w.q(gen, step).to("cuda")
     if q_scale != 1.0:
@@ -120,6 +120,23 @@ def test_determinism_and_fresh_workspace(lib, orc):
     fresh.workspace.fill_(0x7F7F7F7F)
     kvq.decode_step(gw.cache, params, q, gw.block_table, gw.seq_lens, fresh, gw.head_sink)
     assert torch.equal(fresh.out, ref)
+
+
+@pytest.mark.parametrize("name,kw", [("mixed", dict(batch=5, max_ctx=6000)), ("spec", dict(ctx=700, batch=2))])
+def test_early_inputs_flag_gives_the_same_bits(lib, orc, name, kw):
+    """KVQ_DECODE_EARLY_INPUTS only moves the reads of q, the block table,
+    seq_lens and the static scales ahead of the wait on the preceding kernel
+    (here kvq_append, which writes none of them): the result is bitwise the
+    default path's, on both decode kernels."""
+    w = synth.make(name, **kw)
+    gw, params, bufs, q, _ = run_case(orc, w)
+    ref, ref_lse = bufs.out.clone(), bufs.lse.clone()
+    k_new, v_new, slots = gw.new_tokens()
+    early = gw.params(flags=kvq.DECODE_EARLY_INPUTS)
+    for _ in range(3):
+        out, lse = gw.step(q, k_new, v_new, slots, early, bufs)
+        assert torch.equal(out, ref) and torch.equal(lse, ref_lse)
+    assert kvq.kvq_get_device_error() == 0
 
 
 def test_large_per_channel_k_scale_with_zero_codes_is_finite(lib, orc):
