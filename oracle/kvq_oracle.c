@@ -37,14 +37,15 @@
  *  query head for every query token; R16 an empty key set gives o = 0 and
  *  lse = -inf.  For the prologue before the cache write: R19 RMSNorm, then
  *  RoPE; R20 RMSNorm per (token, head) over the D channels with one bf16 weight
- *  vector per side, in fp32 with a fixed operation order (its bf16 result
- *  decides the codes) and a single bf16 rounding at the end;
+ *  vector per side, evaluated here in fp64 from the definition (the pages fix
+ *  no evaluation order) with a single bf16 rounding at the end;
  *  R21 RoPE angles come as caller tables cos/sin [max_pos, rotary_dim/2]
  *  indexed by the token's position, half-split pairs unless interleaved is
  *  asked for; R22 on the cache side only K takes the prologue, V is written as
  *  given; R23 the optional Walsh-Hadamard rotation (onnxruntime PR #32515,
  *  note on the stacked change that adds it) comes after RoPE, on Q and K
- *  alike (so dot products are unchanged), in Sylvester order.  For the
+ *  alike (so dot products are unchanged), in Sylvester order, orthonormal
+ *  (entries +-1/sqrt(D)).  For the
  *  group-wise scales the kv-quant-attn page lists as not done (section
  *  "Requirements and limits"): R25 a group is a run of group_size consecutive channels of
  *  one (token, kv head) row (group_size divides D), quantized exactly like a
@@ -316,85 +317,67 @@ uint16_t orc_f64_to_bf16(double v) {
   return (uint16_t)(u >> 16);
 }
 
-/* One row of D values.  The bf16 result decides the quantized codes, so it is
- * taken in the kernel's precision, fp32, with every operation in a fixed order
- * (reading R20; each step is one IEEE binary32 operation, no contraction):
- *   RMSNorm (w != NULL): lane l = 0..31 owns channels l*E .. l*E + E - 1
- *     (E = D/32) and sums their squares in channel order (s = s + x*x); then,
- *     for o = 16, 8, 4, 2, 1, every lane's partial becomes its own plus lane
- *     (l xor o)'s; r = 1 / sqrt(s / D + eps); y_d = (x_d * r) * w_d;
+/* One row of D values, written out from the definitions in double precision
+ * (reading R20: the pages state the operations, not an evaluation order; fp64
+ * leaves any order's rounding far below one bf16 unit):
+ *   RMSNorm (w != NULL): y_d = x_d * r * w_d, r = 1 / sqrt(sum_d x_d^2 / D + eps);
  *   RoPE (rd > 0) on channels [off, off + rd), angle index i in [0, rd/2):
  *     the pair (a, b) = (off + i, off + i + rd/2) (half split) or
  *     (off + 2i, off + 2i + 1) (interleaved) becomes
- *     (a*cos_i - b*sin_i, b*cos_i + a*sin_i), cos_i = cs[i], sin_i = sn[i]
+ *     (a cos_i - b sin_i, b cos_i + a sin_i), cos_i = cs[i], sin_i = sn[i]
  *     (the caller's table row of the token's position);
- * then (optionally) the Walsh-Hadamard rotation below, then round to nearest
- * even to bf16. */
-void orc_norm_rope_row(const uint16_t* x, int D, const uint16_t* w, float eps, int rd, int off,
-                       int interleaved, const float* cs, const float* sn, int hadamard, uint16_t* out) {
-  float y[512];
-  for (int d = 0; d < D; ++d) y[d] = orc_bf16_to_f32(x[d]);
+ *   Walsh-Hadamard (hadamard != 0): y <- H y with the Sylvester-order matrix
+ *     H[i][j] = (-1)^popcount(i & j) / sqrt(D), a plain matrix-vector product;
+ * then one round-to-nearest-even to bf16 per value.  out64 (may be NULL)
+ * receives the values before that rounding. */
+void orc_norm_rope_row(const uint16_t* x, int D, const uint16_t* w, double eps, int rd, int off,
+                       int interleaved, const float* cs, const float* sn, int hadamard, uint16_t* out,
+                       double* out64) {
+  double y[512];
+  for (int d = 0; d < D; ++d) y[d] = (double)orc_bf16_to_f32(x[d]);
   if (w) {
-    int E = D / 32;
-    float part[32], nxt[32];
-    for (int l = 0; l < 32; ++l) {
-      float acc = 0.0f;
-      for (int e = 0; e < E; ++e) {
-        float sq = y[l * E + e] * y[l * E + e];
-        acc = acc + sq;
-      }
-      part[l] = acc;
-    }
-    for (int o = 16; o > 0; o >>= 1) {
-      for (int l = 0; l < 32; ++l) nxt[l] = part[l] + part[l ^ o];
-      memcpy(part, nxt, sizeof part);
-    }
-    float ms = part[0] / (float)D;
-    float r = 1.0f / sqrtf(ms + eps);
-    for (int d = 0; d < D; ++d) {
-      float t = y[d] * r;
-      y[d] = t * orc_bf16_to_f32(w[d]);
-    }
+    double ss = 0.0;
+    for (int d = 0; d < D; ++d) ss += y[d] * y[d];
+    double r = 1.0 / sqrt(ss / (double)D + eps);
+    for (int d = 0; d < D; ++d) y[d] = y[d] * r * (double)orc_bf16_to_f32(w[d]);
   }
   if (rd > 0) {
-    float z[512];
-    memcpy(z, y, sizeof(float) * (size_t)D);
+    double z[512];
+    memcpy(z, y, sizeof(double) * (size_t)D);
     for (int i = 0; i < rd / 2; ++i) {
       int a = interleaved ? off + 2 * i : off + i;
       int b = interleaved ? a + 1 : a + rd / 2;
-      float ac = y[a] * cs[i], bs = y[b] * sn[i], bc = y[b] * cs[i], as = y[a] * sn[i];
-      z[a] = ac - bs;
-      z[b] = bc + as;
+      double c = (double)cs[i], s = (double)sn[i];
+      z[a] = y[a] * c - y[b] * s;
+      z[b] = y[b] * c + y[a] * s;
     }
-    memcpy(y, z, sizeof(float) * (size_t)D);
+    memcpy(y, z, sizeof(double) * (size_t)D);
   }
   if (hadamard) {
-    /* orthonormal Walsh-Hadamard rotation (Sylvester order, entry (i, j) =
-     * (-1)^popcount(i & j) / sqrt(D)): butterflies of span 1, 2, 4, ...,
-     * D/2, each pair (i, i + span) with i & span == 0 becoming
-     * (a + b, a - b) in fp32, then every value times fl32(1 / fl32(sqrt(D))) */
-    for (int span = 1; span < D; span <<= 1)
-      for (int i = 0; i < D; ++i)
-        if (!(i & span)) {
-          float a = y[i], b = y[i + span];
-          y[i] = a + b;
-          y[i + span] = a - b;
-        }
-    float sc = 1.0f / sqrtf((float)D);
-    for (int d = 0; d < D; ++d) y[d] = y[d] * sc;
+    double z[512];
+    double inv = 1.0 / sqrt((double)D);
+    for (int i = 0; i < D; ++i) {
+      double acc = 0.0;
+      for (int j = 0; j < D; ++j) acc += (__builtin_popcount((unsigned)(i & j)) & 1) ? -y[j] : y[j];
+      z[i] = acc * inv;
+    }
+    memcpy(y, z, sizeof(double) * (size_t)D);
   }
-  for (int d = 0; d < D; ++d) out[d] = orc_f64_to_bf16((double)y[d]);
+  for (int d = 0; d < D; ++d) {
+    out[d] = orc_f64_to_bf16(y[d]);
+    if (out64) out64[d] = y[d];
+  }
 }
 
-/* The prologue over x [n_tokens, H, D] -> out (same shape, bf16 bits).  The
- * RoPE tables are [max_pos, rd/2]; a token whose position lies outside
- * [0, max_pos) while rd > 0 is left untouched in out and counted in the
- * return value. */
-int orc_norm_rope(const uint16_t* x, int n_tokens, int H, int D, const uint16_t* w, float eps, int rd,
+/* The prologue over x [n_tokens, H, D] -> out (same shape, bf16 bits; out64,
+ * if not NULL, the same values before the bf16 rounding).  The RoPE tables are
+ * [max_pos, rd/2]; a token whose position lies outside [0, max_pos) while
+ * rd > 0 is left untouched in out and counted in the return value. */
+int orc_norm_rope(const uint16_t* x, int n_tokens, int H, int D, const uint16_t* w, double eps, int rd,
                   int off, int interleaved, const float* cos_tab, const float* sin_tab, int max_pos,
-                  const int64_t* positions, int hadamard, uint16_t* out) {
+                  const int64_t* positions, int hadamard, uint16_t* out, double* out64) {
   int bad = 0;
-  if (D > 512 || D % 32 || rd < 0 || rd % 2 || off < 0 || off + rd > D || (hadamard && (D & (D - 1))))
+  if (D <= 0 || D > 512 || rd < 0 || rd % 2 || off < 0 || off + rd > D || (hadamard && (D & (D - 1))))
     return -1;
   for (int n = 0; n < n_tokens; ++n) {
     int64_t pos = rd > 0 ? positions[n] : 0;
@@ -404,9 +387,11 @@ int orc_norm_rope(const uint16_t* x, int n_tokens, int H, int D, const uint16_t*
     }
     const float* cs = rd > 0 ? cos_tab + (size_t)pos * (rd / 2) : NULL;
     const float* sn = rd > 0 ? sin_tab + (size_t)pos * (rd / 2) : NULL;
-    for (int h = 0; h < H; ++h)
-      orc_norm_rope_row(x + ((size_t)n * H + h) * D, D, w, eps, rd, off, interleaved, cs, sn, hadamard,
-                        out + ((size_t)n * H + h) * D);
+    for (int h = 0; h < H; ++h) {
+      size_t o = ((size_t)n * H + h) * D;
+      orc_norm_rope_row(x + o, D, w, eps, rd, off, interleaved, cs, sn, hadamard, out + o,
+                        out64 ? out64 + o : NULL);
+    }
   }
   return bad;
 }

@@ -88,8 +88,8 @@ def lib():
             L.orc_attend.argtypes = [ctypes.POINTER(_Cache), ctypes.POINTER(_Params), vp, vp, vp, vp,
                                      vp, i32, vp, vp, i32]
             L.orc_attend.restype = i32
-            L.orc_norm_rope.argtypes = [vp, i32, i32, i32, vp, ctypes.c_float, i32, i32, i32, vp, vp, i32,
-                                        vp, i32, vp]
+            L.orc_norm_rope.argtypes = [vp, i32, i32, i32, vp, ctypes.c_double, i32, i32, i32, vp, vp, i32,
+                                        vp, i32, vp, vp]
             L.orc_norm_rope.restype = i32
             L.orc_f64_to_bf16.argtypes = [ctypes.c_double]
             L.orc_f64_to_bf16.restype = ctypes.c_uint16
@@ -116,8 +116,9 @@ def f64_to_bf16(v: float) -> int:
 
 def norm_rope(x_bf16: np.ndarray, *, norm_weight=None, eps: float = 1e-6, rotary_dim: int = 0,
               rotary_offset: int = 0, interleaved: bool = False, cos=None, sin=None, positions=None,
-              hadamard: bool = False):
-    """QK-RMSNorm then RoPE on x [N, H, D] (bf16 bits) -> (bf16 bits, rows skipped).
+              hadamard: bool = False, return_f64: bool = False):
+    """QK-RMSNorm then RoPE on x [N, H, D] (bf16 bits) -> (bf16 bits, rows skipped)
+    or, with return_f64, (bf16 bits, rows skipped, the values before rounding).
 
     onnxruntime PR #29912, Summary of Changes (q_norm_weight / k_norm_weight,
     qk_norm_epsilon default 1e-6, rotary_offset; QkNormRotaryTNH).  Per row:
@@ -125,13 +126,13 @@ def norm_rope(x_bf16: np.ndarray, *, norm_weight=None, eps: float = 1e-6, rotary
     (a cos - b sin, b cos + a sin) with cos / sin the tables' row for the
     token's position, then (hadamard) the orthonormal Walsh-Hadamard
     rotation (named as the follow-up to the int4 cache in onnxruntime PR
-    #32515's stacked-change note); fp32 in the fixed order kvq_oracle.c
-    states (the bf16 result
-    decides the codes), one bf16 rounding.  Tokens whose position is outside
-    the tables are left zero and counted."""
+    #32515's stacked-change note); fp64 from the definitions, one bf16
+    rounding.  eps is the fp32 value the library's descriptor carries.
+    Tokens whose position is outside the tables are left zero and counted."""
     x = np.ascontiguousarray(x_bf16, dtype=np.uint16)
     N, H, D = x.shape
     out = np.zeros_like(x)
+    out64 = np.zeros(x.shape, np.float64)
     w = None if norm_weight is None else np.ascontiguousarray(norm_weight, dtype=np.uint16)
     if rotary_dim > 0:
         cs = np.ascontiguousarray(cos, dtype=np.float32)
@@ -141,12 +142,12 @@ def norm_rope(x_bf16: np.ndarray, *, norm_weight=None, eps: float = 1e-6, rotary
     else:
         cs = sn = pos = None
         max_pos = 0
-    bad = lib().orc_norm_rope(_ptr(x), N, H, D, _ptr(w), float(eps), int(rotary_dim), int(rotary_offset),
-                              1 if interleaved else 0, _ptr(cs), _ptr(sn), int(max_pos), _ptr(pos),
-                              1 if hadamard else 0, _ptr(out))
+    bad = lib().orc_norm_rope(_ptr(x), N, H, D, _ptr(w), float(np.float32(eps)), int(rotary_dim),
+                              int(rotary_offset), 1 if interleaved else 0, _ptr(cs), _ptr(sn), int(max_pos),
+                              _ptr(pos), 1 if hadamard else 0, _ptr(out), _ptr(out64))
     if bad < 0:
         raise ValueError("norm_rope: bad shape")
-    return out, bad
+    return (out, bad, out64) if return_f64 else (out, bad)
 
 
 def row_bytes(dtype: int, D: int) -> int:

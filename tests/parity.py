@@ -75,6 +75,21 @@ class OracleSide:
                                  window=window, head_sink=s, rows=r, nthreads=nthreads)
 
 
+def bf16_bits_to_f64(u) -> np.ndarray:
+    return (np.asarray(u, np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def bf16_neighbours(v):
+    """(lower, upper) bf16 values around each fp64 value v (finite) and the
+    midpoint between them, exactly in fp64 (spacing 2^(e-7) in the binade
+    [2^e, 2^(e+1)), 2^-133 below 2^-126)."""
+    v = np.asarray(v, np.float64)
+    e = np.floor(np.log2(np.maximum(np.abs(v), 2.0 ** -126)))
+    q = np.ldexp(1.0, (e - 7).astype(int))
+    lo = np.floor(v / q) * q
+    return lo, lo + q, lo + q / 2
+
+
 def rel_l2(got: np.ndarray, ref: np.ndarray) -> float:
     n = np.linalg.norm(ref)
     return float(np.linalg.norm(got - ref) / n) if n > 0 else float(np.linalg.norm(got))
