@@ -48,6 +48,8 @@ def parse():
     p.add_argument("--no-prologue", action="store_true", help="skip the QK-RMSNorm + RoPE prologue timing")
     p.add_argument("--no-prefill", action="store_true", help="skip the chunked-prefill timing")
     p.add_argument("--no-group", action="store_true", help="skip the group-wise-scale decode timing")
+    p.add_argument("--no-configs", action="store_true",
+                   help="skip the other workloads (tiny, paged, spec, mixed) beside the default line")
     return p.parse_args()
 
 
@@ -176,103 +178,187 @@ def make_workload(args):
 
 # --------------------------------------------------------------------------- GPU arm
 
-def measure(w, steps, warmup, *, windows=(0,), e2e=False, reps=0):
-    """Time `steps` decode steps of workload w on the current GPU.  Caches are
-    replicated so that consecutive steps read different memory and the
-    replicas together exceed 4x the L2 size (inputs larger than L2)."""
-    import numpy as np
-    import torch
-    from decode_attention_quantized_gb300 import kvq, synth
-    from decode_attention_quantized_gb300.workload import GpuWorkload
+class Rig:
+    """Workload w on the current GPU: one cache filled through kvq_append and
+    replicated so that consecutive launches read different memory and the
+    replicas together exceed 4x the L2 size (inputs larger than L2); decode
+    buffers per window; eight query draws."""
 
-    dev = torch.cuda.current_device()
-    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    kv_bytes = synth.step_bytes(w)["kv"]
-    if reps <= 0:
-        reps = min(512, max(2, math.ceil(4 * l2 / max(kv_bytes, 1))))
-    gws = [GpuWorkload(w, device=f"cuda:{dev}", gen_device="cuda")]
-    gws[0].fill_history()
-    for _ in range(reps - 1):
-        g = GpuWorkload.__new__(GpuWorkload)
-        g.__dict__.update(gws[0].__dict__)
-        src = gws[0].cache
-        c = kvq.QuantizedPagedCache.__new__(kvq.QuantizedPagedCache)
-        c.__dict__.update(src.__dict__)
-        c.k_codes, c.v_codes = src.k_codes.clone(), src.v_codes.clone()
-        c.k_scale, c.v_scale = src.k_scale.clone(), src.v_scale.clone()
-        g.cache = c
-        gws.append(g)
-    k_new, v_new, slots = gws[0].new_tokens()
-    nq = 8
-    qs = [w.q("cuda", i).to(f"cuda:{dev}") for i in range(nq)]
-    # q, the block table and seq_lens are never written by the kernel before
-    # kvq_decode (kvq_append): the decode may read them while append finishes
-    plist = [gws[0].params(window=wd, flags=kvq.DECODE_EARLY_INPUTS) for wd in windows]
-    bufs = [gws[0].buffers(p) for p in plist]
-    stream = torch.cuda.current_stream()
+    def __init__(self, w, windows=(0,), reps=0):
+        import torch
+        from decode_attention_quantized_gb300 import kvq, synth
+        from decode_attention_quantized_gb300.workload import GpuWorkload
 
-    def step_args(i):
-        g = gws[i % reps]
-        j = i % len(windows)
-        return g, plist[j], bufs[j], qs[i % nq]
+        self.w, self.windows = w, tuple(windows)
+        dev = torch.cuda.current_device()
+        self.l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+        kv_bytes = synth.step_bytes(w)["kv"]
+        if reps <= 0:
+            reps = min(512, max(2, math.ceil(4 * self.l2 / max(kv_bytes, 1))))
+        self.reps = reps
+        gws = [GpuWorkload(w, device=f"cuda:{dev}", gen_device="cuda")]
+        gws[0].fill_history()
+        for _ in range(reps - 1):
+            g = GpuWorkload.__new__(GpuWorkload)
+            g.__dict__.update(gws[0].__dict__)
+            src = gws[0].cache
+            c = kvq.QuantizedPagedCache.__new__(kvq.QuantizedPagedCache)
+            c.__dict__.update(src.__dict__)
+            c.k_codes, c.v_codes = src.k_codes.clone(), src.v_codes.clone()
+            c.k_scale, c.v_scale = src.k_scale.clone(), src.v_scale.clone()
+            g.cache = c
+            gws.append(g)
+        self.gws = gws
+        self.k_new, self.v_new, self.slots = gws[0].new_tokens()
+        self.qs = [w.q("cuda", i).to(f"cuda:{dev}") for i in range(8)]
+        # q, the block table and seq_lens are never written by the kernel before
+        # kvq_decode (kvq_append): the decode may read them while append finishes
+        self.plist = [gws[0].params(window=wd, flags=kvq.DECODE_EARLY_INPUTS) for wd in self.windows]
+        self.bufs = [gws[0].buffers(p) for p in self.plist]
+        self.stream = torch.cuda.current_stream()
 
-    def k_append(i):
-        g, p, b, q = step_args(i)
-        kvq.kvq_append(g.cache, k_new, v_new, slots)
+    def _args(self, i, j=None):
+        j = i % len(self.windows) if j is None else j
+        return self.gws[i % self.reps], self.plist[j], self.bufs[j], self.qs[i % len(self.qs)]
 
-    def k_decode(i):
-        g, p, b, q = step_args(i)
+    def append(self, i, j=None):
+        from decode_attention_quantized_gb300 import kvq
+        g, p, b, q = self._args(i, j)
+        kvq.kvq_append(g.cache, self.k_new, self.v_new, self.slots)
+
+    def decode(self, i, j=None):
+        from decode_attention_quantized_gb300 import kvq
+        g, p, b, q = self._args(i, j)
         kvq.kvq_decode(g.cache, p, q, g.block_table, g.seq_lens, b.workspace)
 
-    def k_combine(i):
-        g, p, b, q = step_args(i)
+    def combine(self, i, j=None):
+        from decode_attention_quantized_gb300 import kvq
+        g, p, b, q = self._args(i, j)
         kvq.kvq_combine(g.cache, p, b.workspace, g.head_sink, b.out, b.lse)
 
-    def one(i):
-        k_append(i)
-        k_decode(i)
-        k_combine(i)
+    def step(self, i):
+        self.append(i)
+        self.decode(i)
+        self.combine(i)
 
-    for i in range(warmup):  # eager warm-up: per-device set-up, plan cache, smem limits
-        one(i)
-    torch.cuda.synchronize()
-    assert kvq.kvq_get_device_error() == 0, "device error flags set during warm-up"
-
-    def graph_of(fn):
-        """K launches of fn captured once (the ABI is capture-safe)."""
+    def graph_ms(self, fn, steps, first):
+        """Total ms of `steps` launches fn(first), fn(first + 1), ... captured
+        once in a CUDA graph (the ABI is capture-safe) and replayed between
+        CUDA events on the launching stream."""
+        import torch
         gr = torch.cuda.CUDAGraph()
         with torch.cuda.graph(gr):
             for i in range(steps):
-                fn(warmup + i)
+                fn(first + i)
         gr.replay()  # warm replay
         torch.cuda.synchronize()
-        return gr
-
-    def timed(gr):
         t0 = torch.cuda.Event(enable_timing=True)
         t1 = torch.cuda.Event(enable_timing=True)
-        torch.cuda.synchronize()
-        t0.record(stream)
+        t0.record(self.stream)
         gr.replay()
-        t1.record(stream)
+        t1.record(self.stream)
         torch.cuda.synchronize()
         return t0.elapsed_time(t1)
 
-    g_step = graph_of(one)
-    total_ms = timed(g_step)
-    dec_ms = timed(graph_of(k_decode)) / steps
-    app_ms = timed(graph_of(k_append)) / steps
-    comb_ms = timed(graph_of(k_combine)) / steps
+    def per_launch_ms(self, n, first, j=None):
+        """n decode launches, each bracketed by its own pair of CUDA events.  A
+        sleep kernel ahead of them keeps the GPU busy while the host enqueues
+        them all, so no launch waits on the host; consecutive launches read
+        different cache replicas (L2-cold)."""
+        import torch
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        torch.cuda.synchronize()
+        torch.cuda._sleep(int(2e5 * n + 2e6))  # about 0.1 ms per launch at 2 GHz: longer than their enqueue
+        for i in range(n):
+            ev[i][0].record(self.stream)
+            self.decode(first + i, j)
+            ev[i][1].record(self.stream)
+        torch.cuda.synchronize()
+        return [a.elapsed_time(b) for a, b in ev]
+
+
+def pct(xs, q):
+    """q-th percentile (linear interpolation) of a list."""
+    xs = sorted(xs)
+    k = (len(xs) - 1) * q / 100.0
+    f = math.floor(k)
+    c = min(f + 1, len(xs) - 1)
+    return xs[f] + (xs[c] - xs[f]) * (k - f)
+
+
+def measure(w, steps, warmup, *, windows=(0,), e2e=False, reps=0, per_launch=0):
+    """Time `steps` decode steps of workload w on the current GPU (graphs of K
+    launches), and optionally `per_launch` decode launches one by one per
+    window (median and p10 / p90)."""
+    import torch
+    from decode_attention_quantized_gb300 import kvq, synth
+
+    rig = Rig(w, windows, reps)
+    for i in range(warmup):  # eager warm-up: per-device set-up, plan cache, smem limits
+        rig.step(i)
+    torch.cuda.synchronize()
+    assert kvq.kvq_get_device_error() == 0, "device error flags set during warm-up"
+    total_ms = rig.graph_ms(rig.step, steps, warmup)
+    dec_ms = rig.graph_ms(rig.decode, steps, warmup) / steps
+    app_ms = rig.graph_ms(rig.append, steps, warmup) / steps
+    comb_ms = rig.graph_ms(rig.combine, steps, warmup) / steps
     assert kvq.kvq_get_device_error() == 0, "device error flags set during the timed steps"
     res = dict(total_ms=total_ms, steps=steps, decode_ms=[dec_ms], append_ms=[app_ms], combine_ms=[comb_ms],
-               launches=3 * steps, reps=reps, l2=l2)
+               launches=3 * steps, reps=rig.reps, l2=rig.l2)
     sb = [synth.step_bytes(w, wd) for wd in windows]
     res["step_bytes"] = sum(sum(sb[i % len(windows)].values()) for i in range(warmup, warmup + steps))
     res["decode_bytes"] = [synth.decode_bytes(w, windows[i % len(windows)]) for i in range(warmup, warmup + steps)]
-
+    if per_launch:
+        res["per_launch"] = []
+        for j, wd in enumerate(windows):
+            for i in range(3):  # warm the per-launch path (events, sleep)
+                rig.decode(i, j)
+            ms = rig.per_launch_ms(per_launch, warmup + steps, j)
+            res["per_launch"].append(dict(window=wd, ms=ms, bytes=synth.decode_bytes(w, wd)))
+        assert kvq.kvq_get_device_error() == 0, "device error flags set during the per-launch timing"
     if e2e:
-        res["e2e"] = measure_e2e(w, gws, plist, windows, steps, warmup, k_new, v_new, slots, qs)
+        res["e2e"] = measure_e2e(w, rig.gws, rig.plist, windows, steps, warmup, rig.k_new, rig.v_new, rig.slots,
+                                 rig.qs)
+    del rig
+    torch.cuda.empty_cache()
     return res
+
+
+def launch_stats(pl, peak):
+    """Median and p10 / p90 of per-launch decode times, with GB/s and the
+    fraction of the HBM peak at the median."""
+    ms = pl["ms"]
+    med = statistics.median(ms)
+    gbs = pl["bytes"] / (med * 1e-3) / 1e9
+    return {"decode_us_median": round(1e3 * med, 2), "decode_us_p10": round(1e3 * pct(ms, 10), 2),
+            "decode_us_p90": round(1e3 * pct(ms, 90), 2), "launches": len(ms),
+            "decode_gbs_at_median": round(gbs, 1), "frac_of_hbm_at_median": round(gbs / peak, 3),
+            "algorithmic_bytes_per_launch": int(pl["bytes"])}
+
+
+def measure_configs(names, steps, warmup, peak, per_launch):
+    """The other workloads of the benchmark at full size, each with its
+    graph-mean decode time and per-launch percentiles (the mixed workload's
+    full and windowed calls separately)."""
+    import torch
+    from decode_attention_quantized_gb300 import synth
+    out = []
+    for name in names:
+        w = synth.make(name)
+        windows = (w.window_for_call(0), w.window_for_call(1)) if w.window else (0,)
+        r = measure(w, steps, warmup, windows=windows, per_launch=per_launch)
+        for j, pl in enumerate(r["per_launch"]):
+            ent = {"name": name if len(windows) == 1 else f"{name}-{'window' if pl['window'] else 'full'}",
+                   "workload": describe(w, pl["window"]), "replicas": r["reps"]}
+            ent.update(launch_stats(pl, peak))
+            if name == "tiny":
+                ent["roofline"] = "latency-bound: no bandwidth claim"
+            out.append(ent)
+        out[-1]["graph_mean_decode_us_all_calls"] = round(1e3 * statistics.mean(r["decode_ms"]), 2)
+        out[-1]["graph_mean_step_us_all_calls"] = round(1e3 * r["total_ms"] / r["steps"], 2)
+        del r
+        torch.cuda.empty_cache()
+    return out
 
 
 def measure_e2e(w, gws, plist, windows, steps, warmup, k_new, v_new, slots, qs):
@@ -506,6 +592,16 @@ def measure_group(w, steps, warmup, peak, group_size=64):
             "algorithmic_bytes_per_launch": int(dec_bytes)}
 
 
+def decode_kernel_name(w):
+    """The decode kernel a workload runs on: the tensor-memory kernel for
+    17..48 query rows per kv head at head_dim 256 (17..64 at 128) without
+    group scales, else the mma.sync kernel."""
+    rows = w.group * w.q_tokens
+    tc = (17 <= rows <= (48 if w.head_dim == 256 else 64) and w.head_dim in (128, 256)
+          and 4 not in (w.k_mode, w.v_mode))
+    return "decode_tc_kernel" if tc else "decode_kernel"
+
+
 def traffic_from_profiles(kernel_tag: str):
     """DRAM bytes per launch of the decode kernel from the committed ncu
     summary, if it was taken on the current kernel source."""
@@ -538,7 +634,9 @@ def run_ours(args):
     barrier(world)
     torch.cuda.synchronize()
     clocks.start()
-    res = measure(w, args.steps, args.warmup, windows=windows, e2e=not args.no_e2e, reps=args.reps)
+    n_pl = max(50, args.steps)
+    res = measure(w, args.steps, args.warmup, windows=windows, e2e=not args.no_e2e, reps=args.reps,
+                  per_launch=n_pl)
     clk = clocks.stop()
     barrier(world)
     total_ms = max_over_ranks(res["total_ms"], world)
@@ -551,15 +649,18 @@ def run_ours(args):
                 wc = w
             else:
                 wc = synth.make("gqa", ctx=ctx)
-                r = measure(wc, max(10, args.steps), max(3, args.warmup))
+                r = measure(wc, max(10, args.steps), max(3, args.warmup), per_launch=n_pl)
             dec_ms = statistics.mean(r["decode_ms"])
             kvb = synth.decode_bytes(wc)
-            sweep.append({"ctx": ctx, "us_per_step": round(1e3 * r["total_ms"] / r["steps"], 2),
-                          "decode_us": round(1e3 * dec_ms, 2),
-                          "decode_gbs": round(kvb / (dec_ms * 1e-3) / 1e9, 1),
-                          "frac_of_hbm": round(kvb / (dec_ms * 1e-3) / 1e9 / peak, 3),
-                          "cache_mb": round(synth.step_bytes(wc)["kv"] / 1e6, 2),
-                          "replicas": r["reps"]})
+            ent = {"ctx": ctx, "us_per_step": round(1e3 * r["total_ms"] / r["steps"], 2),
+                   "decode_us": round(1e3 * dec_ms, 2),
+                   "decode_gbs": round(kvb / (dec_ms * 1e-3) / 1e9, 1),
+                   "frac_of_hbm": round(kvb / (dec_ms * 1e-3) / 1e9 / peak, 3),
+                   "cache_mb": round(synth.step_bytes(wc)["kv"] / 1e6, 2),
+                   "replicas": r["reps"]}
+            ent["per_launch"] = {k: v for k, v in launch_stats(r["per_launch"][0], peak).items()
+                                 if k.startswith("decode_us") or k.startswith("frac")}
+            sweep.append(ent)
             del r
             torch.cuda.empty_cache()
 
@@ -590,7 +691,8 @@ def run_ours(args):
             "compute": "f16 x f16 -> f32 tensor-core mma, fp32 softmax",
             "step": "kvq_append (new tokens) + kvq_decode (flags KVQ_DECODE_EARLY_INPUTS) + kvq_combine",
             "timing": "K steps captured once in a CUDA graph and replayed between CUDA events; per-kernel "
-                      "times from graphs of K launches of that kernel alone",
+                      "times from graphs of K launches of that kernel alone; decode_per_launch and configs: "
+                      f"{n_pl} decode launches each bracketed by its own CUDA events (median, p10, p90)",
             "windows_per_call": list(windows),
             "l2": f"inputs larger than L2: {res['reps']} cache replicas rotated per step, "
                   f"{res['reps'] * synth.step_bytes(w)['kv'] / 1e6:.0f} MB total vs L2 {res['l2'] / 1e6:.0f} MB",
@@ -601,8 +703,9 @@ def run_ours(args):
             "decode": round(1e3 * statistics.mean(res["decode_ms"]), 2),
             "combine": round(1e3 * statistics.mean(res["combine_ms"]), 2),
         },
+        "decode_per_launch": [dict(window=pl["window"], **launch_stats(pl, peak)) for pl in res["per_launch"]],
         "roofline": {
-            "kernel": "decode_kernel",
+            "kernel": decode_kernel_name(w),
             "bound": "hbm",
             "achieved": round(achieved, 1),
             "peak": peak,
@@ -623,6 +726,11 @@ def run_ours(args):
         line["e2e"] = {"value": round(step_bytes / e2e_wall / 1e9, 1), "unit": "GB/s",
                        "us_per_step": round(1e6 * e2e_wall / K, 2),
                        "h2d_bytes_per_step": e["h2d"], "d2h_bytes_per_step": e["d2h"]}
+    if rank == 0 and world == 1 and args.workload == "gqa" and not args.no_configs:
+        head = {"name": f"gqa-{int(w.seq_lens.max())}", "workload": describe(w), "replicas": res["reps"]}
+        head.update(launch_stats(res["per_launch"][0], peak))
+        line["configs"] = [head] + measure_configs(["tiny", "paged", "spec", "mixed"], args.steps, args.warmup,
+                                                   peak, n_pl)
     if rank == 0 and world == 1 and not args.no_prologue:
         line["prologue"] = measure_prologue(w, args.steps, args.warmup, peak)
     if rank == 0 and world == 1 and not args.no_prefill:

@@ -35,14 +35,20 @@ def _nvcc() -> str:
     raise RuntimeError("nvcc not found: the CUDA toolkit is required to build libkvq.so")
 
 
+HEADERS = ["kvq_internal.h", "ptx.cuh", "pipeline.cuh", "decode.cuh", "decode_tc.cuh"]
+
+
 def _stamp() -> str:
+    """Digest of the library's own source files (a fixed list, so stray files
+    in the folders change nothing) and the compiler flags, with the flags'
+    machine-specific include paths left out."""
     h = hashlib.sha256()
-    h.update(" ".join(NVCC_FLAGS).encode())
-    for d in (CSRC, INCLUDE):
-        for name in sorted(os.listdir(d)):
-            with open(os.path.join(d, name), "rb") as f:
-                h.update(name.encode())
-                h.update(f.read())
+    h.update(" ".join(f for f in NVCC_FLAGS if not f.startswith("-I")).encode())
+    files = [os.path.join(CSRC, n) for n in SOURCES + HEADERS] + [os.path.join(INCLUDE, "kvq.h")]
+    for path in files:
+        with open(path, "rb") as f:
+            h.update(os.path.basename(path).encode())
+            h.update(f.read().replace(b"\r\n", b"\n"))
     return h.hexdigest()
 
 
