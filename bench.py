@@ -594,11 +594,10 @@ def measure_group(w, steps, warmup, peak, group_size=64):
 
 def decode_kernel_name(w):
     """The decode kernel a workload runs on: the tensor-memory kernel for
-    17..48 query rows per kv head at head_dim 256 (17..64 at 128) without
-    group scales, else the mma.sync kernel."""
+    17..48 query rows per kv head at head_dim 256 (17..64 at 128), else the
+    mma.sync kernel."""
     rows = w.group * w.q_tokens
-    tc = (17 <= rows <= (48 if w.head_dim == 256 else 64) and w.head_dim in (128, 256)
-          and 4 not in (w.k_mode, w.v_mode))
+    tc = 17 <= rows <= (48 if w.head_dim == 256 else 64) and w.head_dim in (128, 256)
     return "decode_tc_kernel" if tc else "decode_kernel"
 
 

@@ -25,7 +25,8 @@ ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-fvisibility=hidden",
               "-I" + INCLUDE, "-I" + CSRC] + ARCH
 SOURCES = ["api.cu", "append.cu", "combine.cu", "decode_int8.cu", "decode_fp8.cu", "decode_int4.cu",
-           "decode_tc_int8.cu", "decode_tc_fp8.cu", "decode_tc_int4.cu", "noalloc.cu"]
+           "decode_tc_int8.cu", "decode_tc_fp8.cu", "decode_tc_int4.cu", "decode_tc_grp_int8.cu",
+           "decode_tc_grp_fp8.cu", "decode_tc_grp_int4.cu", "noalloc.cu"]
 
 
 def _nvcc() -> str:

@@ -194,14 +194,15 @@ int tc_rows(const kvq_cache* c, const kvq_decode_params* p, int rows) {
 kvq_status make_plan_tc(const kvq_cache* c, const kvq_decode_params* p, const DeviceInfo& dev, Plan* P) {
   const int B = p->batch > 0 ? p->batch : 1;
   const int dp = row_bytes(c);
+  const int stride = tc_stage_stride(dp, scales_per_row(c, c->k_mode), scales_per_row(c, c->v_mode));
   constexpr size_t kMaxSmem = 227 * 1024;  // per CTA
   int stages = 0;
   for (int s = kMaxStages; s >= 2 && stages == 0; --s)
-    if ((size_t)tc_smem_layout(c->head_dim, dp, P->tc_nr, s, B).total + 1024 <= kMaxSmem) stages = s;
+    if ((size_t)tc_smem_layout(c->head_dim, dp, P->tc_nr, s, B, stride).total + 1024 <= kMaxSmem) stages = s;
   if (stages == 0) return KVQ_ERR_UNSUPPORTED;
   P->stages = stages;
-  P->stride = (size_t)tc_stage_stride(dp);
-  P->smem = (size_t)tc_smem_layout(c->head_dim, dp, P->tc_nr, stages, B).total + 1024;
+  P->stride = (size_t)stride;
+  P->smem = (size_t)tc_smem_layout(c->head_dim, dp, P->tc_nr, stages, B, stride).total + 1024;
   P->threads = kTcWarps * 32;
   P->row_groups = 0;
   P->key_warps = 0;
@@ -219,10 +220,7 @@ kvq_status make_plan_uncached(const kvq_cache* c, const kvq_decode_params* p, co
   Plan P{};
   const int G = p->num_q_heads / c->num_kv_heads;
   P.rows = G * p->q_tokens;
-  // a PER_GROUP side scales each channel group of a key separately, which the
-  // tensor-memory kernel's single QK^T per tile cannot: the grouped layout
-  // takes every row count
-  P.tc_nr = any_group(c) ? 0 : tc_rows(c, p, P.rows);
+  P.tc_nr = tc_rows(c, p, P.rows);
   if (P.tc_nr) {
     if (kvq_status s = make_plan_tc(c, p, dev, &P)) return s;
     const int B = p->batch > 0 ? p->batch : 1;
@@ -462,6 +460,7 @@ kvq_status decode_impl(const kvq_cache* cache, const kvq_decode_params* params, 
   a.v_mode = cache->v_mode;
   a.sk_n = scales_per_row(cache, cache->k_mode);
   a.sv_n = scales_per_row(cache, cache->v_mode);
+  a.log2_gs = any_group(cache) ? ilog2(cache->group_size) : 0;
   a.num_blocks = cache->num_blocks;
   a.block_size = cache->block_size;
   a.log2_bs = ilog2(cache->block_size);
@@ -494,7 +493,13 @@ kvq_status decode_impl(const kvq_cache* cache, const kvq_decode_params* params, 
 
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e;
-  if (P.tc_nr) {
+  if (P.tc_nr && any_group(cache)) {
+    switch (cache->dtype) {
+      case KVQ_INT8: e = launch_decode_tc_grp_int8(cache->head_dim, P.tc_nr, tk, tv, a, P.grid, P.smem, st); break;
+      case KVQ_FP8_E4M3: e = launch_decode_tc_grp_fp8(cache->head_dim, P.tc_nr, tk, tv, a, P.grid, P.smem, st); break;
+      default: e = launch_decode_tc_grp_int4(cache->head_dim, P.tc_nr, tk, tv, a, P.grid, P.smem, st); break;
+    }
+  } else if (P.tc_nr) {
     switch (cache->dtype) {
       case KVQ_INT8: e = launch_decode_tc_int8(cache->head_dim, P.tc_nr, tk, tv, a, P.grid, P.smem, st); break;
       case KVQ_FP8_E4M3: e = launch_decode_tc_fp8(cache->head_dim, P.tc_nr, tk, tv, a, P.grid, P.smem, st); break;

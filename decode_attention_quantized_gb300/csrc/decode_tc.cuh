@@ -207,7 +207,7 @@ __device__ __forceinline__ void tmem_st_cols(uint32_t taddr, const float (&v)[N]
 
 }  // namespace dev
 
-template <int DT, int D, int NR>
+template <int DT, int D, int NR, bool GRP>
 __global__ void __launch_bounds__(kTcWarps * 32, 1)
     decode_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                      const DecodeArgs a) {
@@ -220,7 +220,7 @@ __global__ void __launch_bounds__(kTcWarps * 32, 1)
   extern __shared__ __align__(16) uint8_t smem_raw[];
   const uint32_t pad = (1024u - (ptx::smem_u32(smem_raw) & 1023u)) & 1023u;
   uint8_t* base = smem_raw + pad;
-  const TcSmem lay = tc_smem_layout(D, Gm::DP, NR, a.stages, a.batch);
+  const TcSmem lay = tc_smem_layout(D, Gm::DP, NR, a.stages, a.batch, a.stage_stride);
   uint8_t* ring = base + lay.ring;
   uint8_t* q_s = base + lay.q;
   uint8_t* p_s = base + lay.p;
@@ -287,6 +287,15 @@ __global__ void __launch_bounds__(kTcWarps * 32, 1)
     if (!ptx::mbar_try_wait(bar, parity)) dev::wait_or_abort(bar, parity, abort_flag, a.err);
   };
   const bool k_row = a.k_mode == KVQ_SCALE_PER_ROW, v_row = a.v_mode == KVQ_SCALE_PER_ROW;
+  // group-wise scales (a stage holds K's [KT][nk] and V's [KT][nv] of them;
+  // only the GRP instances carry their code)
+  const bool k_grp = GRP && a.k_mode == KVQ_SCALE_PER_GROUP, v_grp = GRP && a.v_mode == KVQ_SCALE_PER_GROUP;
+  const int nk = a.sk_n, nv = a.sv_n, lg = a.log2_gs;
+  // V scales in a stage, and the stage stride (compile-time without groups)
+  const uint32_t v_sc_off = 2 * Gm::CODE_BYTES + KT * 4 * (GRP && nk > 1 ? nk : 1);
+  const uint32_t stage_bytes = GRP ? (uint32_t)a.stage_stride : (uint32_t)Gm::STAGE_STRIDE;
+  // logits take a per-key factor; V^T columns carry scales under the normaliser 2^F
+  const bool k_sc = k_row || k_grp, v_sc = v_row || v_grp;
 
   if (warp == kProducer) {
     // ============================================================ producer
@@ -295,7 +304,10 @@ __global__ void __launch_bounds__(kTcWarps * 32, 1)
     // ========================================================== K dequant
     // thread = key 32 q + lane of the tile = TMEM lane of the K operand; the
     // two channel halves are written (and freed by QK^T) one after the other,
-    // each converted before the wait for the QK^T that frees it
+    // each converted before the wait for the QK^T that frees it.  Per-group K
+    // scales: the key's columns carry code * s_g / 2^E, 2^E the power of two
+    // at or above its largest group scale (the softmax multiplies the logit
+    // by 2^E, as by a per-row scale)
     const int q = warp - kDqK, kk = 32 * q + lane;
     const uint32_t t_k = tmem + ((uint32_t)(32 * q) << 16) + C::K_COL;
     constexpr int HCH = Gm::NCH / 2;  // 16-byte chunks of a channel half
@@ -307,7 +319,14 @@ __global__ void __launch_bounds__(kTcWarps * 32, 1)
       for (int key0 = k0; key0 < k1; key0 += KT, ++it, rp.next(a.stages)) {
         const uint32_t stage = rp.stage;
         wait(&bar_full[stage], rp.phase);
-        const uint8_t* st = ring + (size_t)stage * Gm::STAGE_STRIDE;
+        const uint8_t* st = ring + (size_t)stage * stage_bytes;
+        const float* kgs = reinterpret_cast<const float*>(st + 2 * Gm::CODE_BYTES) + kk * nk;
+        float kinv = 0.0f;
+        if (k_grp) {
+          float mx = 0.0f;
+          for (int g = 0; g < nk; ++g) mx = fmaxf(mx, kgs[g]);
+          kinv = mx > 0.0f ? dev::pow2i(-min(126, max(-126, dev::ceil_log2(mx)))) : 0.0f;
+        }
 #pragma unroll 1
         for (int half = 0; half < 2; ++half) {
           // the half's codes are read and converted before the wait for the
@@ -323,6 +342,16 @@ __global__ void __launch_bounds__(kTcWarps * 32, 1)
           uint32_t v[HCH * CW];
 #pragma unroll
           for (int jj = 0; jj < HCH; ++jj) dev::k_cols<DT>(w[jj], v + CW * jj);
+          if (k_grp) {
+            constexpr int CHC = DT == KVQ_INT4 ? 32 : 16;  // channels of a 16-byte chunk (one group)
+#pragma unroll
+            for (int jj = 0; jj < HCH; ++jj) {
+              const float r = kgs[((half * HCH + jj) * CHC) >> lg] * kinv;
+              const uint32_t rr = dev::pack_h2(r, r);
+#pragma unroll
+              for (int m = 0; m < CW; ++m) v[CW * jj + m] = ptx::hmul2_u32(v[CW * jj + m], rr);
+            }
+          }
           if (it > 0) {
             if (half == 0) wait(b_kh0, (it - 1) & 1);                        // QK^T(t-1) read channel half 0
             else wait(&b_qk[(it - 1) & 1], ((it - 1) >> 1) & 1);             // QK^T(t-1) complete
@@ -346,7 +375,10 @@ __global__ void __launch_bounds__(kTcWarps * 32, 1)
     // lane quarter q of each 128-channel half: two 16-lane tiles of V^T.
     // Per-row V scale: the columns of key k carry vs_k / 2^F, F the power of
     // two at or above the largest scale of the piece so far (keys past the
-    // sequence end get 0); the softmax warps track the same F.
+    // sequence end get 0); the softmax warps track the same F.  Per-group: the
+    // same with the scale of the group of this warp's channels (the 32
+    // channels a lane quarter holds in one half lie in one group), F over
+    // every group of the piece's keys.
     const int q = warp - kDqV;
     const int ld_key = ((lane >> 3) & 1) * 8 + (lane & 7), ld_chunk = lane >> 4;
     const int c = lane & 3;
@@ -359,29 +391,42 @@ __global__ void __launch_bounds__(kTcWarps * 32, 1)
       for (int key0 = k0; key0 < k1; key0 += KT, ++it, rp.next(a.stages)) {
         const uint32_t stage = rp.stage;
         wait(&bar_full[stage], rp.phase);
-        const uint8_t* st = ring + (size_t)stage * Gm::STAGE_STRIDE;
+        const uint8_t* st = ring + (size_t)stage * stage_bytes;
         const uint32_t sv = ptx::smem_u32(st) + Gm::CODE_BYTES;
+        const float* vsp = reinterpret_cast<const float*>(st + v_sc_off);
         uint32_t s_lo[8], s_hi[8];
-        if (v_row) {
-          const float* vsp = reinterpret_cast<const float*>(st + 2 * Gm::CODE_BYTES) + KT;
-          float vm = 0.0f;
-#pragma unroll
-          for (int i = 0; i < KT / 32; ++i)
-            if (key0 + 32 * i + lane < L) vm = fmaxf(vm, vsp[32 * i + lane]);
-          vm = ptx::redux_max(vm);
-          if (vm > 0.0f) F = max(F, min(126, max(-126, dev::ceil_log2(vm))));
-          const float inv = dev::pow2i(-F);
+        float vinv = 0.0f;
+        // the scale pairs of keys (2c, 2c + 1) and (2c + 8, 2c + 9) of each
+        // 16-key group, scale index j of a key = key * stride + j
+        auto v_pairs = [&](int stride, int j) {
 #pragma unroll
           for (int kg = 0; kg < 8; ++kg) {
             const int ka = 16 * kg + 2 * c, kb = ka + 8;
-            const float2 va = *reinterpret_cast<const float2*>(vsp + ka);
-            const float2 vb = *reinterpret_cast<const float2*>(vsp + kb);
-            s_lo[kg] = dev::pack_h2(key0 + ka < L ? va.x * inv : 0.0f, key0 + ka + 1 < L ? va.y * inv : 0.0f);
-            s_hi[kg] = dev::pack_h2(key0 + kb < L ? vb.x * inv : 0.0f, key0 + kb + 1 < L ? vb.y * inv : 0.0f);
+            s_lo[kg] = dev::pack_h2(key0 + ka < L ? vsp[ka * stride + j] * vinv : 0.0f,
+                                    key0 + ka + 1 < L ? vsp[(ka + 1) * stride + j] * vinv : 0.0f);
+            s_hi[kg] = dev::pack_h2(key0 + kb < L ? vsp[kb * stride + j] * vinv : 0.0f,
+                                    key0 + kb + 1 < L ? vsp[(kb + 1) * stride + j] * vinv : 0.0f);
           }
+        };
+        if (v_row || v_grp) {
+          float vm = 0.0f;
+#pragma unroll
+          for (int i = 0; i < KT / 32; ++i)
+            if (key0 + 32 * i + lane < L) {
+              if (v_row) {
+                vm = fmaxf(vm, vsp[32 * i + lane]);
+              } else {
+                for (int g = 0; g < nv; ++g) vm = fmaxf(vm, vsp[(32 * i + lane) * nv + g]);
+              }
+            }
+          vm = ptx::redux_max(vm);
+          if (vm > 0.0f) F = max(F, min(126, max(-126, dev::ceil_log2(vm))));
+          vinv = dev::pow2i(-F);
+          if (v_row) v_pairs(1, 0);
         }
 #pragma unroll 1
         for (int hh = 0; hh < C::NH; ++hh) {
+          if (v_grp) v_pairs(nv, (128 * hh + 32 * q) >> lg);
           uint32_t f0[32], f1[32];  // lane tiles 0 / 1: 8 key groups x 4 registers
           if constexpr (DT == KVQ_INT4) {
             // chunk 4 hh + q (32 channels): tile t = channel pair t of each 4
@@ -413,7 +458,7 @@ __global__ void __launch_bounds__(kTcWarps * 32, 1)
               dev::v_frag<DT>(R[2], R[3], 0, &f1[4 * kg]);
             }
           }
-          if (v_row) {
+          if (v_row || v_grp) {
 #pragma unroll
             for (int kg = 0; kg < 8; ++kg) {
               f0[4 * kg] = ptx::hmul2_u32(f0[4 * kg], s_lo[kg]);
@@ -550,7 +595,7 @@ __global__ void __launch_bounds__(kTcWarps * 32, 1)
     auto epilogue = [&](int u, uint32_t last, float m0, float m1, int F) {
       wait(&b_pv[last & 1], (last >> 1) & 1);
       ptx::tc_fence_after();
-      float to_true = v_row ? dev::pow2i(F) : 1.0f;
+      float to_true = v_sc ? dev::pow2i(F) : 1.0f;
       if constexpr (DT == KVQ_FP8_E4M3) to_true *= 256.0f;
       float* lse = a.part_lse + (size_t)u * rows;
 #pragma unroll 1
@@ -694,7 +739,7 @@ __global__ void __launch_bounds__(kTcWarps * 32, 1)
       ptx::named_bar_sync(1, 128);  // this piece's row factors are visible
 
       float mu0 = -INFINITY, mu1 = -INFINITY;  // reference maxima of rows lane, lane + 32
-      int F = v_row ? -126 : 0;                // V-scale normaliser exponent
+      int F = v_sc ? -126 : 0;                 // V-scale normaliser exponent
       for (int key0 = k0; key0 < k1; key0 += KT, ++it, rp.next(a.stages)) {
         const bool first = key0 == k0;
         const uint32_t stage = rp.stage;
@@ -704,11 +749,26 @@ __global__ void __launch_bounds__(kTcWarps * 32, 1)
 
         const int key = key0 + kk;
         float ks = 1.0f, vs = 0.0f;  // vs only sets the normaliser F here; V^T carries the scale
-        if (k_row || v_row) {
+        if (k_sc || v_sc) {
           wait(&bar_full[stage], rp.phase);
-          const float* sc = reinterpret_cast<const float*>(ring + (size_t)stage * Gm::STAGE_STRIDE + 2 * Gm::CODE_BYTES);
-          if (k_row) ks = sc[kk];
-          if (v_row && key < L) vs = sc[KT + kk];
+          const uint8_t* st = ring + (size_t)stage * stage_bytes;
+          const float* sc = reinterpret_cast<const float*>(st + 2 * Gm::CODE_BYTES);
+          const float* scv = reinterpret_cast<const float*>(st + v_sc_off);
+          if (k_row) {
+            ks = sc[kk];
+          } else if (k_grp) {
+            // the power of two the K dequant divided this key's columns by
+            float mx = 0.0f;
+            for (int g = 0; g < nk; ++g) mx = fmaxf(mx, sc[kk * nk + g]);
+            ks = mx > 0.0f ? dev::pow2i(min(126, max(-126, dev::ceil_log2(mx)))) : 1.0f;
+          }
+          if (key < L) {
+            if (v_row) {
+              vs = scv[kk];
+            } else if (v_grp) {
+              for (int g = 0; g < nv; ++g) vs = fmaxf(vs, scv[kk * nv + g]);
+            }
+          }
         }
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(&bar_empty[stage]);
@@ -732,7 +792,7 @@ __global__ void __launch_bounds__(kTcWarps * 32, 1)
               y[r + 2] = softcap * dev::tanh_fast(y[r + 2] * ks * a4.z * inv_cap) * kLog2e;
               y[r + 3] = softcap * dev::tanh_fast(y[r + 3] * ks * a4.w * inv_cap) * kLog2e;
             }
-          } else if (k_row) {
+          } else if (k_sc) {
 #pragma unroll
             for (int r = 0; r < NR; ++r) y[r] *= ks;
           }
@@ -775,7 +835,7 @@ __global__ void __launch_bounds__(kTcWarps * 32, 1)
         const bool ovf = __any_sync(0xffffffffu, dmax > 8.0f);
         float* f_flag = f_vmax + 8 * (it & 1);  // [4] overflow flags, [4] V-scale maxima; by tile parity
         {
-          const float vm = v_row ? ptx::redux_max(vs) : 0.0f;
+          const float vm = v_sc ? ptx::redux_max(vs) : 0.0f;
           if (lane == 0) {
             f_flag[q] = ovf ? 1.0f : 0.0f;
             f_flag[4 + q] = vm;
@@ -786,7 +846,7 @@ __global__ void __launch_bounds__(kTcWarps * 32, 1)
 
         // V-scale normaliser (the dequant warps track the same F)
         float fs = 1.0f;
-        if (v_row) {
+        if (v_sc) {
           const float vm = fmaxf(fmaxf(f_flag[4], f_flag[5]), fmaxf(f_flag[6], f_flag[7]));
           if (vm > 0.0f) {
             const int fn = min(126, max(-126, dev::ceil_log2(vm)));
@@ -903,7 +963,7 @@ __global__ void __launch_bounds__(kTcWarps * 32, 1)
 
 // Raises (never lowers) the kernel's dynamic shared-memory limit on the
 // current device, then launches one CTA per grid slot.
-template <int DT, int D, int NR>
+template <int DT, int D, int NR, bool GRP>
 cudaError_t launch_decode_tc_d(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeArgs& a, int grid,
                                size_t smem, cudaStream_t stream) {
   static int smem_set[64] = {};
@@ -912,24 +972,24 @@ cudaError_t launch_decode_tc_d(const CUtensorMap& tk, const CUtensorMap& tv, con
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (smem_set[dev] < (int)smem) {
-    e = cudaFuncSetAttribute(decode_tc_kernel<DT, D, NR>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    e = cudaFuncSetAttribute(decode_tc_kernel<DT, D, NR, GRP>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     smem_set[dev] = (int)smem;
   }
-  return launch_pdl(decode_tc_kernel<DT, D, NR>, grid, kTcWarps * 32, smem, stream, tk, tv, a);
+  return launch_pdl(decode_tc_kernel<DT, D, NR, GRP>, grid, kTcWarps * 32, smem, stream, tk, tv, a);
 }
 
 // head_dim 256: nr 32 or 48; head_dim 128: nr 32, 48 or 64.
-template <int DT>
+template <int DT, bool GRP>
 cudaError_t dispatch_decode_tc(int head_dim, int nr, const CUtensorMap& tk, const CUtensorMap& tv,
                                const DecodeArgs& a, int grid, size_t smem, cudaStream_t stream) {
   if (head_dim == 256) {
-    if (nr == 32) return launch_decode_tc_d<DT, 256, 32>(tk, tv, a, grid, smem, stream);
-    if (nr == 48) return launch_decode_tc_d<DT, 256, 48>(tk, tv, a, grid, smem, stream);
+    if (nr == 32) return launch_decode_tc_d<DT, 256, 32, GRP>(tk, tv, a, grid, smem, stream);
+    if (nr == 48) return launch_decode_tc_d<DT, 256, 48, GRP>(tk, tv, a, grid, smem, stream);
   } else if (head_dim == 128) {
-    if (nr == 32) return launch_decode_tc_d<DT, 128, 32>(tk, tv, a, grid, smem, stream);
-    if (nr == 48) return launch_decode_tc_d<DT, 128, 48>(tk, tv, a, grid, smem, stream);
-    if (nr == 64) return launch_decode_tc_d<DT, 128, 64>(tk, tv, a, grid, smem, stream);
+    if (nr == 32) return launch_decode_tc_d<DT, 128, 32, GRP>(tk, tv, a, grid, smem, stream);
+    if (nr == 48) return launch_decode_tc_d<DT, 128, 48, GRP>(tk, tv, a, grid, smem, stream);
+    if (nr == 64) return launch_decode_tc_d<DT, 128, 64, GRP>(tk, tv, a, grid, smem, stream);
   }
   return cudaErrorInvalidValue;
 }

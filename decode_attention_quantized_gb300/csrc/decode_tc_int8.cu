@@ -6,7 +6,7 @@ namespace kvq {
 
 cudaError_t launch_decode_tc_int8(int head_dim, int nr, const CUtensorMap& tk, const CUtensorMap& tv,
                                  const DecodeArgs& a, int grid, size_t smem, cudaStream_t stream) {
-  return dispatch_decode_tc<KVQ_INT8>(head_dim, nr, tk, tv, a, grid, smem, stream);
+  return dispatch_decode_tc<KVQ_INT8, false>(head_dim, nr, tk, tv, a, grid, smem, stream);
 }
 
 }  // namespace kvq

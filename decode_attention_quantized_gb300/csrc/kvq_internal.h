@@ -65,7 +65,8 @@ struct DecodeArgs {
   const float* v_scale;
   int k_mode, v_mode;
   int sk_n, sv_n;     // fp32 scales per cached row of K / V: 1 PER_ROW, groups PER_GROUP, 0 static
-                      // (the group size itself is the kernel instance's)
+                      // (the mma.sync kernel's group size is its instance's)
+  int log2_gs;        // PER_GROUP: log2 of the channels per group (the tensor-memory kernel); else 0
   int num_blocks, block_size, log2_bs, num_kv_heads;
   int batch, num_q_heads, q_tokens, group, rows, max_blocks_per_seq, max_seq_len;
   float sm_scale, softcap;
@@ -105,18 +106,23 @@ struct TcSmem {
   int ring, q, p, scr, pre, bars, slot, total;
 };
 
-__host__ __device__ constexpr int tc_stage_stride(int row_bytes) {
-  return (2 * kTcKeys * row_bytes + 2 * kTcKeys * 4 + 1023) / 1024 * 1024;
+// One stage: the K and V code rows of kTcKeys keys, then K's [kTcKeys][nk] and
+// V's [kTcKeys][nv] fp32 scales (nk, nv = scales per cached row: 1 per-row,
+// D / group_size per-group; a side with static scales still keeps one slot per
+// key), in 1 KB multiples.
+__host__ __device__ constexpr int tc_stage_stride(int row_bytes, int nk = 1, int nv = 1) {
+  return (2 * kTcKeys * row_bytes + kTcKeys * 4 * ((nk > 1 ? nk : 1) + (nv > 1 ? nv : 1)) + 1023) / 1024 * 1024;
 }
 
 // ring: stages x stage stride; q: [D/64 slabs][nr rows][128 B] f16; p: two
 // [2 slabs][nr rows][128 B] f16 buffers; scr: row factors, positions and the
 // per-warp row maxima / reference maxima / rescale factors; pre: split plan;
 // bars: mbarriers; slot: TMEM address + abort flag.
-__host__ __device__ constexpr TcSmem tc_smem_layout(int head_dim, int row_bytes, int nr, int stages, int batch) {
+__host__ __device__ constexpr TcSmem tc_smem_layout(int head_dim, int row_bytes, int nr, int stages, int batch,
+                                                    int stage_stride) {
   TcSmem s{};
   s.ring = 0;
-  s.q = stages * tc_stage_stride(row_bytes);
+  s.q = stages * stage_stride;
   s.p = s.q + nr * 2 * head_dim;
   s.scr = s.p + 2 * nr * 2 * kTcKeys;
   s.pre = s.scr + (2 * nr + 3 * 4 * nr + 16) * 4;
@@ -168,6 +174,13 @@ cudaError_t launch_decode_tc_fp8(int head_dim, int nr, const CUtensorMap& tk, co
                                  const DecodeArgs& a, int grid, size_t smem, cudaStream_t stream);
 cudaError_t launch_decode_tc_int4(int head_dim, int nr, const CUtensorMap& tk, const CUtensorMap& tv,
                                   const DecodeArgs& a, int grid, size_t smem, cudaStream_t stream);
+// The same with group-wise scales on either side.
+cudaError_t launch_decode_tc_grp_int8(int head_dim, int nr, const CUtensorMap& tk, const CUtensorMap& tv,
+                                      const DecodeArgs& a, int grid, size_t smem, cudaStream_t stream);
+cudaError_t launch_decode_tc_grp_fp8(int head_dim, int nr, const CUtensorMap& tk, const CUtensorMap& tv,
+                                     const DecodeArgs& a, int grid, size_t smem, cudaStream_t stream);
+cudaError_t launch_decode_tc_grp_int4(int head_dim, int nr, const CUtensorMap& tk, const CUtensorMap& tv,
+                                      const DecodeArgs& a, int grid, size_t smem, cudaStream_t stream);
 
 cudaError_t occupancy_decode_int8(int head_dim, int nt, int threads, size_t smem, int* blocks_per_sm);
 cudaError_t occupancy_decode_fp8(int head_dim, int nt, int threads, size_t smem, int* blocks_per_sm);

@@ -1,8 +1,9 @@
 """Group-wise scales (KVQ_SCALE_PER_GROUP) on the GPU against the fp64 oracle:
 kvq_append's codes and group scales byte for byte, kvq_decode + kvq_combine
 within the decode tolerance, over element types, head dims, group sizes,
-scale-mode pairs and query-row counts (every row count runs on the mma.sync
-kernel's grouped layout when a side is PER_GROUP)."""
+scale-mode pairs and query-row counts: up to 16 rows per kv head (and above
+the tensor-memory bound) on the mma.sync kernel's grouped layout, 17..48 rows
+at head_dim 256 and 17..64 at 128 on the tensor-memory kernel."""
 import math
 
 import numpy as np
@@ -72,10 +73,38 @@ def test_group_with_the_other_modes(lib, orc, dt, km, vm):
     run(orc, workload(dt, km, vm, 128, 32, seed=10 * km + vm + dt))
 
 
+TC_GROUP = [  # dtype, D, group size, k_mode, v_mode, G, T (17..48 rows at D 256, 17..64 at 128)
+    (kvq.INT4, 256, 64, 4, 4, 6, 8), (kvq.INT8, 256, 32, 4, 4, 8, 6), (kvq.FP8_E4M3, 256, 128, 4, 4, 4, 5),
+    (kvq.INT4, 128, 32, 4, 4, 8, 8), (kvq.INT8, 128, 128, 4, 1, 5, 7), (kvq.FP8_E4M3, 128, 64, 1, 4, 3, 6),
+    (kvq.INT4, 256, 32, 4, 3, 6, 6), (kvq.INT8, 128, 64, 2, 4, 8, 4), (kvq.INT4, 128, 128, 3, 4, 7, 7),
+]
+
+
+@pytest.mark.parametrize("case", TC_GROUP, ids=lambda c: f"dt{c[0]}-D{c[1]}-g{c[2]}-km{c[3]}vm{c[4]}-rows{c[5] * c[6]}")
+def test_group_on_the_tensor_memory_kernel(lib, orc, case):
+    """Group scales on the tcgen05 kernel: K columns carry code x group scale
+    over a per-key power of two, V^T columns the group scale under the
+    running normaliser; several 128-key tiles and pieces, ragged lengths."""
+    dt, D, gs, km, vm, G, T = case
+    w = workload(dt, km, vm, D, gs, G=G, T=T, L=(1500, T - 1, 129, 700), bs=32, seed=D + gs + G * T)
+    gw, params, bufs, q, _ = run(orc, w)
+    ref = bufs.out.clone()
+    kvq.decode_step(gw.cache, params, q, gw.block_table, gw.seq_lens, bufs, gw.head_sink)
+    assert torch.equal(bufs.out, ref)
+
+
+def test_group_on_the_tensor_memory_kernel_with_sink_softcap_window(lib, orc):
+    w = workload(kvq.INT4, kvq.PER_GROUP, kvq.PER_GROUP, 256, 64, G=6, T=8, L=(900, 300, 33), bs=32,
+                 use_sink=True, softcap=30.0, seed=77)
+    run(orc, w)
+    run(orc, w, window=200)
+
+
 @pytest.mark.parametrize("G,T", [(1, 1), (8, 1), (6, 8), (8, 8), (3, 5)])
 def test_group_row_counts(lib, orc, G, T):
-    """1 to 64 query rows per kv head, all on the grouped layout (row groups of
-    8, one key warp each above 32 rows)."""
+    """1 to 64 query rows per kv head: the grouped layout up to 16 rows and
+    above 48 at head_dim 256 (row groups of 8, one key warp each above 32
+    rows), the tensor-memory kernel for 48."""
     run(orc, workload(kvq.INT4, kvq.PER_GROUP, kvq.PER_GROUP, 256, 64, G=G, T=T, L=(200, T, 66), seed=G + T))
 
 
