@@ -79,7 +79,11 @@ kvq_status check_cache(const kvq_cache* c) {
   if (c->num_blocks <= 0 || c->num_kv_heads <= 0 || c->head_dim <= 0) return KVQ_ERR_INVALID_ARG;
   if (!pow2(c->block_size) || c->block_size < 16 || c->block_size > (1 << 20)) return KVQ_ERR_INVALID_ARG;
   if ((long long)c->num_blocks * c->block_size > (1LL << 31) - 1) return KVQ_ERR_INVALID_ARG;
-  if (c->head_dim != 64 && c->head_dim != 128 && c->head_dim != 256) return KVQ_ERR_UNSUPPORTED;
+  // head_dim 576 (absorbed MLA: 512 latent + 64 rotary channels): LATENT with
+  // 8-bit codes and per-row or static scales, on the mma.sync wide layout
+  const bool latent576 = c->head_dim == 576 && c->layout == KVQ_LAYOUT_LATENT && c->dtype != KVQ_INT4 &&
+                         c->k_mode != KVQ_SCALE_PER_GROUP;
+  if (c->head_dim != 64 && c->head_dim != 128 && c->head_dim != 256 && !latent576) return KVQ_ERR_UNSUPPORTED;
   if (!c->k_codes || !c->v_codes || !c->k_scale || !c->v_scale) return KVQ_ERR_INVALID_ARG;
   if (!aligned(c->k_codes, 16) || !aligned(c->v_codes, 16)) return KVQ_ERR_INVALID_ARG;
   if (!aligned(c->k_scale, scales_per_row(c, c->k_mode) ? 16 : 4)) return KVQ_ERR_INVALID_ARG;
@@ -148,13 +152,14 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 // per-group scales only when a side has them (a 16-row fp8 stage of head_dim
 // 128 is then 16 KB, so four CTAs with three stages each fit on an SM): K's
 // [kTile][sk_n] floats, then V's [kTile][sv_n] at kTile * max(1, sk_n)
-// floats.  1 KB multiples keep every stage on the 128-byte swizzle's
-// alignment.
-size_t stage_stride(const kvq_cache* c) {
+// floats.  A LATENT cache on the mma.sync kernel (alias) keeps the K side
+// only: V is read from it.  1 KB multiples keep every stage on the 128-byte
+// swizzle's alignment.
+size_t stage_stride(const kvq_cache* c, bool alias) {
   const size_t code = (size_t)kTile * row_bytes(c);
-  const int nk = scales_per_row(c, c->k_mode), nv = scales_per_row(c, c->v_mode);
-  const size_t sc = (nk || nv) ? (size_t)kTile * 4 * ((nk > 1 ? nk : 1) + (nv > 1 ? nv : 1)) : 0;
-  return (2 * code + sc + 1023) / 1024 * 1024;
+  const int nk = scales_per_row(c, c->k_mode), nv = alias ? 0 : scales_per_row(c, c->v_mode);
+  const size_t sc = (nk || nv) ? (size_t)kTile * 4 * ((nk > 1 ? nk : 1) + (alias ? 0 : (nv > 1 ? nv : 1))) : 0;
+  return ((alias ? 1 : 2) * code + sc + 1023) / 1024 * 1024;
 }
 
 size_t fixed_smem(const kvq_cache* c, int row_groups, int key_warps, int nt, int batch, int stages) {
@@ -235,9 +240,16 @@ kvq_status make_plan_uncached(const kvq_cache* c, const kvq_decode_params* p, co
   P.row_groups = (P.rows + 7) / 8;
   P.key_warps = P.row_groups <= 2 ? 4 : (P.row_groups <= 4 ? 2 : 1);
   // 17..48 rows (e.g. drafts x GQA group): the wide layout, 4 key quarters x 2
-  // row halves of nt n-tiles, when a channel quarter spans >= 2 code chunks
+  // row halves of nt n-tiles, when a channel quarter spans >= 2 code chunks;
+  // head_dim 576 takes it for every row count up to 48 (its rows are too long
+  // for one warp's registers)
   const bool wide_fits = c->dtype == KVQ_INT4 ? c->head_dim == 256 : c->head_dim >= 128;
-  P.nt = (wide_fits && !any_group(c) && P.row_groups >= 3 && P.row_groups <= 6) ? (P.row_groups + 1) / 2 : 0;
+  if (c->head_dim == 576) {
+    if (P.rows > 48) return KVQ_ERR_UNSUPPORTED;
+    P.nt = (P.row_groups + 1) / 2;
+  } else {
+    P.nt = (wide_fits && !any_group(c) && P.row_groups >= 3 && P.row_groups <= 6) ? (P.row_groups + 1) / 2 : 0;
+  }
   if (P.nt > 0) {
     P.row_groups = 2;
     P.key_warps = 4;
@@ -245,7 +257,7 @@ kvq_status make_plan_uncached(const kvq_cache* c, const kvq_decode_params* p, co
   const int n_cw = P.row_groups * P.key_warps;
   P.threads = 32 * (n_cw + 1);
   const int B = p->batch > 0 ? p->batch : 1;
-  const size_t stride = stage_stride(c);
+  const size_t stride = stage_stride(c, c->layout == KVQ_LAYOUT_LATENT);
   P.stride = stride;
   // the most CTAs per SM whose ring still holds >= 3 stages (more warps per
   // SM hide more latency); one CTA with >= 2 stages as the last resort
@@ -288,7 +300,7 @@ kvq_status make_plan_uncached(const kvq_cache* c, const kvq_decode_params* p, co
 // shapes reuse it (no occupancy query on the hot path).
 struct PlanKey {
   int dev, dtype, k_mode, v_mode, group_size, head_dim, num_kv_heads, block_size, batch, num_q_heads,
-      q_tokens, max_blocks_per_seq, max_seq_len, no_tc;
+      q_tokens, max_blocks_per_seq, max_seq_len, no_tc, layout;
   bool operator==(const PlanKey& o) const { return std::memcmp(this, &o, sizeof(PlanKey)) == 0; }
 };
 constexpr int kPlanCache = 64;
@@ -313,6 +325,7 @@ kvq_status make_plan(const kvq_cache* c, const kvq_decode_params* p, const Devic
   k.max_blocks_per_seq = p->max_blocks_per_seq;
   k.max_seq_len = p->max_seq_len;
   k.no_tc = (p->flags & KVQ_DECODE_NO_TCGEN05) ? 1 : 0;
+  k.layout = c->layout;
   {
     std::lock_guard<std::mutex> lk(g_mu);
     for (int i = 0; i < g_plan_count; ++i)
@@ -335,7 +348,7 @@ kvq_status encode_codes_map(const kvq_cache* c, void* base, CUtensorMap* tm) {
   PFN_cuTensorMapEncodeTiled_v12000 enc;
   if (kvq_status s = encoder(&enc)) return s;
   const int dp = row_bytes(c);
-  const int span = dp >= 128 ? 128 : dp;
+  const int span = dp % 128 == 0 ? 128 : (dp % 64 == 0 ? 64 : 32);  // a 576-byte row: nine 64-byte slabs
   const cuuint64_t dims[4] = {(cuuint64_t)dp, (cuuint64_t)c->block_size, (cuuint64_t)c->num_kv_heads,
                               (cuuint64_t)c->num_blocks};
   const cuuint64_t strides[3] = {(cuuint64_t)dp, (cuuint64_t)dp * c->block_size,
@@ -375,6 +388,7 @@ kvq_status check_norm_rope(const kvq_norm_rope* p, int head_dim, const int64_t* 
   r.interleaved = p->rotary_interleaved ? 1 : 0;
   r.max_pos = rd > 0 ? p->max_position : 0;
   if (p->hadamard != 0 && p->hadamard != 1) return KVQ_ERR_INVALID_ARG;
+  if (p->hadamard && (head_dim & (head_dim - 1))) return KVQ_ERR_UNSUPPORTED;  // a power of two
   r.hadamard = p->hadamard;
   r.had_scale = 1.0f / std::sqrt((float)head_dim);
   *out = r;
@@ -484,6 +498,8 @@ kvq_status decode_impl(const kvq_cache* cache, const kvq_decode_params* params, 
   // role pipeline) is charged as a few tiles when the split is planned
   a.piece_cost = P.tc_nr ? kTcPieceCost : kPieceCost;
   a.bt_div = bt_div;
+  // the mma.sync kernel reads a LATENT cache's V from the K codes it loaded
+  a.v_alias = (cache->layout == KVQ_LAYOUT_LATENT && !P.tc_nr) ? 1 : 0;
   a.early_reads = early_reads;
   char* ws = static_cast<char*>(workspace);
   a.plan = reinterpret_cast<int*>(ws);
@@ -565,7 +581,7 @@ KVQ_API kvq_status kvq_append_norm_rope(const kvq_cache* cache, const kvq_norm_r
 KVQ_API kvq_status kvq_norm_rope_apply(const kvq_norm_rope* prologue, const void* x, void* y,
                                        const int64_t* positions, int32_t n_tokens, int32_t num_heads,
                                        int32_t head_dim, kvq_stream_t stream) {
-  if (head_dim != 64 && head_dim != 128 && head_dim != 256) return KVQ_ERR_UNSUPPORTED;
+  if (head_dim != 64 && head_dim != 128 && head_dim != 256 && head_dim != 576) return KVQ_ERR_UNSUPPORTED;
   if (n_tokens < 0 || num_heads <= 0) return KVQ_ERR_INVALID_ARG;
   NormRopeArgs a{};
   if (kvq_status s = check_norm_rope(prologue, head_dim, positions, &a.pro)) return s;

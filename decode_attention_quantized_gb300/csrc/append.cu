@@ -39,9 +39,13 @@ __device__ __forceinline__ void load_bf16(const uint16_t* p, float (&x)[E]) {
     x[2] = __uint_as_float(v.y << 16);
     x[3] = __uint_as_float(v.y & 0xFFFF0000u);
   } else {
-    uint32_t v = *reinterpret_cast<const uint32_t*>(p);
-    x[0] = __uint_as_float(v << 16);
-    x[1] = __uint_as_float(v & 0xFFFF0000u);
+    // E even (2, or 18 at head_dim 576): 32-bit loads
+#pragma unroll
+    for (int i = 0; i < E / 2; ++i) {
+      const uint32_t v = reinterpret_cast<const uint32_t*>(p)[i];
+      x[2 * i] = __uint_as_float(v << 16);
+      x[2 * i + 1] = __uint_as_float(v & 0xFFFF0000u);
+    }
   }
 }
 
@@ -56,8 +60,13 @@ __device__ __forceinline__ void store_bytes(uint8_t* dst, const uint8_t (&b)[NB]
     *reinterpret_cast<uint32_t*>(dst) = b[0] | (b[1] << 8) | (b[2] << 16) | ((uint32_t)b[3] << 24);
   } else if constexpr (NB == 2) {
     *reinterpret_cast<uint16_t*>(dst) = (uint16_t)(b[0] | (b[1] << 8));
+  } else if constexpr (NB % 2 == 0) {
+    // 18 bytes (head_dim 576): 16-bit stores
+#pragma unroll
+    for (int i = 0; i < NB / 2; ++i) reinterpret_cast<uint16_t*>(dst)[i] = (uint16_t)(b[2 * i] | (b[2 * i + 1] << 8));
   } else {
-    dst[0] = b[0];
+#pragma unroll
+    for (int i = 0; i < NB; ++i) dst[i] = b[i];
   }
 }
 
@@ -128,6 +137,7 @@ __device__ bool norm_rope_row(const NormRope& p, int n, int lane, float (&x)[E],
     }
     __syncwarp();
   }
+  if constexpr ((E & (E - 1)) == 0) {  // a power of two (the host checks head_dim)
   if (p.hadamard) {
     // Sylvester-order butterflies: span s pairs channels c and c + s (c & s
     // == 0) into (a + b, a - b); spans below E stay inside the lane, the rest
@@ -153,6 +163,7 @@ __device__ bool norm_rope_row(const NormRope& p, int n, int lane, float (&x)[E],
     }
 #pragma unroll
     for (int e = 0; e < E; ++e) x[e] = __fmul_rn(x[e], p.had_scale);
+  }
   }
 #pragma unroll
   for (int e = 0; e < E; ++e) x[e] = bf16_rne(x[e]);
@@ -288,7 +299,9 @@ __global__ void __launch_bounds__(256) norm_rope_kernel(const NormRopeArgs a) {
     v.x = b[0] | ((uint32_t)b[1] << 16); v.y = b[2] | ((uint32_t)b[3] << 16);
     *reinterpret_cast<uint2*>(a.y + off) = v;
   } else {
-    *reinterpret_cast<uint32_t*>(a.y + off) = b[0] | ((uint32_t)b[1] << 16);
+#pragma unroll
+    for (int i = 0; i < E / 2; ++i)
+      reinterpret_cast<uint32_t*>(a.y + off)[i] = b[2 * i] | ((uint32_t)b[2 * i + 1] << 16);
   }
 }
 
@@ -301,6 +314,7 @@ cudaError_t launch_norm_rope(const NormRopeArgs& a, cudaStream_t stream) {
     case 64: return launch_pdl(norm_rope_kernel<64>, blocks, 256, 0, stream, a);
     case 128: return launch_pdl(norm_rope_kernel<128>, blocks, 256, 0, stream, a);
     case 256: return launch_pdl(norm_rope_kernel<256>, blocks, 256, 0, stream, a);
+    case 576: return launch_pdl(norm_rope_kernel<576>, blocks, 256, 0, stream, a);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -312,6 +326,7 @@ cudaError_t launch_append(const AppendArgs& a, cudaStream_t stream) {
     case 64: return launch_pdl(append_kernel<64>, blocks, 256, 0, stream, a);
     case 128: return launch_pdl(append_kernel<128>, blocks, 256, 0, stream, a);
     case 256: return launch_pdl(append_kernel<256>, blocks, 256, 0, stream, a);
+    case 576: return launch_pdl(append_kernel<576>, blocks, 256, 0, stream, a);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -140,8 +140,14 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const Combi
     *reinterpret_cast<uint4*>(dst) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
   } else if constexpr (E == 4) {
     *reinterpret_cast<uint2*>(dst) = make_uint2(packed[0], packed[1]);
-  } else {
+  } else if constexpr (E == 2) {
     *reinterpret_cast<uint32_t*>(dst) = packed[0];
+  } else {
+    // head_dim 576: 18 channels a lane, the leading v_head_size (a multiple of
+    // 8) written pair by pair
+#pragma unroll
+    for (int j = 0; j < E / 2; ++j)
+      if (lane * E + 2 * j < a.out_dim) reinterpret_cast<uint32_t*>(dst)[j] = packed[j];
   }
 }
 
@@ -188,6 +194,7 @@ cudaError_t launch_combine(const CombineArgs& a, cudaStream_t stream) {
     case 64: return launch_pdl(combine_kernel<64>, blocks, threads, 0, stream, a);
     case 128: return launch_pdl(combine_kernel<128>, blocks, threads, 0, stream, a);
     case 256: return launch_pdl(combine_kernel<256>, blocks, threads, 0, stream, a);
+    case 576: return launch_pdl(combine_kernel<576>, blocks, threads, 0, stream, a);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -243,6 +243,77 @@ __device__ __forceinline__ float q_prologue(const DecodeArgs& a, int rq, int b, 
   return fminf(alpha, 3.4028234e38f);
 }
 
+// The same Q prologue for rows too long to hold in registers (head_dim 576,
+// 8-bit codes): two passes over the row (its maximum, then the f16 operand),
+// each k-slot pair handed to store(k, value) as it is made; lane group c
+// holds channels 16 j + 4 c .. + 3 of k-step j, placed in k-slots 16 j + 2 c
+// (channels + 0, + 1) and 16 j + 8 + 2 c (+ 2, + 3), as q_prologue does.
+template <int DT, int D, class Store>
+__device__ __forceinline__ float q_prologue_long(const DecodeArgs& a, int rq, int b, int h, int c, Store store) {
+  static_assert(DT != KVQ_INT4, "8-bit codes: four channels per lane of each k-step");
+  constexpr float kLog2e = 1.4426950408889634f;
+  constexpr int NKS = D / 16;
+  const int G = a.group, T = a.q_tokens, Hq = a.num_q_heads;
+  const bool qvalid = rq < a.rows;
+  const int tq = qvalid ? div_small(rq, __frcp_rn((float)G)) : 0, gq = qvalid ? rq - tq * G : 0;
+  const uint16_t* qp = a.q + (((size_t)b * T + tq) * Hq + (size_t)h * G + gq) * D;
+  const bool kc = a.k_mode == KVQ_SCALE_PER_CHANNEL;
+  const float* ksp = a.k_scale + (size_t)h * D;
+  auto load = [&](int j, float (&v)[4]) {
+    const uint2 w = qvalid ? *reinterpret_cast<const uint2*>(qp + 16 * j + 4 * c) : make_uint2(0, 0);
+    v[0] = __uint_as_float(w.x << 16);
+    v[1] = __uint_as_float(w.x & 0xFFFF0000u);
+    v[2] = __uint_as_float(w.y << 16);
+    v[3] = __uint_as_float(w.y & 0xFFFF0000u);
+  };
+  int e_tot = 0;
+  float sk = 1.0f;
+  if (kc) {
+    float km = 0.0f;
+#pragma unroll 4
+    for (int j = 0; j < NKS; ++j)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) km = fmaxf(km, fabsf(ksp[16 * j + 4 * c + i]));
+    km = fmaxf(km, __shfl_xor_sync(0xffffffffu, km, 1));
+    km = fmaxf(km, __shfl_xor_sync(0xffffffffu, km, 2));
+    const int ek = km > 0.0f ? min(126, max(-126, ceil_log2(km))) : 0;
+    sk = pow2i(-ek);
+    e_tot += ek;
+  }
+  float qm = 0.0f;
+#pragma unroll 4
+  for (int j = 0; j < NKS; ++j) {
+    float v[4];
+    load(j, v);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      if (kc) v[i] *= ksp[16 * j + 4 * c + i] * sk;
+      qm = fmaxf(qm, fabsf(v[i]));
+    }
+  }
+  qm = fmaxf(qm, __shfl_xor_sync(0xffffffffu, qm, 1));
+  qm = fmaxf(qm, __shfl_xor_sync(0xffffffffu, qm, 2));
+  const int eq = qm > 0.0f ? min(126, max(-126, ceil_log2(qm))) : 0;
+  const float sq = pow2i(-eq);
+  e_tot += eq;
+#pragma unroll 4
+  for (int j = 0; j < NKS; ++j) {
+    float v[4];
+    load(j, v);
+    if (kc) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) v[i] *= ksp[16 * j + 4 * c + i] * sk;
+    }
+    store(16 * j + 2 * c, pack_h2(v[0] * sq, v[1] * sq));
+    store(16 * j + 8 + 2 * c, pack_h2(v[2] * sq, v[3] * sq));
+  }
+  float base = a.sm_scale;
+  if (a.k_mode == KVQ_SCALE_PER_TENSOR) base *= a.k_scale[0];
+  float alpha = ldexpf(base, e_tot);
+  if (a.softcap <= 0.0f) alpha *= kLog2e;
+  return fminf(alpha, 3.4028234e38f);
+}
+
 }  // namespace dev
 
 // Shared floats of the wide consumer layout with NT n-tiles per row half: the
@@ -287,11 +358,12 @@ __global__ void __launch_bounds__(288, MINB)
     }
     ptx::fence_mbar_init();
   }
-  // Only inputs that no kvq kernel writes (seq_lens, block table, q, static
-  // scales) are read before the wait on the preceding grid on the stream:
-  // the producer waits before its first cache read and the consumers before
-  // their first workspace write, so the plan, the first block ids and the Q
-  // prologue overlap that grid's tail.
+  // With early reads (KVQ_DECODE_EARLY_INPUTS) the inputs the caller vouches
+  // for (seq_lens, block table, q, static scales) are read before the wait on
+  // the preceding grid on the stream: the producer waits before its first
+  // cache read and the consumers before their first workspace write, so the
+  // plan, the first block ids and the Q prologue overlap that grid's tail.
+  // Without them build_slice waits first.
   const Slice<kTile> sp = build_slice<kTile>(a, pl_pre, pl_misc);
   const int t_begin = sp.t_begin, t_end = sp.t_end;
   auto piece = [&](int gt, int& b, int& h, int& k0, int& k1, int& L, int& slot, int& next) {
@@ -352,13 +424,19 @@ __global__ void __launch_bounds__(288, MINB)
       // Q of n-tile kq of this half (warps kq < NT), stored in k-slot order so
       // that ldmatrix yields the B fragments; the rows' logit factors beside it
       if (kq < NT) {
-        uint32_t qf[Gm::NMT][2];
         const int row = rh * RW + kq * 8 + g;
-        const float ag = dev::q_prologue<DT, D>(a, row, b, h, c, qf);
+        float ag;
+        if constexpr (D <= 256) {
+          uint32_t qf[Gm::NMT][2];
+          ag = dev::q_prologue<DT, D>(a, row, b, h, c, qf);
 #pragma unroll
-        for (int ks = 0; ks < Gm::NMT; ++ks) {
-          ptx::st_shared_u32(q_base + q_off(row, ks * 16 + 2 * c), qf[ks][0]);
-          ptx::st_shared_u32(q_base + q_off(row, ks * 16 + 8 + 2 * c), qf[ks][1]);
+          for (int ks = 0; ks < Gm::NMT; ++ks) {
+            ptx::st_shared_u32(q_base + q_off(row, ks * 16 + 2 * c), qf[ks][0]);
+            ptx::st_shared_u32(q_base + q_off(row, ks * 16 + 8 + 2 * c), qf[ks][1]);
+          }
+        } else {
+          ag = dev::q_prologue_long<DT, D>(a, row, b, h, c,
+                                           [&](int k, uint32_t v) { ptx::st_shared_u32(q_base + q_off(row, k), v); });
         }
         if (c == 0) s_alpha[row] = ag;
       }
@@ -392,9 +470,10 @@ __global__ void __launch_bounds__(288, MINB)
         }
         const uint8_t* st = ring + (size_t)stage * a.stage_stride;
         const uint32_t sk_base = ptx::smem_u32(st);
-        const uint32_t sv_base = sk_base + Gm::CODE_BYTES;
-        const float* ks_row = reinterpret_cast<const float*>(st + 2 * Gm::CODE_BYTES);
-        const float* vs_row = ks_row + kTile;
+        // LATENT (v_alias): V is the K codes and scales of the stage
+        const uint32_t sv_base = sk_base + (a.v_alias ? 0 : Gm::CODE_BYTES);
+        const float* ks_row = reinterpret_cast<const float*>(st + (a.v_alias ? 1 : 2) * Gm::CODE_BYTES);
+        const float* vs_row = a.v_alias ? ks_row : ks_row + kTile;
 
         // ---- phase A: scores of this warp's 16 keys x NT n-tiles of rows
         const int kb = key0 + kq * kSub;
@@ -633,6 +712,33 @@ __global__ void __launch_bounds__(288, MINB)
               }
             }
           }
+          if constexpr (QCH % 2 == 1) {
+            // an odd last chunk of the quarter (head_dim 576: nine per quarter):
+            // keys 0-7 and 8-15 of one chunk by a two-matrix load (lanes 0-15
+            // give the row addresses)
+            static_assert(DT != KVQ_INT4, "odd quarters only with 8-bit codes");
+            constexpr int jl = QCH - 1;
+            const uint32_t byte = (uint32_t)(QCH * kq + jl) * 16;
+            const uint32_t addr =
+                sv_base + (byte / Gm::SPAN) * (kTile * Gm::SPAN) + dev::swz<Gm::SPAN>(vrow_off + byte % Gm::SPAN);
+            uint32_t R[2];
+            ptx::ldmatrix_x2_trans(R, addr);
+            uint32_t A[4];
+            if constexpr (DT == KVQ_INT8) {
+              const uint32_t xl = R[0] ^ 0x80808080u, xh = R[1] ^ 0x80808080u;
+              A[0] = dev::i8pair(xl, 0x4240u);
+              A[1] = dev::i8pair(xl, 0x4341u);
+              A[2] = dev::i8pair(xh, 0x4240u);
+              A[3] = dev::i8pair(xh, 0x4341u);
+            } else {
+              A[0] = dev::f8cvt(R[0], 0x0020u);
+              A[1] = dev::f8cvt(R[0], 0x0031u);
+              A[2] = dev::f8cvt(R[1], 0x0020u);
+              A[3] = dev::f8cvt(R[1], 0x0031u);
+            }
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) ptx::mma_16816(acc[jl][nt], A, pb[nt][0], pb[nt][1]);
+          }
         }
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(&bar_empty[stage]);
@@ -743,9 +849,10 @@ __global__ void __launch_bounds__(288, MINB)
       }
       const uint8_t* st = ring + (size_t)stage * a.stage_stride;
       const uint32_t sk_base = ptx::smem_u32(st);
-      const uint32_t sv_base = sk_base + Gm::CODE_BYTES;
-      const float* ks_row = reinterpret_cast<const float*>(st + 2 * Gm::CODE_BYTES);
-      const float* vs_row = ks_row + kTile * (GRP && ngk > 1 ? ngk : 1);
+      // LATENT (v_alias): V is the K codes and scales of the stage
+      const uint32_t sv_base = sk_base + (a.v_alias ? 0 : Gm::CODE_BYTES);
+      const float* ks_row = reinterpret_cast<const float*>(st + (a.v_alias ? 1 : 2) * Gm::CODE_BYTES);
+      const float* vs_row = a.v_alias ? ks_row : ks_row + kTile * (GRP && ngk > 1 ? ngk : 1);
       for (int sub = kw; ok && sub < kTile / kSub; sub += a.key_warps) {
         const int kb = key0 + sub * kSub;
         if (kb >= k1) break;
@@ -1075,7 +1182,8 @@ struct KernelCfg {
 };
 
 // Dispatch on head_dim and on nt (0: grouped layout; -32, -64, -128: grouped
-// layout with per-group scales of that many channels; 2, 3: wide layout).
+// layout with per-group scales of that many channels; 2, 3: wide layout; head
+// dim 576, 8-bit codes only: the wide layout with nt = 1, 2 or 3).
 template <int DT, bool Query>
 cudaError_t dispatch_decode(int head_dim, int nt, const CUtensorMap* tk, const CUtensorMap* tv, const DecodeArgs* a,
                             int grid, int threads, size_t smem, cudaStream_t stream, int* blocks_per_sm) {
@@ -1104,6 +1212,13 @@ cudaError_t dispatch_decode(int head_dim, int nt, const CUtensorMap* tk, const C
     case 64: return by_nt(std::integral_constant<int, 64>{});
     case 128: return by_nt(std::integral_constant<int, 128>{});
     case 256: return by_nt(std::integral_constant<int, 256>{});
+    case 576:
+      if constexpr (DT != KVQ_INT4) {
+        if (nt == 1) return go(KernelCfg<576, 1, 1>{});
+        if (nt == 2) return go(KernelCfg<576, 1, 2>{});
+        if (nt == 3) return go(KernelCfg<576, 1, 3>{});
+      }
+      return cudaErrorInvalidValue;
     default: return cudaErrorInvalidValue;
   }
 }

@@ -270,12 +270,13 @@ __global__ void __launch_bounds__(kTcWarps * 32, 1)
     ptx::tmem_alloc(tmem_slot, C::TMEM_COLS);
     ptx::tc_fence_before();
   }
-  // Only inputs that no kvq kernel writes (seq_lens, block table, q, static
-  // scales) are read before the wait on the preceding grid on the stream:
-  // the producer waits before its first cache read, the softmax warps before
-  // their first workspace write (the other roles touch only shared memory and
-  // TMEM), so the plan, the first block ids and the Q prologue overlap that
-  // grid's tail.
+  // With early reads (KVQ_DECODE_EARLY_INPUTS) the inputs the caller vouches
+  // for (seq_lens, block table, q, static scales) are read before the wait on
+  // the preceding grid on the stream: the producer waits before its first
+  // cache read, the softmax warps before their first workspace write (the
+  // other roles touch only shared memory and TMEM), so the plan, the first
+  // block ids and the Q prologue overlap that grid's tail.  Without them
+  // build_slice waits first.
   const Slice<KT> sp = build_slice<KT>(a, pl_pre, pl_misc);
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;

@@ -76,6 +76,8 @@ struct DecodeArgs {
   int units_max;    // partial slots (grid + batch * Hkv)
   int piece_cost;   // tiles' worth of time a CTA spends on each piece change (split planning)
   int bt_div;       // block-table row of sequence b is b / bt_div (prefill: virtual sequences)
+  int v_alias;      // LATENT on the mma.sync kernel: a stage holds the K codes (and K scales) only,
+                    // and V is read from them (one copy of each cache row per key)
   int early_reads;  // 1: read seq_lens, block table and q before the wait on the preceding grid
   int* plan;        // workspace: [0] cost per CTA, [1] total tiles, [2] piece cost, [3] slots, then tile prefix[B+1]
   float* part_lse;  // [units_max, rows]   base-2 log-sum-exp of each piece

@@ -27,7 +27,9 @@ template <int DT, int D_, int KT = kTile>
 struct Geo {
   static constexpr int D = D_;
   static constexpr int DP = DT == KVQ_INT4 ? D_ / 2 : D_;  // bytes per cached row
-  static constexpr int SPAN = DP >= 128 ? 128 : DP;      // TMA box inner bytes = swizzle span
+  // TMA box inner bytes = swizzle span: the widest of 128 / 64 / 32 bytes that
+  // divides the row (a 576-byte row is nine 64-byte slabs)
+  static constexpr int SPAN = DP % 128 == 0 ? 128 : (DP % 64 == 0 ? 64 : 32);
   static constexpr int SLABS = DP / SPAN;                // column slabs per row
   static constexpr int NCH = DP / 16;                    // 16-byte chunks per row
   static constexpr int NMT = D_ / 16;                      // 16-channel MMA tiles
@@ -111,10 +113,10 @@ struct Slice {
 };
 
 // Builds the plan in shared memory (pl_pre [B + 1], pl_misc [4]); every
-// thread of the CTA calls it.  It reads only seq_lens, which no kvq kernel
-// writes, so it runs before the wait on the preceding grid; the producer
-// publishes the plan to the workspace after that wait (publish_slice).
-// Flags seq_lens outside [0, capacity].
+// thread of the CTA calls it.  It reads only seq_lens: with early_reads
+// (KVQ_DECODE_EARLY_INPUTS) before the wait on the preceding grid, else after
+// it; the producer publishes the plan to the workspace after that wait
+// (publish_slice).  Flags seq_lens outside [0, capacity].
 template <int KT>
 __device__ Slice<KT> build_slice(const DecodeArgs& a, int* pl_pre, int* pl_misc) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -198,9 +200,9 @@ __device__ __forceinline__ void publish_slice(const DecodeArgs& a, const int* pl
 
 // The producer warp.  The whole warp fetches a piece's block ids 32 pages at
 // a time (one coalesced load per 32 pages, the next batch loaded while the
-// current one is used) and hands them to lane 0 by shuffles.  The first piece's ids are read before the wait on the preceding
-// grid (no kvq kernel writes the block table); the cache is read, and the
-// plan published, only after it.  Lane 0 waits for a free stage and issues,
+// current one is used) and hands them to lane 0 by shuffles.  With early
+// reads the first piece's ids are read before the wait on the preceding grid;
+// the cache is read, and the plan published, only after it.  Lane 0 waits for a free stage and issues,
 // per page segment of the stage, one TMA tensor copy per (slab, side) with
 // the block id as the outer coordinate, plus 1-D bulk copies of the per-row
 // scales.  kBurst: the whole stage's block ids are resolved first and its
@@ -227,12 +229,14 @@ __device__ void produce(const DecodeArgs& a, const Slice<Gm::KEYS>& sp, const CU
     waited = true;
   };
   // per-row / per-group scales: nk (nv) floats per K (V) row, K's [KT][nk]
-  // after the codes, V's [KT][nv] at KT * max(1, nk) floats after that
-  const int nk = a.sk_n, nv = a.sv_n;
-  const uint32_t v_sc = 2 * Gm::CODE_BYTES + KT * 4 * (nk > 1 ? nk : 1);
+  // after the codes, V's [KT][nv] at KT * max(1, nk) floats after that.  With
+  // v_alias (LATENT) a stage holds the K side only: no V codes, no V scales.
+  const int nk = a.sk_n, nv = a.v_alias ? 0 : a.sv_n;
+  const uint32_t sc_off = (a.v_alias ? 1 : 2) * Gm::CODE_BYTES;
+  const uint32_t v_sc = sc_off + KT * 4 * (nk > 1 ? nk : 1);
   const int Hkv = a.num_kv_heads;
   const int seg_rows = min(a.block_size, kTile);  // rows of one TMA box
-  const uint32_t seg_bytes = (uint32_t)seg_rows * (2 * Gm::DP + 4 * nk + 4 * nv);
+  const uint32_t seg_bytes = (uint32_t)seg_rows * ((a.v_alias ? 1 : 2) * Gm::DP + 4 * nk + 4 * nv);
   const uint32_t S = (uint32_t)a.stages;
   uint32_t it = 0;
   RingPos rp;
@@ -302,11 +306,12 @@ __device__ void produce(const DecodeArgs& a, const Slice<Gm::KEYS>& sp, const CU
             for (int sl = 0; sl < Gm::SLABS; ++sl) {
               uint8_t* dk = st + sl * (KT * Gm::SPAN) + s * seg_rows * Gm::SPAN;
               ptx::tma_load_4d(dk, tmk, sl * Gm::SPAN, row0, h, blk[s], &bar_full[stage]);
-              ptx::tma_load_4d(dk + Gm::CODE_BYTES, tmv, sl * Gm::SPAN, row0, h, blk[s], &bar_full[stage]);
+              if (!a.v_alias)
+                ptx::tma_load_4d(dk + Gm::CODE_BYTES, tmv, sl * Gm::SPAN, row0, h, blk[s], &bar_full[stage]);
             }
             const size_t srow = ((size_t)blk[s] * Hkv + h) * a.block_size + row0;
             if (nk)
-              ptx::bulk_load(st + 2 * Gm::CODE_BYTES + s * seg_rows * 4 * nk, a.k_scale + srow * nk,
+              ptx::bulk_load(st + sc_off + s * seg_rows * 4 * nk, a.k_scale + srow * nk,
                              seg_rows * 4 * nk, &bar_full[stage]);
             if (nv)
               ptx::bulk_load(st + v_sc + s * seg_rows * 4 * nv, a.v_scale + srow * nv, seg_rows * 4 * nv,
@@ -334,11 +339,12 @@ __device__ void produce(const DecodeArgs& a, const Slice<Gm::KEYS>& sp, const CU
               for (int sl = 0; sl < Gm::SLABS; ++sl) {
                 uint8_t* dk = st + sl * (KT * Gm::SPAN) + s * seg_rows * Gm::SPAN;
                 ptx::tma_load_4d(dk, tmk, sl * Gm::SPAN, row0, h, id, &bar_full[stage]);
-                ptx::tma_load_4d(dk + Gm::CODE_BYTES, tmv, sl * Gm::SPAN, row0, h, id, &bar_full[stage]);
+                if (!a.v_alias)
+                  ptx::tma_load_4d(dk + Gm::CODE_BYTES, tmv, sl * Gm::SPAN, row0, h, id, &bar_full[stage]);
               }
               const size_t srow = ((size_t)id * Hkv + h) * a.block_size + row0;
               if (nk)
-                ptx::bulk_load(st + 2 * Gm::CODE_BYTES + s * seg_rows * 4 * nk, a.k_scale + srow * nk,
+                ptx::bulk_load(st + sc_off + s * seg_rows * 4 * nk, a.k_scale + srow * nk,
                                seg_rows * 4 * nk, &bar_full[stage]);
               if (nv)
                 ptx::bulk_load(st + v_sc + s * seg_rows * 4 * nv, a.v_scale + srow * nv, seg_rows * 4 * nv,

@@ -45,9 +45,12 @@
  *   seq_lens    int32  [batch]   (each includes the q_tokens new tokens)
  *   lse_out     fp32   [batch, q_tokens, num_q_heads] (natural log)
  *
- * Supported on the GPU path: head_dim in {64, 128, 256}; num_q_heads a
- * multiple of num_kv_heads with a ratio of at most 8; q_tokens in [1, 8];
- * block_size a power of two >= 16; batch <= 1024.  Pointers 16-byte aligned.
+ * Supported on the GPU path: head_dim in {64, 128, 256}, and 576 for a LATENT
+ * cache (absorbed MLA, e.g. 512 latent + 64 rotary channels) with int8 or
+ * e4m3 codes and per-row, per-tensor or per-channel scales, at most 48 query
+ * rows per kv head; num_q_heads a multiple of num_kv_heads with a ratio of at
+ * most 8; q_tokens in [1, 8]; block_size a power of two >= 16; batch <= 1024.
+ * Pointers 16-byte aligned.
  */
 #ifndef KVQ_H
 #define KVQ_H
@@ -127,9 +130,8 @@ typedef struct {
   int32_t layout;       /* kvq_layout; LATENT: v_codes, v_scale, v_mode are ignored (V is the K
                            row, with K's scales) and may be NULL / 0; kvq_append writes K only
                            and ignores v_new; kvq_combine writes out [B, T, Hq, v_head_size] */
-  int32_t v_head_size;  /* LATENT: channels of V, a multiple of 8 in [8, head_dim]; 0 = head_dim.
-                           The pages' DeepSeek-V3 example (576/512) is above this library's
-                           head_dim limit of 256. */
+  int32_t v_head_size;  /* LATENT: channels of V, a multiple of 8 in [8, head_dim]; 0 = head_dim
+                           (the pages' DeepSeek-V3 example: head_dim 576, v_head_size 512) */
   int32_t group_size;   /* PER_GROUP on either side: channels per scale group, 32, 64 or 128
                            and at most head_dim (one group size for both sides); otherwise
                            ignored.  Decode with a PER_GROUP side runs on the mma.sync
@@ -238,7 +240,8 @@ typedef struct {
  * before kvq_decode.  positions int64 [n_tokens] (device; may be NULL when
  * rotary_dim == 0): a position outside [0, max_position) sets
  * KVQ_DEVERR_POSITION and leaves that token's rows of y unwritten.
- * head_dim in {64, 128, 256}; x, y 16-byte aligned. */
+ * head_dim in {64, 128, 256, 576} (the Hadamard rotation: powers of two only);
+ * x, y 16-byte aligned. */
 KVQ_API kvq_status kvq_norm_rope_apply(const kvq_norm_rope* prologue, const void* x, void* y,
                                        const int64_t* positions, int32_t n_tokens,
                                        int32_t num_heads, int32_t head_dim, kvq_stream_t stream);

@@ -333,7 +333,7 @@ uint16_t orc_f64_to_bf16(double v) {
 void orc_norm_rope_row(const uint16_t* x, int D, const uint16_t* w, double eps, int rd, int off,
                        int interleaved, const float* cs, const float* sn, int hadamard, uint16_t* out,
                        double* out64) {
-  double y[512];
+  double y[1024];
   for (int d = 0; d < D; ++d) y[d] = (double)orc_bf16_to_f32(x[d]);
   if (w) {
     double ss = 0.0;
@@ -342,7 +342,7 @@ void orc_norm_rope_row(const uint16_t* x, int D, const uint16_t* w, double eps, 
     for (int d = 0; d < D; ++d) y[d] = y[d] * r * (double)orc_bf16_to_f32(w[d]);
   }
   if (rd > 0) {
-    double z[512];
+    double z[1024];
     memcpy(z, y, sizeof(double) * (size_t)D);
     for (int i = 0; i < rd / 2; ++i) {
       int a = interleaved ? off + 2 * i : off + i;
@@ -354,7 +354,7 @@ void orc_norm_rope_row(const uint16_t* x, int D, const uint16_t* w, double eps, 
     memcpy(y, z, sizeof(double) * (size_t)D);
   }
   if (hadamard) {
-    double z[512];
+    double z[1024];
     double inv = 1.0 / sqrt((double)D);
     for (int i = 0; i < D; ++i) {
       double acc = 0.0;
@@ -377,7 +377,7 @@ int orc_norm_rope(const uint16_t* x, int n_tokens, int H, int D, const uint16_t*
                   int off, int interleaved, const float* cos_tab, const float* sin_tab, int max_pos,
                   const int64_t* positions, int hadamard, uint16_t* out, double* out64) {
   int bad = 0;
-  if (D <= 0 || D > 512 || rd < 0 || rd % 2 || off < 0 || off + rd > D || (hadamard && (D & (D - 1))))
+  if (D <= 0 || D > 1024 || rd < 0 || rd % 2 || off < 0 || off + rd > D || (hadamard && (D & (D - 1))))
     return -1;
   for (int n = 0; n < n_tokens; ++n) {
     int64_t pos = rd > 0 ? positions[n] : 0;

@@ -239,3 +239,27 @@ def test_wait_check_rejects_bad_limits_on_the_host(kvq):
     lib = kvq.load()
     assert lib.kvq_check_wait_timeout(0, None) == 1
     assert lib.kvq_check_wait_timeout(2000001, None) == 1
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(head_dim=576), 2),                                                   # SEPARATE at 576
+    (dict(head_dim=576, layout=1, v_head_size=512, dtype=3), 2),               # int4 codes
+    (dict(head_dim=576, layout=1, v_head_size=512, k_mode=4, v_mode=4, group_size=64), 2),
+    (dict(head_dim=576, layout=1, v_head_size=520), 0),
+    (dict(head_dim=576, layout=1, v_head_size=512, dtype=2), 0),
+    (dict(head_dim=576, layout=1, v_head_size=0, k_mode=3, v_mode=3), 0),
+])
+def test_head_dim_576_only_for_a_latent_cache_of_8_bit_codes(kvq, kw, status):
+    """Absorbed MLA's 576 = 512 latent + 64 rotary channels: a LATENT cache with
+    int8 or e4m3 codes and per-row or static scales."""
+    lib = kvq.load()
+    c = good_cache(kvq, **kw)
+    assert lib.kvq_append(ctypes.byref(c), FAKE, FAKE, FAKE, 0, None) == status
+
+
+def test_hadamard_needs_a_power_of_two_head_dim(kvq):
+    lib = kvq.load()
+    p = good_norm_rope(kvq, rotary_dim=0, cos_cache=None, sin_cache=None, max_position=0, hadamard=1)
+    assert lib.kvq_norm_rope_apply(ctypes.byref(p), FAKE, FAKE, None, 4, 2, 576, None) == 2
+    p = good_norm_rope(kvq, rotary_dim=64, rotary_offset=512)
+    assert lib.kvq_norm_rope_apply(ctypes.byref(p), FAKE, FAKE, FAKE, 0, 2, 576, None) == 0
