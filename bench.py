@@ -48,6 +48,7 @@ def parse():
     p.add_argument("--no-prologue", action="store_true", help="skip the QK-RMSNorm + RoPE prologue timing")
     p.add_argument("--no-prefill", action="store_true", help="skip the chunked-prefill timing")
     p.add_argument("--no-group", action="store_true", help="skip the group-wise-scale decode timing")
+    p.add_argument("--no-latent", action="store_true", help="skip the head_dim 576 latent-cache timing")
     p.add_argument("--no-configs", action="store_true",
                    help="skip the other workloads (tiny, paged, spec, mixed) beside the default line")
     return p.parse_args()
@@ -592,6 +593,89 @@ def measure_group(w, steps, warmup, peak, group_size=64):
             "algorithmic_bytes_per_launch": int(dec_bytes)}
 
 
+def measure_latent(steps, warmup, peak, *, B=4, Hq=8, T=1, ctx=32768, bs=64):
+    """A LATENT cache at the pages' absorbed-MLA shape (head_dim 576 = 512
+    latent + 64 rotary channels, v_head_size 512; one kv head shared by Hq
+    query heads), int8 per-row scales: decode timed as a graph of K launches
+    over rotated cache replicas (inputs larger than L2), and per launch.  Each
+    cached row is read once (V is its leading 512 channels): algorithmic bytes
+    per key = 576 codes + 4 scale bytes."""
+    import torch
+    from decode_attention_quantized_gb300 import kvq, synth
+
+    dev = torch.cuda.current_device()
+    D, Dv, Hkv = 576, 512, 1
+    mb = (ctx + bs - 1) // bs
+    NB = B * mb
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    cache_bytes = NB * bs * Hkv * (D + 4)
+    reps = min(64, max(2, math.ceil(4 * l2 / cache_bytes)))
+    table = torch.arange(NB, dtype=torch.int32, device=f"cuda:{dev}").reshape(B, mb)
+    lens = torch.full((B,), ctx, dtype=torch.int32, device=f"cuda:{dev}")
+    caches = []
+    base = kvq.QuantizedPagedCache(kvq.INT8, kvq.PER_ROW, kvq.PER_ROW, NB, bs, Hkv, D, device=f"cuda:{dev}",
+                                   latent=True, v_head_size=Dv)
+    chunk = 1 << 15
+    for t0 in range(0, B * ctx, chunk):
+        n = min(chunk, B * ctx - t0)
+        k = synth.randn_bf16((n, Hkv, D), f"cuda:{dev}", "bench", "mla-k", t0)
+        slots = torch.arange(t0, t0 + n, dtype=torch.int64, device=f"cuda:{dev}")  # table is in order
+        kvq.kvq_append(base, k, None, slots)
+    caches.append(base)
+    for _ in range(reps - 1):
+        c = kvq.QuantizedPagedCache.__new__(kvq.QuantizedPagedCache)
+        c.__dict__.update(base.__dict__)
+        c.k_codes = base.k_codes.clone()
+        c.v_codes = c.k_codes
+        c.k_scale = base.k_scale.clone()
+        c.v_scale = c.k_scale
+        caches.append(c)
+    q = synth.randn_bf16((B, T, Hq, D), f"cuda:{dev}", "bench", "mla-q")
+    params = kvq.make_params(B, Hq, T, mb, max_seq_len=ctx, flags=kvq.DECODE_EARLY_INPUTS)
+    bufs = kvq.alloc_decode_buffers(base, params)
+
+    def dec(i):
+        kvq.kvq_decode(caches[i % reps], params, q, table, lens, bufs.workspace)
+
+    for i in range(max(3, warmup)):
+        dec(i)
+        kvq.kvq_combine(caches[i % reps], params, bufs.workspace, None, bufs.out, bufs.lse)
+    torch.cuda.synchronize()
+    gr = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gr):
+        for i in range(steps):
+            dec(i)
+    gr.replay()
+    torch.cuda.synchronize()
+    t0e, t1e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0e.record()
+    gr.replay()
+    t1e.record()
+    torch.cuda.synchronize()
+    ms = t0e.elapsed_time(t1e) / steps
+    n = max(50, steps)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    torch.cuda.synchronize()
+    torch.cuda._sleep(int(2e5 * n + 2e6))
+    for i in range(n):
+        ev[i][0].record()
+        dec(i)
+        ev[i][1].record()
+    torch.cuda.synchronize()
+    per = [a.elapsed_time(b) for a, b in ev]
+    assert kvq.kvq_get_device_error() == 0, "device error flags set in the latent timing"
+    nbytes = B * ctx * Hkv * (D + 4) + B * T * Hq * D * 2 + B * mb * 4 + B * 4
+    del caches, base, bufs
+    torch.cuda.empty_cache()
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    med = statistics.median(per)
+    return {"workload": f"latent int8 per-row, head_dim {D} (v_head_size {Dv}), B={B} Hq={Hq} Hkv={Hkv} T={T} "
+                        f"block={bs} ctx={ctx}", "decode_us": round(1e3 * ms, 2), "decode_gbs": round(gbs, 1),
+            "frac_of_hbm": round(gbs / peak, 3), "decode_us_median": round(1e3 * med, 2),
+            "decode_us_p10": round(1e3 * pct(per, 10), 2), "decode_us_p90": round(1e3 * pct(per, 90), 2),
+            "algorithmic_bytes_per_launch": int(nbytes), "bytes_per_key": D + 4, "replicas": reps}
+
+
 def decode_kernel_name(w):
     """The decode kernel a workload runs on: the tensor-memory kernel for
     17..48 query rows per kv head at head_dim 256 (17..64 at 128), else the
@@ -730,6 +814,8 @@ def run_ours(args):
         head.update(launch_stats(res["per_launch"][0], peak))
         line["configs"] = [head] + measure_configs(["tiny", "paged", "spec", "mixed"], args.steps, args.warmup,
                                                    peak, n_pl)
+    if rank == 0 and world == 1 and args.workload == "gqa" and not args.no_latent:
+        line["latent"] = measure_latent(args.steps, args.warmup, peak)
     if rank == 0 and world == 1 and not args.no_prologue:
         line["prologue"] = measure_prologue(w, args.steps, args.warmup, peak)
     if rank == 0 and world == 1 and not args.no_prefill:

@@ -266,7 +266,9 @@ kvq_status make_plan_uncached(const kvq_cache* c, const kvq_decode_params* p, co
     // per-SM shared memory is 228 KiB with 1 KiB reserved per resident CTA
     const size_t budget = (size_t)228 * 1024 / target - 1024;
     const size_t fixed = fixed_smem(c, P.row_groups, P.key_warps, P.nt, B, 0);
-    const int min_stages = target > 1 ? 3 : 2;
+    // head_dim 576 stages are 37 KB: two CTAs of two stages each still keep
+    // 148 KB in flight per SM, and twice the warps hide more latency
+    const int min_stages = target > 1 && c->head_dim != 576 ? 3 : 2;
     if (fixed + (size_t)min_stages * (stride + 16) > budget) continue;
     int stages = (int)((budget - fixed) / (stride + 16));
     stages = stages > kMaxStages ? kMaxStages : stages;

@@ -243,77 +243,6 @@ __device__ __forceinline__ float q_prologue(const DecodeArgs& a, int rq, int b, 
   return fminf(alpha, 3.4028234e38f);
 }
 
-// The same Q prologue for rows too long to hold in registers (head_dim 576,
-// 8-bit codes): two passes over the row (its maximum, then the f16 operand),
-// each k-slot pair handed to store(k, value) as it is made; lane group c
-// holds channels 16 j + 4 c .. + 3 of k-step j, placed in k-slots 16 j + 2 c
-// (channels + 0, + 1) and 16 j + 8 + 2 c (+ 2, + 3), as q_prologue does.
-template <int DT, int D, class Store>
-__device__ __forceinline__ float q_prologue_long(const DecodeArgs& a, int rq, int b, int h, int c, Store store) {
-  static_assert(DT != KVQ_INT4, "8-bit codes: four channels per lane of each k-step");
-  constexpr float kLog2e = 1.4426950408889634f;
-  constexpr int NKS = D / 16;
-  const int G = a.group, T = a.q_tokens, Hq = a.num_q_heads;
-  const bool qvalid = rq < a.rows;
-  const int tq = qvalid ? div_small(rq, __frcp_rn((float)G)) : 0, gq = qvalid ? rq - tq * G : 0;
-  const uint16_t* qp = a.q + (((size_t)b * T + tq) * Hq + (size_t)h * G + gq) * D;
-  const bool kc = a.k_mode == KVQ_SCALE_PER_CHANNEL;
-  const float* ksp = a.k_scale + (size_t)h * D;
-  auto load = [&](int j, float (&v)[4]) {
-    const uint2 w = qvalid ? *reinterpret_cast<const uint2*>(qp + 16 * j + 4 * c) : make_uint2(0, 0);
-    v[0] = __uint_as_float(w.x << 16);
-    v[1] = __uint_as_float(w.x & 0xFFFF0000u);
-    v[2] = __uint_as_float(w.y << 16);
-    v[3] = __uint_as_float(w.y & 0xFFFF0000u);
-  };
-  int e_tot = 0;
-  float sk = 1.0f;
-  if (kc) {
-    float km = 0.0f;
-#pragma unroll 4
-    for (int j = 0; j < NKS; ++j)
-#pragma unroll
-      for (int i = 0; i < 4; ++i) km = fmaxf(km, fabsf(ksp[16 * j + 4 * c + i]));
-    km = fmaxf(km, __shfl_xor_sync(0xffffffffu, km, 1));
-    km = fmaxf(km, __shfl_xor_sync(0xffffffffu, km, 2));
-    const int ek = km > 0.0f ? min(126, max(-126, ceil_log2(km))) : 0;
-    sk = pow2i(-ek);
-    e_tot += ek;
-  }
-  float qm = 0.0f;
-#pragma unroll 4
-  for (int j = 0; j < NKS; ++j) {
-    float v[4];
-    load(j, v);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      if (kc) v[i] *= ksp[16 * j + 4 * c + i] * sk;
-      qm = fmaxf(qm, fabsf(v[i]));
-    }
-  }
-  qm = fmaxf(qm, __shfl_xor_sync(0xffffffffu, qm, 1));
-  qm = fmaxf(qm, __shfl_xor_sync(0xffffffffu, qm, 2));
-  const int eq = qm > 0.0f ? min(126, max(-126, ceil_log2(qm))) : 0;
-  const float sq = pow2i(-eq);
-  e_tot += eq;
-#pragma unroll 4
-  for (int j = 0; j < NKS; ++j) {
-    float v[4];
-    load(j, v);
-    if (kc) {
-#pragma unroll
-      for (int i = 0; i < 4; ++i) v[i] *= ksp[16 * j + 4 * c + i] * sk;
-    }
-    store(16 * j + 2 * c, pack_h2(v[0] * sq, v[1] * sq));
-    store(16 * j + 8 + 2 * c, pack_h2(v[2] * sq, v[3] * sq));
-  }
-  float base = a.sm_scale;
-  if (a.k_mode == KVQ_SCALE_PER_TENSOR) base *= a.k_scale[0];
-  float alpha = ldexpf(base, e_tot);
-  if (a.softcap <= 0.0f) alpha *= kLog2e;
-  return fminf(alpha, 3.4028234e38f);
-}
-
 }  // namespace dev
 
 // Shared floats of the wide consumer layout with NT n-tiles per row half: the
@@ -423,22 +352,102 @@ __global__ void __launch_bounds__(288, MINB)
       piece(gt, b, h, k0, k1, L, u, next);
       // Q of n-tile kq of this half (warps kq < NT), stored in k-slot order so
       // that ldmatrix yields the B fragments; the rows' logit factors beside it
-      if (kq < NT) {
-        const int row = rh * RW + kq * 8 + g;
-        float ag;
-        if constexpr (D <= 256) {
+      if constexpr (D <= 256) {
+        if (kq < NT) {
+          const int row = rh * RW + kq * 8 + g;
           uint32_t qf[Gm::NMT][2];
-          ag = dev::q_prologue<DT, D>(a, row, b, h, c, qf);
+          const float ag = dev::q_prologue<DT, D>(a, row, b, h, c, qf);
 #pragma unroll
           for (int ks = 0; ks < Gm::NMT; ++ks) {
             ptx::st_shared_u32(q_base + q_off(row, ks * 16 + 2 * c), qf[ks][0]);
             ptx::st_shared_u32(q_base + q_off(row, ks * 16 + 8 + 2 * c), qf[ks][1]);
           }
-        } else {
-          ag = dev::q_prologue_long<DT, D>(a, row, b, h, c,
-                                           [&](int k, uint32_t v) { ptx::st_shared_u32(q_base + q_off(row, k), v); });
+          if (c == 0) s_alpha[row] = ag;
         }
-        if (c == 0) s_alpha[row] = ag;
+      } else {
+        // long rows: every warp takes k-step quarter kq of each row of its half
+        // (the rows' maxima and the per-channel scales' maximum meet in shared
+        // memory), the same arithmetic as q_prologue: q * (k_scale / 2^ek),
+        // then / 2^eq, to f16 in the k-slot order
+        static_assert(DT != KVQ_INT4, "8-bit codes");
+        constexpr int KQ = D / 64;  // k-steps of a quarter
+        const bool kc = a.k_mode == KVQ_SCALE_PER_CHANNEL;
+        const float* ksp = a.k_scale + (size_t)h * D;
+        auto row_ptr = [&](int r) {
+          const int tq = dev::div_small(r, inv_g), gq = r - tq * G;
+          return a.q + (((size_t)b * T + tq) * a.num_q_heads + (size_t)h * G + gq) * D;
+        };
+        auto load4 = [&](const uint16_t* qp, int j, float (&v)[4]) {
+          const uint2 w = *reinterpret_cast<const uint2*>(qp + 16 * j + 4 * c);
+          v[0] = __uint_as_float(w.x << 16);
+          v[1] = __uint_as_float(w.x & 0xFFFF0000u);
+          v[2] = __uint_as_float(w.y << 16);
+          v[3] = __uint_as_float(w.y & 0xFFFF0000u);
+        };
+        float km = 0.0f;
+        if (kc) {
+#pragma unroll 3
+          for (int j = kq * KQ; j < (kq + 1) * KQ; ++j)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) km = fmaxf(km, fabsf(ksp[16 * j + 4 * c + i]));
+        }
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          const int r = rh * RW + nt * 8 + g;
+          float m = 0.0f;
+          if (r < a.rows) {
+            const uint16_t* qp = row_ptr(r);
+#pragma unroll 3
+            for (int j = kq * KQ; j < (kq + 1) * KQ; ++j) {
+              float v[4];
+              load4(qp, j, v);
+#pragma unroll
+              for (int i = 0; i < 4; ++i) m = fmaxf(m, fabsf(kc ? v[i] * ksp[16 * j + 4 * c + i] : v[i]));
+            }
+          }
+          m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+          m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+          if (c == 0) s_max[kq * ROWS + r] = m;
+        }
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) km = fmaxf(km, __shfl_xor_sync(0xffffffffu, km, o));
+        if (lane == 0) s_vmax[warp] = km;  // eight slots
+        ptx::named_bar_sync(1, 8 * 32);
+        int ek = 0;
+        if (kc) {
+          float kmax = s_vmax[0];
+#pragma unroll
+          for (int w = 1; w < 8; ++w) kmax = fmaxf(kmax, s_vmax[w]);
+          ek = kmax > 0.0f ? min(126, max(-126, dev::ceil_log2(kmax))) : 0;
+        }
+        const float sk = dev::pow2i(-ek);
+        float base = a.sm_scale;
+        if (a.k_mode == KVQ_SCALE_PER_TENSOR) base *= a.k_scale[0];
+        if (softcap <= 0.0f) base *= kLog2e;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          const int r = rh * RW + nt * 8 + g;
+          // (the quarters' maxima are of q * k_scale; times 2^-ek exactly)
+          const float qm = fmaxf(fmaxf(s_max[r], s_max[ROWS + r]), fmaxf(s_max[2 * ROWS + r], s_max[3 * ROWS + r])) * sk;
+          const int eq = qm > 0.0f ? min(126, max(-126, dev::ceil_log2(qm))) : 0;
+          const float sq = dev::pow2i(-eq);
+          const uint16_t* qp = row_ptr(r < a.rows ? r : 0);
+#pragma unroll 3
+          for (int j = kq * KQ; j < (kq + 1) * KQ; ++j) {
+            float v[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+            if (r < a.rows) load4(qp, j, v);
+            if (kc) {
+#pragma unroll
+              for (int i = 0; i < 4; ++i) v[i] *= ksp[16 * j + 4 * c + i] * sk;
+            }
+            ptx::st_shared_u32(q_base + q_off(r, 16 * j + 2 * c), dev::pack_h2(v[0] * sq, v[1] * sq));
+            ptx::st_shared_u32(q_base + q_off(r, 16 * j + 8 + 2 * c), dev::pack_h2(v[2] * sq, v[3] * sq));
+          }
+          if (kq == 0 && c == 0) {
+            float alpha = ldexpf(base, ek + eq);
+            s_alpha[r] = fminf(alpha, 3.4028234e38f);
+          }
+        }
       }
       ptx::griddep_wait();  // before the first workspace write (no-op after the first)
       ptx::named_bar_sync(1, 8 * 32);
@@ -482,9 +491,15 @@ __global__ void __launch_bounds__(288, MINB)
         float x[NT][4];
         float vpa = 0.0f, vpb = 0.0f;
         if (active) {
-          float sacc[NT][4];
+          // long rows (head_dim 576: 36 k-steps) of one n-tile accumulate in
+          // four independent chains, summed at the end, so the MMAs do not wait
+          // on one another (with more n-tiles the extra registers spill)
+          constexpr int NCHAIN = D > 256 && NT == 1 ? 4 : 1;
+          float sacc[NCHAIN][NT][4];
 #pragma unroll
-          for (int nt = 0; nt < NT; ++nt) sacc[nt][0] = sacc[nt][1] = sacc[nt][2] = sacc[nt][3] = 0.0f;
+          for (int ch = 0; ch < NCHAIN; ++ch)
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) sacc[ch][nt][0] = sacc[ch][nt][1] = sacc[ch][nt][2] = sacc[ch][nt][3] = 0.0f;
           const uint32_t row_off = (uint32_t)(kq * kSub + ld_key) * Gm::SPAN;
           // B fragments of k-step ks for every n-tile of this half, from Q
           auto qfrag = [&](int ks, uint32_t (&bq)[NT][2]) {
@@ -526,18 +541,26 @@ __global__ void __launch_bounds__(288, MINB)
                   uint32_t bq[NT][2];
                   qfrag(2 * j + t, bq);
 #pragma unroll
-                  for (int nt = 0; nt < NT; ++nt) ptx::mma_16816(sacc[nt], A, bq[nt][0], bq[nt][1]);
+                  for (int nt = 0; nt < NT; ++nt) ptx::mma_16816(sacc[0][nt], A, bq[nt][0], bq[nt][1]);
                 }
               } else {
                 uint32_t A[4];
                 dev::k_frag<DT>(wl, wh, 0, A);
                 uint32_t bq[NT][2];
                 qfrag(j, bq);
+                constexpr int chain = NCHAIN > 1 ? 1 : 0;  // (kk & 1) * 2 + h2 below when chained
 #pragma unroll
-                for (int nt = 0; nt < NT; ++nt) ptx::mma_16816(sacc[nt], A, bq[nt][0], bq[nt][1]);
+                for (int nt = 0; nt < NT; ++nt)
+                  ptx::mma_16816(sacc[chain ? ((kk & 1) * 2 + h2) % NCHAIN : 0][nt], A, bq[nt][0], bq[nt][1]);
               }
             }
           }
+#pragma unroll
+          for (int ch = 1; ch < NCHAIN; ++ch)
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+              for (int e = 0; e < 4; ++e) sacc[0][nt][e] += sacc[ch][nt][e];
           float ksa = 1.0f, ksb = 1.0f;
           if (k_row) {
             ksa = ks_row[kq * kSub + g];
@@ -545,10 +568,10 @@ __global__ void __launch_bounds__(288, MINB)
           }
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) {
-            x[nt][0] = sacc[nt][0] * al[nt][0] * ksa;
-            x[nt][1] = sacc[nt][1] * al[nt][1] * ksa;
-            x[nt][2] = sacc[nt][2] * al[nt][0] * ksb;
-            x[nt][3] = sacc[nt][3] * al[nt][1] * ksb;
+            x[nt][0] = sacc[0][nt][0] * al[nt][0] * ksa;
+            x[nt][1] = sacc[0][nt][1] * al[nt][1] * ksa;
+            x[nt][2] = sacc[0][nt][2] * al[nt][0] * ksb;
+            x[nt][3] = sacc[0][nt][3] * al[nt][1] * ksb;
             if (softcap > 0.0f) {
 #pragma unroll
               for (int e = 0; e < 4; ++e) x[nt][e] = softcap * dev::tanh_fast(x[nt][e] * inv_cap) * kLog2e;
@@ -1214,7 +1237,7 @@ cudaError_t dispatch_decode(int head_dim, int nt, const CUtensorMap* tk, const C
     case 256: return by_nt(std::integral_constant<int, 256>{});
     case 576:
       if constexpr (DT != KVQ_INT4) {
-        if (nt == 1) return go(KernelCfg<576, 1, 1>{});
+        if (nt == 1) return go(KernelCfg<576, 2, 1>{});  // two CTAs per SM (96 registers)
         if (nt == 2) return go(KernelCfg<576, 1, 2>{});
         if (nt == 3) return go(KernelCfg<576, 1, 3>{});
       }
