@@ -585,13 +585,28 @@ def measure_prefill(w, steps, warmup, peak, chunk=64):
     assert kvq.kvq_get_device_error() == 0, "device error flags set in the prefill timing"
     ms = t0.elapsed_time(t1) / steps
     one_pass = synth.decode_bytes(w)
+    # attention FLOPs of the chunk: 4 D per (query row, visible key)
+    seen = sum(min(int(L), max(0, int(L) - C + t + 1)) for L in w.seq_lens for t in range(C))
+    flops = 4.0 * w.head_dim * w.num_q_heads * seen
+    G = w.group
+    qt = w.head_dim == 256 and w.k_mode != synth.PER_GROUP and w.v_mode != synth.PER_GROUP
+    tq = 0
+    if qt:
+        tq = min(128 // G, C)
+        while C % tq:
+            tq -= 1
+        qt = tq * G >= 64
+    T = tq if qt else max(t for t in (8, 4, 2, 1) if C % t == 0)
     del gw, q, out, lse, ws
     torch.cuda.empty_cache()
     return {"chunk_tokens": C, "us_per_chunk": round(1e3 * ms, 2),
             "tokens_per_s": round(w.batch * C / (ms * 1e-3), 1),
+            "kernel": ("query tiles of %d tokens x %d heads (tcgen05, rows as M)" % (T, G)) if qt
+                      else "virtual decode sequences of %d tokens" % T,
+            "groups_per_sequence": C // T,
+            "attention_tflops": round(flops / (ms * 1e-3) / 1e12, 1),
             "single_pass_gbs": round(one_pass / (ms * 1e-3) / 1e9, 1),
-            "single_pass_frac_of_hbm": round(one_pass / (ms * 1e-3) / 1e9 / peak, 3),
-            "groups_per_sequence": C // max(t for t in (8, 4, 2, 1) if C % t == 0)}
+            "single_pass_frac_of_hbm": round(one_pass / (ms * 1e-3) / 1e9 / peak, 3)}
 
 
 def measure_group(w, steps, warmup, peak, group_size=64):

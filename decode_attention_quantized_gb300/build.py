@@ -26,7 +26,8 @@ NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-fvisibilit
               "-I" + INCLUDE, "-I" + CSRC] + ARCH
 SOURCES = ["api.cu", "append.cu", "combine.cu", "decode_int8.cu", "decode_fp8.cu", "decode_int4.cu",
            "decode_tc_int8.cu", "decode_tc_fp8.cu", "decode_tc_int4.cu", "decode_tc_grp_int8.cu",
-           "decode_tc_grp_fp8.cu", "decode_tc_grp_int4.cu", "noalloc.cu"]
+           "decode_tc_grp_fp8.cu", "decode_tc_grp_int4.cu", "decode_qt_int8.cu", "decode_qt_fp8.cu",
+           "decode_qt_int4.cu", "noalloc.cu"]
 
 
 def _nvcc() -> str:
@@ -36,7 +37,7 @@ def _nvcc() -> str:
     raise RuntimeError("nvcc not found: the CUDA toolkit is required to build libkvq.so")
 
 
-HEADERS = ["kvq_internal.h", "ptx.cuh", "pipeline.cuh", "decode.cuh", "decode_tc.cuh"]
+HEADERS = ["kvq_internal.h", "ptx.cuh", "pipeline.cuh", "decode.cuh", "decode_tc.cuh", "decode_qt.cuh"]
 
 
 def _stamp() -> str:

@@ -117,7 +117,10 @@ kvq_status resolve_cache(const kvq_cache* c, kvq_cache* eff) {
   return check_cache(eff);
 }
 
-kvq_status check_params(const kvq_cache* c, const kvq_decode_params* p) {
+// qt: the query-tile layout of kvq_prefill's virtual sequences, whose
+// tokens x group may reach kQtRows rows (any token count); else at most 8
+// tokens of at most 8 query heads per kv head.
+kvq_status check_params(const kvq_cache* c, const kvq_decode_params* p, bool qt = false) {
   if (!p) return KVQ_ERR_INVALID_ARG;
   if (p->batch < 0 || p->num_q_heads <= 0 || p->q_tokens <= 0 || p->max_blocks_per_seq <= 0 ||
       p->max_seq_len < 0 || p->window < 0)
@@ -126,7 +129,9 @@ kvq_status check_params(const kvq_cache* c, const kvq_decode_params* p) {
   if (!std::isfinite(p->sm_scale) || !std::isfinite(p->softcap) || p->softcap < 0.0f) return KVQ_ERR_INVALID_ARG;
   if (p->flags & ~(KVQ_DECODE_EARLY_INPUTS | KVQ_DECODE_NO_TCGEN05)) return KVQ_ERR_INVALID_ARG;
   if ((long long)p->max_blocks_per_seq * c->block_size > (1LL << 30)) return KVQ_ERR_INVALID_ARG;
-  if (p->num_q_heads / c->num_kv_heads > 8 || p->q_tokens > 8 || p->batch > kMaxBatch) return KVQ_ERR_UNSUPPORTED;
+  if (p->num_q_heads / c->num_kv_heads > 8 || p->batch > kMaxBatch) return KVQ_ERR_UNSUPPORTED;
+  if (qt ? (long long)p->q_tokens * (p->num_q_heads / c->num_kv_heads) > kQtRows : p->q_tokens > 8)
+    return KVQ_ERR_UNSUPPORTED;
   // the tile space of all (sequence, kv head) ranges must index with int
   const long long tiles = (long long)p->max_blocks_per_seq * c->block_size / kTile + 1;
   if ((long long)p->batch * c->num_kv_heads * tiles >= (1LL << 31)) return KVQ_ERR_UNSUPPORTED;
@@ -138,11 +143,12 @@ kvq_status check_params(const kvq_cache* c, const kvq_decode_params* p) {
 // workload's decode went from 249 to 206 us, paged from 120 to 118 us, spec
 // from 67.8 to 64.8 us).
 constexpr int kTcPieceCost = 3;
+constexpr int kQtPieceCost = 8;
 constexpr int kPieceCost = 3;
 
 // Launch shape of the decode kernel and the workspace it implies.
 struct Plan {
-  int rows, row_groups, key_warps, nt, tc_nr, threads, stages, grid, units_max;
+  int rows, row_groups, key_warps, nt, tc_nr, qt, threads, stages, grid, units_max;
   size_t stride, smem, ws_plan, ws_lse, ws_o, ws_total;
 };
 
@@ -221,10 +227,56 @@ kvq_status make_plan_tc(const kvq_cache* c, const kvq_decode_params* p, const De
   return KVQ_OK;
 }
 
-kvq_status make_plan_uncached(const kvq_cache* c, const kvq_decode_params* p, const DeviceInfo& dev, Plan* out) {
+// Whether kvq_prefill takes the query-tile kernel: head_dim 256, no
+// group-wise scales, the tcgen05 kernels allowed.  The kernel also runs at
+// head_dim 128, but there some CTAs of a ragged batch stall for microseconds
+// at a time and the virtual decode sequences are faster (measured).
+bool qt_ok(const kvq_cache* c, const kvq_decode_params* p) {
+  return !(p->flags & KVQ_DECODE_NO_TCGEN05) && c->head_dim == 256 && !any_group(c);
+}
+
+// The query-tile kernel: one CTA per SM (it holds all of the SM's TMEM), the
+// mma.sync kernel's 64-key stages, as many of them as fit beside the two
+// double-buffered f16 tiles.
+kvq_status make_plan_qt(const kvq_cache* c, const kvq_decode_params* p, const DeviceInfo& dev, Plan* P) {
+  const int B = p->batch > 0 ? p->batch : 1;
+  const size_t stride = stage_stride(c, false);
+  constexpr size_t kMaxSmem = 227 * 1024;  // per CTA
+  int stages = 0;
+  for (int s = kMaxStages; s >= 2 && stages == 0; --s)
+    if ((size_t)qt_smem_layout(c->head_dim, s, B, (int)stride).total + 1024 <= kMaxSmem) stages = s;
+  if (stages == 0) return KVQ_ERR_UNSUPPORTED;
+  P->qt = 1;
+  P->stages = stages;
+  P->stride = stride;
+  P->smem = (size_t)qt_smem_layout(c->head_dim, stages, B, (int)stride).total + 1024;
+  P->threads = kQtWarps * 32;
+  const long long cap = (long long)p->max_blocks_per_seq * c->block_size;
+  const long long maxlen = (p->max_seq_len > 0 && p->max_seq_len < cap) ? p->max_seq_len : cap;
+  long long grid = dev.sms;
+  const long long useful = (long long)B * c->num_kv_heads * ((maxlen + kTile - 1) / kTile + 1);
+  if (grid > useful) grid = useful;
+  P->grid = (int)(grid < 1 ? 1 : grid);
+  return KVQ_OK;
+}
+
+kvq_status make_plan_uncached(const kvq_cache* c, const kvq_decode_params* p, const DeviceInfo& dev, bool qt,
+                              Plan* out) {
   Plan P{};
   const int G = p->num_q_heads / c->num_kv_heads;
   P.rows = G * p->q_tokens;
+  if (qt) {
+    if (!qt_ok(c, p) || P.rows > kQtRows) return KVQ_ERR_UNSUPPORTED;
+    if (kvq_status s = make_plan_qt(c, p, dev, &P)) return s;
+    const int B = p->batch > 0 ? p->batch : 1;
+    P.units_max = P.grid + B * c->num_kv_heads;
+    P.ws_plan = align256((size_t)(4 + B + 1) * 4);
+    P.ws_lse = align256((size_t)P.units_max * P.rows * 4);
+    P.ws_o = (size_t)P.units_max * P.rows * c->head_dim * 4;
+    P.ws_total = P.ws_plan + P.ws_lse + P.ws_o;
+    *out = P;
+    return KVQ_OK;
+  }
   P.tc_nr = tc_rows(c, p, P.rows);
   if (P.tc_nr) {
     if (kvq_status s = make_plan_tc(c, p, dev, &P)) return s;
@@ -302,7 +354,7 @@ kvq_status make_plan_uncached(const kvq_cache* c, const kvq_decode_params* p, co
 // shapes reuse it (no occupancy query on the hot path).
 struct PlanKey {
   int dev, dtype, k_mode, v_mode, group_size, head_dim, num_kv_heads, block_size, batch, num_q_heads,
-      q_tokens, max_blocks_per_seq, max_seq_len, no_tc, layout;
+      q_tokens, max_blocks_per_seq, max_seq_len, no_tc, layout, qt;
   bool operator==(const PlanKey& o) const { return std::memcmp(this, &o, sizeof(PlanKey)) == 0; }
 };
 constexpr int kPlanCache = 64;
@@ -310,7 +362,8 @@ PlanKey g_plan_keys[kPlanCache];
 Plan g_plans[kPlanCache];
 int g_plan_count = 0, g_plan_next = 0;
 
-kvq_status make_plan(const kvq_cache* c, const kvq_decode_params* p, const DeviceInfo& dev, Plan* out) {
+kvq_status make_plan(const kvq_cache* c, const kvq_decode_params* p, const DeviceInfo& dev, Plan* out,
+                     bool qt = false) {
   PlanKey k;
   std::memset(&k, 0, sizeof k);
   if (cudaGetDevice(&k.dev) != cudaSuccess) return KVQ_ERR_CUDA;
@@ -328,6 +381,7 @@ kvq_status make_plan(const kvq_cache* c, const kvq_decode_params* p, const Devic
   k.max_seq_len = p->max_seq_len;
   k.no_tc = (p->flags & KVQ_DECODE_NO_TCGEN05) ? 1 : 0;
   k.layout = c->layout;
+  k.qt = qt ? 1 : 0;
   {
     std::lock_guard<std::mutex> lk(g_mu);
     for (int i = 0; i < g_plan_count; ++i)
@@ -337,7 +391,7 @@ kvq_status make_plan(const kvq_cache* c, const kvq_decode_params* p, const Devic
       }
   }
   Plan P;
-  if (kvq_status s = make_plan_uncached(c, p, dev, &P)) return s;
+  if (kvq_status s = make_plan_uncached(c, p, dev, qt, &P)) return s;
   std::lock_guard<std::mutex> lk(g_mu);
   const int slot = g_plan_count < kPlanCache ? g_plan_count++ : (g_plan_next++ % kPlanCache);
   g_plan_keys[slot] = k;
@@ -447,11 +501,11 @@ kvq_status append_common(const kvq_cache* cache, const kvq_norm_rope* k_prologue
 // sequences, whose lengths that grid writes).
 kvq_status decode_impl(const kvq_cache* cache, const kvq_decode_params* params, const void* q,
                        const int32_t* block_table, const int32_t* seq_lens, int bt_div, int early_reads,
-                       void* workspace, size_t workspace_bytes, kvq_stream_t stream) {
+                       bool qt, void* workspace, size_t workspace_bytes, kvq_stream_t stream) {
   kvq_cache eff_;
   if (kvq_status s = resolve_cache(cache, &eff_)) return s;
   cache = &eff_;
-  if (kvq_status s = check_params(cache, params)) return s;
+  if (kvq_status s = check_params(cache, params, qt)) return s;
   if (params->batch == 0) return KVQ_OK;
   if (!q || !block_table || !seq_lens || !workspace) return KVQ_ERR_INVALID_ARG;
   if (!aligned(q, 16) || !aligned(block_table, 4) || !aligned(seq_lens, 4) || !aligned(workspace, 256))
@@ -459,7 +513,7 @@ kvq_status decode_impl(const kvq_cache* cache, const kvq_decode_params* params, 
   DeviceInfo* dev;
   if (kvq_status s = current_device(&dev)) return s;
   Plan P;
-  if (kvq_status s = make_plan(cache, params, *dev, &P)) return s;
+  if (kvq_status s = make_plan(cache, params, *dev, &P, qt)) return s;
   if (workspace_bytes < P.ws_total) return KVQ_ERR_WORKSPACE_TOO_SMALL;
 
   alignas(64) CUtensorMap tk, tv;
@@ -498,10 +552,11 @@ kvq_status decode_impl(const kvq_cache* cache, const kvq_decode_params* params, 
   a.units_max = P.units_max;
   // a piece change (query prologue, merge and partial write, refill of the
   // role pipeline) is charged as a few tiles when the split is planned
-  a.piece_cost = P.tc_nr ? kTcPieceCost : kPieceCost;
+  a.piece_cost = P.qt ? kQtPieceCost : (P.tc_nr ? kTcPieceCost : kPieceCost);
   a.bt_div = bt_div;
   // the mma.sync kernel reads a LATENT cache's V from the K codes it loaded
-  a.v_alias = (cache->layout == KVQ_LAYOUT_LATENT && !P.tc_nr) ? 1 : 0;
+  // (the tensor-memory kernels load both sides)
+  a.v_alias = (cache->layout == KVQ_LAYOUT_LATENT && !P.tc_nr && !P.qt) ? 1 : 0;
   a.early_reads = early_reads;
   char* ws = static_cast<char*>(workspace);
   a.plan = reinterpret_cast<int*>(ws);
@@ -511,7 +566,13 @@ kvq_status decode_impl(const kvq_cache* cache, const kvq_decode_params* params, 
 
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e;
-  if (P.tc_nr && any_group(cache)) {
+  if (P.qt) {
+    switch (cache->dtype) {
+      case KVQ_INT8: e = launch_decode_qt_int8(cache->head_dim, tk, tv, a, P.grid, P.smem, st); break;
+      case KVQ_FP8_E4M3: e = launch_decode_qt_fp8(cache->head_dim, tk, tv, a, P.grid, P.smem, st); break;
+      default: e = launch_decode_qt_int4(cache->head_dim, tk, tv, a, P.grid, P.smem, st); break;
+    }
+  } else if (P.tc_nr && any_group(cache)) {
     switch (cache->dtype) {
       case KVQ_INT8: e = launch_decode_tc_grp_int8(cache->head_dim, P.tc_nr, tk, tv, a, P.grid, P.smem, st); break;
       case KVQ_FP8_E4M3: e = launch_decode_tc_grp_fp8(cache->head_dim, P.tc_nr, tk, tv, a, P.grid, P.smem, st); break;
@@ -534,18 +595,92 @@ kvq_status decode_impl(const kvq_cache* cache, const kvq_decode_params* params, 
 }
 
 // A prefill chunk of C tokens per sequence as virtual decode sequences of T
-// tokens (T the largest of 8, 4, 2, 1 dividing C), n = C / T per sequence.
-kvq_status prefill_shape(const kvq_decode_params* p, kvq_decode_params* v, int* n) {
+// tokens each, n = C / T per sequence.  On the query-tile kernel (qt), T is
+// the largest divisor of C whose T x G rows fit its 128-row tile, when that
+// gives at least 64 rows; otherwise the decode kernels take the largest of
+// 8, 4, 2, 1 dividing C.
+kvq_status prefill_shape(const kvq_cache* c, const kvq_decode_params* p, kvq_decode_params* v, int* n,
+                         bool* qt) {
   if (!p || p->q_tokens < 1 || p->batch < 0) return KVQ_ERR_INVALID_ARG;
   const int C = p->q_tokens;
+  const int G = c->num_kv_heads > 0 && p->num_q_heads % c->num_kv_heads == 0 ? p->num_q_heads / c->num_kv_heads : 0;
   int T = 8;
-  while (C % T) T >>= 1;
+  *qt = false;
+  if (G > 0 && qt_ok(c, p)) {
+    int tq = kQtRows / G;
+    if (tq > C) tq = C;
+    while (C % tq) --tq;
+    if (tq * G >= 64) {
+      T = tq;
+      *qt = true;
+    }
+  }
+  if (!*qt)
+    while (C % T) T >>= 1;
   const long long vb = (long long)p->batch * (C / T);
   if (vb > kMaxBatch) return KVQ_ERR_UNSUPPORTED;
   *v = *p;
   v->batch = (int32_t)vb;
   v->q_tokens = T;
   *n = C / T;
+  return KVQ_OK;
+}
+
+// kvq_combine over the plan of decode_impl (qt: the query-tile layout of a
+// prefill's virtual sequences).
+kvq_status combine_impl(const kvq_cache* cache, const kvq_decode_params* params, bool qt, const void* workspace,
+                        size_t workspace_bytes, const float* head_sink, void* out, float* lse_out,
+                        kvq_stream_t stream) {
+  kvq_cache eff_;
+  if (kvq_status s = resolve_cache(cache, &eff_)) return s;
+  cache = &eff_;
+  if (kvq_status s = check_params(cache, params, qt)) return s;
+  if (params->batch == 0) return KVQ_OK;
+  if (!workspace || !out) return KVQ_ERR_INVALID_ARG;
+  if (!aligned(workspace, 256) || !aligned(out, 16) || (lse_out && !aligned(lse_out, 4)) ||
+      (head_sink && !aligned(head_sink, 4)))
+    return KVQ_ERR_INVALID_ARG;
+  DeviceInfo* dev;
+  if (kvq_status s = current_device(&dev)) return s;
+  Plan P;
+  if (kvq_status s = make_plan(cache, params, *dev, &P, qt)) return s;
+  if (workspace_bytes < P.ws_total) return KVQ_ERR_WORKSPACE_TOO_SMALL;
+  const char* ws = static_cast<const char*>(workspace);
+  CombineArgs a{};
+  a.plan = reinterpret_cast<const int*>(ws);
+  a.part_lse = reinterpret_cast<const float*>(ws + P.ws_plan);
+  a.part_o = reinterpret_cast<const float*>(ws + P.ws_plan + P.ws_lse);
+  a.head_sink = head_sink;
+  a.v_mode = cache->v_mode;
+  // per-row and per-group V scales are applied inside the decode kernel
+  a.v_scale = (cache->v_mode == KVQ_SCALE_PER_ROW || cache->v_mode == KVQ_SCALE_PER_GROUP) ? nullptr
+                                                                                          : cache->v_scale;
+  a.out = static_cast<uint16_t*>(out);
+  a.lse_out = lse_out;
+  a.batch = params->batch;
+  a.q_tokens = params->q_tokens;
+  a.num_q_heads = params->num_q_heads;
+  a.num_kv_heads = cache->num_kv_heads;
+  a.group = params->num_q_heads / cache->num_kv_heads;
+  a.rows = P.rows;
+  a.head_dim = cache->head_dim;
+  a.out_dim = cache->v_head_size;
+  return from_cuda(launch_combine(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+
+kvq_status decode_workspace_size(const kvq_cache* cache, const kvq_decode_params* params, bool qt,
+                                 size_t* workspace_bytes) {
+  kvq_cache eff_;
+  if (kvq_status s = resolve_cache(cache, &eff_)) return s;
+  cache = &eff_;
+  if (kvq_status s = check_params(cache, params, qt)) return s;
+  if (!workspace_bytes) return KVQ_ERR_INVALID_ARG;
+  DeviceInfo* dev;
+  if (kvq_status s = current_device(&dev)) return s;
+  Plan P;
+  if (kvq_status s = make_plan(cache, params, *dev, &P, qt)) return s;
+  *workspace_bytes = P.ws_total;
   return KVQ_OK;
 }
 
@@ -603,74 +738,34 @@ KVQ_API kvq_status kvq_norm_rope_apply(const kvq_norm_rope* prologue, const void
 
 KVQ_API kvq_status kvq_decode_workspace_size(const kvq_cache* cache, const kvq_decode_params* params,
                                              size_t* workspace_bytes) {
-  kvq_cache eff_;
-  if (kvq_status s = resolve_cache(cache, &eff_)) return s;
-  cache = &eff_;
-  if (kvq_status s = check_params(cache, params)) return s;
-  if (!workspace_bytes) return KVQ_ERR_INVALID_ARG;
-  DeviceInfo* dev;
-  if (kvq_status s = current_device(&dev)) return s;
-  Plan P;
-  if (kvq_status s = make_plan(cache, params, *dev, &P)) return s;
-  *workspace_bytes = P.ws_total;
-  return KVQ_OK;
+  return decode_workspace_size(cache, params, false, workspace_bytes);
 }
 
 KVQ_API kvq_status kvq_decode(const kvq_cache* cache, const kvq_decode_params* params, const void* q,
                               const int32_t* block_table, const int32_t* seq_lens, void* workspace,
                               size_t workspace_bytes, kvq_stream_t stream) {
   const int early = (params && (params->flags & KVQ_DECODE_EARLY_INPUTS)) ? 1 : 0;
-  return decode_impl(cache, params, q, block_table, seq_lens, 1, early, workspace, workspace_bytes, stream);
+  return decode_impl(cache, params, q, block_table, seq_lens, 1, early, false, workspace, workspace_bytes,
+                     stream);
 }
 
 KVQ_API kvq_status kvq_combine(const kvq_cache* cache, const kvq_decode_params* params, const void* workspace,
                                size_t workspace_bytes, const float* head_sink, void* out, float* lse_out,
                                kvq_stream_t stream) {
-  kvq_cache eff_;
-  if (kvq_status s = resolve_cache(cache, &eff_)) return s;
-  cache = &eff_;
-  if (kvq_status s = check_params(cache, params)) return s;
-  if (params->batch == 0) return KVQ_OK;
-  if (!workspace || !out) return KVQ_ERR_INVALID_ARG;
-  if (!aligned(workspace, 256) || !aligned(out, 16) || (lse_out && !aligned(lse_out, 4)) ||
-      (head_sink && !aligned(head_sink, 4)))
-    return KVQ_ERR_INVALID_ARG;
-  DeviceInfo* dev;
-  if (kvq_status s = current_device(&dev)) return s;
-  Plan P;
-  if (kvq_status s = make_plan(cache, params, *dev, &P)) return s;
-  if (workspace_bytes < P.ws_total) return KVQ_ERR_WORKSPACE_TOO_SMALL;
-  const char* ws = static_cast<const char*>(workspace);
-  CombineArgs a{};
-  a.plan = reinterpret_cast<const int*>(ws);
-  a.part_lse = reinterpret_cast<const float*>(ws + P.ws_plan);
-  a.part_o = reinterpret_cast<const float*>(ws + P.ws_plan + P.ws_lse);
-  a.head_sink = head_sink;
-  a.v_mode = cache->v_mode;
-  // per-row and per-group V scales are applied inside the decode kernel
-  a.v_scale = (cache->v_mode == KVQ_SCALE_PER_ROW || cache->v_mode == KVQ_SCALE_PER_GROUP) ? nullptr
-                                                                                          : cache->v_scale;
-  a.out = static_cast<uint16_t*>(out);
-  a.lse_out = lse_out;
-  a.batch = params->batch;
-  a.q_tokens = params->q_tokens;
-  a.num_q_heads = params->num_q_heads;
-  a.num_kv_heads = cache->num_kv_heads;
-  a.group = params->num_q_heads / cache->num_kv_heads;
-  a.rows = P.rows;
-  a.head_dim = cache->head_dim;
-  a.out_dim = cache->v_head_size;
-  return from_cuda(launch_combine(a, reinterpret_cast<cudaStream_t>(stream)));
+  return combine_impl(cache, params, false, workspace, workspace_bytes, head_sink, out, lse_out, stream);
 }
 
 KVQ_API kvq_status kvq_prefill_workspace_size(const kvq_cache* cache, const kvq_decode_params* params,
                                               size_t* workspace_bytes) {
   if (!workspace_bytes) return KVQ_ERR_INVALID_ARG;
+  kvq_cache eff_;
+  if (kvq_status s = resolve_cache(cache, &eff_)) return s;
   kvq_decode_params v;
   int n = 0;
-  if (kvq_status s = prefill_shape(params, &v, &n)) return s;
+  bool qt = false;
+  if (kvq_status s = prefill_shape(&eff_, params, &v, &n, &qt)) return s;
   size_t ws = 0;
-  if (kvq_status s = kvq_decode_workspace_size(cache, &v, &ws)) return s;
+  if (kvq_status s = decode_workspace_size(&eff_, &v, qt, &ws)) return s;
   *workspace_bytes = align256((size_t)v.batch * 4) + ws;
   return KVQ_OK;
 }
@@ -684,8 +779,9 @@ KVQ_API kvq_status kvq_prefill(const kvq_cache* cache, const kvq_decode_params* 
   cache = &eff_;
   kvq_decode_params v;
   int n = 0;
-  if (kvq_status s = prefill_shape(params, &v, &n)) return s;
-  if (kvq_status s = check_params(cache, &v)) return s;
+  bool qt = false;
+  if (kvq_status s = prefill_shape(cache, params, &v, &n, &qt)) return s;
+  if (kvq_status s = check_params(cache, &v, qt)) return s;
   if (params->batch == 0) return KVQ_OK;
   if (!q || !block_table || !seq_lens || !workspace || !out) return KVQ_ERR_INVALID_ARG;
   if (!aligned(q, 16) || !aligned(block_table, 4) || !aligned(seq_lens, 4) || !aligned(workspace, 256) ||
@@ -702,9 +798,9 @@ KVQ_API kvq_status kvq_prefill(const kvq_cache* cache, const kvq_decode_params* 
   if (cudaError_t e = launch_prefill_lens(seq_lens, lens, params->batch, n, params->q_tokens, v.q_tokens, st))
     return from_cuda(e);
   char* ws = static_cast<char*>(workspace) + head;
-  if (kvq_status s = decode_impl(cache, &v, q, block_table, lens, n, 0, ws, workspace_bytes - head, stream))
+  if (kvq_status s = decode_impl(cache, &v, q, block_table, lens, n, 0, qt, ws, workspace_bytes - head, stream))
     return s;
-  return kvq_combine(cache, &v, ws, workspace_bytes - head, head_sink, out, lse_out, stream);
+  return combine_impl(cache, &v, qt, ws, workspace_bytes - head, head_sink, out, lse_out, stream);
 }
 
 KVQ_API kvq_status kvq_check_wait_timeout(uint32_t limit_us, kvq_stream_t stream) {

@@ -1,0 +1,11 @@
+// decode_qt_int4.cu -- the query-tile kernel's int4 instance (head_dim 256).
+#include "decode_qt.cuh"
+
+namespace kvq {
+
+cudaError_t launch_decode_qt_int4(int head_dim, const CUtensorMap& tk, const CUtensorMap& tv, const DecodeArgs& a,
+                                  int grid, size_t smem, cudaStream_t stream) {
+  return dispatch_decode_qt<KVQ_INT4>(head_dim, tk, tv, a, grid, smem, stream);
+}
+
+}  // namespace kvq

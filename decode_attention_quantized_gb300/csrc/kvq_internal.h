@@ -129,6 +129,35 @@ __host__ __device__ constexpr TcSmem tc_smem_layout(int head_dim, int row_bytes,
   s.scr = s.p + 2 * nr * 2 * kTcKeys;
   s.pre = s.scr + (2 * nr + 3 * 4 * nr + 16) * 4;
   s.bars = (s.pre + (batch + 5) * 4 + 7) / 8 * 8;
+  s.slot = s.bars + (2 * stages + 20) * 8;
+  s.total = s.slot + 16;
+  return s;
+}
+
+// The query-tile kernel (query rows as the MMA's M dimension: a prefill
+// chunk's tokens x the GQA group, up to 128 rows per kv head): 64-key stages
+// (the mma.sync kernel's ring), 14 warps, f16 K and V tiles double-buffered in
+// shared memory.  Byte offsets from the 1024-aligned base.
+constexpr int kQtWarps = 15;
+constexpr int kQtRows = 128;
+
+struct QtSmem {
+  int ring, kf, vf, sc, pre, bars, slot, total;
+};
+
+// ring: stages x stage stride; kf, vf: two [D/64 slabs][kTile keys][128 B] f16
+// tiles each; sc: four [kTile] K scales and four V-normaliser exponents (the
+// per-row scales a tile's softmax needs, copied out of the stage so that the
+// stage is released early); pre: split plan; bars: mbarriers; slot: TMEM
+// address + abort flag.
+__host__ __device__ constexpr QtSmem qt_smem_layout(int head_dim, int stages, int batch, int stage_stride) {
+  QtSmem s{};
+  s.ring = 0;
+  s.kf = stages * stage_stride;
+  s.vf = s.kf + 2 * (head_dim / 64) * kTile * 128;
+  s.sc = s.vf + 2 * (head_dim / 64) * kTile * 128;
+  s.pre = s.sc + 4 * kTile * 4 + 4 * 4;
+  s.bars = (s.pre + (batch + 5) * 4 + 7) / 8 * 8;
   s.slot = s.bars + (2 * stages + 16) * 8;
   s.total = s.slot + 16;
   return s;
@@ -183,6 +212,14 @@ cudaError_t launch_decode_tc_grp_fp8(int head_dim, int nr, const CUtensorMap& tk
                                      const DecodeArgs& a, int grid, size_t smem, cudaStream_t stream);
 cudaError_t launch_decode_tc_grp_int4(int head_dim, int nr, const CUtensorMap& tk, const CUtensorMap& tv,
                                       const DecodeArgs& a, int grid, size_t smem, cudaStream_t stream);
+
+// The query-tile kernel (head_dim 256; no group-wise scales).
+cudaError_t launch_decode_qt_int8(int head_dim, const CUtensorMap& tk, const CUtensorMap& tv, const DecodeArgs& a,
+                                  int grid, size_t smem, cudaStream_t stream);
+cudaError_t launch_decode_qt_fp8(int head_dim, const CUtensorMap& tk, const CUtensorMap& tv, const DecodeArgs& a,
+                                 int grid, size_t smem, cudaStream_t stream);
+cudaError_t launch_decode_qt_int4(int head_dim, const CUtensorMap& tk, const CUtensorMap& tv, const DecodeArgs& a,
+                                  int grid, size_t smem, cudaStream_t stream);
 
 cudaError_t occupancy_decode_int8(int head_dim, int nt, int threads, size_t smem, int* blocks_per_sm);
 cudaError_t occupancy_decode_fp8(int head_dim, int nt, int threads, size_t smem, int* blocks_per_sm);

@@ -74,6 +74,29 @@ static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parit
   return false;
 }
 
+// The same wait with the waiting thread suspended between polls (a suspend
+// hint of hint_ns: the thread resumes when the phase completes or the hint
+// runs out), so that the pollers of a stalled pipeline leave the issue slots
+// and the shared-memory pipe to the warps that do the work.
+__device__ __forceinline__ bool mbar_try_wait_hint(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\tselp.u32 %0, 1, 0, "
+      "p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+static __device__ __noinline__ bool mbar_wait_slow_suspend(uint64_t* bar, uint32_t parity) {
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t i = 0; i < (1u << 24); ++i) {
+    if (mbar_try_wait_hint(bar, parity, 20000u)) return true;
+    if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+  }
+  return false;
+}
+
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
   if (mbar_try_wait(bar, parity)) return true;
   return mbar_wait_slow(bar, parity);
@@ -189,6 +212,27 @@ __device__ __forceinline__ float fast_log2(float x) {
   float y;
   asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+
+// Packed fp32 pairs (sm_100-family f32x2 arithmetic: one instruction for two
+// IEEE round-to-nearest results).
+__device__ __forceinline__ void mul_x2(float& d0, float& d1, float a0, float a1, float b0, float b1) {
+  asm("{\n\t.reg .b64 a, b, d;\n\tmov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
+      "mul.rn.f32x2 d, a, b;\n\tmov.b64 {%0, %1}, d;\n\t}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+__device__ __forceinline__ void add_x2(float& d0, float& d1, float a0, float a1, float b0, float b1) {
+  asm("{\n\t.reg .b64 a, b, d;\n\tmov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
+      "add.rn.f32x2 d, a, b;\n\tmov.b64 {%0, %1}, d;\n\t}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+// max(a, b, c) in one instruction (sm_100 family).
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
 }
 
 // Programmatic dependent launch: wait until the preceding grid on the stream
@@ -316,6 +360,14 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
          ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
 }
 
+// The same swizzle for an MN-major operand (N contiguous: rows of 128 bytes
+// along K, 64-element column slabs `lbo` bytes apart, 8-row groups 1024 bytes
+// apart).
+__device__ __forceinline__ uint64_t smem_desc_sw128_mn(uint32_t addr, uint32_t lbo) {
+  return (uint64_t)((addr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+         ((uint64_t)(1024 >> 4) << 32) | ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+
 // Instruction descriptor of kind::f16 with f16 A and B (both K-major) and an
 // fp32 accumulator, M x N.
 __host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N) {
@@ -356,6 +408,49 @@ __device__ __forceinline__ void mma_f16_ts_x4(uint32_t d_tmem, uint32_t a_tmem, 
       "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a2], b2, %5, t;\n\t"
       "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a3], b3, %5, t;\n\t}" ::"r"(d_tmem),
       "r"(a_tmem), "r"(a_step), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// The same four k-steps with the B descriptor advanced by b_step (in 16-byte
+// units) per step: an MN-major B, whose k-step is 16 rows of 128 bytes.
+__device__ __forceinline__ void mma_f16_ts_x4_step(uint32_t d_tmem, uint32_t a_tmem, uint32_t a_step, uint32_t b_lo,
+                                                   uint32_t b_step, uint32_t b_hi, uint32_t idesc,
+                                                   uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, t, e;\n\t.reg .b32 a1, a2, a3, l1, l2, l3;\n\t.reg .b64 b0, b1, b2, b3;\n\t"
+      "setp.ne.b32 p, %7, 0;\n\tsetp.ne.b32 t, %6, 0;\n\t"
+      "add.u32 a1, %1, %2;\n\tadd.u32 a2, a1, %2;\n\tadd.u32 a3, a2, %2;\n\t"
+      "add.u32 l1, %3, %4;\n\tadd.u32 l2, l1, %4;\n\tadd.u32 l3, l2, %4;\n\t"
+      "mov.b64 b0, {%3, %5};\n\tmov.b64 b1, {l1, %5};\n\tmov.b64 b2, {l2, %5};\n\tmov.b64 b3, {l3, %5};\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], b0, %6, p;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a1], b1, %6, t;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a2], b2, %6, t;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a3], b3, %6, t;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "r"(a_step), "r"(b_lo), "r"(b_step), "r"(b_hi), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Four consecutive k-steps of D (+)= A[smem] * B[smem]^T: A K-major in the
+// 128-byte swizzle (descriptor low half a_lo + 2 j: one 32-byte step of its
+// 128-byte rows), B's low half advanced by b_step per step.  Called by a
+// whole converged warp.
+__device__ __forceinline__ void mma_f16_ss_x4(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo, uint32_t b_step,
+                                              uint32_t d_hi, uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, t, e;\n\t.reg .b32 a1, a2, a3, l1, l2, l3;\n\t"
+      ".reg .b64 a0d, a1d, a2d, a3d, b0, b1, b2, b3;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\tsetp.ne.b32 t, %5, 0;\n\t"
+      "add.u32 a1, %1, 2;\n\tadd.u32 a2, %1, 4;\n\tadd.u32 a3, %1, 6;\n\t"
+      "add.u32 l1, %2, %3;\n\tadd.u32 l2, l1, %3;\n\tadd.u32 l3, l2, %3;\n\t"
+      "mov.b64 a0d, {%1, %4};\n\tmov.b64 a1d, {a1, %4};\n\tmov.b64 a2d, {a2, %4};\n\tmov.b64 a3d, {a3, %4};\n\t"
+      "mov.b64 b0, {%2, %4};\n\tmov.b64 b1, {l1, %4};\n\tmov.b64 b2, {l2, %4};\n\tmov.b64 b3, {l3, %4};\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a0d, b0, %5, p;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a1d, b1, %5, t;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a2d, b2, %5, t;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a3d, b3, %5, t;\n\t}" ::"r"(d_tmem),
+      "r"(a_lo), "r"(b_lo), "r"(b_step), "r"(d_hi), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 

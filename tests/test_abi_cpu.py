@@ -182,9 +182,16 @@ def test_prefill_rejects_bad_arguments_on_the_host(kvq):
     assert lib.kvq_prefill_workspace_size(ctypes.byref(c), ctypes.byref(p), ctypes.byref(n)) == 1
     assert lib.kvq_prefill(ctypes.byref(c), ctypes.byref(p), FAKE, FAKE, FAKE, None, FAKE, None, FAKE, 1 << 30,
                            None) == 1
-    # 200 sequences x 64 tokens = 1600 virtual sequences of 8: beyond the plan's 1024
-    p = good_params(kvq, batch=200, q_tokens=64)
+    # 200 sequences x 64 tokens = 1600 virtual sequences of 8 on the decode
+    # kernels: beyond the plan's 1024
+    p = good_params(kvq, batch=200, q_tokens=64, flags=kvq.DECODE_NO_TCGEN05)
     assert lib.kvq_prefill_workspace_size(ctypes.byref(c), ctypes.byref(p), ctypes.byref(n)) == 2
+    # on the query-tile kernel (head_dim 256, 4 query heads per kv head:
+    # 32-token tiles of 128 rows) 600 x 64 tokens are 1200 virtual sequences:
+    # beyond it as well
+    c256 = good_cache(kvq, head_dim=256)
+    p = good_params(kvq, batch=600, q_tokens=64)
+    assert lib.kvq_prefill_workspace_size(ctypes.byref(c256), ctypes.byref(p), ctypes.byref(n)) == 2
     # missing or misaligned pointers
     p = good_params(kvq, q_tokens=12)
     for args in [(None, FAKE, FAKE, None, FAKE), (FAKE, FAKE, None, None, FAKE), (FAKE, FAKE, FAKE, None, None),
