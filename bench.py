@@ -589,7 +589,7 @@ def measure_prefill(w, steps, warmup, peak, chunk=64):
     seen = sum(min(int(L), max(0, int(L) - C + t + 1)) for L in w.seq_lens for t in range(C))
     flops = 4.0 * w.head_dim * w.num_q_heads * seen
     G = w.group
-    qt = w.head_dim == 256 and w.k_mode != synth.PER_GROUP and w.v_mode != synth.PER_GROUP
+    qt = w.head_dim in (128, 256) and w.k_mode != synth.PER_GROUP and w.v_mode != synth.PER_GROUP
     tq = 0
     if qt:
         tq = min(128 // G, C)

@@ -143,7 +143,12 @@ kvq_status check_params(const kvq_cache* c, const kvq_decode_params* p, bool qt 
 // workload's decode went from 249 to 206 us, paged from 120 to 118 us, spec
 // from 67.8 to 64.8 us).
 constexpr int kTcPieceCost = 3;
+// The query-tile kernel: a piece change (Q prologue, epilogue, pipeline
+// refill) costs about 8 of its tiles; its ring is capped at 3 stages (with
+// 7-8 stages at head_dim 128, a quarter of the CTAs of a ragged batch ran
+// 3-4x slower than the rest; 3 stages measured balanced and fastest).
 constexpr int kQtPieceCost = 8;
+constexpr int kQtMaxStages = 3;
 constexpr int kPieceCost = 3;
 
 // Launch shape of the decode kernel and the workspace it implies.
@@ -227,12 +232,10 @@ kvq_status make_plan_tc(const kvq_cache* c, const kvq_decode_params* p, const De
   return KVQ_OK;
 }
 
-// Whether kvq_prefill takes the query-tile kernel: head_dim 256, no
-// group-wise scales, the tcgen05 kernels allowed.  The kernel also runs at
-// head_dim 128, but there some CTAs of a ragged batch stall for microseconds
-// at a time and the virtual decode sequences are faster (measured).
+// Whether kvq_prefill takes the query-tile kernel: head_dim 128 or 256, no
+// group-wise scales, the tcgen05 kernels allowed.
 bool qt_ok(const kvq_cache* c, const kvq_decode_params* p) {
-  return !(p->flags & KVQ_DECODE_NO_TCGEN05) && c->head_dim == 256 && !any_group(c);
+  return !(p->flags & KVQ_DECODE_NO_TCGEN05) && (c->head_dim == 128 || c->head_dim == 256) && !any_group(c);
 }
 
 // The query-tile kernel: one CTA per SM (it holds all of the SM's TMEM), the
@@ -243,7 +246,7 @@ kvq_status make_plan_qt(const kvq_cache* c, const kvq_decode_params* p, const De
   const size_t stride = stage_stride(c, false);
   constexpr size_t kMaxSmem = 227 * 1024;  // per CTA
   int stages = 0;
-  for (int s = kMaxStages; s >= 2 && stages == 0; --s)
+  for (int s = kQtMaxStages; s >= 2 && stages == 0; --s)
     if ((size_t)qt_smem_layout(c->head_dim, s, B, (int)stride).total + 1024 <= kMaxSmem) stages = s;
   if (stages == 0) return KVQ_ERR_UNSUPPORTED;
   P->qt = 1;

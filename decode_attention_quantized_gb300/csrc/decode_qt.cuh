@@ -79,19 +79,6 @@ __device__ __forceinline__ void v_cols(const uint4 w4, uint32_t* v) {
   }
 }
 
-// The slow path of a bounded wait (as dev::wait_or_abort), its polls
-// suspended: in a stalled pipeline of fifteen warps, spinning pollers would
-// take the issue slots and the shared-memory pipe from the warps that can
-// make progress.
-static __device__ __noinline__ void qt_wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                                     unsigned int* err) {
-  if (*abort_flag) return;
-  if (!ptx::mbar_wait_slow_suspend(bar, parity)) {
-    *abort_flag = 1;
-    atomicOr(err, KVQ_DEVERR_TIMEOUT);
-  }
-}
-
 // Address of 16-byte f16 chunk c (K or N index 8c .. 8c + 7) of key row kk in
 // an f16 tile: 64-element slabs of [KT rows][128 B], the chunk index XORed
 // with kk & 7 (the tensor core's 128-byte swizzle).
@@ -167,7 +154,7 @@ __global__ void __launch_bounds__(kQtWarps * 32, 1)
   // Bounded wait: after a timeout every later wait of the CTA is skipped, the
   // results are flagged, and the CTA reaches its end.
   auto wait = [&](uint64_t* bar, uint32_t parity) {
-    if (!ptx::mbar_try_wait(bar, parity)) dev::qt_wait_or_abort(bar, parity, abort_flag, a.err);
+    if (!ptx::mbar_try_wait(bar, parity)) dev::wait_or_abort(bar, parity, abort_flag, a.err);
   };
   const bool k_row = a.k_mode == KVQ_SCALE_PER_ROW, v_row = a.v_mode == KVQ_SCALE_PER_ROW;
 
@@ -276,6 +263,17 @@ __global__ void __launch_bounds__(kQtWarps * 32, 1)
     const uint32_t k_lo = (uint32_t)kd, d_hi = (uint32_t)(kd >> 32);
     const uint32_t v_lo = (uint32_t)ptx::smem_desc_sw128_mn(vf, C::SLAB);
     const bool qk_warp = warp == kMma;
+    // PV of tile j (A = P, B = its V tile); the first of a piece overwrites O
+    auto issue_pv = [&](uint32_t j, bool first) {
+      const uint32_t buf = j & 1;
+      wait(&b_pfull[buf], (j >> 1) & 1);
+      wait(&b_vfull[buf], (j >> 1) & 1);
+      __syncwarp();
+      ptx::tc_fence_after();
+      ptx::mma_f16_ts_x4_step(tmem + C::O_COL, tmem + C::P_COL + (KT / 2) * buf, 8, v_lo + buf * (C::TILE >> 4),
+                              (16 * 128) >> 4, d_hi, idesc_pv, first ? 0u : 1u);
+      ptx::mma_commit(&b_pv[buf]);
+    };
     uint32_t it = 0;
     int pc = 0;
     for (int gt = sp.t_begin, next; gt < sp.t_end; gt = next, ++pc) {
@@ -298,13 +296,7 @@ __global__ void __launch_bounds__(kQtWarps * 32, 1)
           ptx::mma_commit(&b_qk[sb]);
           ptx::mma_commit(&b_kfree[buf]);
         } else {
-          wait(&b_pfull[buf], (it >> 1) & 1);
-          wait(&b_vfull[buf], (it >> 1) & 1);
-          __syncwarp();
-          ptx::tc_fence_after();
-          ptx::mma_f16_ts_x4_step(tmem + C::O_COL, tmem + C::P_COL + (KT / 2) * buf, 8, v_lo + buf * (C::TILE >> 4),
-                                  (16 * 128) >> 4, d_hi, idesc_pv, first ? 0u : 1u);
-          ptx::mma_commit(&b_pv[buf]);
+          issue_pv(it, first);
         }
       }
     }
@@ -634,12 +626,11 @@ cudaError_t launch_decode_qt_d(const CUtensorMap& tk, const CUtensorMap& tv, con
   return launch_pdl(decode_qt_kernel<DT, D>, grid, kQtWarps * 32, smem, stream, tk, tv, a);
 }
 
-// head_dim 256 (the template also holds 128: two S buffers fit its TMEM;
-// kvq_prefill does not take it there, see qt_ok in api.cu).
 template <int DT>
 cudaError_t dispatch_decode_qt(int head_dim, const CUtensorMap& tk, const CUtensorMap& tv, const DecodeArgs& a,
                                int grid, size_t smem, cudaStream_t stream) {
   if (head_dim == 256) return launch_decode_qt_d<DT, 256>(tk, tv, a, grid, smem, stream);
+  if (head_dim == 128) return launch_decode_qt_d<DT, 128>(tk, tv, a, grid, smem, stream);
   return cudaErrorInvalidValue;
 }
 

@@ -1,4 +1,4 @@
-// decode_qt_fp8.cu -- the query-tile kernel's fp8 instance (head_dim 256).
+// decode_qt_fp8.cu -- the query-tile kernel's fp8 instances (head_dim 128, 256).
 #include "decode_qt.cuh"
 
 namespace kvq {

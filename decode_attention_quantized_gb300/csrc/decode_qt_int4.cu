@@ -1,4 +1,4 @@
-// decode_qt_int4.cu -- the query-tile kernel's int4 instance (head_dim 256).
+// decode_qt_int4.cu -- the query-tile kernel's int4 instances (head_dim 128, 256).
 #include "decode_qt.cuh"
 
 namespace kvq {

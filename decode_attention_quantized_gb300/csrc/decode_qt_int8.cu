@@ -1,4 +1,4 @@
-// decode_qt_int8.cu -- the query-tile kernel's int8 instance (head_dim 256).
+// decode_qt_int8.cu -- the query-tile kernel's int8 instances (head_dim 128, 256).
 #include "decode_qt.cuh"
 
 namespace kvq {

@@ -213,7 +213,7 @@ cudaError_t launch_decode_tc_grp_fp8(int head_dim, int nr, const CUtensorMap& tk
 cudaError_t launch_decode_tc_grp_int4(int head_dim, int nr, const CUtensorMap& tk, const CUtensorMap& tv,
                                       const DecodeArgs& a, int grid, size_t smem, cudaStream_t stream);
 
-// The query-tile kernel (head_dim 256; no group-wise scales).
+// The query-tile kernel (head_dim 128 or 256; no group-wise scales).
 cudaError_t launch_decode_qt_int8(int head_dim, const CUtensorMap& tk, const CUtensorMap& tv, const DecodeArgs& a,
                                   int grid, size_t smem, cudaStream_t stream);
 cudaError_t launch_decode_qt_fp8(int head_dim, const CUtensorMap& tk, const CUtensorMap& tv, const DecodeArgs& a,

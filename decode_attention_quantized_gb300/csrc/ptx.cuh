@@ -74,29 +74,6 @@ static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parit
   return false;
 }
 
-// The same wait with the waiting thread suspended between polls (a suspend
-// hint of hint_ns: the thread resumes when the phase completes or the hint
-// runs out), so that the pollers of a stalled pipeline leave the issue slots
-// and the shared-memory pipe to the warps that do the work.
-__device__ __forceinline__ bool mbar_try_wait_hint(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\tselp.u32 %0, 1, 0, "
-      "p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
-      : "memory");
-  return ok != 0;
-}
-static __device__ __noinline__ bool mbar_wait_slow_suspend(uint64_t* bar, uint32_t parity) {
-  const uint64_t t0 = globaltimer_ns();
-  for (uint32_t i = 0; i < (1u << 24); ++i) {
-    if (mbar_try_wait_hint(bar, parity, 20000u)) return true;
-    if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
-  }
-  return false;
-}
-
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
   if (mbar_try_wait(bar, parity)) return true;
   return mbar_wait_slow(bar, parity);
@@ -428,29 +405,6 @@ __device__ __forceinline__ void mma_f16_ts_x4_step(uint32_t d_tmem, uint32_t a_t
       "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a2], b2, %6, t;\n\t"
       "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a3], b3, %6, t;\n\t}" ::"r"(d_tmem),
       "r"(a_tmem), "r"(a_step), "r"(b_lo), "r"(b_step), "r"(b_hi), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// Four consecutive k-steps of D (+)= A[smem] * B[smem]^T: A K-major in the
-// 128-byte swizzle (descriptor low half a_lo + 2 j: one 32-byte step of its
-// 128-byte rows), B's low half advanced by b_step per step.  Called by a
-// whole converged warp.
-__device__ __forceinline__ void mma_f16_ss_x4(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo, uint32_t b_step,
-                                              uint32_t d_hi, uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p, t, e;\n\t.reg .b32 a1, a2, a3, l1, l2, l3;\n\t"
-      ".reg .b64 a0d, a1d, a2d, a3d, b0, b1, b2, b3;\n\t"
-      "setp.ne.b32 p, %6, 0;\n\tsetp.ne.b32 t, %5, 0;\n\t"
-      "add.u32 a1, %1, 2;\n\tadd.u32 a2, %1, 4;\n\tadd.u32 a3, %1, 6;\n\t"
-      "add.u32 l1, %2, %3;\n\tadd.u32 l2, l1, %3;\n\tadd.u32 l3, l2, %3;\n\t"
-      "mov.b64 a0d, {%1, %4};\n\tmov.b64 a1d, {a1, %4};\n\tmov.b64 a2d, {a2, %4};\n\tmov.b64 a3d, {a3, %4};\n\t"
-      "mov.b64 b0, {%2, %4};\n\tmov.b64 b1, {l1, %4};\n\tmov.b64 b2, {l2, %4};\n\tmov.b64 b3, {l3, %4};\n\t"
-      "elect.sync _|e, 0xffffffff;\n\t"
-      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a0d, b0, %5, p;\n\t"
-      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a1d, b1, %5, t;\n\t"
-      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a2d, b2, %5, t;\n\t"
-      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a3d, b3, %5, t;\n\t}" ::"r"(d_tmem),
-      "r"(a_lo), "r"(b_lo), "r"(b_step), "r"(d_hi), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 
