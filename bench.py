@@ -31,6 +31,7 @@ sys.path.insert(0, ROOT)
 METRIC = "decode-attention µs/step and cache GB/s (% of GB300 HBM peak) vs context length"
 SWEEP = [1024, 4096, 16384, 65536, 262144]
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
 
 
 def parse():
@@ -64,6 +65,17 @@ def load_peaks():
         return float(d["hbm_gbs"]), "measured"
     except Exception:
         return FALLBACK_HBM_GBS, "fallback"
+
+
+def load_tensor_peak():
+    """Dense 16-bit tensor throughput (TFLOP/s): the measured bf16 GEMM burst
+    figure (f16 runs at the same rate), else the fallback."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except Exception:
+        return FALLBACK_BF16_TFLOPS, "fallback"
 
 
 class Clocks:
@@ -597,6 +609,7 @@ def measure_prefill(w, steps, warmup, peak, chunk=64):
             tq -= 1
         qt = tq * G >= 64
     T = tq if qt else max(t for t in (8, 4, 2, 1) if C % t == 0)
+    tpeak, tkind = load_tensor_peak()
     del gw, q, out, lse, ws
     torch.cuda.empty_cache()
     return {"chunk_tokens": C, "us_per_chunk": round(1e3 * ms, 2),
@@ -605,6 +618,8 @@ def measure_prefill(w, steps, warmup, peak, chunk=64):
                       else "virtual decode sequences of %d tokens" % T,
             "groups_per_sequence": C // T,
             "attention_tflops": round(flops / (ms * 1e-3) / 1e12, 1),
+            "frac_of_tensor_peak": round(flops / (ms * 1e-3) / 1e12 / tpeak, 3),
+            "tensor_peak_tflops": tpeak, "tensor_peak_kind": f"of {tkind} (bf16 dense GEMM; f16 same rate)",
             "single_pass_gbs": round(one_pass / (ms * 1e-3) / 1e9, 1),
             "single_pass_frac_of_hbm": round(one_pass / (ms * 1e-3) / 1e9 / peak, 3)}
 

@@ -304,13 +304,20 @@ KVQ_API kvq_status kvq_combine(const kvq_cache* cache, const kvq_decode_params* 
  * (kvq_append); token c of sequence b sits at position seq_lens[b] - C + c
  * and sees keys 0..that position (and the window, when set).  q, out bf16
  * [B, C, Hq, D]; lse_out fp32 [B, C, Hq] or NULL; head_sink as in
- * kvq_combine.  It runs as one decode pass and one combine over B * C / T
- * virtual sequences of T tokens each (T the largest of 8, 4, 2, 1 that
- * divides C; B * C / T <= 1024), sequence b's j-th group seeing the prefix
- * seq_lens[b] - C + T (j + 1): each group re-reads its prefix, so a chunk
- * costs about C / T decode steps of cache reads, shared through L2 where they
- * coincide.  C >= 1 (no upper bound besides the virtual batch).  workspace:
- * at least kvq_prefill_workspace_size bytes, 256-byte aligned. */
+ * kvq_combine.  The chunk is cut into groups of T tokens (virtual
+ * sequences; sequence b's j-th group sees the prefix seq_lens[b] - C + T
+ * (j + 1)), run as one attention pass and one combine; B * C / T <= 1024.
+ * With head_dim 128 or 256, no group-wise scales and KVQ_DECODE_NO_TCGEN05
+ * unset, T is the largest divisor of C with T x (Hq / Hkv) <= 128 when that
+ * gives at least 64 query rows per kv head: a group's rows are the M
+ * dimension of tcgen05 MMAs and each key tile of its prefix is dequantized
+ * once for all of them (the kv-quant-attn page, "Requirements and limits":
+ * prefill wants a tiled attention kernel).  Otherwise T is the largest of 8,
+ * 4, 2, 1 dividing C and the groups run on the decode kernels.  Each group
+ * reads its prefix, so a chunk costs C / T passes over the cache, shared
+ * through L2 where they coincide.  C >= 1 (no upper bound besides the
+ * virtual batch).  workspace: at least kvq_prefill_workspace_size bytes,
+ * 256-byte aligned. */
 KVQ_API kvq_status kvq_prefill_workspace_size(const kvq_cache* cache, const kvq_decode_params* params,
                                               size_t* workspace_bytes);
 KVQ_API kvq_status kvq_prefill(const kvq_cache* cache, const kvq_decode_params* params, const void* q,

@@ -1,7 +1,7 @@
 """kvq_prefill on the query-tile kernel (the query rows of a chunk -- tokens x
-GQA group, up to 128 per kv head -- as the MMA's M dimension; head_dim 256, no
-group-wise scales) against oracle attention with the same chunk: every code
-type and scale mode, chunks of 24 to 512 tokens, ragged lengths, window,
+GQA group, up to 128 per kv head -- as the MMA's M dimension; head_dim 128 or
+256, no group-wise scales) against oracle attention with the same chunk: every
+code type and scale mode, chunks of 24 to 512 tokens, ragged lengths, window,
 softcap and head sink.  The same calls with KVQ_DECODE_NO_TCGEN05 (virtual
 decode sequences on the mma.sync kernel) are checked against the oracle too.
 Within 2e-3 relative L2 (8e-3 for any row); LSE within 2e-3; repeated calls
@@ -32,6 +32,10 @@ CASES = [
     ("int8", kvq.PER_ROW, kvq.PER_ROW, 256, 8, 24, (400, 3000), 700, 30.0, True),            # 12 x 8, window, softcap
     ("fp8", kvq.PER_ROW, kvq.PER_ROW, 256, 1, 100, (100, 300), 0, 0.0, False),               # 100 tokens x 1
     ("int4", kvq.PER_ROW, kvq.PER_ROW, 256, 4, 48, (1000, 48), 64, 0.0, False),              # 24 x 4 (a padded warp), window 64
+    ("int8", kvq.PER_TENSOR, kvq.PER_ROW, 128, 8, 32, (300, 45, 999), 0, 0.0, False),        # head_dim 128: 16 x 8
+    ("fp8", kvq.PER_TENSOR, kvq.PER_TENSOR, 128, 4, 64, (70, 2000, 640), 0, 50.0, True),     # 32 x 4, softcap, sink
+    ("int4", kvq.PER_CHANNEL, kvq.PER_ROW, 128, 2, 512, (512, 1300), 0, 0.0, False),         # 64 x 2
+    ("int8", kvq.PER_ROW, kvq.PER_ROW, 128, 1, 100, (100, 300), 37, 0.0, False),             # 100 x 1, window 37
 ]
 
 
