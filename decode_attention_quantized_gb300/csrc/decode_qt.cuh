@@ -120,6 +120,7 @@ __global__ void __launch_bounds__(kQtWarps * 32, 1)
   uint64_t* b_pv = b_qk + 12;             // [2] PV of tile it complete: P buffer and V tile it & 1 free
   uint64_t* b_qfull = b_qk + 14;          // Q of a piece in TMEM
   uint64_t* b_ksc = b_qk + 15;            // [4] K scales of tile it in ksb slot it & 3 (per-row K)
+  uint64_t* b_fx = b_qk + 19;             // [4] V normaliser of tile it in fexp slot it & 3 (per-row V)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + lay.slot);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -139,7 +140,10 @@ __global__ void __launch_bounds__(kQtWarps * 32, 1)
       ptx::mbar_init(&b_pv[i], 1);
     }
     ptx::mbar_init(b_qfull, 4);
-    for (int i = 0; i < 4; ++i) ptx::mbar_init(&b_ksc[i], 2);  // the two K warps of channel half 0
+    for (int i = 0; i < 4; ++i) {
+      ptx::mbar_init(&b_ksc[i], 2);  // the two K warps of channel half 0
+      ptx::mbar_init(&b_fx[i], 1);   // the first V warp
+    }
     *abort_flag = 0;
     ptx::fence_mbar_init();
   }
@@ -209,11 +213,20 @@ __global__ void __launch_bounds__(kQtWarps * 32, 1)
         if (lane == 0) ptx::mbar_arrive(&bar_empty[stage]);
         uint32_t s2 = 0;
         if (is_v && v_row) {
-          // the softmax warps read F of this tile from fexp
           vm = ptx::redux_max(vm);
           if (vm > 0.0f) F = max(F, min(126, max(-126, dev::ceil_log2(vm))));
           const float s = key0 + kk < L ? sc * dev::pow2i(-F) : 0.0f;
           s2 = dev::pack_h2(s, s);
+          // F of this tile for the softmax warps, before the conversion and
+          // the wait for the V tile: the softmax needs the normaliser, not
+          // the tile.  Slot it & 3 was last read by the softmax of tile
+          // it - 4, which finished before the PV of tile it - 3 that this
+          // warp waited for on its previous tile.
+          if (q == 0) {
+            if (lane == 0) fexp[it & 3] = F;
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(&b_fx[it & 3]);
+          }
         }
         uint32_t v[NCC * CW];
 #pragma unroll
@@ -234,15 +247,11 @@ __global__ void __launch_bounds__(kQtWarps * 32, 1)
                        "r"(v[4 * c + 2]), "r"(v[4 * c + 3])
                        : "memory");
         }
-        // the softmax of tile `it` reads slot it & 3 (K scales after b_ksc,
-        // the V normaliser after this tile's V barrier); the slot was last
-        // read by the softmax of tile it - 4, which completed before the MMA
-        // two tiles back that this warp waited for, so each slot's barrier is
-        // never more than one phase ahead of its reader
-        if (hf == 0) {
-          if (!is_v && k_row) ksb[(it & 3) * KT + kk] = sc;
-          if (is_v && v_row && q == 0 && lane == 0) fexp[it & 3] = F;
-        }
+        // the softmax of tile `it` reads the K scales in slot it & 3 after
+        // b_ksc; the slot was last read by the softmax of tile it - 4, which
+        // completed before the MMA two tiles back that this warp waited for,
+        // so the slot's barrier is never more than one phase ahead of its reader
+        if (hf == 0 && !is_v && k_row) ksb[(it & 3) * KT + kk] = sc;
         ptx::fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
@@ -520,7 +529,7 @@ __global__ void __launch_bounds__(kQtWarps * 32, 1)
         }
         float fs = 1.0f;  // growth of the V-scale normaliser
         if (v_row) {
-          wait(&b_vfull[buf], (it >> 1) & 1);  // V of this tile written: its normaliser is in fexp
+          wait(&b_fx[it & 3], (it >> 2) & 1);  // this tile's V normaliser is in fexp
           const int fn = fexp[it & 3];
           if (fn > F) {
             fs = (F - fn < -126) ? 0.0f : dev::pow2i(F - fn);

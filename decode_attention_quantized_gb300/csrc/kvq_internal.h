@@ -129,7 +129,7 @@ __host__ __device__ constexpr TcSmem tc_smem_layout(int head_dim, int row_bytes,
   s.scr = s.p + 2 * nr * 2 * kTcKeys;
   s.pre = s.scr + (2 * nr + 3 * 4 * nr + 16) * 4;
   s.bars = (s.pre + (batch + 5) * 4 + 7) / 8 * 8;
-  s.slot = s.bars + (2 * stages + 20) * 8;
+  s.slot = s.bars + (2 * stages + 24) * 8;
   s.total = s.slot + 16;
   return s;
 }
