@@ -32,6 +32,7 @@ METRIC = "decode-attention µs/step and cache GB/s (% of GB300 HBM peak) vs cont
 SWEEP = [1024, 4096, 16384, 65536, 262144]
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
+EARLY_CACHE = True  # the decode steps' KVQ_DECODE_EARLY_CACHE (see --no-early-cache)
 
 
 def parse():
@@ -50,6 +51,8 @@ def parse():
     p.add_argument("--no-prefill", action="store_true", help="skip the chunked-prefill timing")
     p.add_argument("--no-group", action="store_true", help="skip the group-wise-scale decode timing")
     p.add_argument("--no-latent", action="store_true", help="skip the head_dim 576 latent-cache timing")
+    p.add_argument("--no-early-cache", action="store_true",
+                   help="decode without KVQ_DECODE_EARLY_CACHE (cache reads wait for the step's append)")
     p.add_argument("--no-configs", action="store_true",
                    help="skip the other workloads (tiny, paged, spec, mixed) beside the default line")
     return p.parse_args()
@@ -225,8 +228,10 @@ class Rig:
         self.k_new, self.v_new, self.slots = gws[0].new_tokens()
         self.qs = [w.q("cuda", i).to(f"cuda:{dev}") for i in range(8)]
         # q, the block table and seq_lens are never written by the kernel before
-        # kvq_decode (kvq_append): the decode may read them while append finishes
-        self.plist = [gws[0].params(window=wd, flags=kvq.DECODE_EARLY_INPUTS) for wd in self.windows]
+        # kvq_decode (kvq_append), which writes only the new tokens' cache rows:
+        # the decode may read the inputs and the older rows while append finishes
+        flags = kvq.DECODE_EARLY_INPUTS | (kvq.DECODE_EARLY_CACHE if EARLY_CACHE else 0)
+        self.plist = [gws[0].params(window=wd, flags=flags) for wd in self.windows]
         self.bufs = [gws[0].buffers(p) for p in self.plist]
         self.stream = torch.cuda.current_stream()
 
@@ -758,6 +763,9 @@ def run_ours(args):
     from decode_attention_quantized_gb300 import build as cuda_build
     from decode_attention_quantized_gb300 import kvq, synth
 
+    global EARLY_CACHE
+    EARLY_CACHE = not args.no_early_cache
+
     world, rank, local = dist_setup()
     cuda_build.build()
     kvq.load()
@@ -824,7 +832,8 @@ def run_ours(args):
             "workload": describe(w),
             "cache_dtype": {1: "int8", 2: "fp8-e4m3", 3: "int4"}[w.dtype],
             "compute": "f16 x f16 -> f32 tensor-core mma, fp32 softmax",
-            "step": "kvq_append (new tokens) + kvq_decode (flags KVQ_DECODE_EARLY_INPUTS) + kvq_combine",
+            "step": "kvq_append (new tokens) + kvq_decode (flags KVQ_DECODE_EARLY_INPUTS%s) + kvq_combine"
+                    % (" | KVQ_DECODE_EARLY_CACHE" if EARLY_CACHE else ""),
             "timing": "K steps captured once in a CUDA graph and replayed between CUDA events; per-kernel "
                       "times from graphs of K launches of that kernel alone; decode_per_launch and configs: "
                       f"{n_pl} decode launches each bracketed by its own CUDA events (median, p10, p90)",

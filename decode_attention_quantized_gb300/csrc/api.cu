@@ -127,7 +127,8 @@ kvq_status check_params(const kvq_cache* c, const kvq_decode_params* p, bool qt 
     return KVQ_ERR_INVALID_ARG;
   if (p->num_q_heads % c->num_kv_heads != 0) return KVQ_ERR_INVALID_ARG;
   if (!std::isfinite(p->sm_scale) || !std::isfinite(p->softcap) || p->softcap < 0.0f) return KVQ_ERR_INVALID_ARG;
-  if (p->flags & ~(KVQ_DECODE_EARLY_INPUTS | KVQ_DECODE_NO_TCGEN05)) return KVQ_ERR_INVALID_ARG;
+  if (p->flags & ~(KVQ_DECODE_EARLY_INPUTS | KVQ_DECODE_NO_TCGEN05 | KVQ_DECODE_EARLY_CACHE))
+    return KVQ_ERR_INVALID_ARG;
   if ((long long)p->max_blocks_per_seq * c->block_size > (1LL << 30)) return KVQ_ERR_INVALID_ARG;
   if (p->num_q_heads / c->num_kv_heads > 8 || p->batch > kMaxBatch) return KVQ_ERR_UNSUPPORTED;
   if (qt ? (long long)p->q_tokens * (p->num_q_heads / c->num_kv_heads) > kQtRows : p->q_tokens > 8)
@@ -561,6 +562,7 @@ kvq_status decode_impl(const kvq_cache* cache, const kvq_decode_params* params, 
   // (the tensor-memory kernels load both sides)
   a.v_alias = (cache->layout == KVQ_LAYOUT_LATENT && !P.tc_nr && !P.qt) ? 1 : 0;
   a.early_reads = early_reads;
+  a.early_cache = (early_reads && (params->flags & KVQ_DECODE_EARLY_CACHE)) ? 1 : 0;
   char* ws = static_cast<char*>(workspace);
   a.plan = reinterpret_cast<int*>(ws);
   a.part_lse = reinterpret_cast<float*>(ws + P.ws_plan);

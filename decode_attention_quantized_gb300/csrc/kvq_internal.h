@@ -79,6 +79,7 @@ struct DecodeArgs {
   int v_alias;      // LATENT on the mma.sync kernel: a stage holds the K codes (and K scales) only,
                     // and V is read from them (one copy of each cache row per key)
   int early_reads;  // 1: read seq_lens, block table and q before the wait on the preceding grid
+  int early_cache;  // 1: also load cache rows older than the step's new tokens before that wait
   int* plan;        // workspace: [0] cost per CTA, [1] total tiles, [2] piece cost, [3] slots, then tile prefix[B+1]
   float* part_lse;  // [units_max, rows]   base-2 log-sum-exp of each piece
   float* part_o;    // [units_max, rows, D] normalized piece output

@@ -202,7 +202,9 @@ __device__ __forceinline__ void publish_slice(const DecodeArgs& a, const int* pl
 // a time (one coalesced load per 32 pages, the next batch loaded while the
 // current one is used) and hands them to lane 0 by shuffles.  With early
 // reads the first piece's ids are read before the wait on the preceding grid;
-// the cache is read, and the plan published, only after it.  Lane 0 waits for a free stage and issues,
+// the cache is read, and the plan published, only after it -- except, with
+// early cache reads (KVQ_DECODE_EARLY_CACHE), the stages before the one that
+// holds the step's new tokens.  Lane 0 waits for a free stage and issues,
 // per page segment of the stage, one TMA tensor copy per (slab, side) with
 // the block id as the outer coordinate, plus 1-D bulk copies of the per-row
 // scales.  kBurst: the whole stage's block ids are resolved first and its
@@ -251,7 +253,9 @@ __device__ void produce(const DecodeArgs& a, const Slice<Gm::KEYS>& sp, const CU
     // the next 32 ids are in flight while these are used, so a batch change
     // does not stall the copies on a block-table read
     int nx_id = base + 32 + lane <= p_last ? bt[base + 32 + lane] : -1;
-    gate();
+    // with early cache reads only the stage holding the step's new tokens
+    // waits for the preceding grid (which may be writing those rows)
+    if (!a.early_cache) gate();
     if (gt != sp.t_begin) {
       // the consumers read this piece's query rows once the previous piece
       // ends; the producer runs a ring ahead of them, so it pulls those rows
@@ -264,6 +268,7 @@ __device__ void produce(const DecodeArgs& a, const Slice<Gm::KEYS>& sp, const CU
     }
     for (int key0 = k0; key0 < k1; key0 += KT, ++it, rp.next(S)) {
       const int stage = (int)rp.stage;
+      if (a.early_cache && key0 + KT > L - a.q_tokens) gate();
       if (lane == 0 && it >= S && ok) {
         ok = (kBurst ? ptx::mbar_wait_bounded_inl(&bar_empty[stage], rp.phase ^ 1u)
                      : ptx::mbar_wait_bounded(&bar_empty[stage], rp.phase ^ 1u)) ? 1 : 0;

@@ -20,7 +20,7 @@ from .build import LIB_PATH
 INT8, FP8_E4M3, INT4 = 1, 2, 3
 LAYOUT_SEPARATE, LAYOUT_LATENT = 0, 1
 PER_ROW, PER_TENSOR, PER_CHANNEL, PER_GROUP = 1, 2, 3, 4
-DECODE_EARLY_INPUTS, DECODE_NO_TCGEN05 = 0x1, 0x2  # kvq_decode_params.flags
+DECODE_EARLY_INPUTS, DECODE_NO_TCGEN05, DECODE_EARLY_CACHE = 0x1, 0x2, 0x4  # kvq_decode_params.flags
 DEVERR_SLOT, DEVERR_BLOCK_ID, DEVERR_SEQ_LEN, DEVERR_TIMEOUT, DEVERR_POSITION = 0x1, 0x2, 0x4, 0x8, 0x10
 STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "workspace too small", 4: "CUDA error",
           5: "device timeout"}
@@ -173,8 +173,10 @@ class QuantizedPagedCache:
 def make_params(batch, num_q_heads, q_tokens, max_blocks_per_seq, *, max_seq_len=0, sm_scale=0.0, softcap=0.0,
                 window=0, flags=0) -> DecodeParams:
     """flags: DECODE_EARLY_INPUTS (q, block table, seq_lens and static scales are
-    not written by the kernel enqueued just before kvq_decode) and / or
-    DECODE_NO_TCGEN05 (17..64 query rows per kv head on the mma.sync layouts)."""
+    not written by the kernel enqueued just before kvq_decode), with it
+    DECODE_EARLY_CACHE (that kernel writes no cache row but the step's new
+    tokens'), and / or DECODE_NO_TCGEN05 (17..64 query rows per kv head on the
+    mma.sync layouts)."""
     return DecodeParams(int(batch), int(num_q_heads), int(q_tokens), int(max_blocks_per_seq), int(max_seq_len),
                         float(sm_scale), float(softcap), int(window), int(flags))
 

@@ -176,6 +176,15 @@ typedef struct {
  * (for comparing the two; results agree within the parity tolerance). */
 #define KVQ_DECODE_EARLY_INPUTS 0x1u
 #define KVQ_DECODE_NO_TCGEN05 0x2u
+/* KVQ_DECODE_EARLY_CACHE (with KVQ_DECODE_EARLY_INPUTS): the operation
+ * enqueued just before kvq_decode writes no cache row other than the step's
+ * new tokens (positions seq_lens[b] - q_tokens .. seq_lens[b] - 1): e.g. it
+ * is kvq_append of exactly those tokens, or it writes no cache at all.  The
+ * decode then loads every older row while that operation is still running and
+ * waits for it only before the 64- or 128-key tile that holds the new tokens,
+ * so the first cache reads overlap its tail.  Without KVQ_DECODE_EARLY_INPUTS
+ * the bit has no effect. */
+#define KVQ_DECODE_EARLY_CACHE 0x4u
 
 /* Human-readable name of a status code (static storage). */
 KVQ_API const char* kvq_status_string(kvq_status status);

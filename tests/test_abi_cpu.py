@@ -93,7 +93,7 @@ def test_append_rejects_bad_tokens(kvq):
     (dict(batch=-1), 1), (dict(num_q_heads=7), 1), (dict(num_q_heads=18), 2), (dict(q_tokens=0), 1),
     (dict(q_tokens=9), 2), (dict(max_blocks_per_seq=0), 1), (dict(max_seq_len=-5), 1), (dict(window=-1), 1),
     (dict(softcap=-1.0), 1), (dict(softcap=float("inf")), 1), (dict(sm_scale=float("nan")), 1),
-    (dict(batch=1025), 2), (dict(flags=4), 1), (dict(flags=0x80000001), 1),
+    (dict(batch=1025), 2), (dict(flags=8), 1), (dict(flags=0x80000001), 1),
 ])
 def test_decode_rejects_bad_params(kvq, bad, status):
     lib = kvq.load()

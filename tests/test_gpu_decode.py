@@ -126,16 +126,18 @@ def test_determinism_and_fresh_workspace(lib, orc):
 def test_early_inputs_flag_gives_the_same_bits(lib, orc, name, kw):
     """KVQ_DECODE_EARLY_INPUTS only moves the reads of q, the block table,
     seq_lens and the static scales ahead of the wait on the preceding kernel
-    (here kvq_append, which writes none of them): the result is bitwise the
-    default path's, on both decode kernels."""
+    (here kvq_append, which writes none of them), and KVQ_DECODE_EARLY_CACHE
+    the loads of every cache tile before the one holding the appended tokens:
+    the result is bitwise the default path's, on both decode kernels."""
     w = synth.make(name, **kw)
     gw, params, bufs, q, _ = run_case(orc, w)
     ref, ref_lse = bufs.out.clone(), bufs.lse.clone()
     k_new, v_new, slots = gw.new_tokens()
-    early = gw.params(flags=kvq.DECODE_EARLY_INPUTS)
-    for _ in range(3):
-        out, lse = gw.step(q, k_new, v_new, slots, early, bufs)
-        assert torch.equal(out, ref) and torch.equal(lse, ref_lse)
+    for flags in (kvq.DECODE_EARLY_INPUTS, kvq.DECODE_EARLY_INPUTS | kvq.DECODE_EARLY_CACHE):
+        early = gw.params(flags=flags)
+        for _ in range(3):
+            out, lse = gw.step(q, k_new, v_new, slots, early, bufs)
+            assert torch.equal(out, ref) and torch.equal(lse, ref_lse)
     assert kvq.kvq_get_device_error() == 0
 
 
