@@ -328,6 +328,10 @@ __global__ void __launch_bounds__(288, MINB)
     const uint32_t q_base = ptx::smem_u32(s_q);
     float* s_alpha = s_q + ROWS * (D / 2);               // [ROWS] logit factors
     const int rh = warp & 1, kq = warp >> 1;
+    // a row half past the unit's rows (8 or fewer rows: head_dim 576 with
+    // few query heads) converts no codes and runs no MMAs; its warps still
+    // meet the others at every barrier
+    const bool idle = rh * RW >= a.rows;
     const int g = lane >> 2, c = lane & 3;
     const int G = a.group, W = a.window;
     const float inv_g = __frcp_rn((float)G);  // r / G by dev::div_small
@@ -486,7 +490,7 @@ __global__ void __launch_bounds__(288, MINB)
 
         // ---- phase A: scores of this warp's 16 keys x NT n-tiles of rows
         const int kb = key0 + kq * kSub;
-        const bool active = ok && kb < k1;
+        const bool active = ok && kb < k1 && !idle;
         const int key_a = kb + g, key_b = key_a + 8;
         float x[NT][4];
         float vpa = 0.0f, vpb = 0.0f;
@@ -672,7 +676,7 @@ __global__ void __launch_bounds__(288, MINB)
         ptx::named_bar_sync(1, 8 * 32);
 
         // ---- phase C: channel quarter kq of this half's rows over the tile
-        for (int kg = 0; ok && kg < kTile / kSub; ++kg) {
+        for (int kg = 0; ok && !idle && kg < kTile / kSub; ++kg) {
           if (key0 + kg * kSub >= k1) break;  // that quarter wrote no P this tile
           uint32_t pb[NT][2];
           {
