@@ -635,7 +635,7 @@ kvq_status prefill_shape(const kvq_cache* c, const kvq_decode_params* p, kvq_dec
 // prefill's virtual sequences).
 kvq_status combine_impl(const kvq_cache* cache, const kvq_decode_params* params, bool qt, const void* workspace,
                         size_t workspace_bytes, const float* head_sink, void* out, float* lse_out,
-                        kvq_stream_t stream) {
+                        kvq_stream_t stream, bool warp_rows = false) {
   kvq_cache eff_;
   if (kvq_status s = resolve_cache(cache, &eff_)) return s;
   cache = &eff_;
@@ -670,7 +670,7 @@ kvq_status combine_impl(const kvq_cache* cache, const kvq_decode_params* params,
   a.rows = P.rows;
   a.head_dim = cache->head_dim;
   a.out_dim = cache->v_head_size;
-  return from_cuda(launch_combine(a, reinterpret_cast<cudaStream_t>(stream)));
+  return from_cuda(launch_combine(a, reinterpret_cast<cudaStream_t>(stream), warp_rows));
 }
 
 
@@ -805,7 +805,8 @@ KVQ_API kvq_status kvq_prefill(const kvq_cache* cache, const kvq_decode_params* 
   char* ws = static_cast<char*>(workspace) + head;
   if (kvq_status s = decode_impl(cache, &v, q, block_table, lens, n, 0, qt, ws, workspace_bytes - head, stream))
     return s;
-  return combine_impl(cache, &v, qt, ws, workspace_bytes - head, head_sink, out, lse_out, stream);
+  // a chunk's B x C x Hq rows have few pieces each: one warp per row
+  return combine_impl(cache, &v, qt, ws, workspace_bytes - head, head_sink, out, lse_out, stream, true);
 }
 
 KVQ_API kvq_status kvq_check_wait_timeout(uint32_t limit_us, kvq_stream_t stream) {

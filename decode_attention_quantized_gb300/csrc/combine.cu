@@ -19,6 +19,57 @@ namespace {
 
 constexpr int kCombineWarps = 8;
 
+// The end of one row (every lane of one warp): the merged output acc (this
+// lane's E channels) and weight sum against the row maximum m, the head sink,
+// the static V scale, the bf16 store and the natural-log LSE.
+template <int D>
+__device__ __forceinline__ void combine_finish(const CombineArgs& a, int row_id, int hq, int h, int lane,
+                                               float (&acc)[D / 32], float wsum, float m) {
+  constexpr int E = D / 32;
+  float lse_nat = -INFINITY;
+  if (wsum > 0.0f) {
+    const float inv = 1.0f / wsum;
+    const float lse2 = m + ptx::fast_log2(wsum);
+    lse_nat = lse2 * 0.69314718055994530942f;
+    float f = inv;
+    if (a.head_sink) f = inv / (1.0f + expf(a.head_sink[hq] - lse_nat));
+#pragma unroll
+    for (int e = 0; e < E; ++e) acc[e] *= f;
+    if (a.v_mode == KVQ_SCALE_PER_TENSOR) {
+      const float vs = a.v_scale[0];
+#pragma unroll
+      for (int e = 0; e < E; ++e) acc[e] *= vs;
+    } else if (a.v_mode == KVQ_SCALE_PER_CHANNEL) {
+      const float* vs = a.v_scale + (size_t)h * D + lane * E;
+#pragma unroll
+      for (int e = 0; e < E; ++e) acc[e] *= vs[e];
+    }
+  }
+
+  uint32_t packed[E / 2];
+#pragma unroll
+  for (int e = 0; e < E; e += 2) {
+    const __nv_bfloat162 v = __floats2bfloat162_rn(acc[e], acc[e + 1]);
+    packed[e / 2] = *reinterpret_cast<const uint32_t*>(&v);
+  }
+  if (a.lse_out && lane == 0) a.lse_out[row_id] = lse_nat;
+  if (lane * E >= a.out_dim) return;  // LATENT: only the leading v_head_size channels
+  uint16_t* dst = a.out + (size_t)row_id * a.out_dim + lane * E;
+  if constexpr (E == 8) {
+    *reinterpret_cast<uint4*>(dst) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+  } else if constexpr (E == 4) {
+    *reinterpret_cast<uint2*>(dst) = make_uint2(packed[0], packed[1]);
+  } else if constexpr (E == 2) {
+    *reinterpret_cast<uint32_t*>(dst) = packed[0];
+  } else {
+    // head_dim 576: 18 channels a lane, the leading v_head_size (a multiple of
+    // 8) written pair by pair
+#pragma unroll
+    for (int j = 0; j < E / 2; ++j)
+      if (lane * E + 2 * j < a.out_dim) reinterpret_cast<uint32_t*>(dst)[j] = packed[j];
+  }
+}
+
 // One CTA per output row; warp w folds pieces w, w + 8, ... (ascending), then
 // warp 0 adds the eight warp sums in warp order.  Every split's weight is
 // taken against the row's maximum log-sum-exp, so the result does not depend
@@ -107,48 +158,70 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const Combi
     for (int e = 0; e < E; ++e) acc[e] += s_acc[w][lane * E + e];
   }
 
-  float lse_nat = -INFINITY;
-  if (wsum > 0.0f) {
-    const float inv = 1.0f / wsum;
-    const float lse2 = m + ptx::fast_log2(wsum);
-    lse_nat = lse2 * 0.69314718055994530942f;
-    float f = inv;
-    if (a.head_sink) f = inv / (1.0f + expf(a.head_sink[hq] - lse_nat));
+  combine_finish<D>(a, row_id, hq, h, lane, acc, wsum, m);
+}
+
+// One warp per output row, kCombineWarps rows a CTA: for calls with many rows
+// of few pieces each (a prefill chunk: B x C x Hq rows), where a CTA per row
+// leaves the GPU waiting on launch and latency.  The row's pieces are folded
+// in slot order against the row's maximum, then combine_finish.
+template <int D>
+__global__ void __launch_bounds__(kCombineWarps * 32) combine_rows_kernel(const CombineArgs a) {
+  constexpr int E = D / 32;
+  ptx::griddep_wait();
+  ptx::griddep_launch_dependents();
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const long long row_ll = (long long)blockIdx.x * kCombineWarps + warp;
+  if (row_ll >= (long long)a.batch * a.q_tokens * a.num_q_heads) return;
+  const int row_id = (int)row_ll;
+  const int hq = row_id % a.num_q_heads;
+  const int t = (row_id / a.num_q_heads) % a.q_tokens;
+  const int b = row_id / (a.num_q_heads * a.q_tokens);
+  const int h = hq / a.group;
+  const int r = t * a.group + (hq % a.group);
+  const int W = a.plan[0], c = a.plan[2];
+  const int* pre = a.plan + 4;
+  const int nb = pre[b + 1] - pre[b];
+  const int seg = b * a.num_kv_heads + h;
+  const long long s_cost = (long long)pre[b] * a.num_kv_heads + (long long)h * nb + (long long)c * seg;
+  const int i0 = nb > 0 ? seg + (int)(s_cost / W) : 0;
+  const int i1 = nb > 0 ? seg + (int)((s_cost + nb - 1) / W) + 1 : 0;
+
+  float m = -INFINITY;
+  for (int it = i0 + lane; it < i1; it += 32) m = fmaxf(m, a.part_lse[(size_t)it * a.rows + r]);
 #pragma unroll
-    for (int e = 0; e < E; ++e) acc[e] *= f;
-    if (a.v_mode == KVQ_SCALE_PER_TENSOR) {
-      const float vs = a.v_scale[0];
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  float acc[E];
 #pragma unroll
-      for (int e = 0; e < E; ++e) acc[e] *= vs;
-    } else if (a.v_mode == KVQ_SCALE_PER_CHANNEL) {
-      const float* vs = a.v_scale + (size_t)h * D + lane * E;
+  for (int e = 0; e < E; ++e) acc[e] = 0.0f;
+  float wsum = 0.0f;
+  if (m != -INFINITY) {
+    for (int it = i0; it < i1; ++it) {
+      const size_t u = (size_t)it * a.rows + r;
+      const float l2 = a.part_lse[u];
+      const float w = l2 == -INFINITY ? 0.0f : ptx::fast_exp2(l2 - m);
+      wsum += w;
+      const float* po = a.part_o + u * D + lane * E;
+      if constexpr (E % 4 == 0) {
 #pragma unroll
-      for (int e = 0; e < E; ++e) acc[e] *= vs[e];
+        for (int e = 0; e < E; e += 4) {
+          const float4 v = *reinterpret_cast<const float4*>(po + e);
+          acc[e] += w * v.x;
+          acc[e + 1] += w * v.y;
+          acc[e + 2] += w * v.z;
+          acc[e + 3] += w * v.w;
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < E; e += 2) {
+          const float2 v = *reinterpret_cast<const float2*>(po + e);
+          acc[e] += w * v.x;
+          acc[e + 1] += w * v.y;
+        }
+      }
     }
   }
-
-  uint32_t packed[E / 2];
-#pragma unroll
-  for (int e = 0; e < E; e += 2) {
-    const __nv_bfloat162 v = __floats2bfloat162_rn(acc[e], acc[e + 1]);
-    packed[e / 2] = *reinterpret_cast<const uint32_t*>(&v);
-  }
-  if (a.lse_out && lane == 0) a.lse_out[row_id] = lse_nat;
-  if (lane * E >= a.out_dim) return;  // LATENT: only the leading v_head_size channels
-  uint16_t* dst = a.out + (size_t)row_id * a.out_dim + lane * E;
-  if constexpr (E == 8) {
-    *reinterpret_cast<uint4*>(dst) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
-  } else if constexpr (E == 4) {
-    *reinterpret_cast<uint2*>(dst) = make_uint2(packed[0], packed[1]);
-  } else if constexpr (E == 2) {
-    *reinterpret_cast<uint32_t*>(dst) = packed[0];
-  } else {
-    // head_dim 576: 18 channels a lane, the leading v_head_size (a multiple of
-    // 8) written pair by pair
-#pragma unroll
-    for (int j = 0; j < E / 2; ++j)
-      if (lane * E + 2 * j < a.out_dim) reinterpret_cast<uint32_t*>(dst)[j] = packed[j];
-  }
+  combine_finish<D>(a, row_id, hq, h, lane, acc, wsum, m);
 }
 
 // Sequence lengths of a prefill chunk's virtual sequences (one thread each).
@@ -187,9 +260,20 @@ cudaError_t launch_prefill_lens(const int32_t* seq_lens, int32_t* out, int batch
                     n, C, T);
 }
 
-cudaError_t launch_combine(const CombineArgs& a, cudaStream_t stream) {
-  const unsigned blocks = (unsigned)((long long)a.batch * a.q_tokens * a.num_q_heads);
+cudaError_t launch_combine(const CombineArgs& a, cudaStream_t stream, bool warp_rows) {
+  const long long rows = (long long)a.batch * a.q_tokens * a.num_q_heads;
   constexpr int threads = kCombineWarps * 32;
+  if (warp_rows) {
+    const unsigned blocks = (unsigned)((rows + kCombineWarps - 1) / kCombineWarps);
+    switch (a.head_dim) {
+      case 64: return launch_pdl(combine_rows_kernel<64>, blocks, threads, 0, stream, a);
+      case 128: return launch_pdl(combine_rows_kernel<128>, blocks, threads, 0, stream, a);
+      case 256: return launch_pdl(combine_rows_kernel<256>, blocks, threads, 0, stream, a);
+      case 576: return launch_pdl(combine_rows_kernel<576>, blocks, threads, 0, stream, a);
+      default: return cudaErrorInvalidValue;
+    }
+  }
+  const unsigned blocks = (unsigned)rows;
   switch (a.head_dim) {
     case 64: return launch_pdl(combine_kernel<64>, blocks, threads, 0, stream, a);
     case 128: return launch_pdl(combine_kernel<128>, blocks, threads, 0, stream, a);
