@@ -670,6 +670,11 @@ kvq_status combine_impl(const kvq_cache* cache, const kvq_decode_params* params,
   a.rows = P.rows;
   a.head_dim = cache->head_dim;
   a.out_dim = cache->v_head_size;
+  // a warp per row when the rows have about 16 pieces or fewer on average
+  // (the pieces are the grid's slices plus one per segment); a CTA per row
+  // for few rows of many pieces (one long sequence split over the GPU)
+  const long long segs = (long long)params->batch * cache->num_kv_heads;
+  if ((long long)P.units_max <= 16 * segs) warp_rows = true;
   return from_cuda(launch_combine(a, reinterpret_cast<cudaStream_t>(stream), warp_rows));
 }
 

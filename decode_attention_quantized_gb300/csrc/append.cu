@@ -173,8 +173,12 @@ __device__ bool norm_rope_row(const NormRope& p, int n, int lane, float (&x)[E],
 template <int D>
 __global__ void __launch_bounds__(256) append_kernel(const AppendArgs a) {
   constexpr int E = D / 32;  // channels per lane
-  ptx::griddep_wait();
+  // the next kernel (a decode of these tokens) may be scheduled at once: it
+  // waits for this grid, which waits for the one before it, before it reads
+  // the rows written here or writes anything, so its early work overlaps
+  // both this grid and the combine enqueued before it
   ptx::griddep_launch_dependents();
+  ptx::griddep_wait();
   const int wg = (int)((blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5);
   const int lane = threadIdx.x & 31;
   if (wg >= a.n_tokens * a.num_kv_heads * 2) return;

@@ -162,9 +162,10 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const Combi
 }
 
 // One warp per output row, kCombineWarps rows a CTA: for calls with many rows
-// of few pieces each (a prefill chunk: B x C x Hq rows), where a CTA per row
-// leaves the GPU waiting on launch and latency.  The row's pieces are folded
-// in slot order against the row's maximum, then combine_finish.
+// of few pieces each (a prefill chunk: B x C x Hq rows; a ragged decode
+// batch), where a CTA per row leaves the GPU waiting on launch and latency
+// and takes room the next step's decode could use.  The row's pieces are
+// folded in slot order against the row's maximum, then combine_finish.
 template <int D>
 __global__ void __launch_bounds__(kCombineWarps * 32) combine_rows_kernel(const CombineArgs a) {
   constexpr int E = D / 32;
@@ -196,28 +197,54 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_rows_kernel(const 
   for (int e = 0; e < E; ++e) acc[e] = 0.0f;
   float wsum = 0.0f;
   if (m != -INFINITY) {
-    for (int it = i0; it < i1; ++it) {
-      const size_t u = (size_t)it * a.rows + r;
-      const float l2 = a.part_lse[u];
-      const float w = l2 == -INFINITY ? 0.0f : ptx::fast_exp2(l2 - m);
-      wsum += w;
-      const float* po = a.part_o + u * D + lane * E;
-      if constexpr (E % 4 == 0) {
+    // 32 pieces at a time: lane j takes the weight of piece base + j, the
+    // warp then adds the pieces in order, loading four ahead of their FMAs
+    for (int base = i0; base < i1; base += 32) {
+      const int n = min(32, i1 - base);
+      float wl = 0.0f;
+      if (lane < n) {
+        const float l2 = a.part_lse[(size_t)(base + lane) * a.rows + r];
+        wl = l2 == -INFINITY ? 0.0f : ptx::fast_exp2(l2 - m);
+      }
+      float ws = wl;
 #pragma unroll
-        for (int e = 0; e < E; e += 4) {
-          const float4 v = *reinterpret_cast<const float4*>(po + e);
-          acc[e] += w * v.x;
-          acc[e + 1] += w * v.y;
-          acc[e + 2] += w * v.z;
-          acc[e + 3] += w * v.w;
-        }
-      } else {
+      for (int o = 16; o > 0; o >>= 1) ws += __shfl_xor_sync(0xffffffffu, ws, o);
+      wsum += ws;
+      for (int j = 0; j < n; j += 4) {
+        float v[4][E];
+        float w[4];
 #pragma unroll
-        for (int e = 0; e < E; e += 2) {
-          const float2 v = *reinterpret_cast<const float2*>(po + e);
-          acc[e] += w * v.x;
-          acc[e + 1] += w * v.y;
+        for (int q = 0; q < 4; ++q) {
+          w[q] = __shfl_sync(0xffffffffu, wl, (j + q) & 31);
+          if (j + q < n) {
+            const float* po = a.part_o + ((size_t)(base + j + q) * a.rows + r) * D + lane * E;
+            if constexpr (E % 4 == 0) {
+#pragma unroll
+              for (int e = 0; e < E; e += 4) {
+                const float4 t = *reinterpret_cast<const float4*>(po + e);
+                v[q][e] = t.x;
+                v[q][e + 1] = t.y;
+                v[q][e + 2] = t.z;
+                v[q][e + 3] = t.w;
+              }
+            } else {
+#pragma unroll
+              for (int e = 0; e < E; e += 2) {
+                const float2 t = *reinterpret_cast<const float2*>(po + e);
+                v[q][e] = t.x;
+                v[q][e + 1] = t.y;
+              }
+            }
+          } else {
+            w[q] = 0.0f;
+#pragma unroll
+            for (int e = 0; e < E; ++e) v[q][e] = 0.0f;
+          }
         }
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+#pragma unroll
+          for (int e = 0; e < E; ++e) acc[e] += w[q] * v[q][e];
       }
     }
   }

@@ -453,7 +453,6 @@ __global__ void __launch_bounds__(288, MINB)
           }
         }
       }
-      ptx::griddep_wait();  // before the first workspace write (no-op after the first)
       ptx::named_bar_sync(1, 8 * 32);
       float al[NT][2], m[NT][2], l[NT][2];
       int pos[NT][2];
@@ -783,6 +782,9 @@ __global__ void __launch_bounds__(288, MINB)
           if (g == 0) s_l[kq * ROWS + rh * RW + nt * 8 + 2 * c + i] = v;
         }
       ptx::named_bar_sync(1, 8 * 32);
+      // the tiles above may run while the preceding grid finishes; the
+      // workspace is written only after it (no-op after the first)
+      ptx::griddep_wait();
       float to_true = v_row ? dev::pow2i(F) : 1.0f;
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
@@ -845,7 +847,6 @@ __global__ void __launch_bounds__(288, MINB)
     // ---- Q prologue: this lane's channels of query row g of the row group
     uint32_t qf[Gm::NMT][2];
     const float alpha_g = dev::q_prologue<DT, D>(a, rg * 8 + g, b, h, c, qf);
-    ptx::griddep_wait();  // before the first workspace write (no-op after the first)
     const int r0 = rg * 8 + 2 * c, r1 = r0 + 1;
     // with a softcap the row factors also carry 1/softcap (clamped to FLT_MAX
     // like the factors themselves, so zero codes keep zero scores), and the
@@ -1146,6 +1147,9 @@ __global__ void __launch_bounds__(288, MINB)
       ptx::named_bar_sync(1, (uint32_t)n_cw * 32);
     }
     if (kw == a.key_warps - 1) {
+      // the tiles above may run while the preceding grid finishes; the
+      // workspace is written only after it (no-op after the first)
+      ptx::griddep_wait();
       const float f0 = l0 > 0.0f ? to_true / l0 : 0.0f, f1 = l1 > 0.0f ? to_true / l1 : 0.0f;
       const int rr0 = rg * 8 + 2 * c, rr1 = rr0 + 1;
       float* o0 = a.part_o + ((size_t)u * a.rows + rr0) * D;

@@ -472,8 +472,12 @@ __global__ void __launch_bounds__(kQtWarps * 32, 1)
         // padding rows: their Q (and so S, P and O) is never read
         if (lane == 0) ptx::mbar_arrive(b_qfull);
       }
-      ptx::griddep_wait();  // before the first workspace write (no-op after the first)
-      if (pc > 0) epilogue(e_u, e_last, e_mu, e_l, e_F);
+      if (pc > 0) {
+        // the previous piece's tiles may have run while the preceding grid
+        // finished; the workspace is written only after it
+        ptx::griddep_wait();
+        epilogue(e_u, e_last, e_mu, e_l, e_F);
+      }
       if (!more) break;
 
       float mu = -INFINITY;         // reference maximum of this row (log2 units)

@@ -734,8 +734,12 @@ __global__ void __launch_bounds__(kTcWarps * 32, 1)
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(b_qfull);
       }
-      ptx::griddep_wait();  // before the first workspace write (no-op after the first)
-      if (pc > 0) epilogue(e_u, e_last, e_mu0, e_mu1, e_F);
+      if (pc > 0) {
+        // the previous piece's tiles may have run while the preceding grid
+        // finished; the workspace is written only after it
+        ptx::griddep_wait();
+        epilogue(e_u, e_last, e_mu0, e_mu1, e_F);
+      }
       if (!more) break;
       ptx::named_bar_sync(1, 128);  // this piece's row factors are visible
 

@@ -167,9 +167,11 @@ typedef struct {
  * and the query prologue then overlap that kernel's tail.  Set it only when
  * none of those inputs is written by the operation enqueued just before
  * kvq_decode on the stream: e.g. they were copied from the host, or that
- * operation is kvq_append (which writes only the cache).  It must not be set
- * when that operation is kvq_norm_rope_apply producing q, or any kernel that
- * writes q, block_table or seq_lens.
+ * operation is kvq_append (which writes only the cache) and the one before
+ * the append writes none of them either (kvq_append lets the decode start
+ * while that one finishes: a kvq_combine, say, which writes only out and
+ * lse).  It must not be set when that operation is kvq_norm_rope_apply
+ * producing q, or any kernel that writes q, block_table or seq_lens.
  *
  * KVQ_DECODE_NO_TCGEN05: keep shapes of 17..64 query rows per kv head on the
  * mma.sync kernel's layouts instead of the tensor-memory (tcgen05) kernel
@@ -200,7 +202,11 @@ KVQ_API const char* kvq_status_string(kvq_status status);
  * the nearest e4m3 value (ties to even, finite overflow saturated to 448).
  * slot_mapping int64 [n_tokens] (device): slot < 0 skips the token (padding);
  * slot >= num_blocks * block_size sets KVQ_DEVERR_SLOT and skips it.
- * Rows already in the cache are never touched.  n_tokens == 0 is a no-op. */
+ * Rows already in the cache are never touched.  n_tokens == 0 is a no-op.
+ * Its kernel lets the next kernel on the stream be scheduled at once (that
+ * kernel may then run while this one and the one before it finish); every
+ * kvq kernel waits for its predecessor before it reads what that one writes,
+ * so only a decode with KVQ_DECODE_EARLY_INPUTS reads anything early. */
 KVQ_API kvq_status kvq_append(const kvq_cache* cache, const void* k_new, const void* v_new,
                               const int64_t* slot_mapping, int32_t n_tokens,
                               kvq_stream_t stream);

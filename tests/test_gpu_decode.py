@@ -11,6 +11,7 @@ import torch
 from decode_attention_quantized_gb300 import kvq, synth
 from decode_attention_quantized_gb300.workload import GpuWorkload
 
+from guard import guarded
 from parity import OracleSide, bits, check_lse, check_rows
 
 pytestmark = pytest.mark.gpu
@@ -139,6 +140,47 @@ def test_early_inputs_flag_gives_the_same_bits(lib, orc, name, kw):
             out, lse = gw.step(q, k_new, v_new, slots, early, bufs)
             assert torch.equal(out, ref) and torch.equal(lse, ref_lse)
     assert kvq.kvq_get_device_error() == 0
+
+
+@pytest.mark.parametrize("name,kw", [("gqa", dict(ctx=3000)), ("paged", dict(batch=5, max_ctx=700)),
+                                     ("spec", dict(ctx=700, batch=2)), ("mixed", dict(batch=5, max_ctx=6000))])
+def test_early_flags_back_to_back_steps_with_changing_inputs(lib, orc, name, kw):
+    """Steps enqueued back to back with no host synchronisation (append,
+    decode, combine, append, ...) under both early flags, each step appending
+    other new-token rows at the same slots and decoding another query into its
+    own output: every step gives bitwise what the same step gives alone with
+    the default flags.  A decode that read an appended row before its append
+    finished, or wrote the shared workspace while the previous combine still
+    read it, would return another step's bits."""
+    w = synth.make(name, **kw)
+    gw = GpuWorkload(w, gen_device="cpu")
+    gw.fill_history()
+    k0, v0, slots = gw.new_tokens()
+    kv = [(k0, v0), (torch.roll(k0, 1, dims=-1).contiguous(), (-v0).contiguous())]
+    q0 = w.q("cpu").cuda()
+    qs = [q0, (-q0).contiguous(), torch.flip(q0, dims=(-1,)).contiguous()]
+    base, early = gw.params(), gw.params(flags=kvq.DECODE_EARLY_INPUTS | kvq.DECODE_EARLY_CACHE)
+    bufs = gw.buffers(base)
+    steps = [(i % 2, i % 3) for i in range(8)]
+    ref = {}
+    for key in sorted(set(steps)):
+        k, v = kv[key[0]]
+        kvq.kvq_append(gw.cache, k, v, slots)
+        kvq.decode_step(gw.cache, base, qs[key[1]], gw.block_table, gw.seq_lens, bufs, gw.head_sink)
+        torch.cuda.synchronize()
+        ref[key] = (bufs.out.clone(), bufs.lse.clone())
+    outs = [guarded(torch.empty_like(bufs.out)) for _ in steps]
+    lses = [guarded(torch.empty_like(bufs.lse)) for _ in steps]
+    torch.cuda.synchronize()
+    for i, (a, b) in enumerate(steps):
+        k, v = kv[a]
+        kvq.kvq_append(gw.cache, k, v, slots)
+        kvq.kvq_decode(gw.cache, early, qs[b], gw.block_table, gw.seq_lens, bufs.workspace)
+        kvq.kvq_combine(gw.cache, early, bufs.workspace, gw.head_sink, outs[i], lses[i])
+    torch.cuda.synchronize()
+    assert kvq.kvq_get_device_error() == 0
+    for i, key in enumerate(steps):
+        assert torch.equal(outs[i], ref[key][0]) and torch.equal(lses[i], ref[key][1]), f"step {i} {key}"
 
 
 def test_large_per_channel_k_scale_with_zero_codes_is_finite(lib, orc):
