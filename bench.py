@@ -858,6 +858,9 @@ def run_ours(args):
             "frac": round(achieved / peak, 4),
             "traffic": traffic_from_profiles(tag),
             "algorithmic_bytes_per_launch": int(dec_bytes),
+            "timing": "mean over a CUDA graph of K decode launches back to back; consecutive launches "
+                      "overlap (the next one's plan, copies and tiles run during the previous one's tail), "
+                      "so this is a period per launch; decode_per_launch has single launches",
         },
         "gpu_launches": res["launches"],
         "clocks": clk,

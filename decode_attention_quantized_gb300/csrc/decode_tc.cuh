@@ -734,12 +734,11 @@ __global__ void __launch_bounds__(kTcWarps * 32, 1)
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(b_qfull);
       }
-      if (pc > 0) {
-        // the previous piece's tiles may have run while the preceding grid
-        // finished; the workspace is written only after it
-        ptx::griddep_wait();
-        epilogue(e_u, e_last, e_mu0, e_mu1, e_F);
-      }
+      // before the first tile (not only before the first workspace write, as
+      // in the other kernels): this kernel holds a whole SM, and its tiles
+      // run early only at the cost of the preceding grid's last CTAs
+      ptx::griddep_wait();
+      if (pc > 0) epilogue(e_u, e_last, e_mu0, e_mu1, e_F);
       if (!more) break;
       ptx::named_bar_sync(1, 128);  // this piece's row factors are visible
 
