@@ -183,6 +183,26 @@ def test_early_flags_back_to_back_steps_with_changing_inputs(lib, orc, name, kw)
         assert torch.equal(outs[i], ref[key][0]) and torch.equal(lses[i], ref[key][1]), f"step {i} {key}"
 
 
+def test_combine_of_a_row_with_many_pieces(lib, orc):
+    """A ragged batch whose rows have few pieces on average (so kvq_combine
+    folds each row with one warp) but one long sequence split over about 150
+    CTAs: its rows fold their pieces 32 at a time, the last group partial.
+    Against the oracle, with a head sink, and bitwise repeatable."""
+    B, bs = 40, 256
+    L = np.array([40000] + [16] * (B - 1), np.int32)
+    nb_long = -(-40000 // bs)
+    table = np.zeros((B, nb_long), np.int32)
+    table[0] = np.arange(nb_long)
+    table[1:, 0] = nb_long + np.arange(B - 1)
+    w = synth.Workload("manypieces", kvq.INT8, kvq.PER_CHANNEL, kvq.PER_TENSOR, B, 8, 2, 128, 1, bs, L, table,
+                       nb_long + B - 1, use_sink=True, k_channel_lognormal=0.5, seed=17)
+    gw, params, bufs, q, _ = run_case(orc, w)
+    ref, ref_lse = bufs.out.clone(), bufs.lse.clone()
+    kvq.decode_step(gw.cache, params, q, gw.block_table, gw.seq_lens, bufs, gw.head_sink)
+    torch.cuda.synchronize()
+    assert torch.equal(bufs.out, ref) and torch.equal(bufs.lse, ref_lse)
+
+
 def test_large_per_channel_k_scale_with_zero_codes_is_finite(lib, orc):
     """INT4 PR #32515: q * k_scale far beyond fp16 range with every K code
     zero must not become inf * 0 = NaN; the output is the mean of V."""

@@ -36,6 +36,7 @@ CASES = [
     ("fp8", kvq.PER_TENSOR, kvq.PER_TENSOR, 128, 4, 64, (70, 2000, 640), 0, 50.0, True),     # 32 x 4, softcap, sink
     ("int4", kvq.PER_CHANNEL, kvq.PER_ROW, 128, 2, 512, (512, 1300), 0, 0.0, False),         # 64 x 2
     ("int8", kvq.PER_ROW, kvq.PER_ROW, 128, 1, 100, (100, 300), 37, 0.0, False),             # 100 x 1, window 37
+    ("int8", kvq.PER_ROW, kvq.PER_ROW, 128, 4, 64, (40000, 64), 0, 0.0, True),               # rows of > 32 pieces
 ]
 
 
