@@ -7,8 +7,8 @@
 // per-channel V scale applied to the output (the V half of the per-channel
 // fold): onnxruntime PR #32515, Description.
 //
-// One CTA per output row (b, t, query head); each lane owns D/32 consecutive
-// channels.
+// One CTA per output row (b, t, query head), or one warp per row for calls
+// with many rows of few pieces; each lane owns D/32 consecutive channels.
 #include <cuda_bf16.h>
 
 #include "kvq_internal.h"

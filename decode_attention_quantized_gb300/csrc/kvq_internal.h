@@ -188,7 +188,7 @@ cudaError_t launch_norm_rope(const NormRopeArgs& a, cudaStream_t stream);
 // The bounded-wait check: one wait that runs out after limit_ns.
 cudaError_t launch_wait_probe(unsigned int* err, unsigned long long limit_ns, cudaStream_t stream);
 // warp_rows: one warp per output row (many rows of few pieces: a prefill
-// chunk) instead of one CTA per row.
+// chunk, a ragged decode batch) instead of one CTA per row.
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t stream, bool warp_rows = false);
 // out[b * n + j] = max(0, seq_lens[b] - C + T (j + 1)) for the n = C / T groups
 // of a prefill chunk (virtual sequences of T tokens).
